@@ -1,0 +1,509 @@
+// api.cu -- the C ABI declared in include/cpw_moe.h: handle, argument checks, workspace
+// planning and allocation, weight re-layout, TMA descriptors, and the launch sequence of
+// one forward:
+//   dispatch (cooperative, one CTA per SM)  ->  gate_up GEMM + SwiGLU/requant  ->
+//   down GEMM + weighted scatter  ->  combine reduce + workspace reset
+// all on the caller's stream.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+
+#include "../../include/cpw_moe.h"
+#include "moe_internal.cuh"
+
+using namespace cpw;
+
+struct moe_ctx {
+    int dev = -1;
+    int num_sms = 0;
+    Dims d{};
+    bool reserved = false;
+    bool have_weights = false;
+    Workspace ws{};
+    void *small_mem = nullptr;   // header + routing arrays (size depends on E, R only)
+    void *big_mem = nullptr;     // table, pools, combine, staging (depends on max_tokens)
+    size_t small_bytes = 0, big_bytes = 0;
+    uint8_t *w1 = nullptr;       // [E][2I][H] interleaved gate/up
+    float *s1 = nullptr;         // [E][2I/128][H/128]
+    uint8_t *w2 = nullptr;       // [E][H][I]
+    float *s2 = nullptr;         // [E][H/128][I/128]
+    void *w_mem = nullptr;
+    size_t w_bytes = 0;
+    CUtensorMap tm_pool{}, tm_act{}, tm_w1{}, tm_w2{};
+    // staging buffers of moe_forward_host
+    uint8_t *st_x = nullptr;
+    float *st_sf = nullptr;
+    int64_t *st_idx = nullptr;
+    float *st_w = nullptr;
+    uint16_t *st_out = nullptr;
+    cudaStream_t last_stream = nullptr;
+    bool have_last = false;
+    int last_T = 0;
+    long long timeout_ns = 2000000000LL;
+    int debug_skip_barrier = 0;
+};
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int get_encoder()
+{
+    if (g_encode)
+        return MOE_OK;
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return MOE_ERR_CUDA;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    return MOE_OK;
+}
+
+// 2-D byte matrix [rows][cols] (row-major), tiles of 128 bytes x box_rows, 128-byte swizzle.
+int encode_tile_map(CUtensorMap *m, void *base, uint64_t rows, uint64_t cols, uint32_t box_rows)
+{
+    if (get_encoder() != MOE_OK)
+        return MOE_ERR_CUDA;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols};
+    cuuint32_t box[2] = {128, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
+}
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Bump allocator over one cudaMalloc'd block.
+struct Carver {
+    char *base;
+    size_t off = 0;
+    template <typename T>
+    T *take(size_t count)
+    {
+        off = align_up(off, 256);
+        T *p = reinterpret_cast<T *>(base ? base + off : nullptr);
+        off += count * sizeof(T);
+        return p;
+    }
+};
+
+#define CK(x)                                  \
+    do {                                       \
+        if ((x) != cudaSuccess)                \
+            return MOE_ERR_CUDA;               \
+    } while (0)
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+void free_big(moe_ctx *h)
+{
+    if (h->big_mem)
+        cudaFree(h->big_mem);
+    h->big_mem = nullptr;
+    h->big_bytes = 0;
+    h->reserved = false;
+}
+
+// Carve the max_tokens-dependent part of the workspace; with base == nullptr only sizes it.
+size_t carve_big(moe_ctx *h, char *base, int max_tokens, Workspace &ws)
+{
+    const Dims &d = h->d;
+    Carver c{base};
+    const int tsrc_cap = std::max(1, max_tokens / d.R);
+    const long long routed = static_cast<long long>(max_tokens) * d.K;
+    const int max_blocks = static_cast<int>((routed + BM - 1) / BM) + d.E;
+    const long long P = static_cast<long long>(max_blocks) * BM;
+    ws.tsrc_cap = tsrc_cap;
+    ws.max_blocks = max_blocks;
+    ws.P = static_cast<int>(P);
+    ws.max_tokens = max_tokens;
+    ws.block_expert = c.take<int32_t>(max_blocks);
+    ws.block_rows = c.take<int32_t>(max_blocks);
+    ws.arrive = c.take<uint32_t>(max_blocks);
+    ws.table = c.take<int32_t>(static_cast<size_t>(d.E) * d.R * tsrc_cap);
+    ws.meta = c.take<uint32_t>(static_cast<size_t>(P) * 3);
+    ws.pool_x = c.take<uint8_t>(static_cast<size_t>(P) * d.H);
+    ws.pool_sf = c.take<float>(static_cast<size_t>(P) * (d.H / 128));
+    ws.act = c.take<uint8_t>(static_cast<size_t>(P) * d.I);
+    ws.act_sf = c.take<float>(static_cast<size_t>(P) * (d.I / 128));
+    ws.combine = c.take<uint16_t>(static_cast<size_t>(d.K) * max_tokens * d.H);
+    h->st_x = c.take<uint8_t>(static_cast<size_t>(max_tokens) * d.H);
+    h->st_sf = c.take<float>(static_cast<size_t>(max_tokens) * (d.H / 128));
+    h->st_idx = c.take<int64_t>(static_cast<size_t>(max_tokens) * d.K);
+    h->st_w = c.take<float>(static_cast<size_t>(max_tokens) * d.K);
+    h->st_out = c.take<uint16_t>(static_cast<size_t>(max_tokens) * d.H);
+    return align_up(c.off, 256);
+}
+
+int sync_last(moe_ctx *h)
+{
+    if (h->have_last)
+        CK(cudaStreamSynchronize(h->last_stream));
+    return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *moe_status_string(int s)
+{
+    switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_CUDA: return "CUDA call failed";
+    case MOE_ERR_CAPACITY: return "token count above the reserved maximum";
+    case MOE_ERR_NO_WEIGHTS: return "weights not loaded";
+    case MOE_ERR_UNSUPPORTED_DEVICE: return "unsupported device or shape";
+    case MOE_ERR_BAD_INDEX: return "expert id outside [0,E) (device)";
+    case MOE_ERR_TIMEOUT: return "device wait timed out";
+    case MOE_ERR_SLOT_OVERFLOW: return "more than T/R rows of one source for one expert (device)";
+    case MOE_ERR_NOT_RESERVED: return "workspace not reserved";
+    default: return "unknown status";
+    }
+}
+
+int moe_create(int E, int H, int I, int topk, int R, moe_handle_t *out)
+{
+    if (!out)
+        return MOE_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (E < 1 || E > 1024 || H < 256 || H % 256 != 0 || I < 128 || I % 128 != 0 || topk < 1 ||
+        topk > 32 || topk > E || R < 1 || R > 64 || E * R > 16384)
+        return MOE_ERR_INVALID_ARG;
+    int dev = 0;
+    CK(cudaGetDevice(&dev));
+    cudaDeviceProp prop;
+    CK(cudaGetDeviceProperties(&prop, dev));
+    if (!(prop.major == 10 && prop.minor == 3))
+        return MOE_ERR_UNSUPPORTED_DEVICE;
+    moe_ctx *h = new (std::nothrow) moe_ctx();
+    if (!h)
+        return MOE_ERR_INVALID_ARG;
+    h->dev = dev;
+    h->num_sms = prop.multiProcessorCount;
+    h->d = Dims{E, H, I, topk, R};
+    *out = h;
+    return MOE_OK;
+}
+
+int moe_reserve(moe_handle_t h, int max_tokens)
+{
+    if (!h || max_tokens < 1)
+        return MOE_ERR_INVALID_ARG;
+    if (h->reserved && h->ws.max_tokens >= max_tokens)
+        return MOE_OK;
+    CK(cudaSetDevice(h->dev));
+    if (sync_last(h) != MOE_OK)
+        return MOE_ERR_CUDA;
+    const Dims &d = h->d;
+    if (!h->small_mem) {
+        Carver c{nullptr};
+        Workspace &ws = h->ws;
+        auto carve_small = [&](char *base) {
+            c = Carver{base};
+            ws.hdr = c.take<uint32_t>(HDR_WORDS);
+            ws.send = c.take<unsigned long long>(static_cast<size_t>(d.R) * d.E);
+            ws.counts = c.take<uint32_t>(d.E);
+            ws.recv = c.take<uint32_t>(static_cast<size_t>(d.E) * d.R);
+            ws.blk_off = c.take<int32_t>(d.E + 1);
+            ws.cum_rows = c.take<unsigned long long>(d.E);
+            return align_up(c.off, 256);
+        };
+        const size_t bytes = carve_small(nullptr);
+        CK(cudaMalloc(&h->small_mem, bytes));
+        carve_small(static_cast<char *>(h->small_mem));
+        h->small_bytes = bytes;
+        CK(cudaMemset(h->small_mem, 0, bytes));
+    }
+    free_big(h);
+    Workspace ws = h->ws;
+    const size_t bytes = carve_big(h, nullptr, max_tokens, ws);
+    if (cudaMalloc(&h->big_mem, bytes) != cudaSuccess) {
+        h->big_mem = nullptr;
+        return MOE_ERR_CUDA;
+    }
+    carve_big(h, static_cast<char *>(h->big_mem), max_tokens, ws);
+    h->ws = ws;
+    h->big_bytes = bytes;
+    CK(cudaMemset(ws.arrive, 0, sizeof(uint32_t) * ws.max_blocks));
+    CK(cudaMemset(ws.pool_sf, 0, sizeof(float) * static_cast<size_t>(ws.P) * (d.H / 128)));
+    CK(cudaMemset(ws.act_sf, 0, sizeof(float) * static_cast<size_t>(ws.P) * (d.I / 128)));
+    CK(cudaMemset(ws.pool_x, 0, static_cast<size_t>(ws.P) * d.H));
+    CK(cudaMemset(ws.act, 0, static_cast<size_t>(ws.P) * d.I));
+    if (encode_tile_map(&h->tm_pool, ws.pool_x, ws.P, d.H, BM) != MOE_OK ||
+        encode_tile_map(&h->tm_act, ws.act, ws.P, d.I, BM) != MOE_OK)
+        return MOE_ERR_CUDA;
+    CK(cudaDeviceSynchronize());
+    h->reserved = true;
+    return MOE_OK;
+}
+
+int moe_load_weights(moe_handle_t h, const uint8_t *w_gate_up, const float *sf_gate_up,
+                     const uint8_t *w_down, const float *sf_down, void *stream)
+{
+    if (!h || !w_gate_up || !sf_gate_up || !w_down || !sf_down)
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned(w_gate_up, 16) || !aligned(w_down, 16) || !aligned(sf_gate_up, 4) || !aligned(sf_down, 4))
+        return MOE_ERR_INVALID_ARG;
+    CK(cudaSetDevice(h->dev));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const Dims &d = h->d;
+    const size_t n1 = static_cast<size_t>(d.E) * 2 * d.I * d.H;
+    const size_t ns1 = static_cast<size_t>(d.E) * (2 * d.I / 128) * (d.H / 128);
+    const size_t n2 = static_cast<size_t>(d.E) * d.H * d.I;
+    const size_t ns2 = static_cast<size_t>(d.E) * (d.H / 128) * (d.I / 128);
+    if (!h->w_mem) {
+        Carver c{nullptr};
+        auto carve = [&](char *base) {
+            c = Carver{base};
+            h->w1 = c.take<uint8_t>(n1);
+            h->s1 = c.take<float>(ns1);
+            h->w2 = c.take<uint8_t>(n2);
+            h->s2 = c.take<float>(ns2);
+            return align_up(c.off, 256);
+        };
+        const size_t bytes = carve(nullptr);
+        CK(cudaMalloc(&h->w_mem, bytes));
+        carve(static_cast<char *>(h->w_mem));
+        h->w_bytes = bytes;
+    }
+    if (launch_interleave_gate_up(w_gate_up, h->w1, d.E, d.I, d.H, s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    CK(cudaMemcpyAsync(h->s1, sf_gate_up, ns1 * sizeof(float), cudaMemcpyDeviceToDevice, s));
+    CK(cudaMemcpyAsync(h->w2, w_down, n2, cudaMemcpyDeviceToDevice, s));
+    CK(cudaMemcpyAsync(h->s2, sf_down, ns2 * sizeof(float), cudaMemcpyDeviceToDevice, s));
+    if (encode_tile_map(&h->tm_w1, h->w1, static_cast<uint64_t>(d.E) * 2 * d.I, d.H, BN) != MOE_OK ||
+        encode_tile_map(&h->tm_w2, h->w2, static_cast<uint64_t>(d.E) * d.H, d.I, BN) != MOE_OK)
+        return MOE_ERR_CUDA;
+    h->have_weights = true;
+    h->last_stream = s;
+    h->have_last = true;
+    return MOE_OK;
+}
+
+int moe_forward(moe_handle_t h, int T, const uint8_t *x, const float *x_sf, const int64_t *topk_idx,
+                const float *topk_w, uint16_t *out, void *stream)
+{
+    if (!h || T < 0)
+        return MOE_ERR_INVALID_ARG;
+    if (!h->reserved)
+        return MOE_ERR_NOT_RESERVED;
+    if (!h->have_weights)
+        return MOE_ERR_NO_WEIGHTS;
+    if (T > h->ws.max_tokens)
+        return MOE_ERR_CAPACITY;
+    if (T % h->d.R != 0)
+        return MOE_ERR_INVALID_ARG;
+    if (T == 0)
+        return MOE_OK;
+    if (!x || !x_sf || !topk_idx || !topk_w || !out)
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(out, 16) || !aligned(x_sf, 4) || !aligned(topk_idx, 8) ||
+        !aligned(topk_w, 4))
+        return MOE_ERR_INVALID_ARG;
+    CK(cudaSetDevice(h->dev));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    CallArgs c{T, x, x_sf, topk_idx, topk_w, out, h->timeout_ns, h->debug_skip_barrier};
+    if (launch_dispatch(h->d, h->ws, c, h->num_sms, s) != cudaSuccess ||
+        launch_gemm_gate_up(h->tm_pool, h->tm_w1, h->d, h->ws, c, h->s1, h->num_sms, s) != cudaSuccess ||
+        launch_gemm_down(h->tm_act, h->tm_w2, h->d, h->ws, c, h->s2, h->num_sms, s) != cudaSuccess ||
+        launch_combine(h->d, h->ws, c, h->num_sms, s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    h->last_stream = s;
+    h->have_last = true;
+    h->last_T = T;
+    return MOE_OK;
+}
+
+int moe_forward_host(moe_handle_t h, int T, const uint8_t *host_x, const float *host_x_sf,
+                     const int64_t *host_topk_idx, const float *host_topk_w, uint16_t *host_out,
+                     void *stream)
+{
+    if (!h || T < 0)
+        return MOE_ERR_INVALID_ARG;
+    if (!h->reserved)
+        return MOE_ERR_NOT_RESERVED;
+    if (T > h->ws.max_tokens)
+        return MOE_ERR_CAPACITY;
+    if (T == 0)
+        return MOE_OK;
+    if (!host_x || !host_x_sf || !host_topk_idx || !host_topk_w || !host_out)
+        return MOE_ERR_INVALID_ARG;
+    CK(cudaSetDevice(h->dev));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const Dims &d = h->d;
+    CK(cudaMemcpyAsync(h->st_x, host_x, static_cast<size_t>(T) * d.H, cudaMemcpyHostToDevice, s));
+    CK(cudaMemcpyAsync(h->st_sf, host_x_sf, sizeof(float) * T * (d.H / 128), cudaMemcpyHostToDevice, s));
+    CK(cudaMemcpyAsync(h->st_idx, host_topk_idx, sizeof(int64_t) * T * d.K, cudaMemcpyHostToDevice, s));
+    CK(cudaMemcpyAsync(h->st_w, host_topk_w, sizeof(float) * T * d.K, cudaMemcpyHostToDevice, s));
+    int rc = moe_forward(h, T, h->st_x, h->st_sf, h->st_idx, h->st_w, h->st_out, stream);
+    if (rc != MOE_OK)
+        return rc;
+    CK(cudaMemcpyAsync(host_out, h->st_out, sizeof(uint16_t) * T * d.H, cudaMemcpyDeviceToHost, s));
+    CK(cudaStreamSynchronize(s));
+    return MOE_OK;
+}
+
+int moe_get_error(moe_handle_t h, int *device_status)
+{
+    if (!h || !device_status)
+        return MOE_ERR_INVALID_ARG;
+    *device_status = MOE_OK;
+    if (!h->small_mem)
+        return MOE_OK;
+    CK(cudaSetDevice(h->dev));
+    if (sync_last(h) != MOE_OK)
+        return MOE_ERR_CUDA;
+    uint32_t hdr[HDR_WORDS];
+    CK(cudaMemcpy(hdr, h->ws.hdr, sizeof(hdr), cudaMemcpyDeviceToHost));
+    const uint32_t st = hdr[HDR_ERR_STICKY] ? hdr[HDR_ERR_STICKY] : hdr[HDR_ERR_CALL];
+    if (st != 0) {
+        CK(cudaMemset(h->ws.hdr, 0, sizeof(uint32_t) * HDR_WORDS));
+        CK(cudaMemset(h->ws.send, 0, sizeof(unsigned long long) * h->d.R * h->d.E));
+        if (h->reserved)
+            CK(cudaMemset(h->ws.arrive, 0, sizeof(uint32_t) * h->ws.max_blocks));
+        CK(cudaDeviceSynchronize());
+    }
+    *device_status = static_cast<int>(st);
+    return MOE_OK;
+}
+
+int moe_debug_routing(moe_handle_t h, uint32_t *counts, uint32_t *recv, int32_t *block_offset,
+                      uint32_t *meta, int *P, int *block_m)
+{
+    if (!h)
+        return MOE_ERR_INVALID_ARG;
+    if (!h->reserved)
+        return MOE_ERR_NOT_RESERVED;
+    CK(cudaSetDevice(h->dev));
+    if (sync_last(h) != MOE_OK)
+        return MOE_ERR_CUDA;
+    const Dims &d = h->d;
+    int32_t off_last = 0;
+    CK(cudaMemcpy(&off_last, h->ws.blk_off + d.E, sizeof(int32_t), cudaMemcpyDeviceToHost));
+    if (off_last < 0 || off_last > h->ws.max_blocks)
+        return MOE_ERR_CUDA;
+    if (counts)
+        CK(cudaMemcpy(counts, h->ws.counts, sizeof(uint32_t) * d.E, cudaMemcpyDeviceToHost));
+    if (recv)
+        CK(cudaMemcpy(recv, h->ws.recv, sizeof(uint32_t) * d.E * d.R, cudaMemcpyDeviceToHost));
+    if (block_offset)
+        CK(cudaMemcpy(block_offset, h->ws.blk_off, sizeof(int32_t) * (d.E + 1), cudaMemcpyDeviceToHost));
+    if (meta && off_last > 0)
+        CK(cudaMemcpy(meta, h->ws.meta, sizeof(uint32_t) * 3 * static_cast<size_t>(off_last) * BM,
+                      cudaMemcpyDeviceToHost));
+    if (P)
+        *P = off_last * BM;
+    if (block_m)
+        *block_m = BM;
+    return MOE_OK;
+}
+
+int moe_cumulative_expert_rows(moe_handle_t h, uint64_t *rows)
+{
+    if (!h || !rows)
+        return MOE_ERR_INVALID_ARG;
+    if (!h->small_mem) {
+        std::memset(rows, 0, sizeof(uint64_t) * h->d.E);
+        return MOE_OK;
+    }
+    CK(cudaSetDevice(h->dev));
+    if (sync_last(h) != MOE_OK)
+        return MOE_ERR_CUDA;
+    CK(cudaMemcpy(rows, h->ws.cum_rows, sizeof(uint64_t) * h->d.E, cudaMemcpyDeviceToHost));
+    return MOE_OK;
+}
+
+int moe_debug_buffer(moe_handle_t h, int which, void *host_dst, uint64_t bytes)
+{
+    if (!h || !host_dst)
+        return MOE_ERR_INVALID_ARG;
+    if (!h->reserved)
+        return MOE_ERR_NOT_RESERVED;
+    const Dims &d = h->d;
+    const Workspace &ws = h->ws;
+    const void *src = nullptr;
+    uint64_t need = 0;
+    switch (which) {
+    case MOE_BUF_POOL_X: src = ws.pool_x; need = static_cast<uint64_t>(ws.P) * d.H; break;
+    case MOE_BUF_POOL_SF: src = ws.pool_sf; need = 4ull * ws.P * (d.H / 128); break;
+    case MOE_BUF_ACT: src = ws.act; need = static_cast<uint64_t>(ws.P) * d.I; break;
+    case MOE_BUF_ACT_SF: src = ws.act_sf; need = 4ull * ws.P * (d.I / 128); break;
+    case MOE_BUF_COMBINE: src = ws.combine; need = 2ull * d.K * ws.max_tokens * d.H; break;
+    case MOE_BUF_TABLE: src = ws.table; need = 4ull * d.E * d.R * ws.tsrc_cap; break;
+    default: return MOE_ERR_INVALID_ARG;
+    }
+    if (bytes != need)
+        return MOE_ERR_INVALID_ARG;
+    CK(cudaSetDevice(h->dev));
+    if (sync_last(h) != MOE_OK)
+        return MOE_ERR_CUDA;
+    CK(cudaMemcpy(host_dst, src, bytes, cudaMemcpyDeviceToHost));
+    return MOE_OK;
+}
+
+int moe_get_info(moe_handle_t h, moe_info *info)
+{
+    if (!h || !info)
+        return MOE_ERR_INVALID_ARG;
+    info->E = h->d.E;
+    info->H = h->d.H;
+    info->I = h->d.I;
+    info->topk = h->d.K;
+    info->R = h->d.R;
+    info->max_tokens = h->reserved ? h->ws.max_tokens : 0;
+    info->pool_rows = h->reserved ? h->ws.P : 0;
+    info->block_m = BM;
+    info->block_n = BN;
+    info->num_sms = h->num_sms;
+    info->workspace_bytes = h->small_bytes + h->big_bytes;
+    info->weight_bytes = h->w_bytes;
+    return MOE_OK;
+}
+
+int moe_set_option(moe_handle_t h, int option, int64_t value)
+{
+    if (!h)
+        return MOE_ERR_INVALID_ARG;
+    switch (option) {
+    case MOE_OPT_TIMEOUT_NS:
+        if (value < 1000000 || value > 600000000000LL)
+            return MOE_ERR_INVALID_ARG;
+        h->timeout_ns = value;
+        return MOE_OK;
+    case MOE_OPT_DEBUG_SKIP_BARRIER:
+        h->debug_skip_barrier = value != 0;
+        return MOE_OK;
+    default:
+        return MOE_ERR_INVALID_ARG;
+    }
+}
+
+int moe_destroy(moe_handle_t h)
+{
+    if (!h)
+        return MOE_ERR_INVALID_ARG;
+    cudaSetDevice(h->dev);
+    sync_last(h);
+    free_big(h);
+    if (h->small_mem)
+        cudaFree(h->small_mem);
+    if (h->w_mem)
+        cudaFree(h->w_mem);
+    delete h;
+    return MOE_OK;
+}
+
+}  // extern "C"

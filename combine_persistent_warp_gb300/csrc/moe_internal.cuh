@@ -1,0 +1,94 @@
+// moe_internal.cuh -- workspace layout, kernel argument blocks and launchers shared by
+// the translation units of the CUDA library (not part of the public C ABI).
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace cpw {
+
+constexpr int BM = 128;            // pool rows per M-block = UMMA M = TMEM lanes
+constexpr int BN = 256;            // GEMM tile columns (UMMA N)
+constexpr int BK = 128;            // K per pipeline stage = one fp32 scale block
+constexpr int STAGES = 4;          // TMA -> UMMA shared-memory ring depth
+constexpr int GEMM_THREADS = 384;  // 4 producer/issuer warps + 2 epilogue warpgroups
+constexpr int DISPATCH_THREADS = 512;
+constexpr int COMBINE_THREADS = 256;
+
+constexpr int STAGE_A_BYTES = BM * BK;                 // 16 KB
+constexpr int STAGE_B_BYTES = BN * BK;                 // 32 KB
+constexpr int STAGE_BYTES = STAGE_A_BYTES + STAGE_B_BYTES;
+constexpr int GEMM_SMEM_BYTES = 1024 /*align slack*/ + STAGES * STAGE_BYTES + 4096 /*bars etc*/;
+
+// 32-bit words of the workspace header; hot words sit on separate 128-byte lines.
+enum HdrWord : int {
+    HDR_GRID_SYNC = 0,     // XOR-tag grid barrier counter of the routing kernel
+    HDR_ERR_CALL = 32,     // first device error of the forward in flight
+    HDR_ERR_STICKY = 64,   // errors of finished forwards, until moe_get_error
+    HDR_WORDS = 128
+};
+
+// Device workspace of one handle.  Sizes: P = pool row capacity, MB = P / BM.
+struct Workspace {
+    uint32_t *hdr;                 // [HDR_WORDS]
+    unsigned long long *send;      // [R][E] packed (arrivals << 32 | rows)
+    uint32_t *counts;              // [E] rows per expert (last forward)
+    uint32_t *recv;                // [E][R] rows per (expert, source)
+    int32_t *blk_off;              // [E+1] first M-block of each expert
+    int32_t *block_expert;         // [MB] expert of each M-block
+    int32_t *block_rows;           // [MB] valid rows of each M-block
+    unsigned long long *cum_rows;  // [E] rows per expert over all forwards
+    int32_t *table;                // [E][R][tsrc_cap] token_in_source * topk + k
+    uint8_t *pool_x;               // [P][H]   e4m3 gathered activations
+    float *pool_sf;                // [H/128][P]
+    uint32_t *meta;                // [P][3]   {source, token, topk slot}
+    uint8_t *act;                  // [P][I]   e4m3 SwiGLU output
+    float *act_sf;                 // [I/128][P]
+    uint16_t *combine;             // [topk][max_tokens][H] bf16 weighted expert outputs
+    uint32_t *arrive;              // [MB] rows gathered per M-block
+    int tsrc_cap;                  // max_tokens / R
+    int P;                         // pool rows
+    int max_blocks;                // P / BM
+    int max_tokens;
+};
+
+struct Dims {
+    int E, H, I, K, R;   // K = topk
+};
+
+struct CallArgs {
+    int T;
+    const uint8_t *x;
+    const float *x_sf;
+    const int64_t *idx;
+    const float *w;
+    uint16_t *out;
+    long long timeout_ns;
+    int debug_skip_barrier;
+};
+
+// Device error codes (same values as the public moe_status).
+enum DevErr : uint32_t { DEV_BAD_INDEX = 6, DEV_TIMEOUT = 7, DEV_SLOT_OVERFLOW = 8 };
+
+__device__ __forceinline__ void record_error(uint32_t *hdr, uint32_t code)
+{
+    atomicCAS(hdr + HDR_ERR_CALL, 0u, code);
+}
+
+// Launchers (one per translation unit).
+size_t dispatch_smem_bytes(const Dims &d);
+cudaError_t launch_dispatch(const Dims &d, const Workspace &ws, const CallArgs &c, int num_sms,
+                            cudaStream_t s);
+cudaError_t launch_gemm_gate_up(const CUtensorMap &tm_a, const CUtensorMap &tm_b, const Dims &d,
+                                const Workspace &ws, const CallArgs &c, const float *sf_w,
+                                int num_sms, cudaStream_t s);
+cudaError_t launch_gemm_down(const CUtensorMap &tm_a, const CUtensorMap &tm_b, const Dims &d,
+                             const Workspace &ws, const CallArgs &c, const float *sf_w,
+                             int num_sms, cudaStream_t s);
+cudaError_t launch_combine(const Dims &d, const Workspace &ws, const CallArgs &c, int num_sms,
+                           cudaStream_t s);
+cudaError_t launch_interleave_gate_up(const uint8_t *src, uint8_t *dst, int E, int I, int H,
+                                      cudaStream_t s);
+
+}  // namespace cpw

@@ -1,0 +1,237 @@
+"""ctypes binding of the C ABI in include/cpw_moe.h (argument marshalling only).
+
+Every step of the layer runs in the CUDA library ``libcpw_moe.so``; this module only
+checks tensor shapes/dtypes, passes ``data_ptr()`` values and the CUDA stream handle,
+and turns status codes into exceptions.  There is no fallback: if the library is
+missing or cannot be loaded, importing the layer fails loudly.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(PKG)
+HEADER = os.path.join(ROOT, "include", "cpw_moe.h")
+LIB_PATH = os.path.join(PKG, "libcpw_moe.so")
+
+MOE_OK = 0
+STATUS = {
+    0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_CUDA", 3: "MOE_ERR_CAPACITY",
+    4: "MOE_ERR_NO_WEIGHTS", 5: "MOE_ERR_UNSUPPORTED_DEVICE", 6: "MOE_ERR_BAD_INDEX",
+    7: "MOE_ERR_TIMEOUT", 8: "MOE_ERR_SLOT_OVERFLOW", 9: "MOE_ERR_NOT_RESERVED",
+}
+BUFFERS = {"pool_x": 0, "pool_sf": 1, "act": 2, "act_sf": 3, "combine": 4, "table": 5}
+OPT_TIMEOUT_NS = 0
+OPT_DEBUG_SKIP_BARRIER = 1
+
+
+class MoeError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {STATUS.get(code, code)}")
+        self.code = code
+
+
+class MoeInfo(ctypes.Structure):
+    _fields_ = [("E", ctypes.c_int), ("H", ctypes.c_int), ("I", ctypes.c_int),
+                ("topk", ctypes.c_int), ("R", ctypes.c_int), ("max_tokens", ctypes.c_int),
+                ("pool_rows", ctypes.c_int), ("block_m", ctypes.c_int), ("block_n", ctypes.c_int),
+                ("num_sms", ctypes.c_int), ("workspace_bytes", ctypes.c_uint64),
+                ("weight_bytes", ctypes.c_uint64)]
+
+
+def header_functions() -> list[str]:
+    """Names of the functions declared in include/cpw_moe.h."""
+    text = open(HEADER, encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z_]+)\s*\(", text)))
+
+
+_lib = None
+
+
+def load(build_if_missing: bool = True) -> ctypes.CDLL:
+    global _lib
+    if _lib is not None:
+        return _lib
+    if build_if_missing:
+        from . import build as _build
+        _build.build()
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"CUDA library {LIB_PATH} is not built (run __graft_entry__.build())")
+    L = ctypes.CDLL(LIB_PATH)
+    P, I, I64, U64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_uint64
+    H = ctypes.c_void_p
+    sig = {
+        "moe_create": [I, I, I, I, I, ctypes.POINTER(H)],
+        "moe_reserve": [H, I],
+        "moe_load_weights": [H, P, P, P, P, P],
+        "moe_forward": [H, I, P, P, P, P, P, P],
+        "moe_forward_host": [H, I, P, P, P, P, P, P],
+        "moe_get_error": [H, ctypes.POINTER(I)],
+        "moe_debug_routing": [H, P, P, P, P, ctypes.POINTER(I), ctypes.POINTER(I)],
+        "moe_cumulative_expert_rows": [H, P],
+        "moe_debug_buffer": [H, I, P, U64],
+        "moe_get_info": [H, ctypes.POINTER(MoeInfo)],
+        "moe_set_option": [H, I, I64],
+        "moe_destroy": [H],
+    }
+    for name, args in sig.items():
+        fn = getattr(L, name)
+        fn.argtypes = args
+        fn.restype = ctypes.c_int
+    L.moe_status_string.argtypes = [ctypes.c_int]
+    L.moe_status_string.restype = ctypes.c_char_p
+    _lib = L
+    return L
+
+
+def _check(code: int, what: str):
+    if code != MOE_OK:
+        raise MoeError(code, what)
+
+
+def _stream_handle(stream) -> int:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream)
+
+
+class FusedMoE:
+    """The fused FP8 MoE layer on the current CUDA device (one handle of the C ABI)."""
+
+    def __init__(self, E: int, H: int, I: int, topk: int, R: int):
+        self.lib = load()
+        self.E, self.H, self.I, self.topk, self.R = E, H, I, topk, R
+        h = ctypes.c_void_p()
+        _check(self.lib.moe_create(E, H, I, topk, R, ctypes.byref(h)), "moe_create")
+        self.h = h
+        self.max_tokens = 0
+
+    # -------------------------------------------------------------- set-up ------
+    def reserve(self, max_tokens: int):
+        _check(self.lib.moe_reserve(self.h, max_tokens), "moe_reserve")
+        self.max_tokens = max(self.max_tokens, max_tokens)
+        return self
+
+    def load_weights(self, w_gate_up, sf_gate_up, w_down, sf_down, stream=None):
+        import torch
+        E, H, I = self.E, self.H, self.I
+        _expect(w_gate_up, (E, 2 * I, H), torch.uint8, "w_gate_up")
+        _expect(sf_gate_up, (E, 2 * I // 128, H // 128), torch.float32, "sf_gate_up")
+        _expect(w_down, (E, H, I), torch.uint8, "w_down")
+        _expect(sf_down, (E, H // 128, I // 128), torch.float32, "sf_down")
+        _check(self.lib.moe_load_weights(self.h, w_gate_up.data_ptr(), sf_gate_up.data_ptr(),
+                                         w_down.data_ptr(), sf_down.data_ptr(),
+                                         _stream_handle(stream)), "moe_load_weights")
+        return self
+
+    def set_option(self, option: int, value: int):
+        _check(self.lib.moe_set_option(self.h, option, value), "moe_set_option")
+
+    # -------------------------------------------------------------- forward -----
+    def forward(self, x, x_sf, topk_idx, topk_w, out=None, stream=None):
+        import torch
+        T = x.shape[0]
+        self._check_inputs(x, x_sf, topk_idx, topk_w, T, cuda=True)
+        if out is None:
+            out = torch.empty(T, self.H, dtype=torch.bfloat16, device=x.device)
+        _expect(out, (T, self.H), torch.bfloat16, "out", cuda=True)
+        _check(self.lib.moe_forward(self.h, T, x.data_ptr(), x_sf.data_ptr(), topk_idx.data_ptr(),
+                                    topk_w.data_ptr(), out.data_ptr(), _stream_handle(stream)),
+               "moe_forward")
+        return out
+
+    def forward_host(self, x, x_sf, topk_idx, topk_w, out=None, stream=None):
+        """Same layer from host (ideally pinned) CPU tensors; returns when done."""
+        import torch
+        T = x.shape[0]
+        self._check_inputs(x, x_sf, topk_idx, topk_w, T, cuda=False)
+        if out is None:
+            out = torch.empty(T, self.H, dtype=torch.bfloat16, pin_memory=True)
+        _expect(out, (T, self.H), torch.bfloat16, "out", cuda=False)
+        _check(self.lib.moe_forward_host(self.h, T, x.data_ptr(), x_sf.data_ptr(),
+                                         topk_idx.data_ptr(), topk_w.data_ptr(), out.data_ptr(),
+                                         _stream_handle(stream)), "moe_forward_host")
+        return out
+
+    def _check_inputs(self, x, x_sf, topk_idx, topk_w, T, cuda):
+        import torch
+        _expect(x, (T, self.H), torch.uint8, "x", cuda=cuda)
+        _expect(x_sf, (T, self.H // 128), torch.float32, "x_sf", cuda=cuda)
+        _expect(topk_idx, (T, self.topk), torch.int64, "topk_idx", cuda=cuda)
+        _expect(topk_w, (T, self.topk), torch.float32, "topk_w", cuda=cuda)
+
+    # -------------------------------------------------------------- inspection --
+    def get_error(self) -> int:
+        st = ctypes.c_int(0)
+        _check(self.lib.moe_get_error(self.h, ctypes.byref(st)), "moe_get_error")
+        return st.value
+
+    def info(self) -> MoeInfo:
+        inf = MoeInfo()
+        _check(self.lib.moe_get_info(self.h, ctypes.byref(inf)), "moe_get_info")
+        return inf
+
+    def debug_routing(self, T: int) -> dict:
+        import numpy as np
+        E, R = self.E, self.R
+        inf = self.info()
+        counts = np.zeros(E, np.uint32)
+        recv = np.zeros((E, R), np.uint32)
+        off = np.zeros(E + 1, np.int32)
+        rows_cap = (-(-T * self.topk // inf.block_m) + E) * inf.block_m
+        meta = np.zeros((max(rows_cap, 1), 3), np.uint32)
+        P = ctypes.c_int(0)
+        bm = ctypes.c_int(0)
+        _check(self.lib.moe_debug_routing(self.h, counts.ctypes.data, recv.ctypes.data,
+                                          off.ctypes.data, meta.ctypes.data, ctypes.byref(P),
+                                          ctypes.byref(bm)), "moe_debug_routing")
+        return {"counts": counts, "recv": recv, "block_offset": off, "meta": meta[:P.value],
+                "P": P.value, "block_m": bm.value}
+
+    def cumulative_expert_rows(self):
+        import numpy as np
+        rows = np.zeros(self.E, np.uint64)
+        _check(self.lib.moe_cumulative_expert_rows(self.h, rows.ctypes.data), "moe_cumulative_expert_rows")
+        return rows
+
+    def debug_buffer(self, which: str):
+        import numpy as np
+        inf = self.info()
+        P, H, I, K = inf.pool_rows, self.H, self.I, self.topk
+        shapes = {
+            "pool_x": ((P, H), np.uint8), "pool_sf": ((H // 128, P), np.float32),
+            "act": ((P, I), np.uint8), "act_sf": ((I // 128, P), np.float32),
+            "combine": ((K, inf.max_tokens, H), np.uint16),
+            "table": ((self.E, self.R, max(1, inf.max_tokens // self.R)), np.int32),
+        }
+        shape, dt = shapes[which]
+        a = np.zeros(shape, dt)
+        _check(self.lib.moe_debug_buffer(self.h, BUFFERS[which], a.ctypes.data, a.nbytes),
+               "moe_debug_buffer")
+        return a
+
+    def close(self):
+        if getattr(self, "h", None) is not None and self.h.value:
+            self.lib.moe_destroy(self.h)
+            self.h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def _expect(t, shape, dtype, name, cuda=None):
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: shape {tuple(t.shape)} != {tuple(shape)}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: dtype {t.dtype} != {dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if cuda is not None and t.is_cuda != cuda:
+        raise ValueError(f"{name} must be a {'CUDA' if cuda else 'host'} tensor")

@@ -1,0 +1,158 @@
+/*
+ * cpw_moe.h -- C ABI of the fused FP8 Mixture-of-Experts layer ("Mega-MoE") on one GPU.
+ *
+ * One call of moe_forward computes, for every token t,
+ *     out[t] = bf16( sum_k  w[t,k] * Expert_{idx[t,k]}(x[t]) ),   idx == -1 skipped,
+ * where Expert_e(x) = W_down[e] . requant_1x128( silu(W_gate[e] . x) * (W_up[e] . x) )
+ * with FP8 e4m3 operands and fp32 block scales.  The steps follow the fused layer of the
+ * source pages, on one GPU whose tokens are split into R logical source partitions:
+ *   routing count + packed 64-bit slot claim      ("Mega-MoE 内核代码导读：从 Dispatch 到
+ *                                                   WGMMA 的融合流水线" §4.1-4.2)
+ *   [expert][source][slot] index table            (same page §4.3; Mega-MoE walkthrough,
+ *                                                   part 2, kwkr.cn/news/1317662, §1.1)
+ *   expert segments + round-robin min-peeling      (walkthrough part 2 §2.4-2.5)
+ *   gather into the expert-major FP8 pool          (walkthrough part 2 §2.6)
+ *   grouped FP8 GEMMs gate_up -> SwiGLU -> down    (first page §六, §八)
+ *   weighted scatter through {source,token,topk}   ("DeepGEMM Mega MoE 对称内存（Symmetric
+ *   metadata + top-k combine reduce                 Memory）深度分析" §8-§9)
+ *   Output(T) = sum_k w_k Expert_k(T)              ("Dispatch/Combine: 博客理论 ↔ DeepEP 源码
+ *                                                   ↔ DeepGEMM Mega MoE 三方对比分析" §1)
+ *
+ * Conventions for every call below:
+ *   - All tensor pointers are DEVICE pointers unless the name says host; they are
+ *     row-major, contiguous, and owned by the caller.  FP8 tensors are e4m3 bytes
+ *     (OCP FP8 E4M3, largest finite 448).  FP8 row pointers must be 16-byte aligned.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *   - Every function returns a moe_status code.  Host-detectable problems are returned
+ *     synchronously; problems found by the GPU (bad expert id, slot overflow, a wait
+ *     that ran past its time limit) are recorded in a sticky per-handle word that
+ *     moe_get_error returns; while it is set, forwards skip their work and `out` is
+ *     undefined.
+ *   - A handle serves one forward at a time: its workspace is shared by its calls.
+ */
+#ifndef CPW_MOE_H
+#define CPW_MOE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct moe_ctx *moe_handle_t;
+
+enum moe_status {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,        /* bad size, null or misaligned pointer            */
+    MOE_ERR_CUDA = 2,               /* a CUDA runtime/driver call failed               */
+    MOE_ERR_CAPACITY = 3,           /* T above the reserved maximum                    */
+    MOE_ERR_NO_WEIGHTS = 4,         /* forward before moe_load_weights                 */
+    MOE_ERR_UNSUPPORTED_DEVICE = 5, /* not an sm_103 GPU, or a shape this build lacks  */
+    MOE_ERR_BAD_INDEX = 6,          /* device: an expert id outside [0,E) other than -1 */
+    MOE_ERR_TIMEOUT = 7,            /* device: a bounded wait gave up                  */
+    MOE_ERR_SLOT_OVERFLOW = 8,      /* device: > T/R rows of one source for one expert */
+    MOE_ERR_NOT_RESERVED = 9        /* forward before moe_reserve                      */
+};
+
+/* Create a layer for E experts, hidden size H, expert intermediate size I, top-k, and R
+ * logical source partitions.  Requires H % 256 == 0, I % 128 == 0, 1 <= topk <= 32,
+ * topk <= E <= 1024, 1 <= R <= 64, E*R <= 16384, on the current device, which must be
+ * sm_103.  Allocates no device memory.  *out receives the handle. */
+int moe_create(int E, int H, int I, int topk, int R, moe_handle_t *out);
+
+/* Allocate the device workspace for up to max_tokens tokens per forward (the pages'
+ * host pre-sizing: a larger batch is an error, not a reallocation).  May be called
+ * again to grow; not while a forward is in flight. */
+int moe_reserve(moe_handle_t h, int max_tokens);
+
+/* Copy the expert weights into the handle (re-laid-out for the GEMMs; the caller keeps
+ * ownership of its buffers, which may be freed after the stream has run the copies).
+ *   w_gate_up  [E][2I][H] e4m3, rows 0..I-1 = gate, rows I..2I-1 = up
+ *   sf_gate_up [E][2I/128][H/128] fp32, one scale per 128x128 block
+ *   w_down     [E][H][I] e4m3
+ *   sf_down    [E][H/128][I/128] fp32
+ * The gate/up rows are interleaved in groups of 8 inside the handle
+ * ("DeepGEMM Mega MoE 对称内存（Symmetric Memory）深度分析" §10.2). */
+int moe_load_weights(moe_handle_t h, const uint8_t *w_gate_up, const float *sf_gate_up,
+                     const uint8_t *w_down, const float *sf_down, void *stream);
+
+/* The layer on T tokens (0 <= T <= max_tokens, T % R == 0; source r owns tokens
+ * [r*T/R, (r+1)*T/R)).  Asynchronous on `stream`.
+ *   x        [T][H] e4m3            x_sf [T][H/128] fp32 (1x128 activation scales)
+ *   topk_idx [T][topk] int64, -1 = skip this slot
+ *   topk_w   [T][topk] fp32 gate weights
+ *   out      [T][H] bf16 bits, fully written (a token with no valid slot gets 0). */
+int moe_forward(moe_handle_t h, int T, const uint8_t *x, const float *x_sf,
+                const int64_t *topk_idx, const float *topk_w, uint16_t *out, void *stream);
+
+/* moe_forward from HOST buffers (same shapes as above): copies the inputs to the
+ * handle's device staging buffers, runs the layer and copies `host_out` back, all on
+ * `stream`, and returns after the stream has finished.  Host buffers should be pinned
+ * for the copies to be asynchronous with respect to other host work. */
+int moe_forward_host(moe_handle_t h, int T, const uint8_t *host_x, const float *host_x_sf,
+                     const int64_t *host_topk_idx, const float *host_topk_w,
+                     uint16_t *host_out, void *stream);
+
+/* Wait for the handle's last stream, then return (and clear) the sticky device status in
+ * *device_status (a moe_status value; MOE_OK if none).  Clearing also resets the
+ * workspace counters so the next forward starts clean. */
+int moe_get_error(moe_handle_t h, int *device_status);
+
+/* Routing results of the last forward (host copies, after syncing its stream):
+ *   counts [E] rows per expert, recv [E][R] rows per (expert, source),
+ *   block_offset [E+1] first M-block of each expert in the pool (last = total blocks),
+ *   meta [P][3] {source, token, topk slot} of every pool row (rows past an expert's
+ *   count hold padding), *P = pool rows used = block_offset[E] * block_m,
+ *   *block_m = rows per M-block.  Any output pointer may be NULL.  meta needs room for
+ *   the pool rows of the last forward: (ceil(T*topk/block_m) + E) * block_m rows. */
+int moe_debug_routing(moe_handle_t h, uint32_t *counts, uint32_t *recv, int32_t *block_offset,
+                      uint32_t *meta, int *P, int *block_m);
+
+/* Per-expert routed rows accumulated over every forward since the handle was created
+ * (host copy, [E]). */
+int moe_cumulative_expert_rows(moe_handle_t h, uint64_t *rows);
+
+/* Host copy of an intermediate buffer of the last forward (for stage-by-stage tests):
+ *   MOE_BUF_POOL_X   [P][H] e4m3 gathered rows      MOE_BUF_POOL_SF [H/128][P] fp32
+ *   MOE_BUF_ACT      [P][I] e4m3 SwiGLU output      MOE_BUF_ACT_SF  [I/128][P] fp32
+ *   MOE_BUF_COMBINE  [topk][T][H] bf16 weighted expert outputs
+ *   MOE_BUF_TABLE    [E][R][max_tokens/R] int32 index table (token_in_source*topk + k)
+ * where P is the reserved pool row capacity (moe_info).  `bytes` must equal the
+ * buffer's size; returns MOE_ERR_INVALID_ARG otherwise. */
+enum moe_buffer {
+    MOE_BUF_POOL_X = 0, MOE_BUF_POOL_SF = 1, MOE_BUF_ACT = 2, MOE_BUF_ACT_SF = 3,
+    MOE_BUF_COMBINE = 4, MOE_BUF_TABLE = 5
+};
+int moe_debug_buffer(moe_handle_t h, int which, void *host_dst, uint64_t bytes);
+
+/* Sizes and launch shape of the handle. */
+typedef struct moe_info {
+    int E, H, I, topk, R;
+    int max_tokens;       /* reserved tokens per forward                     */
+    int pool_rows;        /* reserved pool row capacity P                    */
+    int block_m;          /* rows per M-block (GEMM tile rows)               */
+    int block_n;          /* GEMM tile columns                               */
+    int num_sms;          /* persistent grid size                            */
+    uint64_t workspace_bytes;
+    uint64_t weight_bytes;
+} moe_info;
+int moe_get_info(moe_handle_t h, moe_info *info);
+
+/* Options.  MOE_OPT_TIMEOUT_NS: time limit of every device-side wait (default 2e9 ns);
+ * MOE_OPT_DEBUG_SKIP_BARRIER: when 1, one CTA of the routing kernel skips its arrival
+ * at the grid barrier, so the others give up after the time limit and the forward
+ * ends with MOE_ERR_TIMEOUT (failure-path test; never on in normal use). */
+enum moe_option { MOE_OPT_TIMEOUT_NS = 0, MOE_OPT_DEBUG_SKIP_BARRIER = 1 };
+int moe_set_option(moe_handle_t h, int option, int64_t value);
+
+/* Release every device buffer of the handle (after syncing its last stream). */
+int moe_destroy(moe_handle_t h);
+
+/* Static description of a status code. */
+const char *moe_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CPW_MOE_H */

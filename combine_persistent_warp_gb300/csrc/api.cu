@@ -13,6 +13,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <new>
+#include <vector>
 
 #include "../../include/cpw_moe.h"
 #include "moe_internal.cuh"
@@ -47,7 +48,13 @@ struct moe_ctx {
     int last_T = 0;
     long long timeout_ns = 2000000000LL;
     int debug_skip_barrier = 0;
+    // stage profiling (events on the forward's stream)
+    bool profile = false;
+    std::vector<cudaEvent_t> events;   // 5 per recorded forward
+    int prof_calls = 0, prof_dropped = 0;
 };
+
+static constexpr int PROF_MAX_CALLS = 8192;
 
 namespace {
 
@@ -316,10 +323,21 @@ int moe_forward(moe_handle_t h, int T, const uint8_t *x, const float *x_sf, cons
     CK(cudaSetDevice(h->dev));
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     CallArgs c{T, x, x_sf, topk_idx, topk_w, out, h->timeout_ns, h->debug_skip_barrier};
-    if (launch_dispatch(h->d, h->ws, c, h->num_sms, s) != cudaSuccess ||
+    cudaEvent_t *ev = nullptr;
+    if (h->profile) {
+        if (h->prof_calls < PROF_MAX_CALLS)
+            ev = &h->events[static_cast<size_t>(h->prof_calls++) * 5];
+        else
+            ++h->prof_dropped;
+    }
+    auto mark = [&](int i) { return ev ? cudaEventRecord(ev[i], s) : cudaSuccess; };
+    if (mark(0) != cudaSuccess || launch_dispatch(h->d, h->ws, c, h->num_sms, s) != cudaSuccess ||
+        mark(1) != cudaSuccess ||
         launch_gemm_gate_up(h->tm_pool, h->tm_w1, h->d, h->ws, c, h->s1, h->num_sms, s) != cudaSuccess ||
+        mark(2) != cudaSuccess ||
         launch_gemm_down(h->tm_act, h->tm_w2, h->d, h->ws, c, h->s2, h->num_sms, s) != cudaSuccess ||
-        launch_combine(h->d, h->ws, c, h->num_sms, s) != cudaSuccess)
+        mark(3) != cudaSuccess || launch_combine(h->d, h->ws, c, h->num_sms, s) != cudaSuccess ||
+        mark(4) != cudaSuccess)
         return MOE_ERR_CUDA;
     h->last_stream = s;
     h->have_last = true;
@@ -491,12 +509,56 @@ int moe_set_option(moe_handle_t h, int option, int64_t value)
     }
 }
 
+int moe_profile_enable(moe_handle_t h, int enable)
+{
+    if (!h)
+        return MOE_ERR_INVALID_ARG;
+    CK(cudaSetDevice(h->dev));
+    if (enable && h->events.empty()) {
+        h->events.resize(static_cast<size_t>(PROF_MAX_CALLS) * 5);
+        for (auto &e : h->events)
+            CK(cudaEventCreate(&e));
+    }
+    h->profile = enable != 0;
+    h->prof_calls = 0;
+    h->prof_dropped = 0;
+    return MOE_OK;
+}
+
+int moe_profile_read(moe_handle_t h, double *stage_ms, int *calls, int *dropped)
+{
+    if (!h || !stage_ms)
+        return MOE_ERR_INVALID_ARG;
+    CK(cudaSetDevice(h->dev));
+    if (sync_last(h) != MOE_OK)
+        return MOE_ERR_CUDA;
+    for (int j = 0; j < 4; ++j)
+        stage_ms[j] = 0.0;
+    for (int i = 0; i < h->prof_calls; ++i) {
+        for (int j = 0; j < 4; ++j) {
+            float ms = 0.0f;
+            CK(cudaEventElapsedTime(&ms, h->events[static_cast<size_t>(i) * 5 + j],
+                                    h->events[static_cast<size_t>(i) * 5 + j + 1]));
+            stage_ms[j] += ms;
+        }
+    }
+    if (calls)
+        *calls = h->prof_calls;
+    if (dropped)
+        *dropped = h->prof_dropped;
+    h->prof_calls = 0;
+    h->prof_dropped = 0;
+    return MOE_OK;
+}
+
 int moe_destroy(moe_handle_t h)
 {
     if (!h)
         return MOE_ERR_INVALID_ARG;
     cudaSetDevice(h->dev);
     sync_last(h);
+    for (auto &e : h->events)
+        cudaEventDestroy(e);
     free_big(h);
     if (h->small_mem)
         cudaFree(h->small_mem);

@@ -76,6 +76,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         "moe_get_info": [H, ctypes.POINTER(MoeInfo)],
         "moe_set_option": [H, I, I64],
         "moe_destroy": [H],
+        "moe_profile_enable": [H, I],
+        "moe_profile_read": [H, P, ctypes.POINTER(I), ctypes.POINTER(I)],
     }
     for name, args in sig.items():
         fn = getattr(L, name)
@@ -213,6 +215,21 @@ class FusedMoE:
         _check(self.lib.moe_debug_buffer(self.h, BUFFERS[which], a.ctypes.data, a.nbytes),
                "moe_debug_buffer")
         return a
+
+    STAGES = ("dispatch", "gemm_gate_up", "gemm_down", "combine")
+
+    def profile_enable(self, on: bool = True):
+        _check(self.lib.moe_profile_enable(self.h, 1 if on else 0), "moe_profile_enable")
+
+    def profile_read(self) -> dict:
+        import numpy as np
+        ms = np.zeros(4, np.float64)
+        calls = ctypes.c_int(0)
+        dropped = ctypes.c_int(0)
+        _check(self.lib.moe_profile_read(self.h, ms.ctypes.data, ctypes.byref(calls),
+                                         ctypes.byref(dropped)), "moe_profile_read")
+        return {"stage_ms": dict(zip(self.STAGES, ms.tolist())), "calls": calls.value,
+                "dropped": dropped.value}
 
     def close(self):
         if getattr(self, "h", None) is not None and self.h.value:

@@ -10,6 +10,7 @@ EXPECTED = {
     "moe_create", "moe_reserve", "moe_load_weights", "moe_forward", "moe_forward_host",
     "moe_get_error", "moe_debug_routing", "moe_cumulative_expert_rows", "moe_debug_buffer",
     "moe_get_info", "moe_set_option", "moe_destroy", "moe_status_string",
+    "moe_profile_enable", "moe_profile_read",
 }
 
 

@@ -335,27 +335,29 @@ __global__ void __launch_bounds__(COMBINE_THREADS)
     const int K = d.K, H = d.H;
     const uint32_t err = *reinterpret_cast<volatile uint32_t *>(ws.hdr + HDR_ERR_CALL) |
                          *reinterpret_cast<volatile uint32_t *>(ws.hdr + HDR_ERR_STICKY);
-    const int lane = threadIdx.x & 31;
-    const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int nw = (gridDim.x * blockDim.x) >> 5;
     if (err == 0) {
+        // one thread per 16-byte output vector (8 bf16); its top-k plane loads are
+        // independent, so they are all in flight together
         const int H8 = H / 8;
         const long long plane = static_cast<long long>(ws.max_tokens) * H8;   // uint4 per plane
         const uint4 *cb = reinterpret_cast<const uint4 *>(ws.combine);
         uint4 *out = reinterpret_cast<uint4 *>(c.out);
-        for (int t = gw; t < c.T; t += nw) {
-            const bool valid = lane < K && c.idx[static_cast<long long>(t) * K + lane] >= 0;
-            const uint32_t mask = __ballot_sync(0xFFFFFFFFu, valid);
-            for (int v = lane; v < H8; v += 32) {
-                float acc[8];
+        const long long n = static_cast<long long>(c.T) * H8;
+        const long long gthreads_l = static_cast<long long>(gridDim.x) * blockDim.x;
+        for (long long g = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; g < n;
+             g += gthreads_l) {
+            const long long t = g / H8;
+            uint32_t mask = 0;
+            for (int kk = 0; kk < K; ++kk)
+                mask |= (__ldg(c.idx + t * K + kk) >= 0 ? 1u : 0u) << kk;
+            float acc[8];
 #pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    acc[q] = 0.0f;
-                uint32_t m = mask;
-                while (m) {
-                    const int kk = __ffs(m) - 1;
-                    m &= m - 1;
-                    const uint4 u = __ldcs(cb + kk * plane + static_cast<long long>(t) * H8 + v);
+            for (int q = 0; q < 8; ++q)
+                acc[q] = 0.0f;
+#pragma unroll 8
+            for (int kk = 0; kk < K; ++kk) {
+                if (mask & (1u << kk)) {
+                    const uint4 u = __ldcs(cb + kk * plane + g);
                     const __nv_bfloat162 *b = reinterpret_cast<const __nv_bfloat162 *>(&u);
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
@@ -364,13 +366,13 @@ __global__ void __launch_bounds__(COMBINE_THREADS)
                         acc[2 * q + 1] += f.y;
                     }
                 }
-                uint4 o;
-                __nv_bfloat162 *ob = reinterpret_cast<__nv_bfloat162 *>(&o);
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    ob[q] = __floats2bfloat162_rn(acc[2 * q], acc[2 * q + 1]);
-                out[static_cast<long long>(t) * H8 + v] = o;
             }
+            uint4 o;
+            __nv_bfloat162 *ob = reinterpret_cast<__nv_bfloat162 *>(&o);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                ob[q] = __floats2bfloat162_rn(acc[2 * q], acc[2 * q + 1]);
+            out[g] = o;
         }
     }
     // reset for the next forward

@@ -44,7 +44,7 @@ L2_BYTES = 129 * 2 ** 20
 # DRAM bytes per launch from one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum),
 # valid only while the kernel sources hash to `src_sha`; see profiles/.
 NCU_TRAFFIC = {}
-KERNEL_SOURCES = ["combine_persistent_warp_gb300/csrc/gemm.cu",
+KERNEL_SOURCES = ["combine_persistent_warp_gb300/csrc/ffn.cu",
                   "combine_persistent_warp_gb300/csrc/routing.cu",
                   "combine_persistent_warp_gb300/csrc/ptx.cuh",
                   "combine_persistent_warp_gb300/csrc/moe_internal.cuh"]
@@ -194,15 +194,17 @@ def work_model(inp) -> dict:
     w2 = touched * (H * I + (H // 128) * (I // 128) * 4)
     x_rows = M * (H + (H // 128) * 4)            # gathered activation rows + scales
     act_rows = M * (I + (I // 128) * 4)
+    # expert_ffn = gate_up GEMM (W1, gathered rows in, SwiGLU rows out) + down GEMM (W2,
+    # SwiGLU rows in, weighted bf16 rows out); one kernel
     st = {
         "dispatch": {"bytes": T * K * 8 + 2 * x_rows + M * (12 + 8), "flops": 0},
-        "gemm_gate_up": {"bytes": w1 + x_rows + act_rows, "flops": 2 * M * H * 2 * I},
-        "gemm_down": {"bytes": w2 + act_rows + M * H * 2 + M * 16, "flops": 2 * M * I * H},
+        "expert_ffn": {"bytes": w1 + w2 + x_rows + 2 * act_rows + M * H * 2 + M * 16,
+                       "flops": 2 * M * H * 2 * I + 2 * M * I * H},
         "combine": {"bytes": M * H * 2 + T * H * 2 + T * K * 8, "flops": M * H},
     }
     compulsory = (w1 + w2 + T * (H + (H // 128) * 4) + T * K * 12 + T * H * 2)
     return {"M": M, "touched_experts": touched, "stages": st, "compulsory_bytes": compulsory,
-            "flops": 6 * M * H * I}
+            "flops": 6 * M * H * I, "weight_bytes": w1 + w2}
 
 
 def peaks() -> tuple[dict, str]:
@@ -228,7 +230,7 @@ def roofline_for(stage: str, avg_s: float, model: dict, workload: str) -> dict:
     rec = NCU_TRAFFIC.get((workload, stage))
     if rec and rec.get("src_sha") == kernel_sources_sha():
         traffic = rec["bytes"]
-    if t_tensor > t_hbm and stage.startswith("gemm"):
+    if t_tensor > t_hbm and flops:
         achieved = flops / avg_s / 1e12
         return {"bound": "tensor", "kernel": stage, "achieved": achieved, "peak": fp8_peak,
                 "unit": "TFLOP/s", "frac": achieved / fp8_peak, "traffic": traffic,
@@ -350,12 +352,11 @@ def run_ours(args, dist: Dist) -> dict | None:
                    "topk": wl.topk, "R": wl.R, "routing": wl.routing,
                    "routed_rows_per_step": M, "parallelism": f"replicas x{dist.world}",
                    "l2": ("inputs larger than L2: %.2f GB of expert weights streamed per step, "
-                          "no flush" % ((model["stages"]["gemm_gate_up"]["bytes"] +
-                                         model["stages"]["gemm_down"]["bytes"]) / 1e9))},
+                          "no flush" % (model["weight_bytes"] / 1e9))},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                 "entry_point": "moe_forward_host"},
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": 3 * args.steps,
         "roofline": roof,
         "stages_us_per_launch": stages,
         "clocks": sampler.summary(h0, h1),

@@ -1,8 +1,9 @@
 // api.cu -- the C ABI declared in include/cpw_moe.h: handle, argument checks, workspace
 // planning and allocation, weight re-layout, TMA descriptors, and the launch sequence of
 // one forward:
-//   dispatch (cooperative, one CTA per SM)  ->  gate_up GEMM + SwiGLU/requant  ->
-//   down GEMM + weighted scatter  ->  combine reduce + workspace reset
+//   dispatch (cooperative, one CTA per SM)  ->  expert FFN (cooperative, one CTA per SM:
+//   gate_up GEMM + SwiGLU/requant, then down GEMM + weighted scatter)  ->
+//   combine reduce + workspace reset
 // all on the caller's stream.
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -36,7 +37,7 @@ struct moe_ctx {
     float *s2 = nullptr;         // [E][H/128][I/128]
     void *w_mem = nullptr;
     size_t w_bytes = 0;
-    CUtensorMap tm_pool{}, tm_act{}, tm_w1{}, tm_w2{};
+    FfnMaps maps{};              // a1 pool x, b1 W1, a2 act, b2 W2
     // staging buffers of moe_forward_host
     uint8_t *st_x = nullptr;
     float *st_sf = nullptr;
@@ -50,7 +51,7 @@ struct moe_ctx {
     int debug_skip_barrier = 0;
     // stage profiling (events on the forward's stream)
     bool profile = false;
-    std::vector<cudaEvent_t> events;   // 5 per recorded forward
+    std::vector<cudaEvent_t> events;   // 4 per recorded forward
     int prof_calls = 0, prof_dropped = 0;
 };
 
@@ -138,6 +139,7 @@ size_t carve_big(moe_ctx *h, char *base, int max_tokens, Workspace &ws)
     ws.block_expert = c.take<int32_t>(max_blocks);
     ws.block_rows = c.take<int32_t>(max_blocks);
     ws.arrive = c.take<uint32_t>(max_blocks);
+    ws.l1_done = c.take<uint32_t>(max_blocks);
     ws.table = c.take<int32_t>(static_cast<size_t>(d.E) * d.R * tsrc_cap);
     ws.meta = c.take<uint32_t>(static_cast<size_t>(P) * 3);
     ws.pool_x = c.take<uint8_t>(static_cast<size_t>(P) * d.H);
@@ -151,6 +153,16 @@ size_t carve_big(moe_ctx *h, char *base, int max_tokens, Workspace &ws)
     h->st_w = c.take<float>(static_cast<size_t>(max_tokens) * d.K);
     h->st_out = c.take<uint16_t>(static_cast<size_t>(max_tokens) * d.H);
     return align_up(c.off, 256);
+}
+
+// M-blocks per expert wave of the FFN kernel: the SwiGLU output of one wave
+// (blocks x 128 rows x I bytes) should stay within half of the 129 MB L2 until the
+// down-projection tiles of the same wave read it back.
+int wave_blocks(const moe_ctx *h)
+{
+    const long long per_block = static_cast<long long>(BM) * h->d.I;
+    const long long half_l2 = 64ll << 20;
+    return static_cast<int>(std::max(1ll, half_l2 / per_block));
 }
 
 int sync_last(moe_ctx *h)
@@ -245,12 +257,13 @@ int moe_reserve(moe_handle_t h, int max_tokens)
     h->ws = ws;
     h->big_bytes = bytes;
     CK(cudaMemset(ws.arrive, 0, sizeof(uint32_t) * ws.max_blocks));
+    CK(cudaMemset(ws.l1_done, 0, sizeof(uint32_t) * ws.max_blocks));
     CK(cudaMemset(ws.pool_sf, 0, sizeof(float) * static_cast<size_t>(ws.P) * (d.H / 128)));
     CK(cudaMemset(ws.act_sf, 0, sizeof(float) * static_cast<size_t>(ws.P) * (d.I / 128)));
     CK(cudaMemset(ws.pool_x, 0, static_cast<size_t>(ws.P) * d.H));
     CK(cudaMemset(ws.act, 0, static_cast<size_t>(ws.P) * d.I));
-    if (encode_tile_map(&h->tm_pool, ws.pool_x, ws.P, d.H, BM) != MOE_OK ||
-        encode_tile_map(&h->tm_act, ws.act, ws.P, d.I, BM) != MOE_OK)
+    if (encode_tile_map(&h->maps.a1, ws.pool_x, ws.P, d.H, BM) != MOE_OK ||
+        encode_tile_map(&h->maps.a2, ws.act, ws.P, d.I, BM) != MOE_OK)
         return MOE_ERR_CUDA;
     CK(cudaDeviceSynchronize());
     h->reserved = true;
@@ -291,8 +304,8 @@ int moe_load_weights(moe_handle_t h, const uint8_t *w_gate_up, const float *sf_g
     CK(cudaMemcpyAsync(h->s1, sf_gate_up, ns1 * sizeof(float), cudaMemcpyDeviceToDevice, s));
     CK(cudaMemcpyAsync(h->w2, w_down, n2, cudaMemcpyDeviceToDevice, s));
     CK(cudaMemcpyAsync(h->s2, sf_down, ns2 * sizeof(float), cudaMemcpyDeviceToDevice, s));
-    if (encode_tile_map(&h->tm_w1, h->w1, static_cast<uint64_t>(d.E) * 2 * d.I, d.H, BN) != MOE_OK ||
-        encode_tile_map(&h->tm_w2, h->w2, static_cast<uint64_t>(d.E) * d.H, d.I, BN) != MOE_OK)
+    if (encode_tile_map(&h->maps.b1, h->w1, static_cast<uint64_t>(d.E) * 2 * d.I, d.H, BN) != MOE_OK ||
+        encode_tile_map(&h->maps.b2, h->w2, static_cast<uint64_t>(d.E) * d.H, d.I, BN) != MOE_OK)
         return MOE_ERR_CUDA;
     h->have_weights = true;
     h->last_stream = s;
@@ -326,18 +339,16 @@ int moe_forward(moe_handle_t h, int T, const uint8_t *x, const float *x_sf, cons
     cudaEvent_t *ev = nullptr;
     if (h->profile) {
         if (h->prof_calls < PROF_MAX_CALLS)
-            ev = &h->events[static_cast<size_t>(h->prof_calls++) * 5];
+            ev = &h->events[static_cast<size_t>(h->prof_calls++) * 4];
         else
             ++h->prof_dropped;
     }
     auto mark = [&](int i) { return ev ? cudaEventRecord(ev[i], s) : cudaSuccess; };
     if (mark(0) != cudaSuccess || launch_dispatch(h->d, h->ws, c, h->num_sms, s) != cudaSuccess ||
         mark(1) != cudaSuccess ||
-        launch_gemm_gate_up(h->tm_pool, h->tm_w1, h->d, h->ws, c, h->s1, h->num_sms, s) != cudaSuccess ||
-        mark(2) != cudaSuccess ||
-        launch_gemm_down(h->tm_act, h->tm_w2, h->d, h->ws, c, h->s2, h->num_sms, s) != cudaSuccess ||
-        mark(3) != cudaSuccess || launch_combine(h->d, h->ws, c, h->num_sms, s) != cudaSuccess ||
-        mark(4) != cudaSuccess)
+        launch_ffn(h->maps, h->d, h->ws, c, h->s1, h->s2, wave_blocks(h), h->num_sms, s) != cudaSuccess ||
+        mark(2) != cudaSuccess || launch_combine(h->d, h->ws, c, h->num_sms, s) != cudaSuccess ||
+        mark(3) != cudaSuccess)
         return MOE_ERR_CUDA;
     h->last_stream = s;
     h->have_last = true;
@@ -390,8 +401,10 @@ int moe_get_error(moe_handle_t h, int *device_status)
     if (st != 0) {
         CK(cudaMemset(h->ws.hdr, 0, sizeof(uint32_t) * HDR_WORDS));
         CK(cudaMemset(h->ws.send, 0, sizeof(unsigned long long) * h->d.R * h->d.E));
-        if (h->reserved)
+        if (h->reserved) {
             CK(cudaMemset(h->ws.arrive, 0, sizeof(uint32_t) * h->ws.max_blocks));
+            CK(cudaMemset(h->ws.l1_done, 0, sizeof(uint32_t) * h->ws.max_blocks));
+        }
         CK(cudaDeviceSynchronize());
     }
     *device_status = static_cast<int>(st);
@@ -515,7 +528,7 @@ int moe_profile_enable(moe_handle_t h, int enable)
         return MOE_ERR_INVALID_ARG;
     CK(cudaSetDevice(h->dev));
     if (enable && h->events.empty()) {
-        h->events.resize(static_cast<size_t>(PROF_MAX_CALLS) * 5);
+        h->events.resize(static_cast<size_t>(PROF_MAX_CALLS) * 4);
         for (auto &e : h->events)
             CK(cudaEventCreate(&e));
     }
@@ -532,13 +545,13 @@ int moe_profile_read(moe_handle_t h, double *stage_ms, int *calls, int *dropped)
     CK(cudaSetDevice(h->dev));
     if (sync_last(h) != MOE_OK)
         return MOE_ERR_CUDA;
-    for (int j = 0; j < 4; ++j)
+    for (int j = 0; j < 3; ++j)
         stage_ms[j] = 0.0;
     for (int i = 0; i < h->prof_calls; ++i) {
-        for (int j = 0; j < 4; ++j) {
+        for (int j = 0; j < 3; ++j) {
             float ms = 0.0f;
-            CK(cudaEventElapsedTime(&ms, h->events[static_cast<size_t>(i) * 5 + j],
-                                    h->events[static_cast<size_t>(i) * 5 + j + 1]));
+            CK(cudaEventElapsedTime(&ms, h->events[static_cast<size_t>(i) * 4 + j],
+                                    h->events[static_cast<size_t>(i) * 4 + j + 1]));
             stage_ms[j] += ms;
         }
     }

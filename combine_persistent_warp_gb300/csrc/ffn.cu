@@ -1,26 +1,35 @@
-// gemm.cu -- persistent, warp-specialised FP8 grouped GEMM on tcgen05 (sm_103a).
+// ffn.cu -- the expert FFN of the fused MoE layer as ONE persistent, warp-specialised
+// FP8 grouped-GEMM kernel on tcgen05 (sm_103a).
 //
-// One kernel template serves both expert GEMMs of the layer ("Mega-MoE 内核代码导读：从
-// Dispatch 到 WGMMA 的融合流水线" §六: Linear1 gate_up, Linear2 down; §八: per-tile life of
-// a GEMM block):
-//   PHASE 1 (gate_up):  A = expert-major pool [P][H] e4m3 + 1x128 scales,
-//                       B = gate/up-interleaved W1 [E*2I][H] e4m3 + 128x128 scales;
-//                       epilogue: SwiGLU, per-row 1x128 requant to e4m3 -> act [P][I].
-//   PHASE 2 (down):     A = act [P][I] + scales, B = W2 [E*H][I] + 128x128 scales;
-//                       epilogue: multiply by the top-k gate weight, bf16, scatter through
-//                       the {source, token, topk} metadata into combine[topk][T][H]
-//                       ("DeepGEMM Mega MoE 对称内存（Symmetric Memory）深度分析" §8.1).
+// Both expert GEMMs run in the same launch ("Mega-MoE 内核代码导读：从 Dispatch 到 WGMMA 的融合
+// 流水线" §六: Linear1 gate_up then Linear2 down; "MOE融合算子", DeepGEMM MegaMoE §2 and §5:
+// within an expert wave, all Linear1 tiles, then all Linear2 tiles; a Linear2 block waits
+// only for the Linear1 tiles of its own M-block):
+//   phase 1 tile (blk, nt):  A = gathered pool rows [P][H] e4m3 with 1x128 scales,
+//                            B = gate/up-interleaved W1 [E*2I][H] e4m3 with 128x128 scales;
+//                            epilogue: SwiGLU, per-row 1x128 requant -> act [P][I], then
+//                            one release-increment of l1_done[blk] per epilogue warp.
+//   phase 2 tile (blk, nt):  producer first waits for l1_done[blk] == 8 * (2I/256), then
+//                            A = act [P][I] with scales, B = W2 [E*H][I] with 128x128 scales;
+//                            epilogue: times the top-k gate weight, bf16, scatter through the
+//                            {source, token, topk} metadata into combine[topk][T][H]
+//                            ("DeepGEMM Mega MoE 对称内存（Symmetric Memory）深度分析" §8.1).
+// Tiles are listed wave by wave ([phase-1 tiles of the wave's blocks][phase-2 tiles of the
+// same blocks]) and dealt to the persistent CTAs round-robin; every CTA walks its tiles in
+// list order, so a phase-2 wait only ever waits on phase-1 tiles that sit earlier in some
+// CTA's list.  The launch is cooperative (all CTAs resident), so those tiles always finish.
 //
-// Roles of the 12 warps of a CTA (one CTA per SM, persistent over a static tile list):
-//   warp 0     TMA producer: A and B tiles of one 128-deep K block into a 4-stage ring
+// Roles of the 12 warps of a CTA (one CTA per SM):
+//   warp 0     TMA producer: A and B tiles of one 128-deep K block into a 4-stage ring, plus
+//              L2 prefetch of the B tiles PREFETCH_KB blocks ahead
 //   warp 1     UMMA issuer: 4 x (128x256x32) tcgen05.mma into a fresh TMEM partial
-//   warps 2-3  idle (keep the epilogue warpgroups aligned for TMEM lane access)
+//   warps 2-3  idle (the epilogue warpgroups must start at a warpgroup boundary)
 //   warps 4-11 two epilogue warpgroups, columns [0,128) and [128,256) of the tile
 // The fp32 scales are arbitrary per 128-deep K block (1x128 for A rows, 128x128 for B), so
-// each K block's product is accumulated separately in TMEM (double-buffered, 2 x 256
-// columns) and the epilogue warps promote it into fp32 registers with the product of the
-// two scales -- the scale promotion of the pages' SM90 kernel (§8.1 of the first page),
-// here overlapped with the next K block's UMMA through the TMEM full/empty barriers.
+// each K block's product lands in its own TMEM partial (double-buffered, 2 x 256 columns)
+// and the epilogue warps promote it into fp32 registers with the product of the two scales
+// (the promotion of the first page, §8.1), overlapped with the next block's UMMA through
+// the TMEM full/empty barriers.
 // All waits carry a deadline; on expiry the CTA records MOE_ERR_TIMEOUT and leaves after
 // draining the copies and MMAs it has in flight.
 #include <cuda_bf16.h>
@@ -34,8 +43,10 @@ namespace {
 
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t IDESC = ptx::idesc_e4m3_f32(BM, BN);
+constexpr int PREFETCH_KB = 8;          // L2 prefetch distance of the B operand, in K blocks
+constexpr int EPI_WARPS = 8;
 
-struct __align__(8) GemmBars {
+struct __align__(8) FfnBars {
     uint64_t full[STAGES];
     uint64_t empty[STAGES];
     uint64_t tfull[2];
@@ -46,17 +57,43 @@ struct __align__(8) GemmBars {
     float amax[2][2][BM];   // [tile parity][column half][row]
 };
 
+// Tile list: waves of `wave_blocks` M-blocks; inside a wave all phase-1 tiles (block-major,
+// n-tile minor), then all phase-2 tiles of the same blocks.
+struct TileList {
+    int NT1, NT2, nblocks, wave_blocks;
+
+    __device__ __forceinline__ int total() const { return nblocks * (NT1 + NT2); }
+
+    __device__ __forceinline__ void at(int tile, int &phase, int &blk, int &nt) const
+    {
+        const int full = wave_blocks * (NT1 + NT2);
+        const int w = tile / full;
+        const int r = tile - w * full;
+        const int b0 = w * wave_blocks;
+        const int nb = min(wave_blocks, nblocks - b0);
+        if (r < nb * NT1) {
+            phase = 1;
+            blk = b0 + r / NT1;
+            nt = r % NT1;
+        } else {
+            const int r2 = r - nb * NT1;
+            phase = 2;
+            blk = b0 + r2 / NT2;
+            nt = r2 % NT2;
+        }
+    }
+};
+
 }  // namespace
 
-template <int PHASE>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
-    gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
-                const Dims d, const Workspace ws, const CallArgs c, const float *__restrict__ sf_w)
+    ffn_kernel(const __grid_constant__ FfnMaps maps, const Dims d, const Workspace ws, const CallArgs c,
+               const float *__restrict__ sf1, const float *__restrict__ sf2, const int wave_blocks)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
-    GemmBars *bars = reinterpret_cast<GemmBars *>(smem + STAGES * STAGE_BYTES);
+    FfnBars *bars = reinterpret_cast<FfnBars *>(smem + STAGES * STAGE_BYTES);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
@@ -70,9 +107,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             }
             for (int b = 0; b < 2; ++b) {
                 ptx::mbar_init(&bars->tfull[b], 1);
-                ptx::mbar_init(&bars->tempty[b], 8);   // one arrival per epilogue warp
+                ptx::mbar_init(&bars->tempty[b], EPI_WARPS);   // one arrival per epilogue warp
             }
-            ptx::mbar_init(&bars->xbar, 256);          // every epilogue thread, once per tile
+            ptx::mbar_init(&bars->xbar, 32 * EPI_WARPS);       // every epilogue thread
             ptx::fence_mbar_init();
         }
     }
@@ -88,10 +125,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     ptx::tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
 
-    const int Kdim = PHASE == 1 ? d.H : d.I;
-    const int NKB = Kdim / BK;
-    const int NT = PHASE == 1 ? (2 * d.I) / BN : d.H / BN;
-    const int ntiles = ws.blk_off[d.E] * NT;
+    const TileList tl{(2 * d.I) / BN, d.H / BN, ws.blk_off[d.E], wave_blocks};
+    const int ntiles = tl.total();
+    const int NKB1 = d.H / BK, NKB2 = d.I / BK;
+    const uint32_t l1_target = static_cast<uint32_t>(EPI_WARPS * tl.NT1);
     const uint64_t deadline = ptx::globaltimer() + static_cast<uint64_t>(c.timeout_ns);
 
     // Registers: launched at 168 per thread (384 x 168 = 64512); the producer warpgroup
@@ -99,28 +136,53 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     if (warp < 4) {
         ptx::setmaxnreg_dec<40>();   // one instruction for all four warps of the group
         if (warp == 0) {
-            // ------------------------------------------------------------ TMA producer ----
+            // -------------------------------------------------------- TMA producer ----
             if (lane == 0) {
-                ptx::prefetch_tmap(&tm_a);
-                ptx::prefetch_tmap(&tm_b);
+                ptx::prefetch_tmap(&maps.a1);
+                ptx::prefetch_tmap(&maps.b1);
+                ptx::prefetch_tmap(&maps.a2);
+                ptx::prefetch_tmap(&maps.b2);
                 const uint64_t pol_a = ptx::policy_evict_last();
                 const uint64_t pol_b = ptx::policy_evict_first();
                 uint32_t it = 0;
                 bool ok = true;
                 for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
-                    const int blk = tile / NT, nt = tile % NT;
+                    int phase, blk, nt;
+                    tl.at(tile, phase, blk, nt);
                     const int e = ws.block_expert[blk];
-                    const int brow = (PHASE == 1 ? e * 2 * d.I : e * d.H) + nt * BN;
-                    for (int kb = 0; kb < NKB; ++kb, ++it) {
+                    const CUtensorMap *ta = phase == 1 ? &maps.a1 : &maps.a2;
+                    const CUtensorMap *tb = phase == 1 ? &maps.b1 : &maps.b2;
+                    const int nkb = phase == 1 ? NKB1 : NKB2;
+                    const int brow = (phase == 1 ? e * 2 * d.I : e * d.H) + nt * BN;
+                    for (int kb = 0; kb < PREFETCH_KB && kb < nkb; ++kb)
+                        ptx::tma_prefetch_l2_2d(tb, kb * BK, brow);
+                    if (phase == 2) {
+                        // the act rows of this block are complete once every epilogue warp
+                        // of every gate_up tile of the block has released its stores
+                        for (uint32_t i = 0;; ++i) {
+                            if (ptx::ld_acquire_gpu(ws.l1_done + blk) >= l1_target)
+                                break;
+                            if ((i & 63u) == 63u && ptx::globaltimer() > deadline) {
+                                ok = false;
+                                break;
+                            }
+                        }
+                        if (!ok)
+                            break;
+                        ptx::fence_proxy_async_global();
+                    }
+                    for (int kb = 0; kb < nkb; ++kb, ++it) {
                         const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+                        if (kb + PREFETCH_KB < nkb)
+                            ptx::tma_prefetch_l2_2d(tb, (kb + PREFETCH_KB) * BK, brow);
                         if (!ptx::mbar_wait(&bars->empty[s], ph ^ 1u, deadline)) {
                             ok = false;
                             break;
                         }
                         uint8_t *sa = smem + s * STAGE_BYTES;
                         ptx::mbar_arrive_expect_tx(&bars->full[s], STAGE_BYTES);
-                        ptx::tma_load_2d(sa, &tm_a, &bars->full[s], kb * BK, blk * BM, pol_a);
-                        ptx::tma_load_2d(sa + STAGE_A_BYTES, &tm_b, &bars->full[s], kb * BK, brow, pol_b);
+                        ptx::tma_load_2d(sa, ta, &bars->full[s], kb * BK, blk * BM, pol_a);
+                        ptx::tma_load_2d(sa + STAGE_A_BYTES, tb, &bars->full[s], kb * BK, brow, pol_b);
                     }
                 }
                 if (!ok)
@@ -131,12 +193,15 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     ptx::mbar_wait(&bars->full[i % STAGES], (i / STAGES) & 1u, dl);
             }
         } else if (warp == 1) {
-            // ------------------------------------------------------------ UMMA issuer -----
+            // -------------------------------------------------------- UMMA issuer -----
             if (lane == 0) {
                 uint32_t it = 0, pit = 0;
                 bool ok = true;
                 for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
-                    for (int kb = 0; kb < NKB; ++kb, ++it, ++pit) {
+                    int phase, blk, nt;
+                    tl.at(tile, phase, blk, nt);
+                    const int nkb = phase == 1 ? NKB1 : NKB2;
+                    for (int kb = 0; kb < nkb; ++kb, ++it, ++pit) {
                         const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
                         const uint32_t buf = pit & 1u, bph = (pit >> 1) & 1u;
                         if (!ptx::mbar_wait(&bars->full[s], ph, deadline) ||
@@ -149,7 +214,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                         const uint64_t adesc = ptx::sw128_kmajor_desc(a_addr);
                         const uint64_t bdesc = ptx::sw128_kmajor_desc(a_addr + STAGE_A_BYTES);
                         const uint32_t dt = tmem + buf * BN;
-    #pragma unroll
+#pragma unroll
                         for (int k = 0; k < BK / 32; ++k)   // +32 bytes along K = +2 in the >>4 field
                             ptx::umma_f8(dt, adesc + 2 * k, bdesc + 2 * k, IDESC, k > 0 ? 1u : 0u);
                         ptx::umma_commit(&bars->empty[s]);
@@ -165,7 +230,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     ptx::mbar_wait(&bars->empty[i % STAGES], (i / STAGES) & 1u, dl);
                 }
             }
-    }
+        }
     } else {
         // ------------------------------------------------------------ epilogue --------
         ptx::setmaxnreg_inc<232>();
@@ -173,21 +238,22 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         const int q = warp & 3;                  // TMEM lane quarter this warp may access
         const int row = q * 32 + lane;           // tile row = TMEM lane
         const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
-        const float *sfa_base = PHASE == 1 ? ws.pool_sf : ws.act_sf;
-        uint32_t pit = 0, tcount = 0;
+        uint32_t pit = 0, xcount = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, ++tcount) {
-            const int blk = tile / NT, nt = tile % NT;
+        for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+            int phase, blk, nt;
+            tl.at(tile, phase, blk, nt);
             const int e = ws.block_expert[blk];
+            const int nkb = phase == 1 ? NKB1 : NKB2;
             const long long prow = static_cast<long long>(blk) * BM + row;
-            const float *sfa = sfa_base + prow;
+            const float *sfa = (phase == 1 ? ws.pool_sf : ws.act_sf) + prow;
             const float *sb0;
             const float *sb1;
-            if (PHASE == 1) {
-                sb0 = sf_w + (static_cast<long long>(e) * (2 * d.I / 128) + nt) * NKB;              // gate
-                sb1 = sf_w + (static_cast<long long>(e) * (2 * d.I / 128) + d.I / 128 + nt) * NKB;  // up
+            if (phase == 1) {
+                sb0 = sf1 + (static_cast<long long>(e) * (2 * d.I / 128) + nt) * NKB1;              // gate
+                sb1 = sf1 + (static_cast<long long>(e) * (2 * d.I / 128) + d.I / 128 + nt) * NKB1;  // up
             } else {
-                sb0 = sf_w + (static_cast<long long>(e) * (d.H / 128) + 2 * nt + wg) * NKB;
+                sb0 = sf2 + (static_cast<long long>(e) * (d.H / 128) + 2 * nt + wg) * NKB2;
                 sb1 = sb0;
             }
             float acc[128];
@@ -195,9 +261,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             for (int j = 0; j < 128; ++j)
                 acc[j] = 0.0f;
             float a_nx = __ldg(sfa), b0_nx = __ldg(sb0), b1_nx = __ldg(sb1);
-            for (int kb = 0; kb < NKB; ++kb, ++pit) {
+            for (int kb = 0; kb < nkb; ++kb, ++pit) {
                 const float s0 = a_nx * b0_nx, s1 = a_nx * b1_nx;
-                if (kb + 1 < NKB) {
+                if (kb + 1 < nkb) {
                     a_nx = __ldg(sfa + static_cast<long long>(kb + 1) * ws.P);
                     b0_nx = __ldg(sb0 + kb + 1);
                     b1_nx = __ldg(sb1 + kb + 1);
@@ -210,16 +276,26 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 }
                 ptx::tc_fence_after();
                 const uint32_t taddr = tmem + lane_base + buf * BN + wg * 128;
+                if (phase == 1) {
 #pragma unroll
-                for (int ch = 0; ch < 4; ++ch) {
-                    uint32_t r[32];
-                    ptx::tmem_ld32(taddr + ch * 32, r);
-                    ptx::tmem_ld_wait(r);
+                    for (int ch = 0; ch < 4; ++ch) {
+                        uint32_t r[32];
+                        ptx::tmem_ld32(taddr + ch * 32, r);
+                        ptx::tmem_ld_wait(r);
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        // gate/up interleave by 8: columns 8..15 of every 16 are "up"
-                        const float sc = (PHASE == 1 && ((j >> 3) & 1)) ? s1 : s0;
-                        acc[ch * 32 + j] = fmaf(__uint_as_float(r[j]), sc, acc[ch * 32 + j]);
+                        for (int j = 0; j < 32; ++j)   // gate/up interleave by 8: cols 8..15 of 16 are "up"
+                            acc[ch * 32 + j] = fmaf(__uint_as_float(r[j]), ((j >> 3) & 1) ? s1 : s0,
+                                                    acc[ch * 32 + j]);
+                    }
+                } else {
+#pragma unroll
+                    for (int ch = 0; ch < 4; ++ch) {
+                        uint32_t r[32];
+                        ptx::tmem_ld32(taddr + ch * 32, r);
+                        ptx::tmem_ld_wait(r);
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            acc[ch * 32 + j] = fmaf(__uint_as_float(r[j]), s0, acc[ch * 32 + j]);
                     }
                 }
                 ptx::tc_fence_before();
@@ -230,7 +306,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             if (!ok)
                 break;
 
-            if (PHASE == 1) {
+            if (phase == 1) {
                 // SwiGLU on the 64 (gate, up) pairs of this thread's row and column half,
                 // then 1x128 requant of the row's 128 outputs of this n-tile (the two
                 // column halves exchange their absolute maxima through shared memory).
@@ -243,10 +319,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     acc[m] = hval;   // acc[m] is no longer needed as a gate/up input
                     amax = fmaxf(amax, fabsf(hval));
                 }
-                // exchange through slots of this tile's parity, behind a bounded mbarrier
-                // (a slot is rewritten two tiles later, after every thread has passed the
-                // next tile's exchange and so has read it)
-                const uint32_t tp = tcount & 1u;
+                // slots of this tile's parity, behind a bounded mbarrier (a slot is rewritten
+                // two phase-1 tiles later, after every thread has read it)
+                const uint32_t tp = xcount & 1u;
+                ++xcount;
                 bars->amax[tp][wg][row] = amax;
                 ptx::mbar_arrive(&bars->xbar);
                 if (!__all_sync(0xFFFFFFFFu, ptx::mbar_wait(&bars->xbar, tp, deadline))) {
@@ -270,6 +346,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 }
                 if (wg == 0)
                     ws.act_sf[static_cast<long long>(nt) * ws.P + prow] = sf;
+                // publish: this warp's part of the block's act rows is written
+                __syncwarp();
+                ptx::fence_proxy_async_global();
+                if (lane == 0) {
+                    __threadfence();
+                    ptx::red_release_add(ws.l1_done + blk, 1u);
+                }
             } else {
                 if (row < ws.block_rows[blk]) {
                     const uint32_t t = ws.meta[prow * 3 + 1];
@@ -303,35 +386,29 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     }
 }
 
-template <int PHASE>
-static cudaError_t launch_gemm(const CUtensorMap &tm_a, const CUtensorMap &tm_b, const Dims &d,
-                               const Workspace &ws, const CallArgs &c, const float *sf_w, int num_sms,
-                               cudaStream_t s)
+cudaError_t launch_ffn(const FfnMaps &maps, const Dims &d, const Workspace &ws, const CallArgs &c,
+                       const float *sf1, const float *sf2, int wave_blocks, int num_sms, cudaStream_t s)
 {
     static bool configured = false;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_kernel<PHASE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(ffn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              GEMM_SMEM_BYTES);
         if (e != cudaSuccess)
             return e;
         configured = true;
     }
-    gemm_kernel<PHASE><<<num_sms, GEMM_THREADS, GEMM_SMEM_BYTES, s>>>(tm_a, tm_b, d, ws, c, sf_w);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_gemm_gate_up(const CUtensorMap &tm_a, const CUtensorMap &tm_b, const Dims &d,
-                                const Workspace &ws, const CallArgs &c, const float *sf_w, int num_sms,
-                                cudaStream_t s)
-{
-    return launch_gemm<1>(tm_a, tm_b, d, ws, c, sf_w, num_sms, s);
-}
-
-cudaError_t launch_gemm_down(const CUtensorMap &tm_a, const CUtensorMap &tm_b, const Dims &d,
-                             const Workspace &ws, const CallArgs &c, const float *sf_w, int num_sms,
-                             cudaStream_t s)
-{
-    return launch_gemm<2>(tm_a, tm_b, d, ws, c, sf_w, num_sms, s);
+    FfnMaps m = maps;
+    Dims dd = d;
+    Workspace ww = ws;
+    CallArgs cc = c;
+    const float *p1 = sf1;
+    const float *p2 = sf2;
+    int wb = wave_blocks;
+    void *args[] = {&m, &dd, &ww, &cc, &p1, &p2, &wb};
+    // cooperative: phase-2 tiles wait on phase-1 tiles of other CTAs, so all CTAs must be
+    // resident at once
+    return cudaLaunchCooperativeKernel(reinterpret_cast<void *>(ffn_kernel), dim3(num_sms),
+                                       dim3(GEMM_THREADS), args, GEMM_SMEM_BYTES, s);
 }
 
 }  // namespace cpw

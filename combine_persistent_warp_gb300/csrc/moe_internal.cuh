@@ -47,6 +47,7 @@ struct Workspace {
     float *act_sf;                 // [I/128][P]
     uint16_t *combine;             // [topk][max_tokens][H] bf16 weighted expert outputs
     uint32_t *arrive;              // [MB] rows gathered per M-block
+    uint32_t *l1_done;             // [MB] finished gate_up (tile, epilogue warp) pairs
     int tsrc_cap;                  // max_tokens / R
     int P;                         // pool rows
     int max_blocks;                // P / BM
@@ -80,12 +81,12 @@ __device__ __forceinline__ void record_error(uint32_t *hdr, uint32_t code)
 size_t dispatch_smem_bytes(const Dims &d);
 cudaError_t launch_dispatch(const Dims &d, const Workspace &ws, const CallArgs &c, int num_sms,
                             cudaStream_t s);
-cudaError_t launch_gemm_gate_up(const CUtensorMap &tm_a, const CUtensorMap &tm_b, const Dims &d,
-                                const Workspace &ws, const CallArgs &c, const float *sf_w,
-                                int num_sms, cudaStream_t s);
-cudaError_t launch_gemm_down(const CUtensorMap &tm_a, const CUtensorMap &tm_b, const Dims &d,
-                             const Workspace &ws, const CallArgs &c, const float *sf_w,
-                             int num_sms, cudaStream_t s);
+struct FfnMaps {
+    CUtensorMap a1, b1, a2, b2;   // pool x / W1 (gate_up), act / W2 (down)
+};
+cudaError_t launch_ffn(const FfnMaps &maps, const Dims &d, const Workspace &ws, const CallArgs &c,
+                       const float *sf1, const float *sf2, int wave_blocks, int num_sms,
+                       cudaStream_t s);
 cudaError_t launch_combine(const Dims &d, const Workspace &ws, const CallArgs &c, int num_sms,
                            cudaStream_t s);
 cudaError_t launch_interleave_gate_up(const uint8_t *src, uint8_t *dst, int E, int I, int H,

@@ -380,8 +380,10 @@ __global__ void __launch_bounds__(COMBINE_THREADS)
     const int gthreads = gridDim.x * blockDim.x;
     for (int i = gtid; i < d.R * d.E; i += gthreads)
         ws.send[i] = 0ull;
-    for (int i = gtid; i < ws.max_blocks; i += gthreads)
+    for (int i = gtid; i < ws.max_blocks; i += gthreads) {
         ws.arrive[i] = 0u;
+        ws.l1_done[i] = 0u;
+    }
     if (gtid == 0) {
         const uint32_t call = *reinterpret_cast<volatile uint32_t *>(ws.hdr + HDR_ERR_CALL);
         if (call != 0) {

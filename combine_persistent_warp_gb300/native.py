@@ -216,14 +216,14 @@ class FusedMoE:
                "moe_debug_buffer")
         return a
 
-    STAGES = ("dispatch", "gemm_gate_up", "gemm_down", "combine")
+    STAGES = ("dispatch", "expert_ffn", "combine")
 
     def profile_enable(self, on: bool = True):
         _check(self.lib.moe_profile_enable(self.h, 1 if on else 0), "moe_profile_enable")
 
     def profile_read(self) -> dict:
         import numpy as np
-        ms = np.zeros(4, np.float64)
+        ms = np.zeros(len(self.STAGES), np.float64)
         calls = ctypes.c_int(0)
         dropped = ctypes.c_int(0)
         _check(self.lib.moe_profile_read(self.h, ms.ctypes.data, ctypes.byref(calls),

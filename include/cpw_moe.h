@@ -146,10 +146,11 @@ enum moe_option { MOE_OPT_TIMEOUT_NS = 0, MOE_OPT_DEBUG_SKIP_BARRIER = 1 };
 int moe_set_option(moe_handle_t h, int option, int64_t value);
 
 /* Stage timing with CUDA events recorded on the forward's own stream.  While enabled,
- * every moe_forward records an event before and after each of its four kernels
- * (dispatch, gate_up GEMM, down GEMM, combine); moe_profile_read waits for the last
- * stream, returns the summed milliseconds of each stage over the recorded forwards in
- * stage_ms[4] and their number in *calls, and starts a new window.  At most 8192
+ * every moe_forward records an event before and after each of its three kernels
+ * (dispatch; expert FFN = gate_up GEMM + SwiGLU + down GEMM + weighted scatter; combine);
+ * moe_profile_read waits for the last stream, returns the summed milliseconds of each
+ * stage over the recorded forwards in stage_ms[3] and their number in *calls, and starts
+ * a new window.  At most 8192
  * forwards are recorded per window (later ones are counted in *dropped, not timed). */
 int moe_profile_enable(moe_handle_t h, int enable);
 int moe_profile_read(moe_handle_t h, double *stage_ms, int *calls, int *dropped);

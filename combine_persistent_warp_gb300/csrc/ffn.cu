@@ -256,15 +256,36 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 sb0 = sf2 + (static_cast<long long>(e) * (d.H / 128) + 2 * nt + wg) * NKB2;
                 sb1 = sb0;
             }
+            if (phase == 2) {
+                // act_sf of this block is written by other CTAs in this launch: acquire the
+                // block's completion counter (as the producer does before its TMA loads)
+                // before the first scale read, and read the scales coherently (L2), not
+                // through the read-only path.
+                bool ready = true;
+                for (uint32_t i = 0;; ++i) {
+                    if (ptx::ld_acquire_gpu(ws.l1_done + blk) >= l1_target)
+                        break;
+                    if ((i & 63u) == 63u && ptx::globaltimer() > deadline) {
+                        ready = false;
+                        break;
+                    }
+                }
+                if (!__all_sync(0xFFFFFFFFu, ready)) {
+                    ok = false;
+                    break;
+                }
+            }
             float acc[128];
 #pragma unroll
             for (int j = 0; j < 128; ++j)
                 acc[j] = 0.0f;
-            float a_nx = __ldg(sfa), b0_nx = __ldg(sb0), b1_nx = __ldg(sb1);
+            float a_nx = phase == 1 ? __ldg(sfa) : __ldcg(sfa);
+            float b0_nx = __ldg(sb0), b1_nx = __ldg(sb1);
             for (int kb = 0; kb < nkb; ++kb, ++pit) {
                 const float s0 = a_nx * b0_nx, s1 = a_nx * b1_nx;
                 if (kb + 1 < nkb) {
-                    a_nx = __ldg(sfa + static_cast<long long>(kb + 1) * ws.P);
+                    const float *na = sfa + static_cast<long long>(kb + 1) * ws.P;
+                    a_nx = phase == 1 ? __ldg(na) : __ldcg(na);
                     b0_nx = __ldg(sb0 + kb + 1);
                     b1_nx = __ldg(sb1 + kb + 1);
                 }

@@ -78,6 +78,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         "moe_destroy": [H],
         "moe_profile_enable": [H, I],
         "moe_profile_read": [H, P, ctypes.POINTER(I), ctypes.POINTER(I)],
+        "moe_route_noalloc": [I, I, I, I, P, P, P, P, P, P, P],
     }
     for name, args in sig.items():
         fn = getattr(L, name)
@@ -241,6 +242,30 @@ class FusedMoE:
             self.close()
         except Exception:
             pass
+
+
+def route_noalloc(topk_idx, E: int, R: int, stream=None) -> dict:
+    """Routing of one batch through moe_route_noalloc (no device allocation inside the
+    library; the output tensors here are allocated by PyTorch, as a caller would).
+    Returns device tensors counts [E], recv [E,R], block_offset [E+1], meta [rows,3] and
+    status [1]."""
+    import torch
+    T, K = topk_idx.shape
+    _expect(topk_idx, (T, K), torch.int64, "topk_idx", cuda=True)
+    dev = topk_idx.device
+    rows = (-(-T * K // 128) + E) * 128
+    out = {
+        "counts": torch.zeros(E, dtype=torch.int32, device=dev),
+        "recv": torch.zeros(E, R, dtype=torch.int32, device=dev),
+        "block_offset": torch.zeros(E + 1, dtype=torch.int32, device=dev),
+        "meta": torch.full((rows, 3), -1, dtype=torch.int32, device=dev),
+        "status": torch.zeros(1, dtype=torch.int32, device=dev),
+    }
+    _check(load().moe_route_noalloc(T, E, K, R, topk_idx.data_ptr(), out["counts"].data_ptr(),
+                                    out["recv"].data_ptr(), out["block_offset"].data_ptr(),
+                                    out["meta"].data_ptr(), out["status"].data_ptr(),
+                                    _stream_handle(stream)), "moe_route_noalloc")
+    return out
 
 
 def _expect(t, shape, dtype, name, cuda=None):

@@ -155,6 +155,27 @@ int moe_set_option(moe_handle_t h, int option, int64_t value);
 int moe_profile_enable(moe_handle_t h, int enable);
 int moe_profile_read(moe_handle_t h, double *stage_ms, int *calls, int *dropped);
 
+/* Routing without any device allocation, for callers that may not allocate GPU memory
+ * themselves or through this library (code running under another framework's memory
+ * pool or a fixed memory budget, real-time loops that must stay out of the allocator,
+ * plug-ins whose host owns every allocation).  The pages have no counterpart: it is a
+ * deployment convenience, not a step of the method.  It needs no handle and no weights.
+ * It computes what moe_debug_routing reports after a forward: counts [E], recv [E][R],
+ * block_offset [E+1] (M-blocks of 128 rows) and, for every received row, its pool row's
+ * {source, token, topk slot} in meta [(ceil(T*topk/128) + E) * 128][3] (padding rows are
+ * left untouched), plus *status (device int32: MOE_OK, MOE_ERR_BAD_INDEX or
+ * MOE_ERR_SLOT_OVERFLOW; on an error the other outputs are left untouched).  All pointers
+ * are device pointers owned by the caller; topk_idx is [T][topk] int64 with -1 = skip.
+ * Scratch (slot counters and the index table) lives in one fixed array of about 4 MB per
+ * GPU, kept until the process exits; sizes beyond it return MOE_ERR_CAPACITY: at most
+ * E*R <= 4096, T*topk <= 131072 and E*T <= 1048576 (plus the moe_create limits on E, topk
+ * and R, and T % R == 0).  The first call on a device looks up that array's device
+ * address and should come before any stream capture.  Asynchronous on `stream`; calls
+ * that overlap on the GPU share the scratch and race. */
+int moe_route_noalloc(int T, int E, int topk, int R, const int64_t *topk_idx, uint32_t *counts,
+                      uint32_t *recv, int32_t *block_offset, uint32_t *meta, int32_t *status,
+                      void *stream);
+
 /* Release every device buffer of the handle (after syncing its last stream). */
 int moe_destroy(moe_handle_t h);
 

@@ -75,17 +75,21 @@ int get_encoder()
     return MOE_OK;
 }
 
-// 2-D byte matrix [rows][cols] (row-major), tiles of 128 bytes x box_rows, 128-byte swizzle.
+// 2-D byte matrix [rows][cols] (row-major), tiles of BKS bytes x box_rows, swizzled at
+// BKS bytes (the layout the UMMA shared-memory descriptors of the FFN kernel expect).
 int encode_tile_map(CUtensorMap *m, void *base, uint64_t rows, uint64_t cols, uint32_t box_rows)
 {
     if (get_encoder() != MOE_OK)
         return MOE_ERR_CUDA;
     cuuint64_t dims[2] = {cols, rows};
     cuuint64_t strides[1] = {cols};
-    cuuint32_t box[2] = {128, box_rows};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(BKS), box_rows};
     cuuint32_t estr[2] = {1, 1};
+    const CUtensorMapSwizzle sw = BKS == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                  : BKS == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                              : CU_TENSOR_MAP_SWIZZLE_32B;
     CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, strides, box, estr,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
 }
@@ -263,7 +267,9 @@ int moe_reserve(moe_handle_t h, int max_tokens)
     CK(cudaMemset(ws.pool_x, 0, static_cast<size_t>(ws.P) * d.H));
     CK(cudaMemset(ws.act, 0, static_cast<size_t>(ws.P) * d.I));
     if (encode_tile_map(&h->maps.a1, ws.pool_x, ws.P, d.H, BM) != MOE_OK ||
-        encode_tile_map(&h->maps.a2, ws.act, ws.P, d.I, BM) != MOE_OK)
+        encode_tile_map(&h->maps.a2, ws.act, ws.P, d.I, BM) != MOE_OK ||
+        encode_tile_map(&h->maps.a1p, ws.pool_x, ws.P, d.H, A_ROWS_PART) != MOE_OK ||
+        encode_tile_map(&h->maps.a2p, ws.act, ws.P, d.I, A_ROWS_PART) != MOE_OK)
         return MOE_ERR_CUDA;
     CK(cudaDeviceSynchronize());
     h->reserved = true;
@@ -580,5 +586,14 @@ int moe_destroy(moe_handle_t h)
     delete h;
     return MOE_OK;
 }
+
+#ifdef CPW_TRACE
+// Development builds only (-DCPW_TRACE): stamps of the FFN kernel's trace buffer.
+int moe_trace_read(void *dst, uint64_t bytes)
+{
+    return cpw::trace_read(dst, bytes) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+int moe_trace_clear(void) { return cpw::trace_clear() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+#endif
 
 }  // extern "C"

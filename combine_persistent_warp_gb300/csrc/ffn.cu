@@ -15,14 +15,17 @@
 //                            {source, token, topk} metadata into combine[topk][T][H]
 //                            ("DeepGEMM Mega MoE 对称内存（Symmetric Memory）深度分析" §8.1).
 // Tiles are listed wave by wave ([phase-1 tiles of the wave's blocks][phase-2 tiles of the
-// same blocks]) and dealt to the persistent CTAs round-robin; every CTA walks its tiles in
-// list order, so a phase-2 wait only ever waits on phase-1 tiles that sit earlier in some
-// CTA's list.  The launch is cooperative (all CTAs resident), so those tiles always finish.
+// same blocks]) and handed out in list order from one global counter (the producer warp of
+// a CTA takes its next tile when it starts one and passes the index to the UMMA and
+// epilogue warps through a small ring), so a phase-2 wait only ever waits on phase-1 tiles
+// that were handed out earlier: the smallest unfinished phase-1 tile is always being worked
+// on.  The launch is cooperative (all CTAs resident), so those tiles always finish.
 //
 // Roles of the 12 warps of a CTA (one CTA per SM):
-//   warp 0     TMA producer: A and B tiles of one 128-deep K block into a 4-stage ring, plus
-//              L2 prefetch of the B tiles PREFETCH_KB blocks ahead
-//   warp 1     UMMA issuer: 4 x (128x256x32) tcgen05.mma into a fresh TMEM partial
+//   warp 0     TMA producer: A and B tiles of one BKS-deep K slice per stage into a
+//              STAGES-deep ring (192 KB), plus L2 prefetch of B PREFETCH_KB blocks ahead
+//   warp 1     UMMA issuer: (128x256x32) tcgen05.mma, 128/32 of them per scale block, into
+//              a fresh TMEM partial per 128-deep scale block
 //   warps 2-3  idle (the epilogue warpgroups must start at a warpgroup boundary)
 //   warps 4-11 two epilogue warpgroups, columns [0,128) and [128,256) of the tile
 // The fp32 scales are arbitrary per 128-deep K block (1x128 for A rows, 128x128 for B), so
@@ -43,8 +46,38 @@ namespace {
 
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t IDESC = ptx::idesc_e4m3_f32(BM, BN);
-constexpr int PREFETCH_KB = 8;          // L2 prefetch distance of the B operand, in K blocks
+#ifndef CPW_PREFETCH_KB
+#define CPW_PREFETCH_KB 0
+#endif
+constexpr int PREFETCH_KB = CPW_PREFETCH_KB;   // L2 prefetch distance of B, in scale blocks
 constexpr int EPI_WARPS = 8;
+constexpr int TILE_RING = 4;   // tiles the producer may run ahead of the UMMA/epilogue warps
+
+#ifdef CPW_TRACE
+// Development trace (compiled only with -DCPW_TRACE): SM clock stamps of two CTAs, per
+// pipeline stage for the producer (0: load issue) and the UMMA issuer (1: stage full,
+// 2: MMAs issued), per scale block for one epilogue warp (3: TMEM full, 4: promoted,
+// 5: tile epilogue start).
+// 6: producer tile start, 7: producer done waiting for a down tile's gate_up blocks.
+// g_cta_span: global-timer ns at every CTA's start and end (cross-SM comparable).
+constexpr int TRACE_CTAS = 2, TRACE_EVENTS = 8, TRACE_ITERS = 4096, TRACE_MAX_GRID = 1024;
+__device__ unsigned long long g_trace[TRACE_CTAS][TRACE_EVENTS][TRACE_ITERS];
+__device__ unsigned long long g_cta_span[2][TRACE_MAX_GRID];
+__device__ __forceinline__ int trace_slot()
+{
+    return blockIdx.x == 0 ? 0 : (blockIdx.x == gridDim.x / 2 ? 1 : -1);
+}
+#define CPW_STAMP(ev, it)                                                                   \
+    do {                                                                                     \
+        const int ts_ = trace_slot();                                                        \
+        if (ts_ >= 0 && (it) < static_cast<uint32_t>(TRACE_ITERS))                           \
+            g_trace[ts_][ev][it] = static_cast<unsigned long long>(clock64());               \
+    } while (0)
+#else
+#define CPW_STAMP(ev, it) \
+    do {                  \
+    } while (0)
+#endif
 
 struct __align__(8) FfnBars {
     uint64_t full[STAGES];
@@ -52,6 +85,9 @@ struct __align__(8) FfnBars {
     uint64_t tfull[2];
     uint64_t tempty[2];
     uint64_t xbar;          // row-amax exchange between the two epilogue warpgroups
+    uint64_t tile_full[TILE_RING];    // producer -> UMMA issuer + epilogue: next tile index
+    uint64_t tile_empty[TILE_RING];   // UMMA issuer + 8 epilogue warps have read the slot
+    int tile_ring[TILE_RING];
     uint32_t tmem_base;
     int abort;
     float amax[2][2][BM];   // [tile parity][column half][row]
@@ -110,6 +146,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 ptx::mbar_init(&bars->tempty[b], EPI_WARPS);   // one arrival per epilogue warp
             }
             ptx::mbar_init(&bars->xbar, 32 * EPI_WARPS);       // every epilogue thread
+            for (int i = 0; i < TILE_RING; ++i) {
+                ptx::mbar_init(&bars->tile_full[i], 1);
+                ptx::mbar_init(&bars->tile_empty[i], 1 + EPI_WARPS);
+            }
             ptx::fence_mbar_init();
         }
     }
@@ -130,6 +170,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     const int NKB1 = d.H / BK, NKB2 = d.I / BK;
     const uint32_t l1_target = static_cast<uint32_t>(EPI_WARPS * tl.NT1);
     const uint64_t deadline = ptx::globaltimer() + static_cast<uint64_t>(c.timeout_ns);
+#ifdef CPW_TRACE
+    if (threadIdx.x == 0 && blockIdx.x < TRACE_MAX_GRID)
+        g_cta_span[0][blockIdx.x] = ptx::globaltimer();
+#endif
 
     // Registers: launched at 168 per thread (384 x 168 = 64512); the producer warpgroup
     // gives (168-40) x 128 back and the two epilogue warpgroups take (232-168) x 256.
@@ -146,16 +190,38 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 const uint64_t pol_b = ptx::policy_evict_first();
                 uint32_t it = 0;
                 bool ok = true;
-                for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+                uint32_t tcount = 0;
+                while (ok) {
+                    // dynamic tile list: tiles are handed out in list order, one at a time
+                    const int tile = static_cast<int>(atomicAdd(ws.hdr + HDR_TILE_NEXT, 1u));
+                    const uint32_t slot = tcount % TILE_RING, sph = (tcount / TILE_RING) & 1u;
+                    if (!ptx::mbar_wait(&bars->tile_empty[slot], sph ^ 1u, deadline)) {
+                        ok = false;
+                        break;
+                    }
+                    bars->tile_ring[slot] = tile < ntiles ? tile : -1;
+                    ptx::mbar_arrive(&bars->tile_full[slot]);
+                    if (tile >= ntiles)
+                        break;
                     int phase, blk, nt;
                     tl.at(tile, phase, blk, nt);
+                    CPW_STAMP(6, tcount);
+                    ++tcount;
                     const int e = ws.block_expert[blk];
-                    const CUtensorMap *ta = phase == 1 ? &maps.a1 : &maps.a2;
+                    // A rows: a partly filled M-block loads only its 32-row groups that hold
+                    // valid rows (the UMMA still reads 128 rows; the rest only feed padding
+                    // rows of the tile, which are never stored)
+                    const int n_part = (ws.block_rows[blk] + A_ROWS_PART - 1) / A_ROWS_PART;
+                    const bool part = n_part < BM / A_ROWS_PART;
+                    const uint32_t a_bytes = part ? n_part * A_ROWS_PART * BKS : STAGE_A_BYTES;
+                    const CUtensorMap *ta = phase == 1 ? (part ? &maps.a1p : &maps.a1)
+                                                       : (part ? &maps.a2p : &maps.a2);
                     const CUtensorMap *tb = phase == 1 ? &maps.b1 : &maps.b2;
                     const int nkb = phase == 1 ? NKB1 : NKB2;
                     const int brow = (phase == 1 ? e * 2 * d.I : e * d.H) + nt * BN;
                     for (int kb = 0; kb < PREFETCH_KB && kb < nkb; ++kb)
-                        ptx::tma_prefetch_l2_2d(tb, kb * BK, brow);
+                        for (int j = 0; j < SUBS; ++j)
+                            ptx::tma_prefetch_l2_2d(tb, kb * BK + j * BKS, brow);
                     if (phase == 2) {
                         // the act rows of this block are complete once every epilogue warp
                         // of every gate_up tile of the block has released its stores
@@ -169,20 +235,32 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                         }
                         if (!ok)
                             break;
+                        CPW_STAMP(7, tcount);
                         ptx::fence_proxy_async_global();
                     }
-                    for (int kb = 0; kb < nkb; ++kb, ++it) {
-                        const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+                    for (int kb = 0; kb < nkb && ok; ++kb) {
                         if (kb + PREFETCH_KB < nkb)
-                            ptx::tma_prefetch_l2_2d(tb, (kb + PREFETCH_KB) * BK, brow);
-                        if (!ptx::mbar_wait(&bars->empty[s], ph ^ 1u, deadline)) {
-                            ok = false;
-                            break;
+                            for (int j = 0; j < SUBS; ++j)
+                                ptx::tma_prefetch_l2_2d(tb, (kb + PREFETCH_KB) * BK + j * BKS, brow);
+                        for (int j = 0; j < SUBS; ++j, ++it) {
+                            const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+                            if (!ptx::mbar_wait(&bars->empty[s], ph ^ 1u, deadline)) {
+                                ok = false;
+                                break;
+                            }
+                            uint8_t *sa = smem + s * STAGE_BYTES;
+                            CPW_STAMP(0, it);
+                            const int kx = kb * BK + j * BKS;
+                            ptx::mbar_arrive_expect_tx(&bars->full[s], a_bytes + STAGE_B_BYTES);
+                            if (part) {
+                                for (int g = 0; g < n_part; ++g)
+                                    ptx::tma_load_2d(sa + g * A_ROWS_PART * BKS, ta, &bars->full[s], kx,
+                                                     blk * BM + g * A_ROWS_PART, pol_a);
+                            } else {
+                                ptx::tma_load_2d(sa, ta, &bars->full[s], kx, blk * BM, pol_a);
+                            }
+                            ptx::tma_load_2d(sa + STAGE_A_BYTES, tb, &bars->full[s], kx, brow, pol_b);
                         }
-                        uint8_t *sa = smem + s * STAGE_BYTES;
-                        ptx::mbar_arrive_expect_tx(&bars->full[s], STAGE_BYTES);
-                        ptx::tma_load_2d(sa, ta, &bars->full[s], kb * BK, blk * BM, pol_a);
-                        ptx::tma_load_2d(sa + STAGE_A_BYTES, tb, &bars->full[s], kb * BK, brow, pol_b);
                     }
                 }
                 if (!ok)
@@ -195,29 +273,50 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         } else if (warp == 1) {
             // -------------------------------------------------------- UMMA issuer -----
             if (lane == 0) {
-                uint32_t it = 0, pit = 0;
+                uint32_t it = 0, pit = 0, tcount = 0;
                 bool ok = true;
-                for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+                while (ok) {
+                    const uint32_t slot = tcount % TILE_RING, sph = (tcount / TILE_RING) & 1u;
+                    if (!ptx::mbar_wait(&bars->tile_full[slot], sph, deadline)) {
+                        ok = false;
+                        break;
+                    }
+                    const int tile = bars->tile_ring[slot];
+                    ptx::mbar_arrive(&bars->tile_empty[slot]);
+                    ++tcount;
+                    if (tile < 0)
+                        break;
                     int phase, blk, nt;
                     tl.at(tile, phase, blk, nt);
                     const int nkb = phase == 1 ? NKB1 : NKB2;
-                    for (int kb = 0; kb < nkb; ++kb, ++it, ++pit) {
-                        const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+                    for (int kb = 0; kb < nkb && ok; ++kb, ++pit) {
                         const uint32_t buf = pit & 1u, bph = (pit >> 1) & 1u;
-                        if (!ptx::mbar_wait(&bars->full[s], ph, deadline) ||
-                            !ptx::mbar_wait(&bars->tempty[buf], bph ^ 1u, deadline)) {
+                        if (!ptx::mbar_wait(&bars->tempty[buf], bph ^ 1u, deadline)) {
                             ok = false;
                             break;
                         }
-                        ptx::tc_fence_after();
-                        const uint32_t a_addr = ptx::smem_u32(smem + s * STAGE_BYTES);
-                        const uint64_t adesc = ptx::sw128_kmajor_desc(a_addr);
-                        const uint64_t bdesc = ptx::sw128_kmajor_desc(a_addr + STAGE_A_BYTES);
                         const uint32_t dt = tmem + buf * BN;
+                        // the SUBS stages of one scale block accumulate into one TMEM partial
+                        for (int j = 0; j < SUBS; ++j, ++it) {
+                            const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+                            if (!ptx::mbar_wait(&bars->full[s], ph, deadline)) {
+                                ok = false;
+                                break;
+                            }
+                            CPW_STAMP(1, it);
+                            ptx::tc_fence_after();
+                            const uint32_t a_addr = ptx::smem_u32(smem + s * STAGE_BYTES);
+                            const uint64_t adesc = ptx::kmajor_swizzled_desc<BKS>(a_addr);
+                            const uint64_t bdesc = ptx::kmajor_swizzled_desc<BKS>(a_addr + STAGE_A_BYTES);
 #pragma unroll
-                        for (int k = 0; k < BK / 32; ++k)   // +32 bytes along K = +2 in the >>4 field
-                            ptx::umma_f8(dt, adesc + 2 * k, bdesc + 2 * k, IDESC, k > 0 ? 1u : 0u);
-                        ptx::umma_commit(&bars->empty[s]);
+                            for (int k = 0; k < BKS / 32; ++k)   // +32 bytes along K = +2 in the >>4 field
+                                ptx::umma_f8(dt, adesc + 2 * k, bdesc + 2 * k, IDESC,
+                                             (j > 0 || k > 0) ? 1u : 0u);
+                            ptx::umma_commit(&bars->empty[s]);
+                            CPW_STAMP(2, it);
+                        }
+                        if (!ok)
+                            break;
                         ptx::umma_commit(&bars->tfull[buf]);
                     }
                 }
@@ -238,9 +337,21 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         const int q = warp & 3;                  // TMEM lane quarter this warp may access
         const int row = q * 32 + lane;           // tile row = TMEM lane
         const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
-        uint32_t pit = 0, xcount = 0;
+        uint32_t pit = 0, xcount = 0, tcount = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+        while (ok) {
+            const uint32_t slot = tcount % TILE_RING, sph = (tcount / TILE_RING) & 1u;
+            if (!__all_sync(0xFFFFFFFFu, ptx::mbar_wait(&bars->tile_full[slot], sph, deadline))) {
+                ok = false;
+                break;
+            }
+            const int tile = bars->tile_ring[slot];
+            __syncwarp();
+            if (lane == 0)
+                ptx::mbar_arrive(&bars->tile_empty[slot]);
+            ++tcount;
+            if (tile < 0)
+                break;
             int phase, blk, nt;
             tl.at(tile, phase, blk, nt);
             const int e = ws.block_expert[blk];
@@ -295,6 +406,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     ok = false;
                     break;
                 }
+                if (warp == 4 && lane == 0)
+                    CPW_STAMP(3, pit);
                 ptx::tc_fence_after();
                 const uint32_t taddr = tmem + lane_base + buf * BN + wg * 128;
                 if (phase == 1) {
@@ -323,9 +436,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 __syncwarp();
                 if (lane == 0)
                     ptx::mbar_arrive(&bars->tempty[buf]);
+                if (warp == 4 && lane == 0)
+                    CPW_STAMP(4, pit);
             }
             if (!ok)
                 break;
+            if (warp == 4 && lane == 0)
+                CPW_STAMP(5, pit);
 
             if (phase == 1) {
                 // SwiGLU on the 64 (gate, up) pairs of this thread's row and column half,
@@ -401,11 +518,32 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 
     ptx::tc_fence_before();
     __syncthreads();
+#ifdef CPW_TRACE
+    if (threadIdx.x == 0 && blockIdx.x < TRACE_MAX_GRID)
+        g_cta_span[1][blockIdx.x] = ptx::globaltimer();
+#endif
     if (warp == 1) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, TMEM_COLS);
     }
 }
+
+#ifdef CPW_TRACE
+cudaError_t trace_read(void *dst, size_t bytes)
+{
+    if (bytes != sizeof(g_trace) + sizeof(g_cta_span))
+        return cudaErrorInvalidValue;
+    cudaError_t e = cudaMemcpyFromSymbol(dst, g_trace, sizeof(g_trace));
+    if (e != cudaSuccess)
+        return e;
+    return cudaMemcpyFromSymbol(static_cast<char *>(dst) + sizeof(g_trace), g_cta_span, sizeof(g_cta_span));
+}
+cudaError_t trace_clear()
+{
+    static unsigned long long zeros[TRACE_CTAS][TRACE_EVENTS][TRACE_ITERS];
+    return cudaMemcpyToSymbol(g_trace, zeros, sizeof(zeros));
+}
+#endif
 
 cudaError_t launch_ffn(const FfnMaps &maps, const Dims &d, const Workspace &ws, const CallArgs &c,
                        const float *sf1, const float *sf2, int wave_blocks, int num_sms, cudaStream_t s)

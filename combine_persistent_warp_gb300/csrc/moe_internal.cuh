@@ -8,16 +8,23 @@
 
 namespace cpw {
 
+#ifndef CPW_BKS
+#define CPW_BKS 128
+#endif
+
 constexpr int BM = 128;            // pool rows per M-block = UMMA M = TMEM lanes
 constexpr int BN = 256;            // GEMM tile columns (UMMA N)
-constexpr int BK = 128;            // K per pipeline stage = one fp32 scale block
-constexpr int STAGES = 4;          // TMA -> UMMA shared-memory ring depth
+constexpr int BK = 128;            // K of one fp32 scale block = one TMEM partial
+constexpr int BKS = CPW_BKS;       // K (bytes of an FP8 operand row) per pipeline stage
+constexpr int SUBS = BK / BKS;     // pipeline stages per scale block
+constexpr int STAGES = 4 * BK / BKS;   // TMA -> UMMA ring depth (192 KB of operand tiles)
 constexpr int GEMM_THREADS = 384;  // 4 producer/issuer warps + 2 epilogue warpgroups
 constexpr int DISPATCH_THREADS = 512;
 constexpr int COMBINE_THREADS = 256;
+static_assert(BKS == 32 || BKS == 64 || BKS == 128, "stage depth must match a swizzle width");
 
-constexpr int STAGE_A_BYTES = BM * BK;                 // 16 KB
-constexpr int STAGE_B_BYTES = BN * BK;                 // 32 KB
+constexpr int STAGE_A_BYTES = BM * BKS;                // 16 KB at BKS = 128
+constexpr int STAGE_B_BYTES = BN * BKS;                // 32 KB at BKS = 128
 constexpr int STAGE_BYTES = STAGE_A_BYTES + STAGE_B_BYTES;
 constexpr int GEMM_SMEM_BYTES = 1024 /*align slack*/ + STAGES * STAGE_BYTES + 4096 /*bars etc*/;
 
@@ -26,6 +33,7 @@ enum HdrWord : int {
     HDR_GRID_SYNC = 0,     // XOR-tag grid barrier counter of the routing kernel
     HDR_ERR_CALL = 32,     // first device error of the forward in flight
     HDR_ERR_STICKY = 64,   // errors of finished forwards, until moe_get_error
+    HDR_TILE_NEXT = 96,    // next tile of the FFN kernel's dynamic tile list
     HDR_WORDS = 128
 };
 
@@ -81,12 +89,18 @@ __device__ __forceinline__ void record_error(uint32_t *hdr, uint32_t code)
 size_t dispatch_smem_bytes(const Dims &d);
 cudaError_t launch_dispatch(const Dims &d, const Workspace &ws, const CallArgs &c, int num_sms,
                             cudaStream_t s);
+constexpr int A_ROWS_PART = 32;   // row granularity of partial A-tile loads
 struct FfnMaps {
-    CUtensorMap a1, b1, a2, b2;   // pool x / W1 (gate_up), act / W2 (down)
+    CUtensorMap a1, b1, a2, b2;   // pool x / W1 (gate_up), act / W2 (down); 128/256-row boxes
+    CUtensorMap a1p, a2p;         // pool x / act with 32-row boxes (partly filled M-blocks)
 };
 cudaError_t launch_ffn(const FfnMaps &maps, const Dims &d, const Workspace &ws, const CallArgs &c,
                        const float *sf1, const float *sf2, int wave_blocks, int num_sms,
                        cudaStream_t s);
+#ifdef CPW_TRACE
+cudaError_t trace_read(void *dst, size_t bytes);
+cudaError_t trace_clear();
+#endif
 cudaError_t launch_combine(const Dims &d, const Workspace &ws, const CallArgs &c, int num_sms,
                            cudaStream_t s);
 cudaError_t launch_interleave_gate_up(const uint8_t *src, uint8_t *dst, int E, int I, int H,

@@ -167,16 +167,21 @@ __device__ __forceinline__ void umma_commit(uint64_t *bar)
         : "memory");
 }
 
-// Shared-memory matrix descriptor: K-major operand, 128-byte rows, 128-byte swizzle,
-// 8-row swizzle atoms packed every 1024 bytes (stride byte offset), descriptor version 1.
-__device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t smem_addr)
+// Shared-memory matrix descriptor of a K-major operand whose rows are ROW_BYTES (32, 64 or
+// 128) bytes long and swizzled at that width (the layout TMA writes with the matching
+// swizzle mode): 8-row swizzle atoms packed every 8 * ROW_BYTES bytes (stride byte
+// offset), descriptor version 1, layout type 6 / 4 / 2 for 32 / 64 / 128-byte swizzle.
+template <int ROW_BYTES>
+__device__ __forceinline__ uint64_t kmajor_swizzled_desc(uint32_t smem_addr)
 {
+    static_assert(ROW_BYTES == 32 || ROW_BYTES == 64 || ROW_BYTES == 128, "swizzle width");
+    constexpr uint64_t layout = ROW_BYTES == 128 ? 2 : (ROW_BYTES == 64 ? 4 : 6);
     uint64_t d = 0;
     d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);   // start address
     d |= static_cast<uint64_t>(1) << 16;                        // leading byte offset (unused)
-    d |= static_cast<uint64_t>(1024 >> 4) << 32;                // stride byte offset
+    d |= static_cast<uint64_t>((8 * ROW_BYTES) >> 4) << 32;     // stride byte offset
     d |= static_cast<uint64_t>(1) << 46;                        // version
-    d |= static_cast<uint64_t>(2) << 61;                        // 128-byte swizzle
+    d |= layout << 61;                                          // swizzle mode
     return d;
 }
 

@@ -385,6 +385,7 @@ __global__ void __launch_bounds__(COMBINE_THREADS)
         ws.l1_done[i] = 0u;
     }
     if (gtid == 0) {
+        ws.hdr[HDR_TILE_NEXT] = 0u;
         const uint32_t call = *reinterpret_cast<volatile uint32_t *>(ws.hdr + HDR_ERR_CALL);
         if (call != 0) {
             if (ws.hdr[HDR_ERR_STICKY] == 0)

@@ -31,9 +31,9 @@ struct moe_ctx {
     void *small_mem = nullptr;   // header + routing arrays (size depends on E, R only)
     void *big_mem = nullptr;     // table, pools, combine, staging (depends on max_tokens)
     size_t small_bytes = 0, big_bytes = 0;
-    uint8_t *w1 = nullptr;       // [E][2I][H] interleaved gate/up
+    uint8_t *w1 = nullptr;       // [E][2I/256][H/128][256][128] tiles, gate/up interleaved
     float *s1 = nullptr;         // [E][2I/128][H/128]
-    uint8_t *w2 = nullptr;       // [E][H][I]
+    uint8_t *w2 = nullptr;       // [E][H/256][I/128][256][128] tiles
     float *s2 = nullptr;         // [E][H/128][I/128]
     void *w_mem = nullptr;
     size_t w_bytes = 0;
@@ -305,13 +305,14 @@ int moe_load_weights(moe_handle_t h, const uint8_t *w_gate_up, const float *sf_g
         carve(static_cast<char *>(h->w_mem));
         h->w_bytes = bytes;
     }
-    if (launch_interleave_gate_up(w_gate_up, h->w1, d.E, d.I, d.H, s) != cudaSuccess)
+    if (launch_relayout_weights(w_gate_up, h->w1, d.E, 2 * d.I, d.H, d.I, s) != cudaSuccess ||
+        launch_relayout_weights(w_down, h->w2, d.E, d.H, d.I, 0, s) != cudaSuccess)
         return MOE_ERR_CUDA;
     CK(cudaMemcpyAsync(h->s1, sf_gate_up, ns1 * sizeof(float), cudaMemcpyDeviceToDevice, s));
-    CK(cudaMemcpyAsync(h->w2, w_down, n2, cudaMemcpyDeviceToDevice, s));
     CK(cudaMemcpyAsync(h->s2, sf_down, ns2 * sizeof(float), cudaMemcpyDeviceToDevice, s));
-    if (encode_tile_map(&h->maps.b1, h->w1, static_cast<uint64_t>(d.E) * 2 * d.I, d.H, BN) != MOE_OK ||
-        encode_tile_map(&h->maps.b2, h->w2, static_cast<uint64_t>(d.E) * d.H, d.I, BN) != MOE_OK)
+    // weight tiles as rows of 128 bytes: tile (e, nt, kb) starts at row ((e*NT + nt)*KB + kb)*256
+    if (encode_tile_map(&h->maps.b1, h->w1, n1 / 128, 128, BN) != MOE_OK ||
+        encode_tile_map(&h->maps.b2, h->w2, n2 / 128, 128, BN) != MOE_OK)
         return MOE_ERR_CUDA;
     h->have_weights = true;
     h->last_stream = s;

@@ -6,11 +6,12 @@
 // within an expert wave, all Linear1 tiles, then all Linear2 tiles; a Linear2 block waits
 // only for the Linear1 tiles of its own M-block):
 //   phase 1 tile (blk, nt):  A = gathered pool rows [P][H] e4m3 with 1x128 scales,
-//                            B = gate/up-interleaved W1 [E*2I][H] e4m3 with 128x128 scales;
+//                            B = gate/up-interleaved W1 tiles (contiguous 256 x 128-byte
+//                            blocks per 128-deep K block) e4m3 with 128x128 scales;
 //                            epilogue: SwiGLU, per-row 1x128 requant -> act [P][I], then
 //                            one release-increment of l1_done[blk] per epilogue warp.
 //   phase 2 tile (blk, nt):  producer first waits for l1_done[blk] == 8 * (2I/256), then
-//                            A = act [P][I] with scales, B = W2 [E*H][I] with 128x128 scales;
+//                            A = act [P][I] with scales, B = W2 tiles with 128x128 scales;
 //                            epilogue: times the top-k gate weight, bf16, scatter through the
 //                            {source, token, topk} metadata into combine[topk][T][H]
 //                            ("DeepGEMM Mega MoE 对称内存（Symmetric Memory）深度分析" §8.1).
@@ -218,10 +219,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                                                        : (part ? &maps.a2p : &maps.a2);
                     const CUtensorMap *tb = phase == 1 ? &maps.b1 : &maps.b2;
                     const int nkb = phase == 1 ? NKB1 : NKB2;
-                    const int brow = (phase == 1 ? e * 2 * d.I : e * d.H) + nt * BN;
+                    // weight tiles are contiguous [E][NT][KB][256][128]: this tile's K block
+                    // kb starts at row (tile0 + kb) * 256 of the 128-byte-wide tensor map
+                    const int tile0 = (e * (phase == 1 ? tl.NT1 : tl.NT2) + nt) * nkb;
                     for (int kb = 0; kb < PREFETCH_KB && kb < nkb; ++kb)
                         for (int j = 0; j < SUBS; ++j)
-                            ptx::tma_prefetch_l2_2d(tb, kb * BK + j * BKS, brow);
+                            ptx::tma_prefetch_l2_2d(tb, j * BKS, (tile0 + kb) * BN);
                     if (phase == 2) {
                         // the act rows of this block are complete once every epilogue warp
                         // of every gate_up tile of the block has released its stores
@@ -241,7 +244,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     for (int kb = 0; kb < nkb && ok; ++kb) {
                         if (kb + PREFETCH_KB < nkb)
                             for (int j = 0; j < SUBS; ++j)
-                                ptx::tma_prefetch_l2_2d(tb, (kb + PREFETCH_KB) * BK + j * BKS, brow);
+                                ptx::tma_prefetch_l2_2d(tb, j * BKS, (tile0 + kb + PREFETCH_KB) * BN);
                         for (int j = 0; j < SUBS; ++j, ++it) {
                             const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
                             if (!ptx::mbar_wait(&bars->empty[s], ph ^ 1u, deadline)) {
@@ -259,7 +262,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                             } else {
                                 ptx::tma_load_2d(sa, ta, &bars->full[s], kx, blk * BM, pol_a);
                             }
-                            ptx::tma_load_2d(sa + STAGE_A_BYTES, tb, &bars->full[s], kx, brow, pol_b);
+                            ptx::tma_load_2d(sa + STAGE_A_BYTES, tb, &bars->full[s], j * BKS,
+                                             (tile0 + kb) * BN, pol_b);
                         }
                     }
                 }

@@ -91,7 +91,7 @@ cudaError_t launch_dispatch(const Dims &d, const Workspace &ws, const CallArgs &
                             cudaStream_t s);
 constexpr int A_ROWS_PART = 32;   // row granularity of partial A-tile loads
 struct FfnMaps {
-    CUtensorMap a1, b1, a2, b2;   // pool x / W1 (gate_up), act / W2 (down); 128/256-row boxes
+    CUtensorMap a1, b1, a2, b2;   // pool x / W1 tiles (gate_up), act / W2 tiles (down)
     CUtensorMap a1p, a2p;         // pool x / act with 32-row boxes (partly filled M-blocks)
 };
 cudaError_t launch_ffn(const FfnMaps &maps, const Dims &d, const Workspace &ws, const CallArgs &c,
@@ -103,7 +103,7 @@ cudaError_t trace_clear();
 #endif
 cudaError_t launch_combine(const Dims &d, const Workspace &ws, const CallArgs &c, int num_sms,
                            cudaStream_t s);
-cudaError_t launch_interleave_gate_up(const uint8_t *src, uint8_t *dst, int E, int I, int H,
-                                      cudaStream_t s);
+cudaError_t launch_relayout_weights(const uint8_t *src, uint8_t *dst, int E, int N, int K, int gate_up_I,
+                                    cudaStream_t s);
 
 }  // namespace cpw

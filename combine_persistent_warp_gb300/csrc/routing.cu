@@ -4,7 +4,8 @@
 //                     into the expert-major FP8 pool (one cooperative persistent launch);
 //   combine_kernel  : top-k reduce of the weighted expert outputs into token order, then
 //                     the workspace reset for the next forward;
-//   interleave_kernel: gate/up row interleave of the gate_up weights (load time only).
+//   relayout_weights_kernel: load-time weight re-layout into contiguous GEMM tiles, with the
+//                     gate/up row interleave of the gate_up weights.
 //
 // Source pages, by title and section:
 //   "Mega-MoE 内核代码导读：从 Dispatch 到 WGMMA 的融合流水线" §4.1 (token x top-k scan),
@@ -404,33 +405,45 @@ cudaError_t launch_combine(const Dims &d, const Workspace &ws, const CallArgs &c
 }
 
 // ------------------------------------------------------------------ weights -------------
-// dst row n of expert e: within each group of 16 rows, rows 0..7 are gate rows 8j..8j+7 and
-// rows 8..15 are up rows I+8j..I+8j+7 (gate/up interleave with granularity 8, the layout
-// of "DeepGEMM Mega MoE 对称内存（Symmetric Memory）深度分析" §10.2), so one 256-row GEMM tile
-// holds 128 gate rows and the 128 matching up rows.
-__global__ void interleave_kernel(const uint8_t *__restrict__ src, uint8_t *__restrict__ dst, int E,
-                                  int I, int H)
+// Load-time weight re-layout into GEMM tiles.  dst = [E][N/256][K/128][256][128] bytes: every
+// 256-row x 128-byte tile the FFN kernel loads per 128-deep K block is one contiguous 32 KB
+// block, so each weight load streams whole DRAM pages instead of 256 rows 7 KB apart.
+// With gate_up_I > 0 (the gate_up weight, N = 2I) the rows are also gate/up interleaved:
+// within each group of 16 rows, rows 0..7 are gate rows 8j..8j+7 and rows 8..15 are up rows
+// I+8j..I+8j+7 (granularity 8, the layout of "DeepGEMM Mega MoE 对称内存（Symmetric Memory）
+// 深度分析" §10.2), so one 256-row tile holds 128 gate rows and the 128 matching up rows.
+__global__ void relayout_weights_kernel(const uint8_t *__restrict__ src, uint8_t *__restrict__ dst, int E,
+                                        int N, int K, int gate_up_I)
 {
-    const long long rows = static_cast<long long>(E) * 2 * I;
-    const int H16 = H / 16;
-    const int lane = threadIdx.x & 31;
-    for (long long rr = (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) >> 5; rr < rows;
-         rr += (static_cast<long long>(gridDim.x) * blockDim.x) >> 5) {
-        const long long e = rr / (2 * I);
-        const int n = static_cast<int>(rr % (2 * I));
-        const int j = n / 16, i = n % 16;
-        const int srow = i < 8 ? 8 * j + i : I + 8 * j + (i - 8);
-        const uint4 *s = reinterpret_cast<const uint4 *>(src + (e * 2 * I + srow) * static_cast<long long>(H));
-        uint4 *o = reinterpret_cast<uint4 *>(dst + rr * static_cast<long long>(H));
-        for (int q = lane; q < H16; q += 32)
-            o[q] = s[q];
+    const int KB = K / 128, NT = N / BN;
+    const long long chunks = static_cast<long long>(E) * N * (K / 16);
+    for (long long q = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; q < chunks;
+         q += static_cast<long long>(gridDim.x) * blockDim.x) {
+        long long t = q;
+        const int c16 = static_cast<int>(t % 8);
+        t /= 8;
+        const int r = static_cast<int>(t % BN);
+        t /= BN;
+        const int kb = static_cast<int>(t % KB);
+        t /= KB;
+        const int nt = static_cast<int>(t % NT);
+        const long long e = t / NT;
+        const int n = nt * BN + r;
+        int srow = n;
+        if (gate_up_I > 0) {
+            const int j = n / 16, i = n % 16;
+            srow = i < 8 ? 8 * j + i : gate_up_I + 8 * j + (i - 8);
+        }
+        const uint4 *sp = reinterpret_cast<const uint4 *>(src + (e * N + srow) * static_cast<long long>(K) +
+                                                          kb * 128 + c16 * 16);
+        reinterpret_cast<uint4 *>(dst)[q] = *sp;
     }
 }
 
-cudaError_t launch_interleave_gate_up(const uint8_t *src, uint8_t *dst, int E, int I, int H,
-                                      cudaStream_t s)
+cudaError_t launch_relayout_weights(const uint8_t *src, uint8_t *dst, int E, int N, int K, int gate_up_I,
+                                    cudaStream_t s)
 {
-    interleave_kernel<<<1024, 256, 0, s>>>(src, dst, E, I, H);
+    relayout_weights_kernel<<<2048, 256, 0, s>>>(src, dst, E, N, K, gate_up_I);
     return cudaGetLastError();
 }
 

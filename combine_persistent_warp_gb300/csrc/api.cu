@@ -49,6 +49,7 @@ struct moe_ctx {
     int last_T = 0;
     long long timeout_ns = 2000000000LL;
     int debug_skip_barrier = 0;
+    int ffn_mode = 0;            // 0 auto, 1 one CTA per tile, 2 two-CTA clusters
     // stage profiling (events on the forward's stream)
     bool profile = false;
     std::vector<cudaEvent_t> events;   // 4 per recorded forward
@@ -167,6 +168,14 @@ int wave_blocks(const moe_ctx *h)
     const long long per_block = static_cast<long long>(BM) * h->d.I;
     const long long half_l2 = 64ll << 20;
     return static_cast<int>(std::max(1ll, half_l2 / per_block));
+}
+
+// One CTA per tile by default (measured faster on GB300 for every workload shape tried);
+// MOE_OPT_FFN_MODE = 2 selects the 2-CTA cluster mode.
+bool ffn_paired(const moe_ctx *h, int T)
+{
+    (void)T;
+    return h->ffn_mode == 2;
 }
 
 int sync_last(moe_ctx *h)
@@ -312,7 +321,9 @@ int moe_load_weights(moe_handle_t h, const uint8_t *w_gate_up, const float *sf_g
     CK(cudaMemcpyAsync(h->s2, sf_down, ns2 * sizeof(float), cudaMemcpyDeviceToDevice, s));
     // weight tiles as rows of 128 bytes: tile (e, nt, kb) starts at row ((e*NT + nt)*KB + kb)*256
     if (encode_tile_map(&h->maps.b1, h->w1, n1 / 128, 128, BN) != MOE_OK ||
-        encode_tile_map(&h->maps.b2, h->w2, n2 / 128, 128, BN) != MOE_OK)
+        encode_tile_map(&h->maps.b2, h->w2, n2 / 128, 128, BN) != MOE_OK ||
+        encode_tile_map(&h->maps.b1h, h->w1, n1 / 128, 128, BN / 2) != MOE_OK ||
+        encode_tile_map(&h->maps.b2h, h->w2, n2 / 128, 128, BN / 2) != MOE_OK)
         return MOE_ERR_CUDA;
     h->have_weights = true;
     h->last_stream = s;
@@ -353,7 +364,8 @@ int moe_forward(moe_handle_t h, int T, const uint8_t *x, const float *x_sf, cons
     auto mark = [&](int i) { return ev ? cudaEventRecord(ev[i], s) : cudaSuccess; };
     if (mark(0) != cudaSuccess || launch_dispatch(h->d, h->ws, c, h->num_sms, s) != cudaSuccess ||
         mark(1) != cudaSuccess ||
-        launch_ffn(h->maps, h->d, h->ws, c, h->s1, h->s2, wave_blocks(h), h->num_sms, s) != cudaSuccess ||
+        launch_ffn(h->maps, h->d, h->ws, c, h->s1, h->s2, wave_blocks(h), h->num_sms, ffn_paired(h, T), s) !=
+            cudaSuccess ||
         mark(2) != cudaSuccess || launch_combine(h->d, h->ws, c, h->num_sms, s) != cudaSuccess ||
         mark(3) != cudaSuccess)
         return MOE_ERR_CUDA;
@@ -523,6 +535,11 @@ int moe_set_option(moe_handle_t h, int option, int64_t value)
         return MOE_OK;
     case MOE_OPT_DEBUG_SKIP_BARRIER:
         h->debug_skip_barrier = value != 0;
+        return MOE_OK;
+    case MOE_OPT_FFN_MODE:
+        if (value < 0 || value > 2)
+            return MOE_ERR_INVALID_ARG;
+        h->ffn_mode = static_cast<int>(value);
         return MOE_OK;
     default:
         return MOE_ERR_INVALID_ARG;

@@ -38,6 +38,8 @@
 // draining the copies and MMAs it has in flight.
 #include <cuda_bf16.h>
 
+#include <algorithm>
+
 #include "moe_internal.cuh"
 #include "ptx.cuh"
 
@@ -92,6 +94,7 @@ struct __align__(8) FfnBars {
     uint32_t tmem_base;
     int abort;
     float amax[2][2][BM];   // [tile parity][column half][row]
+    int32_t pair_off[1025]; // 2-CTA mode: first block pair of each expert (E <= 1024)
 };
 
 // Tile list: waves of `wave_blocks` M-blocks; inside a wave all phase-1 tiles (block-major,
@@ -123,6 +126,15 @@ struct TileList {
 
 }  // namespace
 
+// Tile of the list as one CTA sees it.  In 2-CTA mode a list entry is a pair of
+// consecutive M-blocks of one expert; CTA rank r takes the r-th block, and an expert with an
+// odd block count leaves rank 1 a null half (it only supplies its half of the weight tile).
+struct TileView {
+    int phase, nt, blk, e;
+    bool null_half;
+};
+
+template <bool PAIRED>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     ffn_kernel(const __grid_constant__ FfnMaps maps, const Dims d, const Workspace ws, const CallArgs c,
                const float *__restrict__ sf1, const float *__restrict__ sf2, const int wave_blocks)
@@ -140,7 +152,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         if (!err) {
             for (int s = 0; s < STAGES; ++s) {
                 ptx::mbar_init(&bars->full[s], 1);
-                ptx::mbar_init(&bars->empty[s], 1);
+                // 2-CTA mode: a stage is free once BOTH CTAs' MMAs have read it (each CTA's
+                // weight half is multicast into both)
+                ptx::mbar_init(&bars->empty[s], PAIRED ? 2 : 1);
             }
             for (int b = 0; b < 2; ++b) {
                 ptx::mbar_init(&bars->tfull[b], 1);
@@ -155,8 +169,30 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         }
     }
     __syncthreads();
-    if (bars->abort)
-        return;
+    uint32_t rank = 0;
+    if constexpr (PAIRED) {
+        // both CTAs' barriers are initialised before any multicast or remote arrive, and
+        // both take the same abort decision (a CTA must not leave while its peer may still
+        // write into its shared memory)
+        ptx::cluster_sync();
+        rank = ptx::cluster_ctarank();
+        const int peer_abort = ptx::ld_cluster_s32(ptx::map_cluster(&bars->abort, rank ^ 1u));
+        const bool stop = bars->abort || peer_abort;
+        ptx::cluster_sync();
+        if (stop)
+            return;
+        if (threadIdx.x == 0) {
+            int acc = 0;
+            for (int e = 0; e < d.E; ++e) {
+                bars->pair_off[e] = acc;
+                acc += (ws.blk_off[e + 1] - ws.blk_off[e] + 1) / 2;
+            }
+            bars->pair_off[d.E] = acc;
+        }
+    } else {
+        if (bars->abort)
+            return;
+    }
     if (warp == 1) {
         ptx::tmem_alloc(&bars->tmem_base, TMEM_COLS);
         ptx::tmem_relinquish();
@@ -166,8 +202,34 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     ptx::tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
 
-    const TileList tl{(2 * d.I) / BN, d.H / BN, ws.blk_off[d.E], wave_blocks};
+    const TileList tl{(2 * d.I) / BN, d.H / BN, PAIRED ? bars->pair_off[d.E] : ws.blk_off[d.E],
+                      PAIRED ? max(1, wave_blocks / 2) : wave_blocks};
     const int ntiles = tl.total();
+    const int nclusters = static_cast<int>(gridDim.x) / 2, cluster_id = static_cast<int>(blockIdx.x) / 2;
+    auto view = [&](int tile) {
+        TileView v;
+        int unit;
+        tl.at(tile, v.phase, unit, v.nt);
+        if (PAIRED) {
+            int lo = 0, hi = d.E - 1;          // expert of pair `unit`: last e with pair_off[e] <= unit
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (bars->pair_off[mid] <= unit)
+                    lo = mid;
+                else
+                    hi = mid - 1;
+            }
+            v.e = lo;
+            const int b = ws.blk_off[lo] + 2 * (unit - bars->pair_off[lo]) + static_cast<int>(rank);
+            v.null_half = b >= ws.blk_off[lo + 1];
+            v.blk = v.null_half ? b - 1 : b;
+        } else {
+            v.blk = unit;
+            v.e = ws.block_expert[unit];
+            v.null_half = false;
+        }
+        return v;
+    };
     const int NKB1 = d.H / BK, NKB2 = d.I / BK;
     const uint32_t l1_target = static_cast<uint32_t>(EPI_WARPS * tl.NT1);
     const uint64_t deadline = ptx::globaltimer() + static_cast<uint64_t>(c.timeout_ns);
@@ -188,13 +250,16 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 ptx::prefetch_tmap(&maps.a2);
                 ptx::prefetch_tmap(&maps.b2);
                 const uint64_t pol_a = ptx::policy_evict_last();
-                const uint64_t pol_b = ptx::policy_evict_first();
+                const uint64_t pol_b_once = ptx::policy_evict_first();    // read by one block
+                const uint64_t pol_b_shared = ptx::policy_evict_normal(); // read by several
                 uint32_t it = 0;
                 bool ok = true;
                 uint32_t tcount = 0;
                 while (ok) {
-                    // dynamic tile list: tiles are handed out in list order, one at a time
-                    const int tile = static_cast<int>(atomicAdd(ws.hdr + HDR_TILE_NEXT, 1u));
+                    // tiles are taken in list order: from the global counter (one CTA per tile),
+                    // or round-robin over clusters (2-CTA mode, both CTAs see the same list)
+                    const int tile = PAIRED ? cluster_id + static_cast<int>(tcount) * nclusters
+                                            : static_cast<int>(atomicAdd(ws.hdr + HDR_TILE_NEXT, 1u));
                     const uint32_t slot = tcount % TILE_RING, sph = (tcount / TILE_RING) & 1u;
                     if (!ptx::mbar_wait(&bars->tile_empty[slot], sph ^ 1u, deadline)) {
                         ok = false;
@@ -204,20 +269,23 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     ptx::mbar_arrive(&bars->tile_full[slot]);
                     if (tile >= ntiles)
                         break;
-                    int phase, blk, nt;
-                    tl.at(tile, phase, blk, nt);
+                    const TileView tv = view(tile);
+                    const int phase = tv.phase, blk = tv.blk, nt = tv.nt, e = tv.e;
                     CPW_STAMP(6, tcount);
                     ++tcount;
-                    const int e = ws.block_expert[blk];
+                    // an expert's weight tile is re-read by each of its M-blocks: keep it in L2
+                    // unless this block is the expert's only one
+                    const uint64_t pol_b = ws.blk_off[e + 1] - ws.blk_off[e] > 1 ? pol_b_shared : pol_b_once;
                     // A rows: a partly filled M-block loads only its 32-row groups that hold
                     // valid rows (the UMMA still reads 128 rows; the rest only feed padding
-                    // rows of the tile, which are never stored)
-                    const int n_part = (ws.block_rows[blk] + A_ROWS_PART - 1) / A_ROWS_PART;
+                    // rows of the tile, which are never stored); a null half loads no A
+                    const int n_part = tv.null_half ? 0 : (ws.block_rows[blk] + A_ROWS_PART - 1) / A_ROWS_PART;
                     const bool part = n_part < BM / A_ROWS_PART;
                     const uint32_t a_bytes = part ? n_part * A_ROWS_PART * BKS : STAGE_A_BYTES;
                     const CUtensorMap *ta = phase == 1 ? (part ? &maps.a1p : &maps.a1)
                                                        : (part ? &maps.a2p : &maps.a2);
-                    const CUtensorMap *tb = phase == 1 ? &maps.b1 : &maps.b2;
+                    const CUtensorMap *tb = PAIRED ? (phase == 1 ? &maps.b1h : &maps.b2h)
+                                                   : (phase == 1 ? &maps.b1 : &maps.b2);
                     const int nkb = phase == 1 ? NKB1 : NKB2;
                     // weight tiles are contiguous [E][NT][KB][256][128]: this tile's K block
                     // kb starts at row (tile0 + kb) * 256 of the 128-byte-wide tensor map
@@ -225,7 +293,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     for (int kb = 0; kb < PREFETCH_KB && kb < nkb; ++kb)
                         for (int j = 0; j < SUBS; ++j)
                             ptx::tma_prefetch_l2_2d(tb, j * BKS, (tile0 + kb) * BN);
-                    if (phase == 2) {
+                    if (phase == 2 && !tv.null_half) {
                         // the act rows of this block are complete once every epilogue warp
                         // of every gate_up tile of the block has released its stores
                         for (uint32_t i = 0;; ++i) {
@@ -262,8 +330,16 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                             } else {
                                 ptx::tma_load_2d(sa, ta, &bars->full[s], kx, blk * BM, pol_a);
                             }
-                            ptx::tma_load_2d(sa + STAGE_A_BYTES, tb, &bars->full[s], j * BKS,
-                                             (tile0 + kb) * BN, pol_b);
+                            if (PAIRED) {
+                                // this CTA's 128-row half of the weight tile, into both CTAs
+                                ptx::tma_load_2d_multicast(sa + STAGE_A_BYTES + rank * (BN / 2) * BKS, tb,
+                                                           &bars->full[s], j * BKS,
+                                                           (tile0 + kb) * BN + static_cast<int>(rank) * (BN / 2),
+                                                           static_cast<uint16_t>(0x3), pol_b);
+                            } else {
+                                ptx::tma_load_2d(sa + STAGE_A_BYTES, tb, &bars->full[s], j * BKS,
+                                                 (tile0 + kb) * BN, pol_b);
+                            }
                         }
                     }
                 }
@@ -290,9 +366,20 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     ++tcount;
                     if (tile < 0)
                         break;
-                    int phase, blk, nt;
-                    tl.at(tile, phase, blk, nt);
-                    const int nkb = phase == 1 ? NKB1 : NKB2;
+                    const TileView tv = view(tile);
+                    const int nkb = tv.phase == 1 ? NKB1 : NKB2;
+                    if (tv.null_half) {
+                        // no MMA: release each stage to both producers once it has landed
+                        for (int q = 0; q < nkb * SUBS && ok; ++q, ++it) {
+                            const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+                            if (!ptx::mbar_wait(&bars->full[s], ph, deadline)) {
+                                ok = false;
+                                break;
+                            }
+                            ptx::umma_commit_multicast(&bars->empty[s], static_cast<uint16_t>(0x3));
+                        }
+                        continue;
+                    }
                     for (int kb = 0; kb < nkb && ok; ++kb, ++pit) {
                         const uint32_t buf = pit & 1u, bph = (pit >> 1) & 1u;
                         if (!ptx::mbar_wait(&bars->tempty[buf], bph ^ 1u, deadline)) {
@@ -316,7 +403,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                             for (int k = 0; k < BKS / 32; ++k)   // +32 bytes along K = +2 in the >>4 field
                                 ptx::umma_f8(dt, adesc + 2 * k, bdesc + 2 * k, IDESC,
                                              (j > 0 || k > 0) ? 1u : 0u);
-                            ptx::umma_commit(&bars->empty[s]);
+                            if (PAIRED)
+                                ptx::umma_commit_multicast(&bars->empty[s], static_cast<uint16_t>(0x3));
+                            else
+                                ptx::umma_commit(&bars->empty[s]);
                             CPW_STAMP(2, it);
                         }
                         if (!ok)
@@ -356,9 +446,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             ++tcount;
             if (tile < 0)
                 break;
-            int phase, blk, nt;
-            tl.at(tile, phase, blk, nt);
-            const int e = ws.block_expert[blk];
+            const TileView tv = view(tile);
+            if (tv.null_half)
+                continue;   // no rows of this CTA in this tile
+            const int phase = tv.phase, blk = tv.blk, nt = tv.nt, e = tv.e;
             const int nkb = phase == 1 ? NKB1 : NKB2;
             const long long prow = static_cast<long long>(blk) * BM + row;
             const float *sfa = (phase == 1 ? ws.pool_sf : ws.act_sf) + prow;
@@ -522,6 +613,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 
     ptx::tc_fence_before();
     __syncthreads();
+    if constexpr (PAIRED)
+        ptx::cluster_sync();   // no multicast into this CTA's shared memory is still in flight
 #ifdef CPW_TRACE
     if (threadIdx.x == 0 && blockIdx.x < TRACE_MAX_GRID)
         g_cta_span[1][blockIdx.x] = ptx::globaltimer();
@@ -550,15 +643,18 @@ cudaError_t trace_clear()
 #endif
 
 cudaError_t launch_ffn(const FfnMaps &maps, const Dims &d, const Workspace &ws, const CallArgs &c,
-                       const float *sf1, const float *sf2, int wave_blocks, int num_sms, cudaStream_t s)
+                       const float *sf1, const float *sf2, int wave_blocks, int num_sms, bool paired,
+                       cudaStream_t s)
 {
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(ffn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             GEMM_SMEM_BYTES);
+    static bool configured[2] = {false, false};
+    static int paired_grid = 0;
+    static int paired_coop = 1;   // cooperative attribute accepted together with clusters
+    void *kern = paired ? reinterpret_cast<void *>(ffn_kernel<true>) : reinterpret_cast<void *>(ffn_kernel<false>);
+    if (!configured[paired]) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM_BYTES);
         if (e != cudaSuccess)
             return e;
-        configured = true;
+        configured[paired] = true;
     }
     FfnMaps m = maps;
     Dims dd = d;
@@ -568,10 +664,44 @@ cudaError_t launch_ffn(const FfnMaps &maps, const Dims &d, const Workspace &ws, 
     const float *p2 = sf2;
     int wb = wave_blocks;
     void *args[] = {&m, &dd, &ww, &cc, &p1, &p2, &wb};
-    // cooperative: phase-2 tiles wait on phase-1 tiles of other CTAs, so all CTAs must be
-    // resident at once
-    return cudaLaunchCooperativeKernel(reinterpret_cast<void *>(ffn_kernel), dim3(num_sms),
-                                       dim3(GEMM_THREADS), args, GEMM_SMEM_BYTES, s);
+    // phase-2 tiles wait on phase-1 tiles of other CTAs, so all CTAs must be resident at once
+    if (!paired)
+        return cudaLaunchCooperativeKernel(kern, dim3(num_sms), dim3(GEMM_THREADS), args, GEMM_SMEM_BYTES, s);
+
+    cudaLaunchAttribute attrs[2];
+    attrs[0].id = cudaLaunchAttributeClusterDimension;
+    attrs[0].val.clusterDim.x = 2;
+    attrs[0].val.clusterDim.y = 1;
+    attrs[0].val.clusterDim.z = 1;
+    attrs[1].id = cudaLaunchAttributeCooperative;
+    attrs[1].val.cooperative = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(GEMM_THREADS);
+    cfg.dynamicSmemBytes = GEMM_SMEM_BYTES;
+    cfg.stream = s;
+    cfg.attrs = attrs;
+    if (paired_grid == 0) {
+        // every cluster resident at once: as many clusters as can be active together
+        cfg.gridDim = dim3(num_sms);
+        cfg.numAttrs = 1;
+        int clusters = 0;
+        cudaError_t e = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
+        if (e != cudaSuccess)
+            return e;
+        if (clusters < 1)
+            return cudaErrorInvalidConfiguration;
+        paired_grid = 2 * std::min(clusters, num_sms / 2);
+    }
+    cfg.gridDim = dim3(paired_grid);
+    if (paired_coop) {
+        cfg.numAttrs = 2;
+        if (cudaLaunchKernelExC(&cfg, kern, args) == cudaSuccess)
+            return cudaSuccess;
+        cudaGetLastError();   // this runtime rejects cooperative + cluster: clusters alone
+        paired_coop = 0;
+    }
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelExC(&cfg, kern, args);
 }
 
 }  // namespace cpw

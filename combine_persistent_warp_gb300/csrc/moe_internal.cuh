@@ -26,7 +26,7 @@ static_assert(BKS == 32 || BKS == 64 || BKS == 128, "stage depth must match a sw
 constexpr int STAGE_A_BYTES = BM * BKS;                // 16 KB at BKS = 128
 constexpr int STAGE_B_BYTES = BN * BKS;                // 32 KB at BKS = 128
 constexpr int STAGE_BYTES = STAGE_A_BYTES + STAGE_B_BYTES;
-constexpr int GEMM_SMEM_BYTES = 1024 /*align slack*/ + STAGES * STAGE_BYTES + 4096 /*bars etc*/;
+constexpr int GEMM_SMEM_BYTES = 1024 /*align slack*/ + STAGES * STAGE_BYTES + 8192 /*bars etc*/;
 
 // 32-bit words of the workspace header; hot words sit on separate 128-byte lines.
 enum HdrWord : int {
@@ -93,9 +93,12 @@ constexpr int A_ROWS_PART = 32;   // row granularity of partial A-tile loads
 struct FfnMaps {
     CUtensorMap a1, b1, a2, b2;   // pool x / W1 tiles (gate_up), act / W2 tiles (down)
     CUtensorMap a1p, a2p;         // pool x / act with 32-row boxes (partly filled M-blocks)
+    CUtensorMap b1h, b2h;         // W1 / W2 tiles with 128-row boxes (half tiles, 2-CTA mode)
 };
+// paired: 2-CTA clusters sharing each weight tile by TMA multicast (shapes with several
+// M-blocks per expert); otherwise one CTA per tile with a dynamic tile counter.
 cudaError_t launch_ffn(const FfnMaps &maps, const Dims &d, const Workspace &ws, const CallArgs &c,
-                       const float *sf1, const float *sf2, int wave_blocks, int num_sms,
+                       const float *sf1, const float *sf2, int wave_blocks, int num_sms, bool paired,
                        cudaStream_t s);
 #ifdef CPW_TRACE
 cudaError_t trace_read(void *dst, size_t bytes);

@@ -25,6 +25,7 @@ STATUS = {
 BUFFERS = {"pool_x": 0, "pool_sf": 1, "act": 2, "act_sf": 3, "combine": 4, "table": 5}
 OPT_TIMEOUT_NS = 0
 OPT_DEBUG_SKIP_BARRIER = 1
+OPT_FFN_MODE = 2
 
 
 class MoeError(RuntimeError):

@@ -141,8 +141,11 @@ int moe_get_info(moe_handle_t h, moe_info *info);
 /* Options.  MOE_OPT_TIMEOUT_NS: time limit of every device-side wait (default 2e9 ns);
  * MOE_OPT_DEBUG_SKIP_BARRIER: when 1, one CTA of the routing kernel skips its arrival
  * at the grid barrier, so the others give up after the time limit and the forward
- * ends with MOE_ERR_TIMEOUT (failure-path test; never on in normal use). */
-enum moe_option { MOE_OPT_TIMEOUT_NS = 0, MOE_OPT_DEBUG_SKIP_BARRIER = 1 };
+ * ends with MOE_ERR_TIMEOUT (failure-path test; never on in normal use);
+ * MOE_OPT_FFN_MODE: how the expert FFN kernel covers its tiles: 0 = automatic (default),
+ * 1 = one CTA per 128-row tile, 2 = pairs of CTAs on two M-blocks of one expert sharing
+ * each weight tile through cluster multicast.  All modes compute the same result. */
+enum moe_option { MOE_OPT_TIMEOUT_NS = 0, MOE_OPT_DEBUG_SKIP_BARRIER = 1, MOE_OPT_FFN_MODE = 2 };
 int moe_set_option(moe_handle_t h, int option, int64_t value);
 
 /* Stage timing with CUDA events recorded on the forward's own stream.  While enabled,

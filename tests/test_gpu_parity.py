@@ -261,3 +261,29 @@ def test_barrier_timeout_is_reported_then_recovers():
     moe.set_option(native.OPT_DEBUG_SKIP_BARRIER, 0)
     moe.set_option(native.OPT_TIMEOUT_NS, 2_000_000_000)
     run_and_compare(moe, inp, inp.topk_idx, inp.topk_w, 64)
+
+
+# ----------------------------------------------------------------- FFN kernel modes -----
+def test_ffn_modes_agree_and_match_oracle():
+    """One CTA per tile vs. 2-CTA clusters sharing weight tiles by multicast: same bits,
+    within tolerance of the oracle, including experts with an odd M-block count (the
+    second CTA of their last pair has no rows and only supplies its weight half)."""
+    T = 1024
+    moe, inp = tiny_layer(T_max=T, E=8, H=256, I=256, k=2, R=2, seed=33)
+    counts, _, _ = oracle.route_counts(inp.topk_idx, 8, 2)
+    blocks = -(-counts.astype(np.int64) // 128)
+    assert np.any(blocks % 2 == 1) and np.any(blocks >= 2)
+    outs = []
+    for mode in (1, 2):
+        moe.set_option(native.OPT_FFN_MODE, mode)
+        out, _ = run_and_compare(moe, inp, inp.topk_idx, inp.topk_w, T)
+        outs.append(out.clone())
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+
+
+def test_paired_mode_with_single_block_experts():
+    """2-CTA mode forced on a batch where every expert has one M-block: every pair has a
+    null half."""
+    moe, inp = tiny_layer()
+    moe.set_option(native.OPT_FFN_MODE, 2)
+    run_and_compare(moe, inp, inp.topk_idx, inp.topk_w, 64)

@@ -284,6 +284,9 @@ def run_ours(args, dist: Dist) -> dict | None:
     M = model["M"]
     moe = FusedMoE(wl.E, wl.H, wl.I, wl.topk, wl.R).reserve(wl.T)
     moe.load_weights(inp.w_gate_up, inp.sf_gate_up, inp.w_down, inp.sf_down)
+    if args.ffn_mode:
+        from combine_persistent_warp_gb300 import native
+        moe.set_option(native.OPT_FFN_MODE, args.ffn_mode)
     out = torch.empty(wl.T, wl.H, dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream(dev)
 
@@ -442,6 +445,8 @@ def main(argv=None):
     ap.add_argument("--cpu-tokens", type=int, default=128)
     ap.add_argument("--ref-budget-s", type=float, default=120.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ffn-mode", type=int, default=0,
+                    help="expert FFN kernel mode: 0 automatic, 1 one CTA per tile, 2 CTA pairs")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -543,14 +543,21 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 // SwiGLU on the 64 (gate, up) pairs of this thread's row and column half,
                 // then 1x128 requant of the row's 128 outputs of this n-tile (the two
                 // column halves exchange their absolute maxima through shared memory).
+                // This tail runs once per tile while the UMMA pipe waits for the next
+                // tile's first promotions, so it is kept short: fast exp and reciprocal,
+                // one multiply per code, and warps whose 32 rows are all padding of a
+                // partly filled block skip it (they only take part in the exchange).
+                const bool live = q * 32 < ws.block_rows[blk];
                 float amax = 0.0f;
+                if (live) {
 #pragma unroll
-                for (int m = 0; m < 64; ++m) {
-                    const float g = acc[(m >> 3) * 16 + (m & 7)];
-                    const float u = acc[(m >> 3) * 16 + 8 + (m & 7)];
-                    const float hval = g / (1.0f + expf(-g)) * u;
-                    acc[m] = hval;   // acc[m] is no longer needed as a gate/up input
-                    amax = fmaxf(amax, fabsf(hval));
+                    for (int m = 0; m < 64; ++m) {
+                        const float g = acc[(m >> 3) * 16 + (m & 7)];
+                        const float u = acc[(m >> 3) * 16 + 8 + (m & 7)];
+                        const float hval = __fdividef(g, 1.0f + __expf(-g)) * u;
+                        acc[m] = hval;   // acc[m] is no longer needed as a gate/up input
+                        amax = fmaxf(amax, fabsf(hval));
+                    }
                 }
                 // slots of this tile's parity, behind a bounded mbarrier (a slot is rewritten
                 // two phase-1 tiles later, after every thread has read it)
@@ -562,30 +569,32 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     ok = false;
                     break;
                 }
-                amax = fmaxf(bars->amax[tp][0][row], bars->amax[tp][1][row]);
-                const float sf = fmaxf(amax, 1e-4f) / 448.0f;
-                uint4 *dst = reinterpret_cast<uint4 *>(ws.act + prow * d.I + nt * 128 + wg * 64);
+                if (live) {
+                    amax = fmaxf(fmaxf(bars->amax[tp][0][row], bars->amax[tp][1][row]), 1e-4f);
+                    const float sf = amax / 448.0f;
+                    const float inv = 448.0f / amax;
+                    uint4 *dst = reinterpret_cast<uint4 *>(ws.act + prow * d.I + nt * 128 + wg * 64);
 #pragma unroll
-                for (int v = 0; v < 4; ++v) {
-                    uint32_t w4[4];
+                    for (int v = 0; v < 4; ++v) {
+                        uint32_t w4[4];
 #pragma unroll
-                    for (int p = 0; p < 4; ++p) {
-                        const int m = v * 16 + p * 4;
-                        const uint32_t lo = ptx::cvt_e4m3x2(__fdiv_rn(acc[m], sf), __fdiv_rn(acc[m + 1], sf));
-                        const uint32_t hi = ptx::cvt_e4m3x2(__fdiv_rn(acc[m + 2], sf), __fdiv_rn(acc[m + 3], sf));
-                        w4[p] = lo | (hi << 16);
+                        for (int p = 0; p < 4; ++p) {
+                            const int m = v * 16 + p * 4;
+                            const uint32_t lo = ptx::cvt_e4m3x2(acc[m] * inv, acc[m + 1] * inv);
+                            const uint32_t hi = ptx::cvt_e4m3x2(acc[m + 2] * inv, acc[m + 3] * inv);
+                            w4[p] = lo | (hi << 16);
+                        }
+                        dst[v] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
                     }
-                    dst[v] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                    if (wg == 0)
+                        ws.act_sf[static_cast<long long>(nt) * ws.P + prow] = sf;
                 }
-                if (wg == 0)
-                    ws.act_sf[static_cast<long long>(nt) * ws.P + prow] = sf;
-                // publish: this warp's part of the block's act rows is written
+                // publish: this warp's part of the block's act rows is written (the warp
+                // barrier orders every lane's stores before lane 0's release)
                 __syncwarp();
                 ptx::fence_proxy_async_global();
-                if (lane == 0) {
-                    __threadfence();
+                if (lane == 0)
                     ptx::red_release_add(ws.l1_done + blk, 1u);
-                }
             } else {
                 if (row < ws.block_rows[blk]) {
                     const uint32_t t = ws.meta[prow * 3 + 1];

@@ -34,6 +34,12 @@
 // and the epilogue warps promote it into fp32 registers with the product of the two scales
 // (the promotion of the first page, §8.1), overlapped with the next block's UMMA through
 // the TMEM full/empty barriers.
+// 2-CTA mode (clusters of two CTAs on neighbouring SMs): one cta_group::2 UMMA of
+// 256 x 256 x 32 covers two M-blocks of one expert; each CTA stages its own 128 A rows and
+// one 128-row half of the weight tile (32 KB per stage, six stages), the even CTA issues
+// the UMMAs and each CTA's epilogue promotes the 128 rows in its own TMEM.  Per FLOP this
+// moves a third fewer operand bytes from L2 than the one-CTA tile; tiles are dealt to the
+// clusters round-robin in list order.
 // All waits carry a deadline; on expiry the CTA records MOE_ERR_TIMEOUT and leaves after
 // draining the copies and MMAs it has in flight.
 #include <cuda_bf16.h>
@@ -55,6 +61,15 @@ constexpr uint32_t IDESC = ptx::idesc_e4m3_f32(BM, BN);
 constexpr int PREFETCH_KB = CPW_PREFETCH_KB;   // L2 prefetch distance of B, in scale blocks
 constexpr int EPI_WARPS = 8;
 constexpr int TILE_RING = 4;   // tiles the producer may run ahead of the UMMA/epilogue warps
+// Two-CTA mode (cta_group::2): one UMMA of M = 256 rows covers two M-blocks, one in each
+// CTA of a cluster pair; each CTA stages its own 128 A rows and one half (128 rows) of the
+// 256-row weight tile, so a stage is 32 KB instead of 48 KB and the same 192 KB holds six.
+constexpr uint32_t PAIR_B_BYTES = STAGE_B_BYTES / 2;
+constexpr uint32_t PAIR_STAGE_BYTES = STAGE_A_BYTES + PAIR_B_BYTES;
+constexpr int PAIR_STAGES = static_cast<int>((STAGES * STAGE_BYTES) / PAIR_STAGE_BYTES);
+constexpr int MAX_STAGES = PAIR_STAGES > STAGES ? PAIR_STAGES : STAGES;
+constexpr uint32_t IDESC_PAIR = ptx::idesc_e4m3_f32(2 * BM, BN);
+static_assert(PAIR_STAGES * PAIR_STAGE_BYTES <= STAGES * STAGE_BYTES, "pair stages exceed the ring");
 
 #ifdef CPW_TRACE
 // Development trace (compiled only with -DCPW_TRACE): SM clock stamps of two CTAs, per
@@ -83,8 +98,8 @@ __device__ __forceinline__ int trace_slot()
 #endif
 
 struct __align__(8) FfnBars {
-    uint64_t full[STAGES];
-    uint64_t empty[STAGES];
+    uint64_t full[MAX_STAGES];
+    uint64_t empty[MAX_STAGES];
     uint64_t tfull[2];
     uint64_t tempty[2];
     uint64_t xbar;          // row-amax exchange between the two epilogue warpgroups
@@ -127,8 +142,9 @@ struct TileList {
 }  // namespace
 
 // Tile of the list as one CTA sees it.  In 2-CTA mode a list entry is a pair of
-// consecutive M-blocks of one expert; CTA rank r takes the r-th block, and an expert with an
-// odd block count leaves rank 1 a null half (it only supplies its half of the weight tile).
+// consecutive M-blocks of one expert (one M = 256 UMMA tile); CTA rank r takes the r-th
+// block, and an expert with an odd block count leaves rank 1 a null half (it loads no A
+// rows, only its half of the weight tile, and stores nothing).
 struct TileView {
     int phase, nt, blk, e;
     bool null_half;
@@ -143,6 +159,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
     FfnBars *bars = reinterpret_cast<FfnBars *>(smem + STAGES * STAGE_BYTES);
+    constexpr int NST = PAIRED ? PAIR_STAGES : STAGES;                  // stages in the ring
+    constexpr uint32_t SBYTES = PAIRED ? PAIR_STAGE_BYTES : STAGE_BYTES;   // bytes per stage
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
@@ -150,15 +168,16 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                              *reinterpret_cast<volatile uint32_t *>(ws.hdr + HDR_ERR_STICKY);
         bars->abort = err != 0;
         if (!err) {
-            for (int s = 0; s < STAGES; ++s) {
+            // 2-CTA mode: only the even CTA's full and TMEM-empty barriers are used; both
+            // CTAs' loads count on its full barrier, both CTAs' epilogue warps arrive on its
+            // TMEM-empty barrier, and its UMMA commits arrive on both CTAs' empty / TMEM-full
+            for (int s = 0; s < NST; ++s) {
                 ptx::mbar_init(&bars->full[s], 1);
-                // 2-CTA mode: a stage is free once BOTH CTAs' MMAs have read it (each CTA's
-                // weight half is multicast into both)
-                ptx::mbar_init(&bars->empty[s], PAIRED ? 2 : 1);
+                ptx::mbar_init(&bars->empty[s], 1);
             }
             for (int b = 0; b < 2; ++b) {
                 ptx::mbar_init(&bars->tfull[b], 1);
-                ptx::mbar_init(&bars->tempty[b], EPI_WARPS);   // one arrival per epilogue warp
+                ptx::mbar_init(&bars->tempty[b], (PAIRED ? 2 : 1) * EPI_WARPS);   // one per epilogue warp
             }
             ptx::mbar_init(&bars->xbar, 32 * EPI_WARPS);       // every epilogue thread
             for (int i = 0; i < TILE_RING; ++i) {
@@ -171,7 +190,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     __syncthreads();
     uint32_t rank = 0;
     if constexpr (PAIRED) {
-        // both CTAs' barriers are initialised before any multicast or remote arrive, and
+        // both CTAs' barriers are initialised before any remote load, commit or arrive, and
         // both take the same abort decision (a CTA must not leave while its peer may still
         // write into its shared memory)
         ptx::cluster_sync();
@@ -194,11 +213,18 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             return;
     }
     if (warp == 1) {
-        ptx::tmem_alloc(&bars->tmem_base, TMEM_COLS);
-        ptx::tmem_relinquish();
+        if constexpr (PAIRED) {
+            ptx::tmem_alloc_pair(&bars->tmem_base, TMEM_COLS);
+            ptx::tmem_relinquish_pair();
+        } else {
+            ptx::tmem_alloc(&bars->tmem_base, TMEM_COLS);
+            ptx::tmem_relinquish();
+        }
     }
     ptx::tc_fence_before();
     __syncthreads();
+    if constexpr (PAIRED)
+        ptx::cluster_sync();   // both CTAs hold their TMEM before the even CTA's first UMMA
     ptx::tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
 
@@ -206,7 +232,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                       PAIRED ? max(1, wave_blocks / 2) : wave_blocks};
     const int ntiles = tl.total();
     const int nclusters = static_cast<int>(gridDim.x) / 2, cluster_id = static_cast<int>(blockIdx.x) / 2;
-    auto view = [&](int tile) {
+    auto view_of = [&](int tile, uint32_t r) {
         TileView v;
         int unit;
         tl.at(tile, v.phase, unit, v.nt);
@@ -220,7 +246,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     hi = mid - 1;
             }
             v.e = lo;
-            const int b = ws.blk_off[lo] + 2 * (unit - bars->pair_off[lo]) + static_cast<int>(rank);
+            const int b = ws.blk_off[lo] + 2 * (unit - bars->pair_off[lo]) + static_cast<int>(r);
             v.null_half = b >= ws.blk_off[lo + 1];
             v.blk = v.null_half ? b - 1 : b;
         } else {
@@ -229,6 +255,16 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             v.null_half = false;
         }
         return v;
+    };
+    auto view = [&](int tile) { return view_of(tile, rank); };
+    // A bytes a CTA stages per K slice for a tile: a partly filled M-block loads only its
+    // 32-row groups that hold valid rows (the UMMA still reads 128 rows; the rest only feed
+    // padding rows of the tile, which are never stored); a null half loads no A
+    auto a_parts = [&](const TileView &v) {
+        return v.null_half ? 0 : (ws.block_rows[v.blk] + A_ROWS_PART - 1) / A_ROWS_PART;
+    };
+    auto a_stage_bytes = [&](int n_part) {
+        return n_part < BM / A_ROWS_PART ? static_cast<uint32_t>(n_part * A_ROWS_PART * BKS) : STAGE_A_BYTES;
     };
     const int NKB1 = d.H / BK, NKB2 = d.I / BK;
     const uint32_t l1_target = static_cast<uint32_t>(EPI_WARPS * tl.NT1);
@@ -276,12 +312,14 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     // an expert's weight tile is re-read by each of its M-blocks: keep it in L2
                     // unless this block is the expert's only one
                     const uint64_t pol_b = ws.blk_off[e + 1] - ws.blk_off[e] > 1 ? pol_b_shared : pol_b_once;
-                    // A rows: a partly filled M-block loads only its 32-row groups that hold
-                    // valid rows (the UMMA still reads 128 rows; the rest only feed padding
-                    // rows of the tile, which are never stored); a null half loads no A
-                    const int n_part = tv.null_half ? 0 : (ws.block_rows[blk] + A_ROWS_PART - 1) / A_ROWS_PART;
+                    const int n_part = a_parts(tv);
                     const bool part = n_part < BM / A_ROWS_PART;
-                    const uint32_t a_bytes = part ? n_part * A_ROWS_PART * BKS : STAGE_A_BYTES;
+                    const uint32_t a_bytes = a_stage_bytes(n_part);
+                    // bytes the stage's full barrier waits for: this CTA's, plus (2-CTA mode,
+                    // even CTA) the odd CTA's, whose loads count on the even CTA's barrier
+                    uint32_t tx_bytes = a_bytes + (PAIRED ? PAIR_B_BYTES : STAGE_B_BYTES);
+                    if (PAIRED && rank == 0)
+                        tx_bytes += a_stage_bytes(a_parts(view_of(tile, 1))) + PAIR_B_BYTES;
                     const CUtensorMap *ta = phase == 1 ? (part ? &maps.a1p : &maps.a1)
                                                        : (part ? &maps.a2p : &maps.a2);
                     const CUtensorMap *tb = PAIRED ? (phase == 1 ? &maps.b1h : &maps.b2h)
@@ -314,29 +352,37 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                             for (int j = 0; j < SUBS; ++j)
                                 ptx::tma_prefetch_l2_2d(tb, j * BKS, (tile0 + kb + PREFETCH_KB) * BN);
                         for (int j = 0; j < SUBS; ++j, ++it) {
-                            const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+                            const uint32_t s = it % NST, ph = (it / NST) & 1u;
                             if (!ptx::mbar_wait(&bars->empty[s], ph ^ 1u, deadline)) {
                                 ok = false;
                                 break;
                             }
-                            uint8_t *sa = smem + s * STAGE_BYTES;
+                            uint8_t *sa = smem + s * SBYTES;
                             CPW_STAMP(0, it);
                             const int kx = kb * BK + j * BKS;
-                            ptx::mbar_arrive_expect_tx(&bars->full[s], a_bytes + STAGE_B_BYTES);
-                            if (part) {
-                                for (int g = 0; g < n_part; ++g)
-                                    ptx::tma_load_2d(sa + g * A_ROWS_PART * BKS, ta, &bars->full[s], kx,
-                                                     blk * BM + g * A_ROWS_PART, pol_a);
+                            if (!PAIRED || rank == 0)
+                                ptx::mbar_arrive_expect_tx(&bars->full[s], tx_bytes);
+                            if constexpr (PAIRED) {
+                                // own A rows and own half of the weight tile, counted on the
+                                // even CTA's full barrier
+                                const uint32_t fb = ptx::map_cluster(&bars->full[s], 0);
+                                if (part) {
+                                    for (int g = 0; g < n_part; ++g)
+                                        ptx::tma_load_2d_pair(sa + g * A_ROWS_PART * BKS, ta, fb, kx,
+                                                              blk * BM + g * A_ROWS_PART, pol_a);
+                                } else {
+                                    ptx::tma_load_2d_pair(sa, ta, fb, kx, blk * BM, pol_a);
+                                }
+                                ptx::tma_load_2d_pair(sa + STAGE_A_BYTES, tb, fb, j * BKS,
+                                                      (tile0 + kb) * BN + static_cast<int>(rank) * (BN / 2), pol_b);
                             } else {
-                                ptx::tma_load_2d(sa, ta, &bars->full[s], kx, blk * BM, pol_a);
-                            }
-                            if (PAIRED) {
-                                // this CTA's 128-row half of the weight tile, into both CTAs
-                                ptx::tma_load_2d_multicast(sa + STAGE_A_BYTES + rank * (BN / 2) * BKS, tb,
-                                                           &bars->full[s], j * BKS,
-                                                           (tile0 + kb) * BN + static_cast<int>(rank) * (BN / 2),
-                                                           static_cast<uint16_t>(0x3), pol_b);
-                            } else {
+                                if (part) {
+                                    for (int g = 0; g < n_part; ++g)
+                                        ptx::tma_load_2d(sa + g * A_ROWS_PART * BKS, ta, &bars->full[s], kx,
+                                                         blk * BM + g * A_ROWS_PART, pol_a);
+                                } else {
+                                    ptx::tma_load_2d(sa, ta, &bars->full[s], kx, blk * BM, pol_a);
+                                }
                                 ptx::tma_load_2d(sa + STAGE_A_BYTES, tb, &bars->full[s], j * BKS,
                                                  (tile0 + kb) * BN, pol_b);
                             }
@@ -345,16 +391,20 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 }
                 if (!ok)
                     record_error(ws.hdr, DEV_TIMEOUT);
-                // drain: every issued load has landed before the CTA may exit
+                // drain: every issued load has landed before the CTA may exit (2-CTA mode:
+                // has been consumed by the UMMA, whose commit reaches both CTAs)
                 const uint64_t dl = ptx::globaltimer() + static_cast<uint64_t>(c.timeout_ns);
-                for (uint32_t i = it > STAGES ? it - STAGES : 0; i < it; ++i)
-                    ptx::mbar_wait(&bars->full[i % STAGES], (i / STAGES) & 1u, dl);
+                for (uint32_t i = it > NST ? it - NST : 0; i < it; ++i)
+                    ptx::mbar_wait(PAIRED ? &bars->empty[i % NST] : &bars->full[i % NST], (i / NST) & 1u, dl);
             }
         } else if (warp == 1) {
             // -------------------------------------------------------- UMMA issuer -----
+            // (2-CTA mode: the even CTA issues every UMMA of the pair; the odd CTA's issuer
+            // only takes its tile slots)
             if (lane == 0) {
                 uint32_t it = 0, pit = 0, tcount = 0;
                 bool ok = true;
+                const bool issuer = !PAIRED || rank == 0;
                 while (ok) {
                     const uint32_t slot = tcount % TILE_RING, sph = (tcount / TILE_RING) & 1u;
                     if (!ptx::mbar_wait(&bars->tile_full[slot], sph, deadline)) {
@@ -366,20 +416,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     ++tcount;
                     if (tile < 0)
                         break;
+                    if (!issuer)
+                        continue;
                     const TileView tv = view(tile);
                     const int nkb = tv.phase == 1 ? NKB1 : NKB2;
-                    if (tv.null_half) {
-                        // no MMA: release each stage to both producers once it has landed
-                        for (int q = 0; q < nkb * SUBS && ok; ++q, ++it) {
-                            const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
-                            if (!ptx::mbar_wait(&bars->full[s], ph, deadline)) {
-                                ok = false;
-                                break;
-                            }
-                            ptx::umma_commit_multicast(&bars->empty[s], static_cast<uint16_t>(0x3));
-                        }
-                        continue;
-                    }
                     for (int kb = 0; kb < nkb && ok; ++kb, ++pit) {
                         const uint32_t buf = pit & 1u, bph = (pit >> 1) & 1u;
                         if (!ptx::mbar_wait(&bars->tempty[buf], bph ^ 1u, deadline)) {
@@ -389,29 +429,37 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                         const uint32_t dt = tmem + buf * BN;
                         // the SUBS stages of one scale block accumulate into one TMEM partial
                         for (int j = 0; j < SUBS; ++j, ++it) {
-                            const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+                            const uint32_t s = it % NST, ph = (it / NST) & 1u;
                             if (!ptx::mbar_wait(&bars->full[s], ph, deadline)) {
                                 ok = false;
                                 break;
                             }
                             CPW_STAMP(1, it);
                             ptx::tc_fence_after();
-                            const uint32_t a_addr = ptx::smem_u32(smem + s * STAGE_BYTES);
+                            const uint32_t a_addr = ptx::smem_u32(smem + s * SBYTES);
                             const uint64_t adesc = ptx::kmajor_swizzled_desc<BKS>(a_addr);
                             const uint64_t bdesc = ptx::kmajor_swizzled_desc<BKS>(a_addr + STAGE_A_BYTES);
 #pragma unroll
-                            for (int k = 0; k < BKS / 32; ++k)   // +32 bytes along K = +2 in the >>4 field
-                                ptx::umma_f8(dt, adesc + 2 * k, bdesc + 2 * k, IDESC,
-                                             (j > 0 || k > 0) ? 1u : 0u);
-                            if (PAIRED)
-                                ptx::umma_commit_multicast(&bars->empty[s], static_cast<uint16_t>(0x3));
+                            for (int k = 0; k < BKS / 32; ++k) {   // +32 bytes along K = +2 in the >>4 field
+                                if constexpr (PAIRED)
+                                    ptx::umma_f8_pair(dt, adesc + 2 * k, bdesc + 2 * k, IDESC_PAIR,
+                                                      (j > 0 || k > 0) ? 1u : 0u);
+                                else
+                                    ptx::umma_f8(dt, adesc + 2 * k, bdesc + 2 * k, IDESC,
+                                                 (j > 0 || k > 0) ? 1u : 0u);
+                            }
+                            if constexpr (PAIRED)
+                                ptx::umma_commit_pair(&bars->empty[s], static_cast<uint16_t>(0x3));
                             else
                                 ptx::umma_commit(&bars->empty[s]);
                             CPW_STAMP(2, it);
                         }
                         if (!ok)
                             break;
-                        ptx::umma_commit(&bars->tfull[buf]);
+                        if constexpr (PAIRED)
+                            ptx::umma_commit_pair(&bars->tfull[buf], static_cast<uint16_t>(0x3));
+                        else
+                            ptx::umma_commit(&bars->tfull[buf]);
                     }
                 }
                 if (!ok)
@@ -420,7 +468,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 if (it > 0) {
                     const uint64_t dl = ptx::globaltimer() + static_cast<uint64_t>(c.timeout_ns);
                     const uint32_t i = it - 1;
-                    ptx::mbar_wait(&bars->empty[i % STAGES], (i / STAGES) & 1u, dl);
+                    ptx::mbar_wait(&bars->empty[i % NST], (i / NST) & 1u, dl);
                 }
             }
         }
@@ -447,10 +495,27 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             if (tile < 0)
                 break;
             const TileView tv = view(tile);
-            if (tv.null_half)
-                continue;   // no rows of this CTA in this tile
             const int phase = tv.phase, blk = tv.blk, nt = tv.nt, e = tv.e;
             const int nkb = phase == 1 ? NKB1 : NKB2;
+            // TMEM-empty arrivals go to the even CTA's barrier in 2-CTA mode
+            const uint32_t tempty0 = PAIRED ? ptx::map_cluster(&bars->tempty[0], 0) : 0u;
+            if (tv.null_half) {
+                // no rows of this CTA in this tile (odd CTA, odd block count): the UMMA still
+                // writes its TMEM partials, so take each one and hand it back unread
+                for (int kb = 0; kb < nkb; ++kb, ++pit) {
+                    const uint32_t buf = pit & 1u, bph = (pit >> 1) & 1u;
+                    if (!__all_sync(0xFFFFFFFFu, ptx::mbar_wait(&bars->tfull[buf], bph, deadline))) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    ptx::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0)
+                        ptx::mbar_arrive_cluster(tempty0 + buf * static_cast<uint32_t>(sizeof(uint64_t)));
+                }
+                continue;
+            }
             const long long prow = static_cast<long long>(blk) * BM + row;
             const float *sfa = (phase == 1 ? ws.pool_sf : ws.act_sf) + prow;
             const float *sb0;
@@ -505,32 +570,39 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     CPW_STAMP(3, pit);
                 ptx::tc_fence_after();
                 const uint32_t taddr = tmem + lane_base + buf * BN + wg * 128;
-                if (phase == 1) {
+                // two 32-column loads in flight per round; the partial is handed back to the
+                // UMMA issuer as soon as its last columns are in registers, before the last
+                // 64 FMAs.  Gate/up interleave by 8: in phase 1 columns 8..15 of every 16 are
+                // "up" (scale s1); in phase 2 s1 == s0.
+                uint32_t r0[32], r1[32];
+                ptx::tmem_ld32(taddr, r0);
+                ptx::tmem_ld32(taddr + 32, r1);
+                ptx::tmem_ld_wait(r0);
+                ptx::reg_tie(r1);
 #pragma unroll
-                    for (int ch = 0; ch < 4; ++ch) {
-                        uint32_t r[32];
-                        ptx::tmem_ld32(taddr + ch * 32, r);
-                        ptx::tmem_ld_wait(r);
-#pragma unroll
-                        for (int j = 0; j < 32; ++j)   // gate/up interleave by 8: cols 8..15 of 16 are "up"
-                            acc[ch * 32 + j] = fmaf(__uint_as_float(r[j]), ((j >> 3) & 1) ? s1 : s0,
-                                                    acc[ch * 32 + j]);
-                    }
-                } else {
-#pragma unroll
-                    for (int ch = 0; ch < 4; ++ch) {
-                        uint32_t r[32];
-                        ptx::tmem_ld32(taddr + ch * 32, r);
-                        ptx::tmem_ld_wait(r);
-#pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            acc[ch * 32 + j] = fmaf(__uint_as_float(r[j]), s0, acc[ch * 32 + j]);
-                    }
+                for (int j = 0; j < 32; ++j) {
+                    const float sj = ((j >> 3) & 1) ? s1 : s0;
+                    acc[j] = fmaf(__uint_as_float(r0[j]), sj, acc[j]);
+                    acc[32 + j] = fmaf(__uint_as_float(r1[j]), sj, acc[32 + j]);
                 }
+                ptx::tmem_ld32(taddr + 64, r0);
+                ptx::tmem_ld32(taddr + 96, r1);
+                ptx::tmem_ld_wait(r0);
+                ptx::reg_tie(r1);
                 ptx::tc_fence_before();
                 __syncwarp();
-                if (lane == 0)
-                    ptx::mbar_arrive(&bars->tempty[buf]);
+                if (lane == 0) {
+                    if constexpr (PAIRED)
+                        ptx::mbar_arrive_cluster(tempty0 + buf * static_cast<uint32_t>(sizeof(uint64_t)));
+                    else
+                        ptx::mbar_arrive(&bars->tempty[buf]);
+                }
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const float sj = ((j >> 3) & 1) ? s1 : s0;
+                    acc[64 + j] = fmaf(__uint_as_float(r0[j]), sj, acc[64 + j]);
+                    acc[96 + j] = fmaf(__uint_as_float(r1[j]), sj, acc[96 + j]);
+                }
                 if (warp == 4 && lane == 0)
                     CPW_STAMP(4, pit);
             }
@@ -623,14 +695,17 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     ptx::tc_fence_before();
     __syncthreads();
     if constexpr (PAIRED)
-        ptx::cluster_sync();   // no multicast into this CTA's shared memory is still in flight
+        ptx::cluster_sync();   // the peer neither reads this CTA's stages nor writes its TMEM any more
 #ifdef CPW_TRACE
     if (threadIdx.x == 0 && blockIdx.x < TRACE_MAX_GRID)
         g_cta_span[1][blockIdx.x] = ptx::globaltimer();
 #endif
     if (warp == 1) {
         ptx::tc_fence_after();
-        ptx::tmem_dealloc(tmem, TMEM_COLS);
+        if constexpr (PAIRED)
+            ptx::tmem_dealloc_pair(tmem, TMEM_COLS);
+        else
+            ptx::tmem_dealloc(tmem, TMEM_COLS);
     }
 }
 

@@ -265,9 +265,10 @@ def test_barrier_timeout_is_reported_then_recovers():
 
 # ----------------------------------------------------------------- FFN kernel modes -----
 def test_ffn_modes_agree_and_match_oracle():
-    """One CTA per tile vs. 2-CTA clusters sharing weight tiles by multicast: same bits,
-    within tolerance of the oracle, including experts with an odd M-block count (the
-    second CTA of their last pair has no rows and only supplies its weight half)."""
+    """One CTA per tile vs. 2-CTA clusters (one 256-row cta_group::2 UMMA over two
+    M-blocks): same bits, within tolerance of the oracle, including experts with an odd
+    M-block count (the second CTA of their last pair has no rows and only supplies its
+    weight half)."""
     T = 1024
     moe, inp = tiny_layer(T_max=T, E=8, H=256, I=256, k=2, R=2, seed=33)
     counts, _, _ = oracle.route_counts(inp.topk_idx, 8, 2)

@@ -43,7 +43,10 @@ L2_BYTES = 129 * 2 ** 20
 
 # DRAM bytes per launch from one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum),
 # valid only while the kernel sources hash to `src_sha`; see profiles/.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    ("decode", "expert_ffn"): {"bytes": 1425239000 + 13639680, "src_sha": "297f7e316e35b898"},
+    ("prefill", "expert_ffn"): {"bytes": 2099004000 + 529623808, "src_sha": "297f7e316e35b898"},
+}
 KERNEL_SOURCES = ["combine_persistent_warp_gb300/csrc/ffn.cu",
                   "combine_persistent_warp_gb300/csrc/routing.cu",
                   "combine_persistent_warp_gb300/csrc/ptx.cuh",

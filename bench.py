@@ -262,15 +262,22 @@ def oracle_rows_per_s(host, tokens, row_mask=None) -> tuple[float, float, int]:
     return rows / dt, dt, rows
 
 
-def cpu_baseline(inp, n_tokens: int) -> dict:
+def cpu_baseline(inp, n_tokens: int, min_seconds: float = 10.0) -> dict:
+    """The oracle on the first `n_tokens` tokens of the batch, repeated until at least
+    `min_seconds` of wall time have passed (at most 50 passes)."""
     import numpy as np
     import oracle
     toks = np.arange(min(n_tokens, inp.wl.T))
     host = oracle.HostInputs.from_inputs(inp)
-    v, dt, rows = oracle_rows_per_s(host, toks)
-    return {"value": v, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": f"{toks.size} tokens ({rows} routed rows) of the {inp.wl.name} batch, "
-                      f"{dt:.1f} s wall"}
+    total_rows, total_dt, passes = 0, 0.0, 0
+    while passes == 0 or (total_dt < min_seconds and passes < 50):
+        _, dt, rows = oracle_rows_per_s(host, toks)
+        total_rows += rows
+        total_dt += dt
+        passes += 1
+    return {"value": total_rows / total_dt, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{toks.size} tokens ({total_rows // passes} routed rows) of the {inp.wl.name} batch, "
+                      f"{passes} passes, {total_dt:.1f} s wall"}
 
 
 # ------------------------------------------------------------------ arms -----------
@@ -368,7 +375,7 @@ def run_ours(args, dist: Dist) -> dict | None:
         "clocks": sampler.summary(h0, h1),
     }
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
-        res["cpu_baseline"] = cpu_baseline(inp, args.cpu_tokens)
+        res["cpu_baseline"] = cpu_baseline(inp, args.cpu_tokens, args.cpu_seconds)
     moe.close()
     return res if dist.rank == 0 else None
 
@@ -446,6 +453,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=300)
     ap.add_argument("--cpu-tokens", type=int, default=128)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="minimum wall time of the oracle baseline sample (repeated passes)")
     ap.add_argument("--ref-budget-s", type=float, default=120.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ffn-mode", type=int, default=0,

@@ -44,18 +44,27 @@ L2_BYTES = 129 * 2 ** 20
 # DRAM bytes per launch from one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum),
 # valid only while the kernel sources hash to `src_sha`; see profiles/.
 NCU_TRAFFIC = {
-    ("decode", "expert_ffn"): {"bytes": 1425239000 + 13639680, "src_sha": "297f7e316e35b898"},
-    ("prefill", "expert_ffn"): {"bytes": 2099004000 + 529623808, "src_sha": "297f7e316e35b898"},
+    ("decode", "expert_ffn"): {"bytes": 1425239000 + 13639680, "src_sha": "13bd1fb1f64bbb6b"},
+    ("prefill", "expert_ffn"): {"bytes": 2099004000 + 529623808, "src_sha": "13bd1fb1f64bbb6b"},
 }
-KERNEL_SOURCES = ["combine_persistent_warp_gb300/csrc/ffn.cu",
-                  "combine_persistent_warp_gb300/csrc/routing.cu",
-                  "combine_persistent_warp_gb300/csrc/ptx.cuh",
-                  "combine_persistent_warp_gb300/csrc/moe_internal.cuh"]
+# sources each stage's kernel is compiled from (a recorded traffic figure is used only while
+# these hash to its `src_sha`)
+KERNEL_SOURCES = {
+    "expert_ffn": ["combine_persistent_warp_gb300/csrc/ffn.cu",
+                   "combine_persistent_warp_gb300/csrc/ptx.cuh",
+                   "combine_persistent_warp_gb300/csrc/moe_internal.cuh"],
+    "dispatch": ["combine_persistent_warp_gb300/csrc/routing.cu",
+                 "combine_persistent_warp_gb300/csrc/route_device.cuh",
+                 "combine_persistent_warp_gb300/csrc/ptx.cuh",
+                 "combine_persistent_warp_gb300/csrc/moe_internal.cuh"],
+    "combine": ["combine_persistent_warp_gb300/csrc/routing.cu",
+                "combine_persistent_warp_gb300/csrc/moe_internal.cuh"],
+}
 
 
-def kernel_sources_sha() -> str:
+def kernel_sources_sha(stage: str = "expert_ffn") -> str:
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in KERNEL_SOURCES[stage]:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -231,7 +240,7 @@ def roofline_for(stage: str, avg_s: float, model: dict, workload: str) -> dict:
     t_tensor = flops / (fp8_peak * 1e12) if flops else 0.0
     traffic = None
     rec = NCU_TRAFFIC.get((workload, stage))
-    if rec and rec.get("src_sha") == kernel_sources_sha():
+    if rec and rec.get("src_sha") == kernel_sources_sha(stage):
         traffic = rec["bytes"]
     if t_tensor > t_hbm and flops:
         achieved = flops / avg_s / 1e12

@@ -1,0 +1,283 @@
+// route_device.cuh -- the routing steps of the fused MoE layer as device functions (count,
+// packed claim, index table, grid barrier, segments, round-robin gather of one row), used by
+// the routing kernel in routing.cu.
+//
+// Source pages, by title and section:
+//   "Mega-MoE 内核代码导读：从 Dispatch 到 WGMMA 的融合流水线" §4.1 (token x top-k scan),
+//     §4.2 (per-expert count with block atomics, packed (1<<32)|count global claim),
+//     §4.3 (index table [local_expert][source][slot] = token*topk + k), §4.4 (grid sync)
+//   Mega-MoE walkthrough part 2 (kwkr.cn/news/1317662) §2.4 (expert segments, pool block
+//     offsets by ceil_div), §2.5 (round-robin source choice by min-peeling), §2.6 (row copy,
+//     scale copy, {source, token, topk} metadata, per-M-block arrival count)
+//   "DeepGEMM Mega MoE 对称内存（Symmetric Memory）深度分析" §6.2 (XOR-tag grid barrier with a
+//     time limit)
+//
+// On one GPU the pages' ranks become R logical source partitions of the token batch:
+// source r owns tokens [r*T/R, (r+1)*T/R).  A "remote" store is a plain global store.
+#pragma once
+
+#include "moe_internal.cuh"
+#include "ptx.cuh"
+
+namespace cpw {
+namespace route {
+
+// XOR-tag grid barrier: CTA 0 adds 0x80000000 - (n-1), every other CTA adds 1, so bit 31
+// of the counter flips exactly when all n CTAs have arrived.  Bounded: on the deadline the
+// CTA records DEV_TIMEOUT and returns false.  `skip_arrive` is the failure-path test hook.
+// Every thread of the CTA calls it; `s_ok` is a shared-memory word.
+__device__ inline bool grid_barrier(uint32_t *counter, uint32_t *hdr, bool skip_arrive, uint64_t deadline,
+                                    volatile int *s_ok)
+{
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int ok = 1;
+        const uint32_t add = blockIdx.x == 0 ? 0x80000000u - (gridDim.x - 1) : 1u;
+        __threadfence();
+        uint32_t old = skip_arrive ? ptx::ld_acquire_gpu(counter) : atomicAdd(counter, add);
+        for (uint32_t i = 0;; ++i) {
+            const uint32_t v = ptx::ld_acquire_gpu(counter);
+            if ((v ^ old) & 0x80000000u)
+                break;
+            if ((i & 255u) == 255u && ptx::globaltimer() > deadline) {
+                record_error(hdr, DEV_TIMEOUT);
+                ok = 0;
+                break;
+            }
+        }
+        __threadfence();
+        *s_ok = ok;
+    }
+    __syncthreads();
+    return *s_ok != 0;
+}
+
+// Largest i in [0, n) with a[i] <= v (a non-decreasing, a[0] <= v).
+__device__ __forceinline__ int last_le(const int32_t *a, int n, int32_t v)
+{
+    int lo = 0, hi = n - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (a[mid] <= v)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    return lo;
+}
+
+// Round-robin by min-peeling: position p among one expert's received rows -> (source,
+// slot).  Each round: A sources with rows left, L = their smallest remainder, A*L rows;
+// position q of the round goes to the (q mod A)-th active source at slot offset + q / A.
+__device__ __forceinline__ void round_robin(const uint32_t *recv, int R, uint32_t p, uint32_t &src,
+                                            uint32_t &slot)
+{
+    uint32_t offset = 0, peeled = 0;   // rows every active source has used so far
+    src = 0;
+    slot = 0;
+    for (int round = 0; round <= R; ++round) {
+        uint32_t A = 0, L = 0xFFFFFFFFu;
+        for (int r = 0; r < R; ++r) {
+            const uint32_t rem = recv[r] > peeled ? recv[r] - peeled : 0u;
+            if (rem > 0) {
+                ++A;
+                L = rem < L ? rem : L;
+            }
+        }
+        if (A == 0)
+            return;
+        if (p < A * L) {
+            const uint32_t which = p % A;
+            uint32_t nth = 0;
+            for (int r = 0; r < R; ++r) {
+                if (recv[r] > peeled) {
+                    if (nth == which) {
+                        src = static_cast<uint32_t>(r);
+                        break;
+                    }
+                    ++nth;
+                }
+            }
+            slot = offset + p / A;
+            return;
+        }
+        p -= A * L;
+        offset += L;
+        peeled += L;
+    }
+}
+
+// Steps of one CTA before the grid barrier, over its contiguous chunk of tokens:
+//   count: shared histogram cnt[R][E] of its (token, k) entries (block atomics);
+//   claim: old = atomicAdd(send[r][e], (1<<32) | count) for every (source, expert) it holds
+//          tokens of (zero counts too, as the pages do); the old low word is its first slot;
+//   table: table[e][r][slot] = token_in_source * topk + k.
+// Bad expert ids and slot overflow are recorded as device errors.  All threads call it.
+__device__ inline void count_claim_table(const Dims &d, const Workspace &ws, const CallArgs &c, uint32_t *cnt)
+{
+    const int E = d.E, R = d.R, K = d.K;
+    const int T = c.T, Tsrc = T / R;
+    const int chunk = (T + gridDim.x - 1) / gridDim.x;
+    const int t0 = min(T, static_cast<int>(blockIdx.x) * chunk);
+    const int t1 = min(T, t0 + chunk);
+    for (int i = threadIdx.x; i < R * E; i += blockDim.x)
+        cnt[i] = 0;
+    __syncthreads();
+    for (long long f = static_cast<long long>(t0) * K + threadIdx.x; f < static_cast<long long>(t1) * K;
+         f += blockDim.x) {
+        const long long e = c.idx[f];
+        if (e == -1)
+            continue;
+        if (e < -1 || e >= E) {
+            record_error(ws.hdr, DEV_BAD_INDEX);
+            continue;
+        }
+        const int r = static_cast<int>(f / K) / Tsrc;
+        atomicAdd(&cnt[r * E + static_cast<int>(e)], 1u);
+    }
+    __syncthreads();
+    if (t1 > t0) {
+        const int r0 = t0 / Tsrc, r1 = (t1 - 1) / Tsrc;
+        const int n = (r1 - r0 + 1) * E;
+        for (int i = threadIdx.x; i < n; i += blockDim.x) {
+            const int r = r0 + i / E, e = i % E;
+            const unsigned long long add = (1ull << 32) | cnt[r * E + e];
+            const unsigned long long old = atomicAdd(&ws.send[r * E + e], add);
+            cnt[r * E + e] = static_cast<uint32_t>(old);
+        }
+    }
+    __syncthreads();
+    for (long long f = static_cast<long long>(t0) * K + threadIdx.x; f < static_cast<long long>(t1) * K;
+         f += blockDim.x) {
+        const long long e = c.idx[f];
+        if (e < 0 || e >= E)
+            continue;
+        const int t = static_cast<int>(f / K), kk = static_cast<int>(f % K);
+        const int r = t / Tsrc;
+        const uint32_t slot = atomicAdd(&cnt[r * E + static_cast<int>(e)], 1u);
+        if (slot >= static_cast<uint32_t>(Tsrc)) {
+            record_error(ws.hdr, DEV_SLOT_OVERFLOW);
+            continue;
+        }
+        ws.table[(static_cast<long long>(e) * R + r) * ws.tsrc_cap + slot] = (t - r * Tsrc) * K + kk;
+    }
+}
+
+// Step after the grid barrier: rows per (expert, source) from the claim words into recv_s
+// [E][R] (shared), expert row prefix cum[E+1] and M-block prefix blk[E+1] (shared, by one
+// warp's scan), then CTA 0 publishes counts, recv, block offsets and the cumulative rows, and
+// the grid writes the M-block map (expert, valid rows of every block).  All threads call it.
+__device__ inline void segments(const Dims &d, const Workspace &ws, uint32_t *recv_s, int32_t *cum, int32_t *blk)
+{
+    const int E = d.E, R = d.R;
+    for (int i = threadIdx.x; i < E * R; i += blockDim.x) {
+        const int e = i / R, r = i % R;
+        recv_s[i] = static_cast<uint32_t>(__ldcg(&ws.send[r * E + e]));
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        const int lane = threadIdx.x;
+        const int per = (E + 31) / 32;
+        const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
+        int rows = 0, blocks = 0;
+        for (int e = e0; e < e1; ++e) {
+            int n = 0;
+            for (int r = 0; r < R; ++r)
+                n += static_cast<int>(recv_s[e * R + r]);
+            rows += n;
+            blocks += (n + BM - 1) / BM;
+        }
+        int inc_rows = rows, inc_blocks = blocks;
+        for (int o = 1; o < 32; o <<= 1) {
+            const int a = __shfl_up_sync(0xFFFFFFFFu, inc_rows, o);
+            const int b = __shfl_up_sync(0xFFFFFFFFu, inc_blocks, o);
+            if (lane >= o) {
+                inc_rows += a;
+                inc_blocks += b;
+            }
+        }
+        int base_rows = inc_rows - rows, base_blocks = inc_blocks - blocks;
+        for (int e = e0; e < e1; ++e) {
+            int n = 0;
+            for (int r = 0; r < R; ++r)
+                n += static_cast<int>(recv_s[e * R + r]);
+            cum[e] = base_rows;
+            blk[e] = base_blocks;
+            base_rows += n;
+            base_blocks += (n + BM - 1) / BM;
+        }
+        if (lane == 31) {
+            cum[E] = inc_rows;
+            blk[E] = inc_blocks;
+        }
+    }
+    __syncthreads();
+    if (blockIdx.x == 0) {
+        for (int e = threadIdx.x; e < E; e += blockDim.x) {
+            const uint32_t n = static_cast<uint32_t>(cum[e + 1] - cum[e]);
+            ws.counts[e] = n;
+            ws.cum_rows[e] += n;
+            for (int r = 0; r < R; ++r)
+                ws.recv[e * R + r] = recv_s[e * R + r];
+        }
+        for (int e = threadIdx.x; e <= E; e += blockDim.x)
+            ws.blk_off[e] = blk[e];
+    }
+    const int gtid = blockIdx.x * blockDim.x + threadIdx.x;
+    const int gthreads = gridDim.x * blockDim.x;
+    for (int g = gtid; g < blk[E]; g += gthreads) {
+        const int e = last_le(blk, E + 1, g);
+        const int n = cum[e + 1] - cum[e];
+        ws.block_expert[g] = e;
+        ws.block_rows[g] = min(BM, n - (g - blk[e]) * BM);
+    }
+}
+
+// Step a5 for pool row j (rows in expert order; e = its expert, recv_e = rows of expert e per
+// source): the round robin picks (source, slot), the table gives (token, k); one warp copies
+// the token's H bytes and H/128 scales into the pool row, writes {source, token, k} and, once
+// every lane's stores are done, adds one to the M-block's arrival count with release
+// semantics (the warp barrier orders the lanes' stores before lane 0's release).
+// U = 16-byte loads in flight per lane.
+template <int U>
+__device__ __forceinline__ void gather_row(const Dims &d, const Workspace &ws, const CallArgs &c, int j, int e,
+                                           const int32_t *cum, const int32_t *blk, const uint32_t *recv_e,
+                                           int lane)
+{
+    const int R = d.R, K = d.K, H = d.H;
+    const int Tsrc = c.T / R;
+    const uint32_t i = static_cast<uint32_t>(j - cum[e]);
+    uint32_t r, slot;
+    round_robin(recv_e, R, i, r, slot);
+    const int v = __ldcg(&ws.table[(static_cast<long long>(e) * R + r) * ws.tsrc_cap + slot]);
+    const int t = static_cast<int>(r) * Tsrc + v / K;
+    const int kk = v % K;
+    const long long row = static_cast<long long>(blk[e]) * BM + i;
+    const uint4 *__restrict__ src = reinterpret_cast<const uint4 *>(c.x + static_cast<long long>(t) * H);
+    uint4 *__restrict__ dst = reinterpret_cast<uint4 *>(ws.pool_x + row * H);
+    const int H16 = H / 16, KBH = H / 128;
+    for (int q0 = lane; q0 < H16; q0 += 32 * U) {
+        uint4 buf[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (q0 + u * 32 < H16)
+                buf[u] = __ldg(src + q0 + u * 32);
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (q0 + u * 32 < H16)
+                dst[q0 + u * 32] = buf[u];
+    }
+    for (int kb = lane; kb < KBH; kb += 32)
+        ws.pool_sf[static_cast<long long>(kb) * ws.P + row] = __ldg(c.x_sf + static_cast<long long>(t) * KBH + kb);
+    if (lane == 0) {
+        ws.meta[row * 3 + 0] = r;
+        ws.meta[row * 3 + 1] = static_cast<uint32_t>(t);
+        ws.meta[row * 3 + 2] = static_cast<uint32_t>(kk);
+    }
+    __syncwarp();
+    if (lane == 0)
+        ptx::red_release_add(ws.arrive + row / BM, 1u);
+}
+
+}  // namespace route
+}  // namespace cpw

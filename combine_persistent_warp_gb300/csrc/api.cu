@@ -375,9 +375,25 @@ int moe_forward(moe_handle_t h, int T, const uint8_t *x, const float *x_sf, cons
     return MOE_OK;
 }
 
-int moe_forward_host(moe_handle_t h, int T, const uint8_t *host_x, const float *host_x_sf,
-                     const int64_t *host_topk_idx, const float *host_topk_w, uint16_t *host_out,
-                     void *stream)
+// Device address of a host buffer the GPU can access in place (pinned, mapped into the
+// device's address space), or nullptr (pageable memory: it goes through a copy).
+static void *mapped_host(const void *p)
+{
+    cudaPointerAttributes a{};
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+}
+
+// Shared body of the host-buffer entry points.  Inputs in pinned memory are read in place by
+// one staging kernel (16-byte aligned buffers), others are copied by the copy engine; the
+// output is written in place by the combine kernel when it is pinned and 16-byte aligned,
+// else copied back from the staging buffer.
+static int forward_host_impl(moe_handle_t h, int T, const uint8_t *host_x, const float *host_x_sf,
+                             const int64_t *host_topk_idx, const float *host_topk_w, uint16_t *host_out,
+                             void *stream, bool wait)
 {
     if (!h || T < 0)
         return MOE_ERR_INVALID_ARG;
@@ -389,19 +405,52 @@ int moe_forward_host(moe_handle_t h, int T, const uint8_t *host_x, const float *
         return MOE_OK;
     if (!host_x || !host_x_sf || !host_topk_idx || !host_topk_w || !host_out)
         return MOE_ERR_INVALID_ARG;
+    if (T % h->d.R != 0)
+        return MOE_ERR_INVALID_ARG;
     CK(cudaSetDevice(h->dev));
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const Dims &d = h->d;
-    CK(cudaMemcpyAsync(h->st_x, host_x, static_cast<size_t>(T) * d.H, cudaMemcpyHostToDevice, s));
-    CK(cudaMemcpyAsync(h->st_sf, host_x_sf, sizeof(float) * T * (d.H / 128), cudaMemcpyHostToDevice, s));
-    CK(cudaMemcpyAsync(h->st_idx, host_topk_idx, sizeof(int64_t) * T * d.K, cudaMemcpyHostToDevice, s));
-    CK(cudaMemcpyAsync(h->st_w, host_topk_w, sizeof(float) * T * d.K, cudaMemcpyHostToDevice, s));
-    int rc = moe_forward(h, T, h->st_x, h->st_sf, h->st_idx, h->st_w, h->st_out, stream);
+    const void *src[4] = {host_x, host_x_sf, host_topk_idx, host_topk_w};
+    void *dst[4] = {h->st_x, h->st_sf, h->st_idx, h->st_w};
+    const long long bytes[4] = {static_cast<long long>(T) * d.H, 4ll * T * (d.H / 128), 8ll * T * d.K,
+                                4ll * T * d.K};
+    const void *dev_src[4];
+    bool in_place = true;
+    for (int i = 0; i < 4 && in_place; ++i) {
+        dev_src[i] = mapped_host(src[i]);
+        in_place = dev_src[i] != nullptr && aligned(dev_src[i], 16);
+    }
+    if (in_place) {
+        CK(launch_stage_inputs(dev_src, dst, bytes, h->num_sms, s));
+    } else {
+        for (int i = 0; i < 4; ++i)
+            CK(cudaMemcpyAsync(dst[i], src[i], static_cast<size_t>(bytes[i]), cudaMemcpyHostToDevice, s));
+    }
+    uint16_t *out_dev = static_cast<uint16_t *>(mapped_host(host_out));
+    const bool out_in_place = out_dev != nullptr && aligned(out_dev, 16);
+    int rc = moe_forward(h, T, h->st_x, h->st_sf, h->st_idx, h->st_w, out_in_place ? out_dev : h->st_out,
+                         stream);
     if (rc != MOE_OK)
         return rc;
-    CK(cudaMemcpyAsync(host_out, h->st_out, sizeof(uint16_t) * T * d.H, cudaMemcpyDeviceToHost, s));
-    CK(cudaStreamSynchronize(s));
+    if (!out_in_place)
+        CK(cudaMemcpyAsync(host_out, h->st_out, sizeof(uint16_t) * T * d.H, cudaMemcpyDeviceToHost, s));
+    if (wait)
+        CK(cudaStreamSynchronize(s));
     return MOE_OK;
+}
+
+int moe_forward_host(moe_handle_t h, int T, const uint8_t *host_x, const float *host_x_sf,
+                     const int64_t *host_topk_idx, const float *host_topk_w, uint16_t *host_out,
+                     void *stream)
+{
+    return forward_host_impl(h, T, host_x, host_x_sf, host_topk_idx, host_topk_w, host_out, stream, true);
+}
+
+int moe_forward_host_async(moe_handle_t h, int T, const uint8_t *host_x, const float *host_x_sf,
+                           const int64_t *host_topk_idx, const float *host_topk_w, uint16_t *host_out,
+                           void *stream)
+{
+    return forward_host_impl(h, T, host_x, host_x_sf, host_topk_idx, host_topk_w, host_out, stream, false);
 }
 
 int moe_get_error(moe_handle_t h, int *device_status)

@@ -166,6 +166,46 @@ cudaError_t launch_combine(const Dims &d, const Workspace &ws, const CallArgs &c
     return cudaGetLastError();
 }
 
+// ------------------------------------------------------------------ host inputs --------
+// Copies of the host-buffer entry point's inputs, read straight from pinned (device-mapped)
+// host memory in one launch instead of one copy-engine transfer per buffer.  Every pointer
+// is 16-byte aligned; a tail of fewer than 16 bytes is copied byte by byte.
+struct StageCopy {
+    const uint8_t *src;
+    uint8_t *dst;
+    long long bytes;
+};
+struct StageArgs {
+    StageCopy cp[4];
+};
+
+__global__ void __launch_bounds__(256) stage_inputs_kernel(const StageArgs a)
+{
+    const long long gtid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const long long gthreads = static_cast<long long>(gridDim.x) * blockDim.x;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const StageCopy c = a.cp[i];
+        const long long n16 = c.bytes / 16;
+        const uint4 *s = reinterpret_cast<const uint4 *>(c.src);
+        uint4 *d = reinterpret_cast<uint4 *>(c.dst);
+        for (long long q = gtid; q < n16; q += gthreads)
+            d[q] = s[q];
+        for (long long b = n16 * 16 + gtid; b < c.bytes; b += gthreads)
+            c.dst[b] = c.src[b];
+    }
+}
+
+cudaError_t launch_stage_inputs(const void *const src[4], void *const dst[4], const long long bytes[4], int num_sms,
+                                cudaStream_t s)
+{
+    StageArgs a;
+    for (int i = 0; i < 4; ++i)
+        a.cp[i] = StageCopy{static_cast<const uint8_t *>(src[i]), static_cast<uint8_t *>(dst[i]), bytes[i]};
+    stage_inputs_kernel<<<num_sms * 2, 256, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
 // ------------------------------------------------------------------ weights -------------
 // Load-time weight re-layout into GEMM tiles.  dst = [E][N/256][K/128][256][128] bytes: every
 // 256-row x 128-byte tile the FFN kernel loads per 128-deep K block is one contiguous 32 KB

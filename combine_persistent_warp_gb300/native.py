@@ -70,6 +70,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         "moe_load_weights": [H, P, P, P, P, P],
         "moe_forward": [H, I, P, P, P, P, P, P],
         "moe_forward_host": [H, I, P, P, P, P, P, P],
+        "moe_forward_host_async": [H, I, P, P, P, P, P, P],
         "moe_get_error": [H, ctypes.POINTER(I)],
         "moe_debug_routing": [H, P, P, P, P, ctypes.POINTER(I), ctypes.POINTER(I)],
         "moe_cumulative_expert_rows": [H, P],
@@ -148,17 +149,20 @@ class FusedMoE:
                "moe_forward")
         return out
 
-    def forward_host(self, x, x_sf, topk_idx, topk_w, out=None, stream=None):
-        """Same layer from host (ideally pinned) CPU tensors; returns when done."""
+    def forward_host(self, x, x_sf, topk_idx, topk_w, out=None, stream=None, wait=True):
+        """Same layer from host (ideally pinned) CPU tensors.  wait=True returns when done;
+        wait=False returns once enqueued (moe_forward_host_async): keep the tensors alive and
+        unchanged, and read `out`, only after the stream has been synchronized."""
         import torch
         T = x.shape[0]
         self._check_inputs(x, x_sf, topk_idx, topk_w, T, cuda=False)
         if out is None:
             out = torch.empty(T, self.H, dtype=torch.bfloat16, pin_memory=True)
         _expect(out, (T, self.H), torch.bfloat16, "out", cuda=False)
-        _check(self.lib.moe_forward_host(self.h, T, x.data_ptr(), x_sf.data_ptr(),
-                                         topk_idx.data_ptr(), topk_w.data_ptr(), out.data_ptr(),
-                                         _stream_handle(stream)), "moe_forward_host")
+        fn = self.lib.moe_forward_host if wait else self.lib.moe_forward_host_async
+        _check(fn(self.h, T, x.data_ptr(), x_sf.data_ptr(), topk_idx.data_ptr(), topk_w.data_ptr(),
+                  out.data_ptr(), _stream_handle(stream)),
+               "moe_forward_host" if wait else "moe_forward_host_async")
         return out
 
     def _check_inputs(self, x, x_sf, topk_idx, topk_w, T, cuda):

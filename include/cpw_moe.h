@@ -85,13 +85,23 @@ int moe_load_weights(moe_handle_t h, const uint8_t *w_gate_up, const float *sf_g
 int moe_forward(moe_handle_t h, int T, const uint8_t *x, const float *x_sf,
                 const int64_t *topk_idx, const float *topk_w, uint16_t *out, void *stream);
 
-/* moe_forward from HOST buffers (same shapes as above): copies the inputs to the
- * handle's device staging buffers, runs the layer and copies `host_out` back, all on
- * `stream`, and returns after the stream has finished.  Host buffers should be pinned
- * for the copies to be asynchronous with respect to other host work. */
+/* moe_forward from HOST buffers (same shapes as above), all on `stream`, returning after
+ * the stream has finished.  Inputs in pinned (page-locked, device-mapped) memory with
+ * 16-byte aligned addresses are read in place by one staging kernel into the handle's
+ * device staging buffers; others are copied there by cudaMemcpyAsync.  A pinned, 16-byte
+ * aligned `host_out` is written in place by the combine kernel; otherwise the result is
+ * copied back from a staging buffer.  Pageable buffers work but are slower. */
 int moe_forward_host(moe_handle_t h, int T, const uint8_t *host_x, const float *host_x_sf,
                      const int64_t *host_topk_idx, const float *host_topk_w,
                      uint16_t *host_out, void *stream);
+
+/* As moe_forward_host, but returns once the work is enqueued: the host buffers must stay
+ * valid and unchanged, and `host_out` is complete, once `stream` has been synchronized
+ * (moe_get_error synchronizes it too).  Forwards enqueued on one stream run in order, so a
+ * caller may enqueue the next batch before the previous one has finished. */
+int moe_forward_host_async(moe_handle_t h, int T, const uint8_t *host_x, const float *host_x_sf,
+                           const int64_t *host_topk_idx, const float *host_topk_w,
+                           uint16_t *host_out, void *stream);
 
 /* Wait for the handle's last stream, then return (and clear) the sticky device status in
  * *device_status (a moe_status value; MOE_OK if none).  Clearing also resets the

@@ -212,12 +212,37 @@ def test_repeat_is_deterministic_and_stats_accumulate():
 
 
 def test_host_entry_point_matches_device_entry_point():
+    """Host-buffer entry point: pinned inputs read in place and pinned output written in
+    place, pageable buffers through copies, a misaligned pinned output through the staging
+    buffer, and the asynchronous variant with two forwards in flight: all equal the device
+    entry point bit for bit."""
     moe, inp = tiny_layer(seed=9)
-    dev = moe.forward(inp.x, inp.x_sf, inp.topk_idx, inp.topk_w)
+    dev = moe.forward(inp.x, inp.x_sf, inp.topk_idx, inp.topk_w).cpu()
     torch.cuda.synchronize()
     pin = lambda t: t.cpu().pin_memory()
-    host = moe.forward_host(pin(inp.x), pin(inp.x_sf), pin(inp.topk_idx), pin(inp.topk_w))
-    assert torch.equal(dev.cpu().view(torch.int16), host.view(torch.int16))
+    px, psf, pidx, pw = pin(inp.x), pin(inp.x_sf), pin(inp.topk_idx), pin(inp.topk_w)
+    host = moe.forward_host(px, psf, pidx, pw)
+    assert torch.equal(dev.view(torch.int16), host.view(torch.int16))
+    pageable = moe.forward_host(inp.x.cpu(), inp.x_sf.cpu(), inp.topk_idx.cpu(), inp.topk_w.cpu(),
+                                out=torch.empty(64, 256, dtype=torch.bfloat16))
+    assert torch.equal(dev.view(torch.int16), pageable.view(torch.int16))
+    big = torch.empty(64 * 256 + 1, dtype=torch.bfloat16).pin_memory()
+    odd = big[1:].view(64, 256)                      # 2-byte offset: not 16-byte aligned
+    moe.forward_host(px, psf, pidx, pw, out=odd)
+    assert torch.equal(dev.view(torch.int16), odd.view(torch.int16))
+    # asynchronous: a second batch (other routing) enqueued before the first has finished
+    idx2 = torch.flip(inp.topk_idx, dims=[1]).contiguous()
+    w2 = torch.flip(inp.topk_w, dims=[1]).contiguous()
+    dev2 = moe.forward(inp.x, inp.x_sf, idx2, w2).cpu()
+    torch.cuda.synchronize()
+    o1 = torch.empty(64, 256, dtype=torch.bfloat16).pin_memory()
+    o2 = torch.empty(64, 256, dtype=torch.bfloat16).pin_memory()
+    pidx2, pw2 = pin(idx2), pin(w2)
+    moe.forward_host(px, psf, pidx, pw, out=o1, wait=False)
+    moe.forward_host(px, psf, pidx2, pw2, out=o2, wait=False)
+    assert moe.get_error() == 0                      # synchronizes the stream
+    assert torch.equal(dev.view(torch.int16), o1.view(torch.int16))
+    assert torch.equal(dev2.view(torch.int16), o2.view(torch.int16))
 
 
 def test_capacity_and_shape_errors():

@@ -44,8 +44,8 @@ L2_BYTES = 129 * 2 ** 20
 # DRAM bytes per launch from one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum),
 # valid only while the kernel sources hash to `src_sha`; see profiles/.
 NCU_TRAFFIC = {
-    ("decode", "expert_ffn"): {"bytes": 1425239000 + 13639680, "src_sha": "13bd1fb1f64bbb6b"},
-    ("prefill", "expert_ffn"): {"bytes": 2099004000 + 529623808, "src_sha": "13bd1fb1f64bbb6b"},
+    ("decode", "expert_ffn"): {"bytes": 1425218048 + 13049856, "src_sha": "3719cb2b1ba980d9"},
+    ("prefill", "expert_ffn"): {"bytes": 2035242240 + 528464896, "src_sha": "3719cb2b1ba980d9"},
 }
 # sources each stage's kernel is compiled from (a recorded traffic figure is used only while
 # these hash to its `src_sha`)

@@ -18,6 +18,9 @@ Pins (what ties each function to something other than itself) are in
                          numpy matmuls + torch FP8 casts; zero down weights; identical
                          experts; linearity in the gate weights
   * combine           -- closed form 0.73*E2(T0) + 0.27*E7(T0)
+  * power-of-two scale rule -- closed forms (exact powers, neighbours), the defining
+                         inequalities sf/2 < q <= sf, and the requantised stage against
+                         numpy with the rule applied by exponent arithmetic
 """
 from __future__ import annotations
 
@@ -55,6 +58,10 @@ def lib():
         L.orc_route_counts.restype = ctypes.c_int
         L.orc_route_counts.argtypes = [ctypes.c_int] * 4 + [P, P, P]
         L.orc_expert_ffn.argtypes = [ctypes.c_int, ctypes.c_int] + [P] * 9
+        L.orc_set_scale_rule.argtypes = [ctypes.c_int]
+        L.orc_set_scale_rule.restype = None
+        L.orc_pow2_ceil.argtypes = [ctypes.c_float]
+        L.orc_pow2_ceil.restype = ctypes.c_float
         L.orc_forward_tokens.restype = ctypes.c_int
         L.orc_forward_tokens.argtypes = [ctypes.c_int] * 5 + [P] * 8 + [ctypes.c_int, P, P, P]
         L.orc_num_threads.restype = ctypes.c_int
@@ -166,6 +173,19 @@ def route_multiset(topk_idx, E: int, R: int):
 
 
 # -------------------------------------------------------------------- numerics -
+def set_scale_rule(rule: str):
+    """SwiGLU re-quantisation scale rule: "fp32" (max(amax,1e-4)/448) or "pow2" (the
+    smallest power of two >= that quotient)."""
+    if rule not in ("fp32", "pow2"):
+        raise ValueError(rule)
+    lib().orc_set_scale_rule(1 if rule == "pow2" else 0)
+
+
+def pow2_ceil(v: float) -> float:
+    """Smallest power of two >= v (positive normal fp32 v)."""
+    return float(lib().orc_pow2_ceil(float(v)))
+
+
 def expert_ffn(x_row, xsf_row, w1_e, s1_e, w2_e, s2_e):
     """One expert on one token: (y [H] float64, hq [I] uint8, hsf [I/128] float32)."""
     x = _np(x_row, np.uint8)

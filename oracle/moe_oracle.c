@@ -17,7 +17,10 @@
  *
  * Readings of points the pages leave open (each is also listed in the design notes):
  *   - quantisation scale of a group: sf = max(amax, 1e-4) / 448 in fp32, not rounded to
- *     a power of two; values are encoded round-to-nearest-even with saturation to +-448;
+ *     a power of two; values are encoded round-to-nearest-even with saturation to +-448.
+ *     The power-of-two variant (UE8M0-representable scales, for the hardware block-scaled
+ *     path): sf = the smallest power of two >= max(amax, 1e-4) / 448 (fp32 quotient), so
+ *     every |value / sf| <= 448;
  *   - SwiGLU: h = silu(gate) * up with silu(z) = z / (1 + exp(-z)), gate = rows 0..I-1 of
  *     the gate_up weight, up = rows I..2I-1; h is rounded to fp32 and re-quantised per
  *     1x128 group before the down projection;
@@ -227,6 +230,20 @@ int orc_route_counts(int T, int k, int E, int R, const int64_t *idx,
  * Every operand is dequantised element by element (code value times its block scale),
  * products are summed in double.  Outputs: y [H] (double); optional hq [I] codes and
  * hsf [I/128] scales of the re-quantised SwiGLU output. */
+/* Scale rule of the SwiGLU re-quantisation: 0 = max(amax, 1e-4) / 448, 1 = the smallest
+ * power of two >= that quotient.  Set before calling the numerics (not thread-safe). */
+static int g_scale_pow2 = 0;
+void orc_set_scale_rule(int pow2) { g_scale_pow2 = pow2 != 0; }
+
+/* Smallest power of two >= v for a positive normal fp32 v: with v = f * 2^e, f in
+ * [0.5, 1), it is v itself when f == 0.5, else 2^e. */
+float orc_pow2_ceil(float v)
+{
+    int e;
+    const float f = frexpf(v, &e);
+    return f == 0.5f ? v : ldexpf(1.0f, e);
+}
+
 void orc_expert_ffn(int H, int I, const uint8_t *x, const float *xsf,
                     const uint8_t *w1, const float *s1,
                     const uint8_t *w2, const float *s2,
@@ -261,6 +278,8 @@ void orc_expert_ffn(int H, int I, const uint8_t *x, const float *xsf,
         for (int n = j * 128; n < j * 128 + 128; ++n)
             amax = fmaxf(amax, fabsf(h[n]));
         float sf = fmaxf(amax, 1e-4f) / 448.0f;
+        if (g_scale_pow2)
+            sf = orc_pow2_ceil(sf);
         for (int n = j * 128; n < j * 128 + 128; ++n) {
             uint8_t q = orc_e4m3_encode(h[n] / sf);
             hd[n] = dec(q) * (double)sf;

@@ -191,7 +191,14 @@ def _dequant(codes, scale, rb, cb):
     return v * np.kron(scale.numpy().astype(np.float64), np.ones((rb, cb)))
 
 
-def _dense_ffn_library(x_row, xs_row, w1, s1, w2, s2):
+def _np_pow2_ceil(v):
+    """Smallest power of two >= v via numpy's frexp (v = m * 2^e, m in [0.5, 1))."""
+    v = np.asarray(v, np.float32)
+    m, e = np.frexp(v)
+    return np.where(m == 0.5, v, np.ldexp(np.float32(1.0), e)).astype(np.float32)
+
+
+def _dense_ffn_library(x_row, xs_row, w1, s1, w2, s2, pow2=False):
     """One expert via numpy matmuls and torch FP8 casts (the single-expert special case)."""
     I = w2.shape[1]
     dx = _dequant(x_row[None, :], xs_row[None, :], 1, 128)[0]
@@ -199,6 +206,8 @@ def _dense_ffn_library(x_row, xs_row, w1, s1, w2, s2):
     g, u = gu[:I], gu[I:]
     h = (g / (1.0 + np.exp(-g)) * u).astype(np.float32).reshape(-1, 128)
     sf = (np.maximum(np.abs(h).max(axis=1), np.float32(1e-4)) / np.float32(448.0)).astype(np.float32)
+    if pow2:
+        sf = _np_pow2_ceil(sf)
     q = torch_e4m3_encode(h / sf[:, None])
     hd = (torch_e4m3_value(q) * sf[:, None].astype(np.float64)).reshape(-1)
     y = _dequant(w2, s2, 128, 128) @ hd
@@ -213,6 +222,44 @@ def test_expert_ffn_matches_dense_library_chain(oracle_mod):
         assert np.array_equal(hsf, sf_ref)
         assert (hq == q_ref).mean() >= 0.995
         assert np.linalg.norm(y - y_ref) <= 1e-6 * np.linalg.norm(y_ref)
+
+
+def test_pow2_ceil_closed_forms(oracle_mod):
+    assert oracle_mod.pow2_ceil(3.0) == 4.0
+    assert oracle_mod.pow2_ceil(4.0) == 4.0
+    assert oracle_mod.pow2_ceil(0.3) == 0.5
+    assert oracle_mod.pow2_ceil(2.0 ** -20) == 2.0 ** -20
+    assert oracle_mod.pow2_ceil(float(np.nextafter(np.float32(2.0 ** -20), np.float32(1)))) == 2.0 ** -19
+    assert oracle_mod.pow2_ceil(float(np.float32(1e-4) / np.float32(448))) == 2.0 ** -22
+
+
+def test_pow2_ceil_defining_inequalities(oracle_mod):
+    rng = np.random.default_rng(5)
+    for q in (10.0 ** rng.uniform(-7, 3, 400)).astype(np.float32):
+        sf = np.float32(oracle_mod.pow2_ceil(float(q)))
+        m, _ = np.frexp(sf)
+        assert m == 0.5 and sf >= q and sf / 2 < q
+
+
+def test_expert_ffn_pow2_rule_matches_dense_chain(oracle_mod):
+    """With the power-of-two rule the re-quantisation scales are the smallest powers of two
+    >= the fp32-rule quotients (numpy frexp arithmetic) and the whole expert matches the
+    numpy chain with that rule."""
+    x, xs, idx, w, w1, s1, w2, s2 = _tiny_inputs(H=384, I=256)
+    try:
+        oracle_mod.set_scale_rule("pow2")
+        for t, e in [(0, 0), (5, 1), (7, 3)]:
+            y, hq, hsf = oracle_mod.expert_ffn(x[t], xs[t], w1[e], s1[e], w2[e], s2[e])
+            y_ref, q_ref, sf_ref = _dense_ffn_library(x[t], xs[t], w1[e], s1[e], w2[e], s2[e], pow2=True)
+            assert np.array_equal(hsf, sf_ref)
+            assert (hq == q_ref).mean() >= 0.995
+            assert np.linalg.norm(y - y_ref) <= 1e-6 * np.linalg.norm(y_ref)
+            # tight: every group's largest code magnitude is at least 448/2 (below it the
+            # next smaller power of two would have been enough)
+            mags = np.abs(torch_e4m3_value(hq.reshape(-1, 128)))
+            assert np.all(mags.max(axis=1) >= 224) and np.all(mags.max(axis=1) <= 448)
+    finally:
+        oracle_mod.set_scale_rule("fp32")
 
 
 def test_forward_single_expert_is_dense_ffn(oracle_mod):

@@ -277,6 +277,7 @@ def cpu_baseline(inp, n_tokens: int, min_seconds: float = 10.0) -> dict:
     import numpy as np
     import oracle
     toks = np.arange(min(n_tokens, inp.wl.T))
+    oracle.set_scale_rule(inp.wl.scales)
     host = oracle.HostInputs.from_inputs(inp)
     total_rows, total_dt, passes = 0, 0.0, 0
     while passes == 0 or (total_dt < min_seconds and passes < 50):
@@ -303,9 +304,11 @@ def run_ours(args, dist: Dist) -> dict | None:
     M = model["M"]
     moe = FusedMoE(wl.E, wl.H, wl.I, wl.topk, wl.R).reserve(wl.T)
     moe.load_weights(inp.w_gate_up, inp.sf_gate_up, inp.w_down, inp.sf_down)
+    from combine_persistent_warp_gb300 import native
     if args.ffn_mode:
-        from combine_persistent_warp_gb300 import native
         moe.set_option(native.OPT_FFN_MODE, args.ffn_mode)
+    if wl.scales == "pow2":   # power-of-two scales: the hardware block-scaled path
+        moe.set_option(native.OPT_SCALE_MODE, 1)
     out = torch.empty(wl.T, wl.H, dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream(dev)
 
@@ -380,7 +383,7 @@ def run_ours(args, dist: Dist) -> dict | None:
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "fp8e4m3 (fp32 accumulate, bf16 out)", "data": "synthetic",
         "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E,
-                   "topk": wl.topk, "R": wl.R, "routing": wl.routing,
+                   "topk": wl.topk, "R": wl.R, "routing": wl.routing, "scales": wl.scales,
                    "routed_rows_per_step": M, "parallelism": f"replicas x{dist.world}",
                    "l2": ("inputs larger than L2: %.2f GB of expert weights streamed per step, "
                           "no flush" % (model["weight_bytes"] / 1e9))},
@@ -409,6 +412,7 @@ def run_reference(args, dist: Dist) -> dict | None:
     if dist.rank != 0:
         return None
     inp = make_inputs(args.workload, device="cpu")
+    oracle.set_scale_rule(inp.wl.scales)
     wl = inp.wl
     host = oracle.HostInputs.from_inputs(inp)
     h_idx = host.idx
@@ -469,7 +473,9 @@ def main(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=50)
-    ap.add_argument("--workload", default="decode")
+    ap.add_argument("--workload", default="decode",
+                    help="tiny, decode, prefill, skewed, large, or one of them with -pow2 "
+                         "(power-of-two scales: the block-scaled UMMA path)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=300)
     ap.add_argument("--cpu-tokens", type=int, default=128)

@@ -15,7 +15,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libcpw_moe.so")
-SOURCES = ["api.cu", "routing.cu", "ffn.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "routing.cu", "ffn.cu", "ffn_bs.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
                 "-I" + os.path.join(ROOT, "include")]

@@ -35,6 +35,10 @@ struct moe_ctx {
     float *s1 = nullptr;         // [E][2I/128][H/128]
     uint8_t *w2 = nullptr;       // [E][H/256][I/128][256][128] tiles
     float *s2 = nullptr;         // [E][H/128][I/128]
+    uint8_t *sfb1 = nullptr;     // UE8M0 scale blocks of the W1 / W2 tiles (1 KB per tile and
+    uint8_t *sfb2 = nullptr;     // 128-deep K block), valid when every weight scale is 2^k
+    uint32_t *sfb_bad = nullptr; // device flag: a weight scale is not a power of two
+    bool weights_pow2 = false;
     void *w_mem = nullptr;
     size_t w_bytes = 0;
     FfnMaps maps{};              // a1 pool x, b1 W1, a2 act, b2 W2
@@ -50,6 +54,7 @@ struct moe_ctx {
     long long timeout_ns = 2000000000LL;
     int debug_skip_barrier = 0;
     int ffn_mode = 0;            // 0 auto, 1 one CTA per tile, 2 two-CTA clusters
+    int scale_mode = 0;          // 0 fp32 scales, 1 power-of-two scales (block-scaled UMMA)
     // stage profiling (events on the forward's stream)
     bool profile = false;
     std::vector<cudaEvent_t> events;   // 4 per recorded forward
@@ -149,8 +154,10 @@ size_t carve_big(moe_ctx *h, char *base, int max_tokens, Workspace &ws)
     ws.meta = c.take<uint32_t>(static_cast<size_t>(P) * 3);
     ws.pool_x = c.take<uint8_t>(static_cast<size_t>(P) * d.H);
     ws.pool_sf = c.take<float>(static_cast<size_t>(P) * (d.H / 128));
+    ws.pool_sfe = c.take<uint8_t>(static_cast<size_t>(P) * (d.H / 32));
     ws.act = c.take<uint8_t>(static_cast<size_t>(P) * d.I);
     ws.act_sf = c.take<float>(static_cast<size_t>(P) * (d.I / 128));
+    ws.act_sfe = c.take<uint8_t>(static_cast<size_t>(P) * (d.I / 32));
     ws.combine = c.take<uint16_t>(static_cast<size_t>(d.K) * max_tokens * d.H);
     h->st_x = c.take<uint8_t>(static_cast<size_t>(max_tokens) * d.H);
     h->st_sf = c.take<float>(static_cast<size_t>(max_tokens) * (d.H / 128));
@@ -202,6 +209,7 @@ const char *moe_status_string(int s)
     case MOE_ERR_TIMEOUT: return "device wait timed out";
     case MOE_ERR_SLOT_OVERFLOW: return "more than T/R rows of one source for one expert (device)";
     case MOE_ERR_NOT_RESERVED: return "workspace not reserved";
+    case MOE_ERR_BAD_SCALE: return "a scale is not a power of two in the block-scaled mode";
     default: return "unknown status";
     }
 }
@@ -307,6 +315,10 @@ int moe_load_weights(moe_handle_t h, const uint8_t *w_gate_up, const float *sf_g
             h->s1 = c.take<float>(ns1);
             h->w2 = c.take<uint8_t>(n2);
             h->s2 = c.take<float>(ns2);
+            // UE8M0 scale blocks: 1 KB per weight tile (256 rows) and 128-deep K block
+            h->sfb1 = c.take<uint8_t>(static_cast<size_t>(d.E) * (2 * d.I / BN) * (d.H / 128) * 1024);
+            h->sfb2 = c.take<uint8_t>(static_cast<size_t>(d.E) * (d.H / BN) * (d.I / 128) * 1024);
+            h->sfb_bad = c.take<uint32_t>(1);
             return align_up(c.off, 256);
         };
         const size_t bytes = carve(nullptr);
@@ -319,6 +331,15 @@ int moe_load_weights(moe_handle_t h, const uint8_t *w_gate_up, const float *sf_g
         return MOE_ERR_CUDA;
     CK(cudaMemcpyAsync(h->s1, sf_gate_up, ns1 * sizeof(float), cudaMemcpyDeviceToDevice, s));
     CK(cudaMemcpyAsync(h->s2, sf_down, ns2 * sizeof(float), cudaMemcpyDeviceToDevice, s));
+    // UE8M0 scale blocks for the block-scaled path; usable only if every scale is 2^k
+    CK(cudaMemsetAsync(h->sfb_bad, 0, sizeof(uint32_t), s));
+    if (launch_build_sfb(sf_gate_up, h->sfb1, d.E, 2 * d.I, d.H, d.I, h->sfb_bad, s) != cudaSuccess ||
+        launch_build_sfb(sf_down, h->sfb2, d.E, d.H, d.I, 0, h->sfb_bad, s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    uint32_t bad = 1;
+    CK(cudaMemcpyAsync(&bad, h->sfb_bad, sizeof(uint32_t), cudaMemcpyDeviceToHost, s));
+    CK(cudaStreamSynchronize(s));
+    h->weights_pow2 = bad == 0;
     // weight tiles as rows of 128 bytes: tile (e, nt, kb) starts at row ((e*NT + nt)*KB + kb)*256
     if (encode_tile_map(&h->maps.b1, h->w1, n1 / 128, 128, BN) != MOE_OK ||
         encode_tile_map(&h->maps.b2, h->w2, n2 / 128, 128, BN) != MOE_OK ||
@@ -353,7 +374,12 @@ int moe_forward(moe_handle_t h, int T, const uint8_t *x, const float *x_sf, cons
         return MOE_ERR_INVALID_ARG;
     CK(cudaSetDevice(h->dev));
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    CallArgs c{T, x, x_sf, topk_idx, topk_w, out, h->timeout_ns, h->debug_skip_barrier};
+    // power-of-two scales: the block-scaled kernel (the weights were checked at load time,
+    // the activation scales are checked by the routing kernel's gather)
+    const bool bs = h->scale_mode == 1;
+    if (bs && !h->weights_pow2)
+        return MOE_ERR_BAD_SCALE;
+    CallArgs c{T, x, x_sf, topk_idx, topk_w, out, h->timeout_ns, h->debug_skip_barrier, bs ? 1 : 0};
     cudaEvent_t *ev = nullptr;
     if (h->profile) {
         if (h->prof_calls < PROF_MAX_CALLS)
@@ -364,7 +390,8 @@ int moe_forward(moe_handle_t h, int T, const uint8_t *x, const float *x_sf, cons
     auto mark = [&](int i) { return ev ? cudaEventRecord(ev[i], s) : cudaSuccess; };
     if (mark(0) != cudaSuccess || launch_dispatch(h->d, h->ws, c, h->num_sms, s) != cudaSuccess ||
         mark(1) != cudaSuccess ||
-        launch_ffn(h->maps, h->d, h->ws, c, h->s1, h->s2, wave_blocks(h), h->num_sms, ffn_paired(h, T), s) !=
+        (bs ? launch_ffn_bs(h->maps, h->d, h->ws, c, h->sfb1, h->sfb2, wave_blocks(h), h->num_sms, s)
+            : launch_ffn(h->maps, h->d, h->ws, c, h->s1, h->s2, wave_blocks(h), h->num_sms, ffn_paired(h, T), s)) !=
             cudaSuccess ||
         mark(2) != cudaSuccess || launch_combine(h->d, h->ws, c, h->num_sms, s) != cudaSuccess ||
         mark(3) != cudaSuccess)
@@ -589,6 +616,11 @@ int moe_set_option(moe_handle_t h, int option, int64_t value)
         if (value < 0 || value > 2)
             return MOE_ERR_INVALID_ARG;
         h->ffn_mode = static_cast<int>(value);
+        return MOE_OK;
+    case MOE_OPT_SCALE_MODE:
+        if (value < 0 || value > 1)
+            return MOE_ERR_INVALID_ARG;
+        h->scale_mode = static_cast<int>(value);
         return MOE_OK;
     default:
         return MOE_ERR_INVALID_ARG;

@@ -50,9 +50,11 @@ struct Workspace {
     int32_t *table;                // [E][R][tsrc_cap] token_in_source * topk + k
     uint8_t *pool_x;               // [P][H]   e4m3 gathered activations
     float *pool_sf;                // [H/128][P]
+    uint8_t *pool_sfe;             // [P/128][H/128][512] UE8M0 scale blocks (block-scaled mode)
     uint32_t *meta;                // [P][3]   {source, token, topk slot}
     uint8_t *act;                  // [P][I]   e4m3 SwiGLU output
     float *act_sf;                 // [I/128][P]
+    uint8_t *act_sfe;              // [P/128][I/128][512] UE8M0 scale blocks (block-scaled mode)
     uint16_t *combine;             // [topk][max_tokens][H] bf16 weighted expert outputs
     uint32_t *arrive;              // [MB] rows gathered per M-block
     uint32_t *l1_done;             // [MB] finished gate_up (tile, epilogue warp) pairs
@@ -75,10 +77,11 @@ struct CallArgs {
     uint16_t *out;
     long long timeout_ns;
     int debug_skip_barrier;
+    int block_scaled;   // 1: power-of-two scales, hardware block-scaled UMMA (ffn_bs.cu)
 };
 
 // Device error codes (same values as the public moe_status).
-enum DevErr : uint32_t { DEV_BAD_INDEX = 6, DEV_TIMEOUT = 7, DEV_SLOT_OVERFLOW = 8 };
+enum DevErr : uint32_t { DEV_BAD_INDEX = 6, DEV_TIMEOUT = 7, DEV_SLOT_OVERFLOW = 8, DEV_BAD_SCALE = 10 };
 
 __device__ __forceinline__ void record_error(uint32_t *hdr, uint32_t code)
 {
@@ -104,6 +107,12 @@ cudaError_t launch_ffn(const FfnMaps &maps, const Dims &d, const Workspace &ws, 
 cudaError_t trace_read(void *dst, size_t bytes);
 cudaError_t trace_clear();
 #endif
+// power-of-two scales: the block-scaled FFN kernel (ffn_bs.cu) and the load-time UE8M0
+// scale blocks of the weight tiles
+cudaError_t launch_ffn_bs(const FfnMaps &maps, const Dims &d, const Workspace &ws, const CallArgs &c,
+                          const uint8_t *sfb1, const uint8_t *sfb2, int wave_blocks, int num_sms, cudaStream_t s);
+cudaError_t launch_build_sfb(const float *s, uint8_t *dst, int E, int N, int K, int gate_up_I, uint32_t *bad,
+                             cudaStream_t st);
 cudaError_t launch_combine(const Dims &d, const Workspace &ws, const CallArgs &c, int num_sms,
                            cudaStream_t s);
 cudaError_t launch_stage_inputs(const void *const src[4], void *const dst[4], const long long bytes[4], int num_sms,

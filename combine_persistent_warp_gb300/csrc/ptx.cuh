@@ -133,6 +133,16 @@ __device__ __forceinline__ void tma_load_2d_pair(void *smem_dst, const CUtensorM
                  : "memory");
 }
 
+// Untiled bulk copy global -> this CTA's shared memory, counted on `bar` (both addresses
+// 16-byte aligned, size a multiple of 16 bytes).
+__device__ __forceinline__ void bulk_load(void *smem_dst, const void *gsrc, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(smem_dst)),
+                 "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
 __device__ __forceinline__ uint32_t cluster_ctarank()
 {
     uint32_t r;

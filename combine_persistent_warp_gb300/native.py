@@ -26,6 +26,7 @@ BUFFERS = {"pool_x": 0, "pool_sf": 1, "act": 2, "act_sf": 3, "combine": 4, "tabl
 OPT_TIMEOUT_NS = 0
 OPT_DEBUG_SKIP_BARRIER = 1
 OPT_FFN_MODE = 2
+OPT_SCALE_MODE = 3
 
 
 class MoeError(RuntimeError):

@@ -36,6 +36,8 @@ class Workload:
     zipf_s: float = 0.0
     skip_frac: float = 0.0     # fraction of topk_idx entries set to -1
     seed: int = 0
+    scales: str = "fp32"       # "fp32": sf = max(amax,1e-4)/448; "pow2": the smallest power
+                               # of two >= that (UE8M0-representable, block-scaled UMMA path)
 
     @property
     def T_src(self) -> int:
@@ -53,6 +55,13 @@ WORKLOADS = {
                        routing="zipf", zipf_s=1.2, skip_frac=0.05, seed=3),
     "large": Workload("large", T=16384, H=4096, I=1536, E=128, topk=8, R=8, seed=4),
 }
+# the same batches with power-of-two (UE8M0-representable) scales everywhere
+POW2_WORKLOADS = {f"{k}-pow2": Workload(**{**asdict(v), "name": f"{k}-pow2", "scales": "pow2"})
+                  for k, v in WORKLOADS.items()}
+
+
+def workload(name: str) -> Workload:
+    return WORKLOADS[name] if name in WORKLOADS else POW2_WORKLOADS[name]
 
 
 def _gen(seed: int, device) -> torch.Generator:
@@ -99,25 +108,36 @@ def make_routing(T: int, E: int, topk: int, *, seed: int, routing: str = "unifor
 
 
 # ------------------------------------------------------ FP8 synthesis -------
-def quantize_1x128(x: torch.Tensor):
+def pow2_ceil(v: torch.Tensor) -> torch.Tensor:
+    """Smallest power of two >= v (positive fp32): v = m * 2^e with m in [0.5, 1)."""
+    m, e = torch.frexp(v)
+    return torch.where(m == 0.5, v, torch.ldexp(torch.ones_like(v), e))
+
+
+def quantize_1x128(x: torch.Tensor, scales: str = "fp32"):
     """fp32 [rows, K] -> (e4m3 bytes uint8 [rows, K], fp32 scales [rows, K/128])."""
     rows, K = x.shape
     g = x.float().view(rows, K // 128, 128)
     sf = g.abs().amax(dim=2).clamp_min(SCALE_FLOOR) / FP8_MAX
+    if scales == "pow2":
+        sf = pow2_ceil(sf)
     q = (g / sf[:, :, None]).to(torch.float8_e4m3fn).view(torch.uint8)
     return q.view(rows, K).contiguous(), sf.contiguous()
 
 
-def quantize_128x128(w: torch.Tensor):
+def quantize_128x128(w: torch.Tensor, scales: str = "fp32"):
     """fp32 [N, K] -> (e4m3 bytes uint8 [N, K], fp32 scales [N/128, K/128])."""
     N, K = w.shape
     g = w.float().view(N // 128, 128, K // 128, 128)
     sf = g.abs().amax(dim=(1, 3)).clamp_min(SCALE_FLOOR) / FP8_MAX
+    if scales == "pow2":
+        sf = pow2_ceil(sf)
     q = (g / sf[:, None, :, None]).to(torch.float8_e4m3fn).view(torch.uint8)
     return q.view(N, K).contiguous(), sf.contiguous()
 
 
-def make_weights(E: int, H: int, I: int, *, seed: int, device="cpu", std: float = 0.02):
+def make_weights(E: int, H: int, I: int, *, seed: int, device="cpu", std: float = 0.02,
+                 scales: str = "fp32"):
     """Expert weights W ~ N(0, std) as FP8 with 128x128 fp32 block scales.
 
     Returns w_gate_up uint8 [E, 2I, H] (rows 0..I-1 gate, I..2I-1 up),
@@ -131,20 +151,20 @@ def make_weights(E: int, H: int, I: int, *, seed: int, device="cpu", std: float 
     s2 = torch.empty(E, H // 128, I // 128, dtype=torch.float32, device=device)
     for e in range(E):
         a = torch.randn(2 * I, H, generator=g, device=device) * std
-        w1[e], s1[e] = quantize_128x128(a)
+        w1[e], s1[e] = quantize_128x128(a, scales)
         b = torch.randn(H, I, generator=g, device=device) * std
-        w2[e], s2[e] = quantize_128x128(b)
+        w2[e], s2[e] = quantize_128x128(b, scales)
     return w1, s1, w2, s2
 
 
-def make_activations(T: int, H: int, *, seed: int, device="cpu"):
+def make_activations(T: int, H: int, *, seed: int, device="cpu", scales: str = "fp32"):
     """x ~ N(0,1), rounded to bf16, then FP8 e4m3 with 1x128 fp32 scales."""
     g = _gen(seed * 15485863 + 11, device)
     x = torch.randn(T, H, generator=g, device=device).to(torch.bfloat16).float()
     if T == 0:
         return (torch.empty(0, H, dtype=torch.uint8, device=device),
                 torch.empty(0, H // 128, dtype=torch.float32, device=device))
-    return quantize_1x128(x)
+    return quantize_1x128(x, scales)
 
 
 @dataclass
@@ -170,13 +190,13 @@ class Inputs:
 def make_inputs(wl: Workload | str, device="cpu", *, T: int | None = None) -> Inputs:
     """All inputs of one workload.  ``T`` overrides the token count (same seed)."""
     if isinstance(wl, str):
-        wl = WORKLOADS[wl]
+        wl = workload(wl)
     if T is not None and T != wl.T:
         wl = Workload(**{**asdict(wl), "T": T})
     idx, w = make_routing(wl.T, wl.E, wl.topk, seed=wl.seed, routing=wl.routing,
                           zipf_s=wl.zipf_s, skip_frac=wl.skip_frac)
-    x, x_sf = make_activations(wl.T, wl.H, seed=wl.seed, device=device)
-    w1, s1, w2, s2 = make_weights(wl.E, wl.H, wl.I, seed=wl.seed, device=device)
+    x, x_sf = make_activations(wl.T, wl.H, seed=wl.seed, device=device, scales=wl.scales)
+    w1, s1, w2, s2 = make_weights(wl.E, wl.H, wl.I, seed=wl.seed, device=device, scales=wl.scales)
     return Inputs(wl, x, x_sf, idx.to(device), w.to(device), w1, s1, w2, s2)
 
 

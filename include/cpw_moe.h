@@ -51,7 +51,9 @@ enum moe_status {
     MOE_ERR_BAD_INDEX = 6,          /* device: an expert id outside [0,E) other than -1 */
     MOE_ERR_TIMEOUT = 7,            /* device: a bounded wait gave up                  */
     MOE_ERR_SLOT_OVERFLOW = 8,      /* device: > T/R rows of one source for one expert */
-    MOE_ERR_NOT_RESERVED = 9        /* forward before moe_reserve                      */
+    MOE_ERR_NOT_RESERVED = 9,       /* forward before moe_reserve                      */
+    MOE_ERR_BAD_SCALE = 10          /* block-scaled mode: a weight scale (at the forward) or
+                                       an activation scale (device) is not a power of two */
 };
 
 /* Create a layer for E experts, hidden size H, expert intermediate size I, top-k, and R
@@ -153,9 +155,22 @@ int moe_get_info(moe_handle_t h, moe_info *info);
  * at the grid barrier, so the others give up after the time limit and the forward
  * ends with MOE_ERR_TIMEOUT (failure-path test; never on in normal use);
  * MOE_OPT_FFN_MODE: how the expert FFN kernel covers its tiles: 0 = automatic (default),
- * 1 = one CTA per 128-row tile, 2 = pairs of CTAs on two M-blocks of one expert sharing
- * each weight tile through cluster multicast.  All modes compute the same result. */
-enum moe_option { MOE_OPT_TIMEOUT_NS = 0, MOE_OPT_DEBUG_SKIP_BARRIER = 1, MOE_OPT_FFN_MODE = 2 };
+ * 1 = one CTA per 128-row tile, 2 = pairs of CTAs (a cluster) on two M-blocks of one expert
+ * with one 256-row two-CTA UMMA.  All modes compute the same result;
+ * MOE_OPT_SCALE_MODE: 0 = arbitrary fp32 block scales (default; the UMMA accumulates each
+ * 128-deep K block in TMEM and the scales are applied on the CUDA cores); 1 = every scale
+ * (x_sf, both weight scale tensors) is a power of two: the UMMA applies them itself as UE8M0
+ * scale factors and accumulates the whole K range in TMEM ("DeepGEMM Mega MoE 对称内存
+ * （Symmetric Memory）深度分析" §8.1), and the SwiGLU requant uses the smallest power-of-two
+ * scale >= max(amax, 1e-4)/448.  Weights that are not all powers of two make moe_forward
+ * return MOE_ERR_BAD_SCALE; an activation scale that is not is reported by the device the
+ * same way (sticky). */
+enum moe_option {
+    MOE_OPT_TIMEOUT_NS = 0,
+    MOE_OPT_DEBUG_SKIP_BARRIER = 1,
+    MOE_OPT_FFN_MODE = 2,
+    MOE_OPT_SCALE_MODE = 3
+};
 int moe_set_option(moe_handle_t h, int option, int64_t value);
 
 /* Stage timing with CUDA events recorded on the forward's own stream.  While enabled,

@@ -180,8 +180,14 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 const uint64_t pol_b_shared = ptx::policy_evict_normal();
                 uint32_t it = 0, tcount = 0;
                 bool ok = true;
+                // tiles are claimed one ahead, so the claim's round trip to L2 overlaps the
+                // loads of the tile before (a CTA holds at most one claimed, unstarted tile;
+                // the smallest unfinished tile is always being worked on)
+                int next = static_cast<int>(atomicAdd(ws.hdr + HDR_TILE_NEXT, 1u));
                 while (ok) {
-                    const int tile = static_cast<int>(atomicAdd(ws.hdr + HDR_TILE_NEXT, 1u));
+                    const int tile = next;
+                    if (tile < ntiles)
+                        next = static_cast<int>(atomicAdd(ws.hdr + HDR_TILE_NEXT, 1u));
                     const uint32_t slot = tcount % TILE_RING, sph = (tcount / TILE_RING) & 1u;
                     if (!ptx::mbar_wait(&bars->tile_empty[slot], sph ^ 1u, deadline)) {
                         ok = false;

@@ -42,6 +42,7 @@ struct moe_ctx {
     void *w_mem = nullptr;
     size_t w_bytes = 0;
     FfnMaps maps{};              // a1 pool x, b1 W1, a2 act, b2 W2
+    SfMaps sf_maps{};            // UE8M0 scale blocks of pool / act rows and weight tiles
     // staging buffers of moe_forward_host
     uint8_t *st_x = nullptr;
     float *st_sf = nullptr;
@@ -96,6 +97,22 @@ int encode_tile_map(CUtensorMap *m, void *base, uint64_t rows, uint64_t cols, ui
                                               : CU_TENSOR_MAP_SWIZZLE_32B;
     CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
+}
+
+// 2-D byte matrix of `bytes` / 256 rows of 256 bytes, boxes of box_rows whole rows, no
+// swizzle (the UE8M0 scale blocks the 2-CTA block-scaled kernel stages by TMA)
+int encode_sf_map(CUtensorMap *m, void *base, uint64_t bytes, uint32_t box_rows)
+{
+    if (get_encoder() != MOE_OK || bytes % 256 != 0)
+        return MOE_ERR_CUDA;
+    cuuint64_t dims[2] = {256, bytes / 256};
+    cuuint64_t strides[1] = {256};
+    cuuint32_t box[2] = {256, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
 }
@@ -286,7 +303,9 @@ int moe_reserve(moe_handle_t h, int max_tokens)
     if (encode_tile_map(&h->maps.a1, ws.pool_x, ws.P, d.H, BM) != MOE_OK ||
         encode_tile_map(&h->maps.a2, ws.act, ws.P, d.I, BM) != MOE_OK ||
         encode_tile_map(&h->maps.a1p, ws.pool_x, ws.P, d.H, A_ROWS_PART) != MOE_OK ||
-        encode_tile_map(&h->maps.a2p, ws.act, ws.P, d.I, A_ROWS_PART) != MOE_OK)
+        encode_tile_map(&h->maps.a2p, ws.act, ws.P, d.I, A_ROWS_PART) != MOE_OK ||
+        encode_sf_map(&h->sf_maps.sfa1, ws.pool_sfe, static_cast<uint64_t>(ws.P) * (d.H / 32), 2) != MOE_OK ||
+        encode_sf_map(&h->sf_maps.sfa2, ws.act_sfe, static_cast<uint64_t>(ws.P) * (d.I / 32), 2) != MOE_OK)
         return MOE_ERR_CUDA;
     CK(cudaDeviceSynchronize());
     h->reserved = true;
@@ -344,7 +363,11 @@ int moe_load_weights(moe_handle_t h, const uint8_t *w_gate_up, const float *sf_g
     if (encode_tile_map(&h->maps.b1, h->w1, n1 / 128, 128, BN) != MOE_OK ||
         encode_tile_map(&h->maps.b2, h->w2, n2 / 128, 128, BN) != MOE_OK ||
         encode_tile_map(&h->maps.b1h, h->w1, n1 / 128, 128, BN / 2) != MOE_OK ||
-        encode_tile_map(&h->maps.b2h, h->w2, n2 / 128, 128, BN / 2) != MOE_OK)
+        encode_tile_map(&h->maps.b2h, h->w2, n2 / 128, 128, BN / 2) != MOE_OK ||
+        encode_sf_map(&h->sf_maps.sfb1, h->sfb1, static_cast<uint64_t>(d.E) * (2 * d.I / BN) * (d.H / 128) * 1024, 4) !=
+            MOE_OK ||
+        encode_sf_map(&h->sf_maps.sfb2, h->sfb2, static_cast<uint64_t>(d.E) * (d.H / BN) * (d.I / 128) * 1024, 4) !=
+            MOE_OK)
         return MOE_ERR_CUDA;
     h->have_weights = true;
     h->last_stream = s;
@@ -390,7 +413,8 @@ int moe_forward(moe_handle_t h, int T, const uint8_t *x, const float *x_sf, cons
     auto mark = [&](int i) { return ev ? cudaEventRecord(ev[i], s) : cudaSuccess; };
     if (mark(0) != cudaSuccess || launch_dispatch(h->d, h->ws, c, h->num_sms, s) != cudaSuccess ||
         mark(1) != cudaSuccess ||
-        (bs ? launch_ffn_bs(h->maps, h->d, h->ws, c, h->sfb1, h->sfb2, wave_blocks(h), h->num_sms, s)
+        (bs ? launch_ffn_bs(h->maps, h->sf_maps, h->d, h->ws, c, h->sfb1, h->sfb2, wave_blocks(h), h->num_sms,
+                            ffn_paired(h, T), s)
             : launch_ffn(h->maps, h->d, h->ws, c, h->s1, h->s2, wave_blocks(h), h->num_sms, ffn_paired(h, T), s)) !=
             cudaSuccess ||
         mark(2) != cudaSuccess || launch_combine(h->d, h->ws, c, h->num_sms, s) != cudaSuccess ||

@@ -29,6 +29,8 @@
 // scale slots 256 + 16*s.  All waits carry a deadline (MOE_ERR_TIMEOUT).
 #include <cuda_bf16.h>
 
+#include <algorithm>
+
 #include "moe_internal.cuh"
 #include "ptx.cuh"
 
@@ -42,32 +44,59 @@ constexpr int TILE_RING = 4;
 constexpr uint32_t SF_COL = 256;          // scale slot s: columns SF_COL + 16*s (A: +0..3, B: +4..11)
 constexpr uint32_t SFA_BYTES = 512, SFB_BYTES = 1024, SF_STAGE_BYTES = SFA_BYTES + SFB_BYTES;
 static_assert(BKS == BK, "the block-scaled kernel stages whole 128-deep K blocks");
+// Two-CTA mode: one M = 256 UMMA covers two M-blocks of an expert, one per CTA of a cluster
+// pair; each CTA stages its 128 A rows, one 128-row half of the weight tile and its own copy
+// of the tile's scale blocks, so an operand stage is 32 KB instead of 48 KB and the same
+// 192 KB ring holds six stages.  Per K block each SM's shared memory then takes 33.5 KB of
+// TMA writes and serves 32 KB of UMMA reads, against 49.5 KB and 48 KB with one CTA per tile.
+constexpr uint32_t PAIR_B_BYTES = STAGE_B_BYTES / 2;
+constexpr uint32_t PAIR_STAGE_BYTES = STAGE_A_BYTES + PAIR_B_BYTES;
+constexpr int PAIR_STAGES = static_cast<int>((STAGES * STAGE_BYTES) / PAIR_STAGE_BYTES);
+static_assert(PAIR_STAGES * PAIR_STAGE_BYTES <= STAGES * STAGE_BYTES, "pair stages exceed the ring");
+static_assert(SF_COL + 16 * PAIR_STAGES <= TMEM_COLS, "scale slots exceed TMEM");
 
 // block-scaled instruction descriptor: B scale slice at bits 4-5, e4m3 A/B (formats 0),
 // K-major A and B, N>>3 at 17-22, UE8M0 scales (bit 23), M>>4 at 24-28, A scale slice at
 // 29-30
+template <int M>
 __device__ __forceinline__ uint32_t idesc_bs(int k)
 {
     return (static_cast<uint32_t>(k) << 4) | (static_cast<uint32_t>(BN >> 3) << 17) | (1u << 23) |
-           (static_cast<uint32_t>(BM >> 4) << 24) | (static_cast<uint32_t>(k) << 29);
+           (static_cast<uint32_t>(M >> 4) << 24) | (static_cast<uint32_t>(k) << 29);
 }
 
+// one CTA: D (128 rows) (+)= A x B^T with scales from this CTA's TMEM.  Two CTAs (issued by
+// the even CTA of the pair): D (256 rows, 128 in each CTA's TMEM at the same address), each
+// CTA holding 128 rows of A and half of B's N rows at the same shared-memory offsets, and
+// each CTA's own TMEM holding the scales of its A rows and of all 256 B rows
+template <bool PAIR>
 __device__ __forceinline__ void umma_bs(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
                                         uint32_t sfb, uint32_t accumulate)
 {
-    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
-                 "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d),
-                 "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
-                 : "memory");
+    if constexpr (PAIR)
+        asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+                     "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d),
+                     "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+                     : "memory");
+    else
+        asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+                     "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d),
+                     "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+                     : "memory");
 }
 
 // shared -> TMEM copy of 32 rows x 16 bytes (no swizzle, 8-row groups 128 B apart) into
-// four columns of every lane quarter
+// four columns of every lane quarter; the two-CTA form, issued by the even CTA, copies each
+// CTA's shared memory at that offset into its own TMEM
+template <bool PAIR>
 __device__ __forceinline__ void sf_copy(uint32_t taddr, uint32_t smem_addr)
 {
     const uint64_t desc = static_cast<uint64_t>((smem_addr >> 4) & 0x3FFF) | (static_cast<uint64_t>(8) << 16) |
                           (static_cast<uint64_t>(128 >> 4) << 32) | (static_cast<uint64_t>(1) << 46);
-    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
+    if constexpr (PAIR)
+        asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
+    else
+        asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
 }
 
 // the smallest power of two >= v for a positive normal fp32 v (exact)
@@ -78,8 +107,8 @@ __device__ __forceinline__ float pow2_ceil(float v)
 }
 
 struct __align__(8) BsBars {
-    uint64_t full[STAGES];
-    uint64_t empty[STAGES];
+    uint64_t full[PAIR_STAGES];
+    uint64_t empty[PAIR_STAGES];
     uint64_t tfull;
     uint64_t tempty;
     uint64_t xbar;
@@ -89,6 +118,7 @@ struct __align__(8) BsBars {
     uint32_t tmem_base;
     int abort;
     float amax[2][2][BM];
+    int32_t pair_off[1025];   // 2-CTA mode: first block pair of each expert (E <= 1024)
 };
 
 struct BsTiles {
@@ -116,17 +146,30 @@ struct BsTiles {
     }
 };
 
+// Tile of the list as one CTA sees it.  In 2-CTA mode a list entry is a pair of
+// consecutive M-blocks of one expert; CTA rank r takes the r-th block, and an expert with an
+// odd block count leaves rank 1 a null half (it loads no A rows and no A scales, only its
+// half of the weight tile and the tile's scales, and stores nothing).
+struct BsView {
+    int phase, nt, blk, e;
+    bool null_half;
+};
+
 }  // namespace
 
+template <bool PAIRED>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
-    ffn_bs_kernel(const __grid_constant__ FfnMaps maps, const Dims d, const Workspace ws, const CallArgs c,
-                  const uint8_t *__restrict__ sfb1, const uint8_t *__restrict__ sfb2, const int wave_blocks)
+    ffn_bs_kernel(const __grid_constant__ FfnMaps maps, const __grid_constant__ SfMaps sfm, const Dims d,
+                  const Workspace ws, const CallArgs c, const uint8_t *__restrict__ sfb1,
+                  const uint8_t *__restrict__ sfb2, const int wave_blocks)
 {
+    constexpr int NST = PAIRED ? PAIR_STAGES : STAGES;                     // stages in the ring
+    constexpr uint32_t SBYTES = PAIRED ? PAIR_STAGE_BYTES : STAGE_BYTES;   // operand bytes per stage
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
     BsBars *bars = reinterpret_cast<BsBars *>(smem + STAGES * STAGE_BYTES);
-    uint8_t *sf_smem = smem + STAGES * STAGE_BYTES + 8192;   // [STAGES][A 512 | B 1024]
+    uint8_t *sf_smem = smem + STAGES * STAGE_BYTES + 8192;   // [NST][A 512 | B 1024]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
@@ -134,12 +177,15 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                              *reinterpret_cast<volatile uint32_t *>(ws.hdr + HDR_ERR_STICKY);
         bars->abort = err != 0;
         if (!err) {
-            for (int s = 0; s < STAGES; ++s) {
+            // 2-CTA mode: only the even CTA's full and TMEM-empty barriers are used; both
+            // CTAs' loads count on its full barrier, both CTAs' epilogue warps arrive on its
+            // TMEM-empty barrier, and its UMMA commits arrive on both CTAs' empty / TMEM-full
+            for (int s = 0; s < NST; ++s) {
                 ptx::mbar_init(&bars->full[s], 1);
                 ptx::mbar_init(&bars->empty[s], 1);
             }
             ptx::mbar_init(&bars->tfull, 1);
-            ptx::mbar_init(&bars->tempty, EPI_WARPS);
+            ptx::mbar_init(&bars->tempty, (PAIRED ? 2 : 1) * EPI_WARPS);
             ptx::mbar_init(&bars->xbar, 32 * EPI_WARPS);
             for (int i = 0; i < TILE_RING; ++i) {
                 ptx::mbar_init(&bars->tile_full[i], 1);
@@ -149,25 +195,92 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         }
     }
     __syncthreads();
-    if (bars->abort)
-        return;
+    uint32_t rank = 0;
+    if constexpr (PAIRED) {
+        // both CTAs' barriers are initialised before any remote load, commit or arrive, and
+        // both take the same abort decision (a CTA must not leave while its peer may still
+        // write into its shared memory)
+        ptx::cluster_sync();
+        rank = ptx::cluster_ctarank();
+        const int peer_abort = ptx::ld_cluster_s32(ptx::map_cluster(&bars->abort, rank ^ 1u));
+        const bool stop = bars->abort || peer_abort;
+        ptx::cluster_sync();
+        if (stop)
+            return;
+        if (threadIdx.x == 0) {
+            int acc = 0;
+            for (int e = 0; e < d.E; ++e) {
+                bars->pair_off[e] = acc;
+                acc += (ws.blk_off[e + 1] - ws.blk_off[e] + 1) / 2;
+            }
+            bars->pair_off[d.E] = acc;
+        }
+    } else {
+        if (bars->abort)
+            return;
+    }
     if (warp == 1) {
-        ptx::tmem_alloc(&bars->tmem_base, TMEM_COLS);
-        ptx::tmem_relinquish();
+        if constexpr (PAIRED) {
+            ptx::tmem_alloc_pair(&bars->tmem_base, TMEM_COLS);
+            ptx::tmem_relinquish_pair();
+        } else {
+            ptx::tmem_alloc(&bars->tmem_base, TMEM_COLS);
+            ptx::tmem_relinquish();
+        }
     }
     ptx::tc_fence_before();
     __syncthreads();
+    if constexpr (PAIRED)
+        ptx::cluster_sync();   // both CTAs hold their TMEM before the even CTA's first copy or UMMA
     ptx::tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
 
-    const BsTiles tl{(2 * d.I) / BN, d.H / BN, ws.blk_off[d.E], wave_blocks};
+    const BsTiles tl{(2 * d.I) / BN, d.H / BN, PAIRED ? bars->pair_off[d.E] : ws.blk_off[d.E],
+                     PAIRED ? max(1, wave_blocks / 2) : wave_blocks};
     const int ntiles = tl.total();
+    const int nclusters = static_cast<int>(gridDim.x) / 2, cluster_id = static_cast<int>(blockIdx.x) / 2;
+    auto view_of = [&](int tile, uint32_t r) {
+        BsView v;
+        int unit;
+        tl.at(tile, v.phase, unit, v.nt);
+        if constexpr (PAIRED) {
+            int lo = 0, hi = d.E - 1;   // expert of pair `unit`: last e with pair_off[e] <= unit
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (bars->pair_off[mid] <= unit)
+                    lo = mid;
+                else
+                    hi = mid - 1;
+            }
+            v.e = lo;
+            const int b = ws.blk_off[lo] + 2 * (unit - bars->pair_off[lo]) + static_cast<int>(r);
+            v.null_half = b >= ws.blk_off[lo + 1];
+            v.blk = v.null_half ? b - 1 : b;
+        } else {
+            v.blk = unit;
+            v.e = ws.block_expert[unit];
+            v.null_half = false;
+        }
+        return v;
+    };
+    auto view = [&](int tile) { return view_of(tile, rank); };
+    // A bytes a CTA stages per K block for a tile (a partly filled M-block loads only the
+    // 32-row groups that hold valid rows; a null half loads none), plus the scale blocks
+    auto a_parts = [&](const BsView &v) {
+        return v.null_half ? 0 : (ws.block_rows[v.blk] + A_ROWS_PART - 1) / A_ROWS_PART;
+    };
+    auto a_stage_bytes = [&](int n_part) {
+        return n_part < BM / A_ROWS_PART ? static_cast<uint32_t>(n_part * A_ROWS_PART * BKS) : STAGE_A_BYTES;
+    };
     const int NKB1 = d.H / BK, NKB2 = d.I / BK;
     const uint32_t l1_target = static_cast<uint32_t>(EPI_WARPS * tl.NT1);
     const uint64_t deadline = ptx::globaltimer() + static_cast<uint64_t>(c.timeout_ns);
 
+    // Registers: launched at 168 per thread (384 x 168 = 64512); the producer / issuer
+    // warpgroup gives (168-72) x 128 back and the two epilogue warpgroups take (216-168) x 256
+    // (the producer keeps the next tile's metadata live without spilling).
     if (warp < 4) {
-        ptx::setmaxnreg_dec<40>();
+        ptx::setmaxnreg_dec<72>();
         if (warp == 0) {
             // -------------------------------------------------------- TMA producer ----
             if (lane == 0) {
@@ -180,14 +293,45 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 const uint64_t pol_b_shared = ptx::policy_evict_normal();
                 uint32_t it = 0, tcount = 0;
                 bool ok = true;
-                // tiles are claimed one ahead, so the claim's round trip to L2 overlaps the
-                // loads of the tile before (a CTA holds at most one claimed, unstarted tile;
-                // the smallest unfinished tile is always being worked on)
-                int next = static_cast<int>(atomicAdd(ws.hdr + HDR_TILE_NEXT, 1u));
+                // One CTA per tile: tiles are claimed from the global counter one ahead (a CTA
+                // holds at most one claimed, unstarted tile; the smallest unfinished tile is
+                // always being worked on).  2-CTA mode: round-robin over clusters in list order
+                // (both CTAs of a pair see the same tiles).
+                auto claim_after = [&](int t) {
+                    return PAIRED ? t + nclusters : static_cast<int>(atomicAdd(ws.hdr + HDR_TILE_NEXT, 1u));
+                };
+                // The next tile is claimed, and its metadata (its M-block's expert and valid
+                // rows, the expert's M-block count, the M-block's gate_up completion count) read,
+                // in three steps taken while the producer waits for free stages of the current
+                // tile, each step's reads landing before the next step uses them.  Otherwise a
+                // chain of dependent global reads sits between a tile's last load and the next
+                // tile's first, and short (down) tiles start with the UMMA pipe dry.
+                int m_tile = PAIRED ? cluster_id : static_cast<int>(atomicAdd(ws.hdr + HDR_TILE_NEXT, 1u));
+                BsView m_v{};
+                int m_rows = 0, m_eblocks = 0;
+                uint32_t m_l1 = 0;
+                auto fetch = [&](int step, int cur) {
+                    if (step == 0) {
+                        m_tile = claim_after(cur);
+                        return;
+                    }
+                    if (m_tile >= ntiles)
+                        return;
+                    if (step == 1) {
+                        m_v = view(m_tile);
+                        m_rows = ws.block_rows[m_v.blk];
+                        m_l1 = m_v.phase == 2 ? ptx::ld_relaxed_gpu(ws.l1_done + m_v.blk) : 0u;
+                    } else {
+                        m_eblocks = ws.blk_off[m_v.e + 1] - ws.blk_off[m_v.e];
+                    }
+                };
+                fetch(1, 0);
+                fetch(2, 0);
                 while (ok) {
-                    const int tile = next;
-                    if (tile < ntiles)
-                        next = static_cast<int>(atomicAdd(ws.hdr + HDR_TILE_NEXT, 1u));
+                    const int tile = m_tile;
+                    const BsView tv = m_v;
+                    const int tv_rows = m_rows, tv_eblocks = m_eblocks;
+                    const uint32_t tv_l1 = m_l1;
                     const uint32_t slot = tcount % TILE_RING, sph = (tcount / TILE_RING) & 1u;
                     if (!ptx::mbar_wait(&bars->tile_empty[slot], sph ^ 1u, deadline)) {
                         ok = false;
@@ -198,69 +342,115 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     ++tcount;
                     if (tile >= ntiles)
                         break;
-                    int phase, blk, nt;
-                    tl.at(tile, phase, blk, nt);
-                    const int e = ws.block_expert[blk];
-                    const uint64_t pol_b = ws.blk_off[e + 1] - ws.blk_off[e] > 1 ? pol_b_shared : pol_b_once;
-                    const int n_part = (ws.block_rows[blk] + A_ROWS_PART - 1) / A_ROWS_PART;
+                    int fstep = 0;   // steps of the next tile's claim and metadata done
+                    const int phase = tv.phase, blk = tv.blk, nt = tv.nt, e = tv.e;
+                    const uint64_t pol_b = tv_eblocks > 1 ? pol_b_shared : pol_b_once;
+                    const int n_part = tv.null_half ? 0 : (tv_rows + A_ROWS_PART - 1) / A_ROWS_PART;
                     const bool part = n_part < BM / A_ROWS_PART;
-                    const uint32_t a_bytes = part ? static_cast<uint32_t>(n_part * A_ROWS_PART * BKS) : STAGE_A_BYTES;
+                    const uint32_t a_bytes = a_stage_bytes(n_part);
+                    // bytes the stage's full barrier waits for: this CTA's, plus (2-CTA mode,
+                    // even CTA) the odd CTA's, whose loads count on the even CTA's barrier
+                    uint32_t tx_bytes = a_bytes + (PAIRED ? PAIR_B_BYTES : STAGE_B_BYTES) +
+                                        (tv.null_half ? 0u : SFA_BYTES) + SFB_BYTES;
+                    if (PAIRED && rank == 0) {
+                        const BsView ov = view_of(tile, 1);
+                        tx_bytes += a_stage_bytes(a_parts(ov)) + PAIR_B_BYTES + (ov.null_half ? 0u : SFA_BYTES) + SFB_BYTES;
+                    }
                     const CUtensorMap *ta = phase == 1 ? (part ? &maps.a1p : &maps.a1) : (part ? &maps.a2p : &maps.a2);
-                    const CUtensorMap *tb = phase == 1 ? &maps.b1 : &maps.b2;
+                    const CUtensorMap *tb = PAIRED ? (phase == 1 ? &maps.b1h : &maps.b2h) : (phase == 1 ? &maps.b1 : &maps.b2);
                     const int nkb = phase == 1 ? NKB1 : NKB2;
                     const int tile0 = (e * (phase == 1 ? tl.NT1 : tl.NT2) + nt) * nkb;
                     // scale blocks: A per (M-block, K block), B per (weight tile, K block)
                     const uint8_t *sfa_src = (phase == 1 ? ws.pool_sfe : ws.act_sfe) +
                                              static_cast<long long>(blk) * nkb * SFA_BYTES;
                     const uint8_t *sfb_src = (phase == 1 ? sfb1 : sfb2) + static_cast<long long>(tile0) * SFB_BYTES;
-                    if (phase == 2) {
+                    if (phase == 2 && !tv.null_half) {
                         // the act rows and their scales of this block are complete once every
                         // epilogue warp of every gate_up tile of the block has released them
-                        for (uint32_t i = 0;; ++i) {
-                            if (ptx::ld_acquire_gpu(ws.l1_done + blk) >= l1_target)
-                                break;
-                            if ((i & 63u) == 63u && ptx::globaltimer() > deadline) {
-                                ok = false;
-                                break;
+                        // (a count read early and already complete is made an acquire by the
+                        // fence; otherwise acquire loads until it is)
+                        if (tv_l1 >= l1_target) {
+                            ptx::fence_acq_rel_gpu();
+                        } else {
+                            for (uint32_t i = 0;; ++i) {
+                                if (ptx::ld_acquire_gpu(ws.l1_done + blk) >= l1_target)
+                                    break;
+                                if ((i & 63u) == 63u && ptx::globaltimer() > deadline) {
+                                    ok = false;
+                                    break;
+                                }
                             }
+                            if (!ok)
+                                break;
                         }
-                        if (!ok)
-                            break;
                         ptx::fence_proxy_async_global();
                     }
                     for (int kb = 0; kb < nkb; ++kb, ++it) {
-                        const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+                        const uint32_t s = it % NST, ph = (it / NST) & 1u;
+                        // a step of the next tile's claim / metadata, only when the stage is
+                        // not free yet (the loads of a starving pipe are never held back)
+                        if (fstep < 3 && !ptx::mbar_try_wait(&bars->empty[s], ph ^ 1u))
+                            fetch(fstep++, tile);
                         if (!ptx::mbar_wait(&bars->empty[s], ph ^ 1u, deadline)) {
                             ok = false;
                             break;
                         }
-                        uint8_t *sa = smem + s * STAGE_BYTES;
+                        uint8_t *sa = smem + s * SBYTES;
                         uint8_t *ss = sf_smem + s * SF_STAGE_BYTES;
-                        ptx::mbar_arrive_expect_tx(&bars->full[s], a_bytes + STAGE_B_BYTES + SF_STAGE_BYTES);
-                        if (part) {
-                            for (int g = 0; g < n_part; ++g)
-                                ptx::tma_load_2d(sa + g * A_ROWS_PART * BKS, ta, &bars->full[s], kb * BK,
-                                                 blk * BM + g * A_ROWS_PART, pol_a);
+                        if (!PAIRED || rank == 0)
+                            ptx::mbar_arrive_expect_tx(&bars->full[s], tx_bytes);
+                        if constexpr (PAIRED) {
+                            // own A rows, own half of the weight tile, own copies of the scale
+                            // blocks (this block's A scales; all 256 weight rows' scales),
+                            // counted on the even CTA's full barrier
+                            const uint32_t fb = ptx::map_cluster(&bars->full[s], 0);
+                            if (part) {
+                                for (int g = 0; g < n_part; ++g)
+                                    ptx::tma_load_2d_pair(sa + g * A_ROWS_PART * BKS, ta, fb, kb * BK,
+                                                          blk * BM + g * A_ROWS_PART, pol_a);
+                            } else {
+                                ptx::tma_load_2d_pair(sa, ta, fb, kb * BK, blk * BM, pol_a);
+                            }
+                            ptx::tma_load_2d_pair(sa + STAGE_A_BYTES, tb, fb, 0,
+                                                  (tile0 + kb) * BN + static_cast<int>(rank) * (BN / 2), pol_b);
+                            if (!tv.null_half)
+                                ptx::tma_load_2d_pair(ss, phase == 1 ? &sfm.sfa1 : &sfm.sfa2, fb, 0,
+                                                      (blk * nkb + kb) * static_cast<int>(SFA_BYTES / 256), pol_a);
+                            ptx::tma_load_2d_pair(ss + SFA_BYTES, phase == 1 ? &sfm.sfb1 : &sfm.sfb2, fb, 0,
+                                                  (tile0 + kb) * static_cast<int>(SFB_BYTES / 256), pol_b);
                         } else {
-                            ptx::tma_load_2d(sa, ta, &bars->full[s], kb * BK, blk * BM, pol_a);
+                            if (part) {
+                                for (int g = 0; g < n_part; ++g)
+                                    ptx::tma_load_2d(sa + g * A_ROWS_PART * BKS, ta, &bars->full[s], kb * BK,
+                                                     blk * BM + g * A_ROWS_PART, pol_a);
+                            } else {
+                                ptx::tma_load_2d(sa, ta, &bars->full[s], kb * BK, blk * BM, pol_a);
+                            }
+                            ptx::tma_load_2d(sa + STAGE_A_BYTES, tb, &bars->full[s], 0, (tile0 + kb) * BN, pol_b);
+                            ptx::bulk_load(ss, sfa_src + kb * SFA_BYTES, SFA_BYTES, &bars->full[s]);
+                            ptx::bulk_load(ss + SFA_BYTES, sfb_src + static_cast<long long>(kb) * SFB_BYTES, SFB_BYTES,
+                                           &bars->full[s]);
                         }
-                        ptx::tma_load_2d(sa + STAGE_A_BYTES, tb, &bars->full[s], 0, (tile0 + kb) * BN, pol_b);
-                        ptx::bulk_load(ss, sfa_src + kb * SFA_BYTES, SFA_BYTES, &bars->full[s]);
-                        ptx::bulk_load(ss + SFA_BYTES, sfb_src + static_cast<long long>(kb) * SFB_BYTES, SFB_BYTES,
-                                       &bars->full[s]);
                     }
+                    while (ok && fstep < 3)
+                        fetch(fstep++, tile);
                 }
                 if (!ok)
                     record_error(ws.hdr, DEV_TIMEOUT);
+                // drain: every issued load has landed before the CTA may exit (2-CTA mode:
+                // has been consumed by the UMMA, whose commit reaches both CTAs)
                 const uint64_t dl = ptx::globaltimer() + static_cast<uint64_t>(c.timeout_ns);
-                for (uint32_t i = it > STAGES ? it - STAGES : 0; i < it; ++i)
-                    ptx::mbar_wait(&bars->full[i % STAGES], (i / STAGES) & 1u, dl);
+                for (uint32_t i = it > NST ? it - NST : 0; i < it; ++i)
+                    ptx::mbar_wait(PAIRED ? &bars->empty[i % NST] : &bars->full[i % NST], (i / NST) & 1u, dl);
             }
         } else if (warp == 1) {
             // -------------------------------------------------------- UMMA issuer -----
+            // (2-CTA mode: the even CTA issues every scale copy, UMMA and commit of the pair;
+            // the odd CTA's issuer only takes its tile slots)
             if (lane == 0) {
                 uint32_t it = 0, tcount = 0, acc_n = 0;
                 bool ok = true;
+                const bool issuer = !PAIRED || rank == 0;
                 while (ok) {
                     const uint32_t slot = tcount % TILE_RING, sph = (tcount / TILE_RING) & 1u;
                     if (!ptx::mbar_wait(&bars->tile_full[slot], sph, deadline)) {
@@ -272,17 +462,20 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     ++tcount;
                     if (tile < 0)
                         break;
-                    int phase, blk, nt;
-                    tl.at(tile, phase, blk, nt);
+                    if (!issuer)
+                        continue;
+                    int phase, unit, nt;
+                    tl.at(tile, phase, unit, nt);
                     const int nkb = phase == 1 ? NKB1 : NKB2;
                     // the previous tile's accumulator has been read by every epilogue warp
+                    // (of both CTAs in 2-CTA mode)
                     if (!ptx::mbar_wait(&bars->tempty, (acc_n & 1u) ^ 1u, deadline)) {
                         ok = false;
                         break;
                     }
                     ptx::tc_fence_after();
                     for (int kb = 0; kb < nkb; ++kb, ++it) {
-                        const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+                        const uint32_t s = it % NST, ph = (it / NST) & 1u;
                         if (!ptx::mbar_wait(&bars->full[s], ph, deadline)) {
                             ok = false;
                             break;
@@ -290,40 +483,49 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                         ptx::tc_fence_after();
                         const uint32_t ss = ptx::smem_u32(sf_smem + s * SF_STAGE_BYTES);
                         const uint32_t sfa = tmem + SF_COL + 16 * s, sfb = sfa + 4;
-                        sf_copy(sfa, ss);
-                        sf_copy(sfb, ss + SFA_BYTES);
-                        sf_copy(sfb + 4, ss + SFA_BYTES + 512);
-                        const uint32_t a_addr = ptx::smem_u32(smem + s * STAGE_BYTES);
+                        sf_copy<PAIRED>(sfa, ss);
+                        sf_copy<PAIRED>(sfb, ss + SFA_BYTES);
+                        sf_copy<PAIRED>(sfb + 4, ss + SFA_BYTES + 512);
+                        const uint32_t a_addr = ptx::smem_u32(smem + s * SBYTES);
                         const uint64_t adesc = ptx::kmajor_swizzled_desc<BKS>(a_addr);
                         const uint64_t bdesc = ptx::kmajor_swizzled_desc<BKS>(a_addr + STAGE_A_BYTES);
 #pragma unroll
                         for (int k = 0; k < BK / 32; ++k)   // +32 bytes along K = +2 in the >>4 field
-                            umma_bs(tmem, adesc + 2 * k, bdesc + 2 * k, idesc_bs(k), sfa, sfb,
-                                    (kb > 0 || k > 0) ? 1u : 0u);
-                        ptx::umma_commit(&bars->empty[s]);
+                            umma_bs<PAIRED>(tmem, adesc + 2 * k, bdesc + 2 * k, idesc_bs<PAIRED ? 2 * BM : BM>(k), sfa,
+                                            sfb, (kb > 0 || k > 0) ? 1u : 0u);
+                        if constexpr (PAIRED)
+                            ptx::umma_commit_pair(&bars->empty[s], static_cast<uint16_t>(0x3));
+                        else
+                            ptx::umma_commit(&bars->empty[s]);
                     }
                     if (!ok)
                         break;
-                    ptx::umma_commit(&bars->tfull);
+                    if constexpr (PAIRED)
+                        ptx::umma_commit_pair(&bars->tfull, static_cast<uint16_t>(0x3));
+                    else
+                        ptx::umma_commit(&bars->tfull);
                     ++acc_n;
                 }
                 if (!ok)
                     record_error(ws.hdr, DEV_TIMEOUT);
+                // drain: the last commit arrives once every issued copy and MMA has completed
                 if (it > 0) {
                     const uint64_t dl = ptx::globaltimer() + static_cast<uint64_t>(c.timeout_ns);
                     const uint32_t i = it - 1;
-                    ptx::mbar_wait(&bars->empty[i % STAGES], (i / STAGES) & 1u, dl);
+                    ptx::mbar_wait(&bars->empty[i % NST], (i / NST) & 1u, dl);
                 }
             }
         }
     } else {
         // ------------------------------------------------------------ epilogue --------
-        ptx::setmaxnreg_inc<232>();
+        ptx::setmaxnreg_inc<216>();
         const int wg = (warp - 4) >> 2;          // column half of the tile
         const int q = warp & 3;                  // TMEM lane quarter this warp may access
         const int row = q * 32 + lane;           // tile row = TMEM lane
         const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
         uint32_t tcount = 0, xcount = 0, acc_n = 0;
+        // TMEM-empty arrivals go to the even CTA's barrier in 2-CTA mode
+        const uint32_t tempty0 = PAIRED ? ptx::map_cluster(&bars->tempty, 0) : 0u;
         bool ok = true;
         while (ok) {
             const uint32_t slot = tcount % TILE_RING, sph = (tcount / TILE_RING) & 1u;
@@ -339,7 +541,16 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             if (tile < 0)
                 break;
             int phase, blk, nt;
-            tl.at(tile, phase, blk, nt);
+            bool null_half = false;
+            if constexpr (PAIRED) {
+                const BsView tv = view(tile);
+                phase = tv.phase;
+                blk = tv.blk;
+                nt = tv.nt;
+                null_half = tv.null_half;
+            } else {
+                tl.at(tile, phase, blk, nt);
+            }
             const long long prow = static_cast<long long>(blk) * BM + row;
             // the whole tile, already scaled, in one read of this warp's 32 rows x 128 columns
             if (!__all_sync(0xFFFFFFFFu, ptx::mbar_wait(&bars->tfull, acc_n & 1u, deadline))) {
@@ -348,6 +559,16 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             }
             ++acc_n;
             ptx::tc_fence_after();
+            if (null_half) {
+                // no rows of this CTA in this tile: the UMMA still wrote its accumulator, so
+                // hand it back unread (after the TMEM-full wait, which keeps both CTAs' arrivals
+                // for one tile in one phase of the even CTA's TMEM-empty barrier)
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    ptx::mbar_arrive_cluster(tempty0);
+                continue;
+            }
             float acc[128];
             const uint32_t taddr = tmem + lane_base + wg * 128;
 #pragma unroll
@@ -365,8 +586,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             }
             ptx::tc_fence_before();
             __syncwarp();
-            if (lane == 0)
-                ptx::mbar_arrive(&bars->tempty);
+            if (lane == 0) {
+                if constexpr (PAIRED)
+                    ptx::mbar_arrive_cluster(tempty0);
+                else
+                    ptx::mbar_arrive(&bars->tempty);
+            }
             const int rows = ws.block_rows[blk];
             if (phase == 1) {
                 // SwiGLU on the 64 (gate, up) pairs of this row and column half, then 1x128
@@ -448,35 +673,83 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 
     ptx::tc_fence_before();
     __syncthreads();
+    if constexpr (PAIRED)
+        ptx::cluster_sync();   // the peer neither reads this CTA's stages nor writes its TMEM any more
     if (warp == 1) {
         ptx::tc_fence_after();
-        ptx::tmem_dealloc(tmem, TMEM_COLS);
+        if constexpr (PAIRED)
+            ptx::tmem_dealloc_pair(tmem, TMEM_COLS);
+        else
+            ptx::tmem_dealloc(tmem, TMEM_COLS);
     }
 }
 
-cudaError_t launch_ffn_bs(const FfnMaps &maps, const Dims &d, const Workspace &ws, const CallArgs &c,
-                          const uint8_t *sfb1, const uint8_t *sfb2, int wave_blocks, int num_sms, cudaStream_t s)
+cudaError_t launch_ffn_bs(const FfnMaps &maps, const SfMaps &sf_maps, const Dims &d, const Workspace &ws,
+                          const CallArgs &c, const uint8_t *sfb1, const uint8_t *sfb2, int wave_blocks, int num_sms,
+                          bool paired, cudaStream_t s)
 {
-    static bool configured = false;
-    constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + 8192 + STAGES * SF_STAGE_BYTES;
+    static bool configured[2] = {false, false};
+    static int paired_grid = 0;
+    static int paired_coop = 1;   // cooperative attribute accepted together with clusters
+    constexpr int SMEM1 = 1024 + STAGES * STAGE_BYTES + 8192 + STAGES * SF_STAGE_BYTES;
+    constexpr int SMEM2 = 1024 + STAGES * STAGE_BYTES + 8192 + PAIR_STAGES * SF_STAGE_BYTES;
     static_assert(sizeof(BsBars) <= 8192, "barrier block");
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(ffn_bs_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+    static_assert(SMEM2 <= 227 * 1024, "shared memory per CTA");
+    const int smem = paired ? SMEM2 : SMEM1;
+    void *kern = paired ? reinterpret_cast<void *>(ffn_bs_kernel<true>) : reinterpret_cast<void *>(ffn_bs_kernel<false>);
+    if (!configured[paired]) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess)
             return e;
-        configured = true;
+        configured[paired] = true;
     }
     FfnMaps m = maps;
+    SfMaps sm = sf_maps;
     Dims dd = d;
     Workspace ww = ws;
     CallArgs cc = c;
     const uint8_t *p1 = sfb1;
     const uint8_t *p2 = sfb2;
     int wb = wave_blocks;
-    void *args[] = {&m, &dd, &ww, &cc, &p1, &p2, &wb};
+    void *args[] = {&m, &sm, &dd, &ww, &cc, &p1, &p2, &wb};
     // down tiles wait on gate_up tiles of other CTAs: all CTAs must be resident at once
-    return cudaLaunchCooperativeKernel(reinterpret_cast<void *>(ffn_bs_kernel), dim3(num_sms), dim3(GEMM_THREADS), args,
-                                       SMEM, s);
+    if (!paired)
+        return cudaLaunchCooperativeKernel(kern, dim3(num_sms), dim3(GEMM_THREADS), args, smem, s);
+
+    cudaLaunchAttribute attrs[2];
+    attrs[0].id = cudaLaunchAttributeClusterDimension;
+    attrs[0].val.clusterDim.x = 2;
+    attrs[0].val.clusterDim.y = 1;
+    attrs[0].val.clusterDim.z = 1;
+    attrs[1].id = cudaLaunchAttributeCooperative;
+    attrs[1].val.cooperative = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(GEMM_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = attrs;
+    if (paired_grid == 0) {
+        // every cluster resident at once: as many clusters as can be active together
+        cfg.gridDim = dim3(num_sms);
+        cfg.numAttrs = 1;
+        int clusters = 0;
+        cudaError_t e = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
+        if (e != cudaSuccess)
+            return e;
+        if (clusters < 1)
+            return cudaErrorInvalidConfiguration;
+        paired_grid = 2 * std::min(clusters, num_sms / 2);
+    }
+    cfg.gridDim = dim3(paired_grid);
+    if (paired_coop) {
+        cfg.numAttrs = 2;
+        if (cudaLaunchKernelExC(&cfg, kern, args) == cudaSuccess)
+            return cudaSuccess;
+        cudaGetLastError();   // this runtime rejects cooperative + cluster: clusters alone
+        paired_coop = 0;
+    }
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelExC(&cfg, kern, args);
 }
 
 // ------------------------------------------------------------------ weight scales -----

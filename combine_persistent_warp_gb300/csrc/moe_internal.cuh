@@ -107,10 +107,17 @@ cudaError_t launch_ffn(const FfnMaps &maps, const Dims &d, const Workspace &ws, 
 cudaError_t trace_read(void *dst, size_t bytes);
 cudaError_t trace_clear();
 #endif
+// UE8M0 scale blocks as 2-D byte maps of 256-byte rows (no swizzle): sfa1 / sfa2 over the
+// pool / act scale blocks with 2-row boxes (512 B, one M-block and K block), sfb1 / sfb2 over
+// the weight tiles' scale blocks with 4-row boxes (1 KB, one weight tile and K block)
+struct SfMaps {
+    CUtensorMap sfa1, sfa2, sfb1, sfb2;
+};
 // power-of-two scales: the block-scaled FFN kernel (ffn_bs.cu) and the load-time UE8M0
-// scale blocks of the weight tiles
-cudaError_t launch_ffn_bs(const FfnMaps &maps, const Dims &d, const Workspace &ws, const CallArgs &c,
-                          const uint8_t *sfb1, const uint8_t *sfb2, int wave_blocks, int num_sms, cudaStream_t s);
+// scale blocks of the weight tiles; paired: 2-CTA clusters (one M = 256 UMMA per block pair)
+cudaError_t launch_ffn_bs(const FfnMaps &maps, const SfMaps &sf_maps, const Dims &d, const Workspace &ws,
+                          const CallArgs &c, const uint8_t *sfb1, const uint8_t *sfb2, int wave_blocks, int num_sms,
+                          bool paired, cudaStream_t s);
 cudaError_t launch_build_sfb(const float *s, uint8_t *dst, int E, int N, int K, int gate_up_I, uint32_t *bad,
                              cudaStream_t st);
 cudaError_t launch_combine(const Dims &d, const Workspace &ws, const CallArgs &c, int num_sms,

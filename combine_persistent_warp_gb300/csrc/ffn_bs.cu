@@ -114,6 +114,7 @@ struct __align__(8) BsBars {
     uint64_t xbar;
     uint64_t tile_full[TILE_RING];
     uint64_t tile_empty[TILE_RING];
+    uint64_t dep[TILE_RING];   // dependency warp -> producer: this slot's tile may be loaded
     int tile_ring[TILE_RING];
     uint32_t tmem_base;
     int abort;
@@ -189,7 +190,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             ptx::mbar_init(&bars->xbar, 32 * EPI_WARPS);
             for (int i = 0; i < TILE_RING; ++i) {
                 ptx::mbar_init(&bars->tile_full[i], 1);
-                ptx::mbar_init(&bars->tile_empty[i], 1 + EPI_WARPS);
+                ptx::mbar_init(&bars->tile_empty[i], 2 + EPI_WARPS);   // issuer, dependency warp, epilogue
+                ptx::mbar_init(&bars->dep[i], 1);
             }
             ptx::fence_mbar_init();
         }
@@ -300,49 +302,53 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 auto claim_after = [&](int t) {
                     return PAIRED ? t + nclusters : static_cast<int>(atomicAdd(ws.hdr + HDR_TILE_NEXT, 1u));
                 };
-                // The next tile is claimed, and its metadata (its M-block's expert and valid
-                // rows, the expert's M-block count, the M-block's gate_up completion count) read,
-                // in three steps taken while the producer waits for free stages of the current
-                // tile, each step's reads landing before the next step uses them.  Otherwise a
-                // chain of dependent global reads sits between a tile's last load and the next
-                // tile's first, and short (down) tiles start with the UMMA pipe dry.
+                // The next tile is claimed, published to the ring (so the issuer, the epilogue
+                // and the dependency warp see it a tile ahead), and its metadata (its M-block's
+                // expert and valid rows, the expert's M-block count) read, in three steps taken
+                // while the producer waits for free stages of the current tile, two K blocks
+                // apart so each step's reads land before the next uses them.  Otherwise a chain of dependent
+                // global reads sits between a tile's last load and the next tile's first, and
+                // short (down) tiles start with the UMMA pipe dry.
+                uint32_t pcount = 0;   // ring slots filled
+                auto push = [&](int t) {
+                    const uint32_t slot = pcount % TILE_RING, sph = (pcount / TILE_RING) & 1u;
+                    if (!ptx::mbar_wait(&bars->tile_empty[slot], sph ^ 1u, deadline))
+                        return false;
+                    bars->tile_ring[slot] = t < ntiles ? t : -1;
+                    ptx::mbar_arrive(&bars->tile_full[slot]);
+                    ++pcount;
+                    return true;
+                };
                 int m_tile = PAIRED ? cluster_id : static_cast<int>(atomicAdd(ws.hdr + HDR_TILE_NEXT, 1u));
                 BsView m_v{};
                 int m_rows = 0, m_eblocks = 0;
-                uint32_t m_l1 = 0;
                 auto fetch = [&](int step, int cur) {
                     if (step == 0) {
                         m_tile = claim_after(cur);
-                        return;
+                        return true;
                     }
-                    if (m_tile >= ntiles)
-                        return;
                     if (step == 1) {
-                        m_v = view(m_tile);
-                        m_rows = ws.block_rows[m_v.blk];
-                        m_l1 = m_v.phase == 2 ? ptx::ld_relaxed_gpu(ws.l1_done + m_v.blk) : 0u;
-                    } else {
+                        if (!push(m_tile))
+                            return false;
+                        if (m_tile < ntiles) {
+                            m_v = view(m_tile);
+                            m_rows = ws.block_rows[m_v.blk];
+                        }
+                    } else if (m_tile < ntiles) {
                         m_eblocks = ws.blk_off[m_v.e + 1] - ws.blk_off[m_v.e];
                     }
+                    return true;
                 };
-                fetch(1, 0);
-                fetch(2, 0);
+                ok = fetch(1, 0) && fetch(2, 0);
                 while (ok) {
                     const int tile = m_tile;
                     const BsView tv = m_v;
                     const int tv_rows = m_rows, tv_eblocks = m_eblocks;
-                    const uint32_t tv_l1 = m_l1;
                     const uint32_t slot = tcount % TILE_RING, sph = (tcount / TILE_RING) & 1u;
-                    if (!ptx::mbar_wait(&bars->tile_empty[slot], sph ^ 1u, deadline)) {
-                        ok = false;
-                        break;
-                    }
-                    bars->tile_ring[slot] = tile < ntiles ? tile : -1;
-                    ptx::mbar_arrive(&bars->tile_full[slot]);
                     ++tcount;
                     if (tile >= ntiles)
                         break;
-                    int fstep = 0;   // steps of the next tile's claim and metadata done
+                    int fstep = 0, fkb = -2;   // next tile's steps done; K block of the last one
                     const int phase = tv.phase, blk = tv.blk, nt = tv.nt, e = tv.e;
                     const uint64_t pol_b = tv_eblocks > 1 ? pol_b_shared : pol_b_once;
                     const int n_part = tv.null_half ? 0 : (tv_rows + A_ROWS_PART - 1) / A_ROWS_PART;
@@ -365,32 +371,28 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                                              static_cast<long long>(blk) * nkb * SFA_BYTES;
                     const uint8_t *sfb_src = (phase == 1 ? sfb1 : sfb2) + static_cast<long long>(tile0) * SFB_BYTES;
                     if (phase == 2 && !tv.null_half) {
-                        // the act rows and their scales of this block are complete once every
-                        // epilogue warp of every gate_up tile of the block has released them
-                        // (a count read early and already complete is made an acquire by the
-                        // fence; otherwise acquire loads until it is)
-                        if (tv_l1 >= l1_target) {
-                            ptx::fence_acq_rel_gpu();
-                        } else {
-                            for (uint32_t i = 0;; ++i) {
-                                if (ptx::ld_acquire_gpu(ws.l1_done + blk) >= l1_target)
-                                    break;
-                                if ((i & 63u) == 63u && ptx::globaltimer() > deadline) {
-                                    ok = false;
-                                    break;
-                                }
-                            }
-                            if (!ok)
-                                break;
+                        // the act rows and their scales of this block are complete: the
+                        // dependency warp has acquired the block's gate_up completion count
+                        // (a GPU-scope acquire here would also wait for this thread's loads in
+                        // flight)
+                        if (!ptx::mbar_wait(&bars->dep[slot], sph, deadline)) {
+                            ok = false;
+                            break;
                         }
                         ptx::fence_proxy_async_global();
                     }
                     for (int kb = 0; kb < nkb; ++kb, ++it) {
                         const uint32_t s = it % NST, ph = (it / NST) & 1u;
-                        // a step of the next tile's claim / metadata, only when the stage is
-                        // not free yet (the loads of a starving pipe are never held back)
-                        if (fstep < 3 && !ptx::mbar_try_wait(&bars->empty[s], ph ^ 1u))
-                            fetch(fstep++, tile);
+                        // a step of the next tile's claim / publication / metadata, only when the
+                        // stage is not free yet (the loads of a starving pipe are never held back)
+                        // and two K blocks after the step before (whose reads it uses)
+                        if (fstep < 3 && kb >= fkb + 2 && !ptx::mbar_try_wait(&bars->empty[s], ph ^ 1u)) {
+                            fkb = kb;
+                            if (!fetch(fstep++, tile)) {
+                                ok = false;
+                                break;
+                            }
+                        }
                         if (!ptx::mbar_wait(&bars->empty[s], ph ^ 1u, deadline)) {
                             ok = false;
                             break;
@@ -433,7 +435,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                         }
                     }
                     while (ok && fstep < 3)
-                        fetch(fstep++, tile);
+                        ok = fetch(fstep++, tile);
                 }
                 if (!ok)
                     record_error(ws.hdr, DEV_TIMEOUT);
@@ -442,6 +444,44 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 const uint64_t dl = ptx::globaltimer() + static_cast<uint64_t>(c.timeout_ns);
                 for (uint32_t i = it > NST ? it - NST : 0; i < it; ++i)
                     ptx::mbar_wait(PAIRED ? &bars->empty[i % NST] : &bars->full[i % NST], (i / NST) & 1u, dl);
+            }
+        } else if (warp == 2) {
+            // -------------------------------------------------------- dependency warp --
+            // A down tile reads act rows and scales that gate_up tiles of other CTAs wrote:
+            // for each published tile this lane acquires (GPU scope) the M-block's gate_up
+            // completion count, then releases the tile to the producer through the slot's
+            // CTA-scope barrier (gate_up tiles and null halves at once).
+            if (lane == 0) {
+                uint32_t tcount = 0;
+                bool ok = true;
+                while (ok) {
+                    const uint32_t slot = tcount % TILE_RING, sph = (tcount / TILE_RING) & 1u;
+                    if (!ptx::mbar_wait(&bars->tile_full[slot], sph, deadline)) {
+                        ok = false;
+                        break;
+                    }
+                    const int tile = bars->tile_ring[slot];
+                    ptx::mbar_arrive(&bars->tile_empty[slot]);
+                    ++tcount;
+                    if (tile < 0)
+                        break;
+                    const BsView v = view(tile);
+                    if (v.phase == 2 && !v.null_half) {
+                        for (uint32_t i = 0;; ++i) {
+                            if (ptx::ld_acquire_gpu(ws.l1_done + v.blk) >= l1_target)
+                                break;
+                            if ((i & 63u) == 63u && ptx::globaltimer() > deadline) {
+                                ok = false;
+                                break;
+                            }
+                        }
+                        if (!ok)
+                            break;
+                    }
+                    ptx::mbar_arrive(&bars->dep[slot]);
+                }
+                if (!ok)
+                    record_error(ws.hdr, DEV_TIMEOUT);
             }
         } else if (warp == 1) {
             // -------------------------------------------------------- UMMA issuer -----
@@ -647,22 +687,62 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 if (lane == 0)
                     ptx::red_release_add(ws.l1_done + blk, 1u);
             } else {
-                if (row < rows) {
-                    const uint32_t t = ws.meta[prow * 3 + 1];
-                    const uint32_t kk = ws.meta[prow * 3 + 2];
-                    const float gw = __ldg(c.w + static_cast<long long>(t) * d.K + kk);
-                    uint4 *dst = reinterpret_cast<uint4 *>(
-                        ws.combine + (static_cast<long long>(kk) * ws.max_tokens + t) * d.H + nt * BN + wg * 128);
+                // Weighted scatter of this warp's 32 rows x 128 columns (256 bytes of bf16 per
+                // row, each row to its own (slot, token) row of the combine buffer).  Stored
+                // straight from the TMEM layout (a lane per row), every store instruction would
+                // touch 32 rows with 16 bytes each, and that stream of partial-line writes holds
+                // up this SM's TMA loads of the next tile.  So each group of 8 lanes first
+                // transposes its 8 rows x 8 16-byte chunks (per 128-byte half) with three
+                // xor-shuffle stages; then store (h, i) has the group write row i's half h as
+                // one full 128-byte line, four lines per instruction.
+                if (q * 32 < rows) {
+                    float gw = 0.0f;
+                    uint32_t roff = 0;   // combine row: slot * max_tokens + token
+                    if (row < rows) {
+                        const uint32_t t = ws.meta[prow * 3 + 1];
+                        const uint32_t kk = ws.meta[prow * 3 + 2];
+                        gw = __ldg(c.w + static_cast<long long>(t) * d.K + kk);
+                        roff = kk * static_cast<uint32_t>(ws.max_tokens) + t;
+                    }
+                    uint32_t w[64];   // chunk k (columns 8k..8k+7) = w[4k..4k+3]
 #pragma unroll
-                    for (int v = 0; v < 16; ++v) {
-                        uint32_t w4[4];
+                    for (int j = 0; j < 64; ++j) {
+                        const __nv_bfloat162 b2 = __floats2bfloat162_rn(gw * acc[2 * j], gw * acc[2 * j + 1]);
+                        w[j] = *reinterpret_cast<const uint32_t *>(&b2);
+                    }
+                    // stage b swaps bit b of (lane, chunk) wherever they differ: afterwards lane
+                    // p of a group holds, in chunk slot 8h + i, chunk 8h + p of the group's row i
+                    const int p8 = lane & 7, g8 = lane & ~7;
 #pragma unroll
-                        for (int p = 0; p < 4; ++p) {
-                            const __nv_bfloat162 b2 = __floats2bfloat162_rn(gw * acc[v * 8 + 2 * p],
-                                                                            gw * acc[v * 8 + 2 * p + 1]);
-                            w4[p] = *reinterpret_cast<const uint32_t *>(&b2);
+                    for (int b = 4; b >= 1; b >>= 1) {
+                        const bool hi = (p8 & b) != 0;
+#pragma unroll
+                        for (int h = 0; h < 2; ++h)
+#pragma unroll
+                            for (int c0 = 0; c0 < 8; ++c0) {
+                                if (c0 & b)
+                                    continue;
+#pragma unroll
+                                for (int u = 0; u < 4; ++u) {
+                                    uint32_t &e0 = w[(8 * h + c0) * 4 + u];
+                                    uint32_t &e1 = w[(8 * h + (c0 | b)) * 4 + u];
+                                    const uint32_t y = __shfl_xor_sync(0xFFFFFFFFu, hi ? e0 : e1, b);
+                                    e0 = hi ? y : e0;
+                                    e1 = hi ? e1 : y;
+                                }
+                            }
+                    }
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const uint32_t ro = __shfl_sync(0xFFFFFFFFu, roff, g8 + i);
+                        if (q * 32 + g8 + i < rows) {
+                            uint16_t *dst = ws.combine + static_cast<long long>(ro) * d.H + nt * BN + wg * 128 + p8 * 8;
+#pragma unroll
+                            for (int h = 0; h < 2; ++h)
+                                *reinterpret_cast<uint4 *>(dst + h * 64) =
+                                    make_uint4(w[(8 * h + i) * 4], w[(8 * h + i) * 4 + 1], w[(8 * h + i) * 4 + 2],
+                                               w[(8 * h + i) * 4 + 3]);
                         }
-                        dst[v] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
                     }
                 }
             }

@@ -384,20 +384,6 @@ __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p)
     return v;
 }
 
-// Relaxed (non-synchronising) read of a counter another SM updates; a later fence_acq_rel_gpu
-// turns an observed value into an acquire of the releases it reflects.
-__device__ __forceinline__ uint32_t ld_relaxed_gpu(const uint32_t *p)
-{
-    uint32_t v;
-    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-
-__device__ __forceinline__ void fence_acq_rel_gpu()
-{
-    asm volatile("fence.acq_rel.gpu;" ::: "memory");
-}
-
 // Warpgroup register rebalancing (every warp of the warpgroup executes it).
 template <uint32_t N>
 __device__ __forceinline__ void setmaxnreg_dec()

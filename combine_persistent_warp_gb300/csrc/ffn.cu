@@ -668,22 +668,63 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 if (lane == 0)
                     ptx::red_release_add(ws.l1_done + blk, 1u);
             } else {
-                if (row < ws.block_rows[blk]) {
-                    const uint32_t t = ws.meta[prow * 3 + 1];
-                    const uint32_t kk = ws.meta[prow * 3 + 2];
-                    const float gw = __ldg(c.w + static_cast<long long>(t) * d.K + kk);
-                    uint4 *dst = reinterpret_cast<uint4 *>(
-                        ws.combine + (static_cast<long long>(kk) * ws.max_tokens + t) * d.H + nt * BN + wg * 128);
+                // Weighted scatter of this warp's 32 rows x 128 columns (256 bytes of bf16 per
+                // row, each row to its own (slot, token) row of the combine buffer).  Stored
+                // straight from the TMEM layout (a lane per row), every store instruction would
+                // touch 32 rows with 16 bytes each, and that stream of partial-line writes holds
+                // up this SM's TMA loads of the next tile.  So each group of 8 lanes first
+                // transposes its 8 rows x 8 16-byte chunks (per 128-byte half) with three
+                // xor-shuffle stages; then store (h, i) has the group write row i's half h as
+                // one full 128-byte line, four lines per instruction.
+                const int rows = ws.block_rows[blk];
+                if (q * 32 < rows) {
+                    float gw = 0.0f;
+                    uint32_t roff = 0;   // combine row: slot * max_tokens + token
+                    if (row < rows) {
+                        const uint32_t t = ws.meta[prow * 3 + 1];
+                        const uint32_t kk = ws.meta[prow * 3 + 2];
+                        gw = __ldg(c.w + static_cast<long long>(t) * d.K + kk);
+                        roff = kk * static_cast<uint32_t>(ws.max_tokens) + t;
+                    }
+                    uint32_t w[64];   // chunk k (columns 8k..8k+7) = w[4k..4k+3]
 #pragma unroll
-                    for (int v = 0; v < 16; ++v) {
-                        uint32_t w4[4];
+                    for (int j = 0; j < 64; ++j) {
+                        const __nv_bfloat162 b2 = __floats2bfloat162_rn(gw * acc[2 * j], gw * acc[2 * j + 1]);
+                        w[j] = *reinterpret_cast<const uint32_t *>(&b2);
+                    }
+                    // stage b swaps bit b of (lane, chunk) wherever they differ: afterwards lane
+                    // p of a group holds, in chunk slot 8h + i, chunk 8h + p of the group's row i
+                    const int p8 = lane & 7, g8 = lane & ~7;
 #pragma unroll
-                        for (int p = 0; p < 4; ++p) {
-                            const __nv_bfloat162 b2 = __floats2bfloat162_rn(gw * acc[v * 8 + 2 * p],
-                                                                            gw * acc[v * 8 + 2 * p + 1]);
-                            w4[p] = *reinterpret_cast<const uint32_t *>(&b2);
+                    for (int b = 4; b >= 1; b >>= 1) {
+                        const bool hi = (p8 & b) != 0;
+#pragma unroll
+                        for (int h = 0; h < 2; ++h)
+#pragma unroll
+                            for (int c0 = 0; c0 < 8; ++c0) {
+                                if (c0 & b)
+                                    continue;
+#pragma unroll
+                                for (int u = 0; u < 4; ++u) {
+                                    uint32_t &e0 = w[(8 * h + c0) * 4 + u];
+                                    uint32_t &e1 = w[(8 * h + (c0 | b)) * 4 + u];
+                                    const uint32_t y = __shfl_xor_sync(0xFFFFFFFFu, hi ? e0 : e1, b);
+                                    e0 = hi ? y : e0;
+                                    e1 = hi ? e1 : y;
+                                }
+                            }
+                    }
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const uint32_t ro = __shfl_sync(0xFFFFFFFFu, roff, g8 + i);
+                        if (q * 32 + g8 + i < rows) {
+                            uint16_t *dst = ws.combine + static_cast<long long>(ro) * d.H + nt * BN + wg * 128 + p8 * 8;
+#pragma unroll
+                            for (int h = 0; h < 2; ++h)
+                                *reinterpret_cast<uint4 *>(dst + h * 64) =
+                                    make_uint4(w[(8 * h + i) * 4], w[(8 * h + i) * 4 + 1], w[(8 * h + i) * 4 + 2],
+                                               w[(8 * h + i) * 4 + 3]);
                         }
-                        dst[v] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
                     }
                 }
             }

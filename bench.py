@@ -44,8 +44,10 @@ L2_BYTES = 129 * 2 ** 20
 # DRAM bytes per launch from one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum),
 # valid only while the kernel sources hash to `src_sha`; see profiles/.
 NCU_TRAFFIC = {
-    ("decode", "expert_ffn"): {"bytes": 1425218048 + 13049856, "src_sha": "3719cb2b1ba980d9"},
-    ("prefill", "expert_ffn"): {"bytes": 2035242240 + 528464896, "src_sha": "3719cb2b1ba980d9"},
+    ("decode", "expert_ffn"): {"bytes": 1425209600 + 13367040, "src_sha": "b7eea1b711ed0325"},
+    ("prefill", "expert_ffn"): {"bytes": 2130786304 + 528295680, "src_sha": "b7eea1b711ed0325"},
+    ("decode-pow2", "expert_ffn"): {"bytes": 1465405952 + 3284480, "src_sha": "47ce09d331634a6c"},
+    ("prefill-pow2", "expert_ffn"): {"bytes": 2202144256 + 517698304, "src_sha": "47ce09d331634a6c"},
 }
 # sources each stage's kernel is compiled from (a recorded traffic figure is used only while
 # these hash to its `src_sha`)
@@ -53,6 +55,10 @@ KERNEL_SOURCES = {
     "expert_ffn": ["combine_persistent_warp_gb300/csrc/ffn.cu",
                    "combine_persistent_warp_gb300/csrc/ptx.cuh",
                    "combine_persistent_warp_gb300/csrc/moe_internal.cuh"],
+    # power-of-two scales: the expert FFN stage runs the block-scaled kernel
+    "expert_ffn_bs": ["combine_persistent_warp_gb300/csrc/ffn_bs.cu",
+                      "combine_persistent_warp_gb300/csrc/ptx.cuh",
+                      "combine_persistent_warp_gb300/csrc/moe_internal.cuh"],
     "dispatch": ["combine_persistent_warp_gb300/csrc/routing.cu",
                  "combine_persistent_warp_gb300/csrc/route_device.cuh",
                  "combine_persistent_warp_gb300/csrc/ptx.cuh",
@@ -60,6 +66,9 @@ KERNEL_SOURCES = {
     "combine": ["combine_persistent_warp_gb300/csrc/routing.cu",
                 "combine_persistent_warp_gb300/csrc/moe_internal.cuh"],
 }
+
+KERNEL_FN = {"expert_ffn": "ffn_kernel", "expert_ffn_bs": "ffn_bs_kernel", "dispatch": "dispatch_kernel",
+             "combine": "combine_kernel"}
 
 
 def kernel_sources_sha(stage: str = "expert_ffn") -> str:
@@ -239,16 +248,19 @@ def roofline_for(stage: str, avg_s: float, model: dict, workload: str) -> dict:
     fp8_peak = pk["bf16_tflops"] * FP8_OVER_BF16
     t_tensor = flops / (fp8_peak * 1e12) if flops else 0.0
     traffic = None
+    src_key = "expert_ffn_bs" if stage == "expert_ffn" and workload.endswith("-pow2") else stage
     rec = NCU_TRAFFIC.get((workload, stage))
-    if rec and rec.get("src_sha") == kernel_sources_sha(stage):
+    if rec and rec.get("src_sha") == kernel_sources_sha(src_key):
         traffic = rec["bytes"]
     if t_tensor > t_hbm and flops:
         achieved = flops / avg_s / 1e12
-        return {"bound": "tensor", "kernel": stage, "achieved": achieved, "peak": fp8_peak,
+        return {"bound": "tensor", "kernel": stage, "kernel_fn": KERNEL_FN.get(src_key, stage),
+                "achieved": achieved, "peak": fp8_peak,
                 "unit": "TFLOP/s", "frac": achieved / fp8_peak, "traffic": traffic,
                 "algorithmic_flops": flops, "peak_source": f"{src} bf16 x {FP8_OVER_BF16} (fp8/bf16 nominal)"}
     achieved = bytes_ / avg_s / 1e9
-    return {"bound": "hbm", "kernel": stage, "achieved": achieved, "peak": pk["hbm_gbs"],
+    return {"bound": "hbm", "kernel": stage, "kernel_fn": KERNEL_FN.get(src_key, stage),
+            "achieved": achieved, "peak": pk["hbm_gbs"],
             "unit": "GB/s", "frac": achieved / pk["hbm_gbs"], "traffic": traffic,
             "algorithmic_bytes": bytes_, "peak_source": f"{src} (hbm_gbs, copy bandwidth)"}
 

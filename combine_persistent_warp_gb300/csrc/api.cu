@@ -55,7 +55,8 @@ struct moe_ctx {
     long long timeout_ns = 2000000000LL;
     int debug_skip_barrier = 0;
     int ffn_mode = 0;            // 0 auto, 1 one CTA per tile, 2 two-CTA clusters
-    int scale_mode = 0;          // 0 fp32 scales, 1 power-of-two scales (block-scaled UMMA)
+    int scale_mode = 2;          // 0 fp32 scales, 1 power-of-two scales (block-scaled UMMA),
+                                 // 2 block-scaled exactly when the weights' scales are 2^k
     // stage profiling (events on the forward's stream)
     bool profile = false;
     std::vector<cudaEvent_t> events;   // 4 per recorded forward
@@ -399,9 +400,9 @@ int moe_forward(moe_handle_t h, int T, const uint8_t *x, const float *x_sf, cons
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     // power-of-two scales: the block-scaled kernel (the weights were checked at load time,
     // the activation scales are checked by the routing kernel's gather)
-    const bool bs = h->scale_mode == 1;
-    if (bs && !h->weights_pow2)
+    if (h->scale_mode == 1 && !h->weights_pow2)
         return MOE_ERR_BAD_SCALE;
+    const bool bs = h->scale_mode == 1 || (h->scale_mode == 2 && h->weights_pow2);
     CallArgs c{T, x, x_sf, topk_idx, topk_w, out, h->timeout_ns, h->debug_skip_barrier, bs ? 1 : 0};
     cudaEvent_t *ev = nullptr;
     if (h->profile) {
@@ -642,7 +643,7 @@ int moe_set_option(moe_handle_t h, int option, int64_t value)
         h->ffn_mode = static_cast<int>(value);
         return MOE_OK;
     case MOE_OPT_SCALE_MODE:
-        if (value < 0 || value > 1)
+        if (value < 0 || value > 2)
             return MOE_ERR_INVALID_ARG;
         h->scale_mode = static_cast<int>(value);
         return MOE_OK;

@@ -21,12 +21,14 @@ STATUS = {
     0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_CUDA", 3: "MOE_ERR_CAPACITY",
     4: "MOE_ERR_NO_WEIGHTS", 5: "MOE_ERR_UNSUPPORTED_DEVICE", 6: "MOE_ERR_BAD_INDEX",
     7: "MOE_ERR_TIMEOUT", 8: "MOE_ERR_SLOT_OVERFLOW", 9: "MOE_ERR_NOT_RESERVED",
+    10: "MOE_ERR_BAD_SCALE",
 }
 BUFFERS = {"pool_x": 0, "pool_sf": 1, "act": 2, "act_sf": 3, "combine": 4, "table": 5}
 OPT_TIMEOUT_NS = 0
 OPT_DEBUG_SKIP_BARRIER = 1
 OPT_FFN_MODE = 2
 OPT_SCALE_MODE = 3
+SCALE_FP32, SCALE_POW2, SCALE_AUTO = 0, 1, 2   # values of OPT_SCALE_MODE (default SCALE_AUTO)
 
 
 class MoeError(RuntimeError):

@@ -157,14 +157,16 @@ int moe_get_info(moe_handle_t h, moe_info *info);
  * MOE_OPT_FFN_MODE: how the expert FFN kernel covers its tiles: 0 = automatic (default),
  * 1 = one CTA per 128-row tile, 2 = pairs of CTAs (a cluster) on two M-blocks of one expert
  * with one 256-row two-CTA UMMA.  All modes compute the same result;
- * MOE_OPT_SCALE_MODE: 0 = arbitrary fp32 block scales (default; the UMMA accumulates each
- * 128-deep K block in TMEM and the scales are applied on the CUDA cores); 1 = every scale
- * (x_sf, both weight scale tensors) is a power of two: the UMMA applies them itself as UE8M0
- * scale factors and accumulates the whole K range in TMEM ("DeepGEMM Mega MoE 对称内存
+ * MOE_OPT_SCALE_MODE: 0 = arbitrary fp32 block scales (the UMMA accumulates each 128-deep
+ * K block in TMEM and the scales are applied on the CUDA cores); 1 = every scale (x_sf, both
+ * weight scale tensors) is a power of two: the UMMA applies them itself as UE8M0 scale
+ * factors and accumulates the whole K range in TMEM ("DeepGEMM Mega MoE 对称内存
  * （Symmetric Memory）深度分析" §8.1), and the SwiGLU requant uses the smallest power-of-two
- * scale >= max(amax, 1e-4)/448.  Weights that are not all powers of two make moe_forward
- * return MOE_ERR_BAD_SCALE; an activation scale that is not is reported by the device the
- * same way (sticky). */
+ * scale >= max(amax, 1e-4)/448; 2 = automatic (default): mode 1 when every scale of the
+ * loaded weights is a power of two (checked by moe_load_weights), else mode 0.  In mode 1
+ * weights that are not all powers of two make moe_forward return MOE_ERR_BAD_SCALE; in
+ * modes 1 and 2 an activation scale that is not, on the block-scaled path, is reported by
+ * the device the same way (sticky). */
 enum moe_option {
     MOE_OPT_TIMEOUT_NS = 0,
     MOE_OPT_DEBUG_SKIP_BARRIER = 1,

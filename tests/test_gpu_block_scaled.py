@@ -170,3 +170,48 @@ def test_block_scaled_paired_mode_single_block_experts():
     moe, inp = layer("tiny-pow2")
     single, paired = _forward_modes(moe, inp)
     assert torch.equal(single.view(torch.int16), paired.view(torch.int16))
+
+
+# ------------------------------------------------------------- automatic scale mode -----
+@pytest.mark.parametrize("name,mode", [("tiny-pow2", 1), ("tiny", 0), ("skewed-pow2", 1)])
+def test_default_scale_mode_follows_the_weight_scales(name, mode):
+    """The default (automatic) scale mode runs the block-scaled kernel exactly when every
+    scale of the loaded weights is a power of two: same bits as the explicit mode."""
+    torch.cuda.set_device(0)
+    inp = make_inputs(name, device="cuda")
+    wl = inp.wl
+    moe = FusedMoE(wl.E, wl.H, wl.I, wl.topk, wl.R).reserve(wl.T)
+    moe.load_weights(inp.w_gate_up, inp.sf_gate_up, inp.w_down, inp.sf_down)
+    auto = moe.forward(inp.x, inp.x_sf, inp.topk_idx, inp.topk_w).clone()
+    torch.cuda.synchronize()
+    assert moe.get_error() == 0
+    moe.set_option(native.OPT_SCALE_MODE, mode)
+    explicit = moe.forward(inp.x, inp.x_sf, inp.topk_idx, inp.topk_w)
+    torch.cuda.synchronize()
+    assert moe.get_error() == 0
+    assert torch.equal(auto.view(torch.int16), explicit.view(torch.int16))
+
+
+def test_scale_mode_values():
+    moe, inp = layer("tiny-pow2")
+    for bad in (-1, 3):
+        with pytest.raises(MoeError) as ei:
+            moe.set_option(native.OPT_SCALE_MODE, bad)
+        assert ei.value.code == 1
+    # automatic mode with power-of-two weights but fp32-rule activation scales: reported
+    # by the gather like mode 1, then the handle recovers
+    fp = make_inputs("tiny", device="cuda")
+    moe.set_option(native.OPT_SCALE_MODE, native.SCALE_AUTO)
+    moe.forward(inp.x, fp.x_sf, inp.topk_idx, inp.topk_w)
+    torch.cuda.synchronize()
+    assert moe.get_error() == 10
+    # mode 0 accepts power-of-two scales as ordinary fp32 scales
+    moe.set_option(native.OPT_SCALE_MODE, native.SCALE_FP32)
+    out = moe.forward(inp.x, inp.x_sf, inp.topk_idx, inp.topk_w)
+    torch.cuda.synchronize()
+    assert moe.get_error() == 0
+    h = oracle.HostInputs.from_inputs(inp)
+    _, ref, _ = oracle.forward_tokens(h, np.arange(inp.wl.T))
+    g = out.float().cpu().numpy()
+    rel = np.linalg.norm(g - ref, axis=1) / np.maximum(np.linalg.norm(ref, axis=1), 1e-30)
+    assert np.all(rel <= TOL), rel.max()

@@ -92,50 +92,73 @@ cudaError_t launch_dispatch(const Dims &d, const Workspace &ws, const CallArgs &
 // Then the workspace reset of the pages' cleanup step: send counts and arrival counters go
 // back to zero; a device error of this forward moves into the sticky word and the grid
 // barrier counter is cleared (an aborted barrier leaves it mid-phase).
-__global__ void __launch_bounds__(COMBINE_THREADS)
+__global__ void __launch_bounds__(COMBINE_THREADS, 2)
     combine_kernel(const Dims d, const Workspace ws, const CallArgs c)
 {
     const int K = d.K, H = d.H;
     const uint32_t err = *reinterpret_cast<volatile uint32_t *>(ws.hdr + HDR_ERR_CALL) |
                          *reinterpret_cast<volatile uint32_t *>(ws.hdr + HDR_ERR_STICKY);
     if (err == 0) {
-        // one thread per 16-byte output vector (8 bf16); its top-k plane loads are
-        // independent, so they are all in flight together
+        // two 16-byte output vectors (8 bf16 each) per thread per round; every valid plane
+        // load of both is issued before any of them is summed
         const int H8 = H / 8;
         const long long plane = static_cast<long long>(ws.max_tokens) * H8;   // uint4 per plane
         const uint4 *cb = reinterpret_cast<const uint4 *>(ws.combine);
         uint4 *out = reinterpret_cast<uint4 *>(c.out);
         const long long n = static_cast<long long>(c.T) * H8;
-        const long long gthreads_l = static_cast<long long>(gridDim.x) * blockDim.x;
-        for (long long g = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; g < n;
-             g += gthreads_l) {
-            const long long t = g / H8;
-            uint32_t mask = 0;
-            for (int kk = 0; kk < K; ++kk)
-                mask |= (__ldg(c.idx + t * K + kk) >= 0 ? 1u : 0u) << kk;
-            float acc[8];
+        const long long G = static_cast<long long>(gridDim.x) * blockDim.x;
+        for (long long g0 = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; g0 < n; g0 += 2 * G) {
+            const long long g[2] = {g0, g0 + G};
+            const bool live1 = g[1] < n;
+            uint32_t mask[2] = {0u, 0u};
 #pragma unroll
-            for (int q = 0; q < 8; ++q)
-                acc[q] = 0.0f;
-#pragma unroll 8
-            for (int kk = 0; kk < K; ++kk) {
-                if (mask & (1u << kk)) {
-                    const uint4 u = __ldcs(cb + kk * plane + g);
-                    const __nv_bfloat162 *b = reinterpret_cast<const __nv_bfloat162 *>(&u);
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const float2 f = __bfloat1622float2(b[q]);
-                        acc[2 * q] += f.x;
-                        acc[2 * q + 1] += f.y;
-                    }
-                }
+            for (int v = 0; v < 2; ++v) {
+                if (v == 1 && !live1)
+                    break;
+                const long long t = g[v] / H8;
+                for (int kk = 0; kk < K; ++kk)
+                    mask[v] |= (__ldg(c.idx + t * K + kk) >= 0 ? 1u : 0u) << kk;
             }
-            uint4 o;
-            __nv_bfloat162 *ob = reinterpret_cast<__nv_bfloat162 *>(&o);
+            float acc[2][8];
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-                ob[q] = __floats2bfloat162_rn(acc[2 * q], acc[2 * q + 1]);
-            out[g] = o;
+            for (int v = 0; v < 2; ++v)
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    acc[v][q] = 0.0f;
+            for (int k0 = 0; k0 < K; k0 += 8) {
+                uint4 u[2][8];
+#pragma unroll
+                for (int v = 0; v < 2; ++v)
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        if ((mask[v] >> (k0 + j)) & 1u)   // bits >= K are clear
+                            u[v][j] = __ldcs(cb + (k0 + j) * plane + g[v]);
+#pragma unroll
+                for (int v = 0; v < 2; ++v)
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        if (!((mask[v] >> (k0 + j)) & 1u))
+                            continue;
+                        const __nv_bfloat162 *b = reinterpret_cast<const __nv_bfloat162 *>(&u[v][j]);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const float2 f = __bfloat1622float2(b[q]);
+                            acc[v][2 * q] += f.x;
+                            acc[v][2 * q + 1] += f.y;
+                        }
+                    }
+            }
+#pragma unroll
+            for (int v = 0; v < 2; ++v) {
+                if (v == 1 && !live1)
+                    break;
+                uint4 o;
+                __nv_bfloat162 *ob = reinterpret_cast<__nv_bfloat162 *>(&o);
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    ob[q] = __floats2bfloat162_rn(acc[v][2 * q], acc[v][2 * q + 1]);
+                out[g[v]] = o;
+            }
         }
     }
     // reset for the next forward
@@ -162,7 +185,8 @@ __global__ void __launch_bounds__(COMBINE_THREADS)
 cudaError_t launch_combine(const Dims &d, const Workspace &ws, const CallArgs &c, int num_sms,
                            cudaStream_t s)
 {
-    combine_kernel<<<num_sms * 4, COMBINE_THREADS, 0, s>>>(d, ws, c);
+    // two CTAs per SM (128 registers a thread keep 16 plane loads in flight), all resident
+    combine_kernel<<<num_sms * 2, COMBINE_THREADS, 0, s>>>(d, ws, c);
     return cudaGetLastError();
 }
 

@@ -19,7 +19,7 @@ constexpr int BKS = CPW_BKS;       // K (bytes of an FP8 operand row) per pipeli
 constexpr int SUBS = BK / BKS;     // pipeline stages per scale block
 constexpr int STAGES = 4 * BK / BKS;   // TMA -> UMMA ring depth (192 KB of operand tiles)
 constexpr int GEMM_THREADS = 384;  // 4 producer/issuer warps + 2 epilogue warpgroups
-constexpr int DISPATCH_THREADS = 512;
+constexpr int DISPATCH_THREADS = 1024;
 constexpr int COMBINE_THREADS = 256;
 static_assert(BKS == 32 || BKS == 64 || BKS == 128, "stage depth must match a swizzle width");
 

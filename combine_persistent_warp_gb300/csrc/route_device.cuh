@@ -235,9 +235,11 @@ __device__ inline void segments(const Dims &d, const Workspace &ws, uint32_t *re
 
 // Step a5 for pool row j (rows in expert order; e = its expert, recv_e = rows of expert e per
 // source): the round robin picks (source, slot), the table gives (token, k); one warp copies
-// the token's H bytes and H/128 scales into the pool row, writes {source, token, k} and, once
-// every lane's stores are done, adds one to the M-block's arrival count with release
-// semantics (the warp barrier orders the lanes' stores before lane 0's release).
+// the token's H bytes and H/128 scales into the pool row, writes {source, token, k} and adds
+// one to the M-block's arrival count.  The FFN kernel that reads the pool is a later launch
+// on the same stream, which already orders these stores before its loads, so the count is
+// a plain (relaxed) increment: a GPU-scope release per row stalled every warp until its
+// row's stores had reached L2.
 // U = 16-byte loads in flight per lane.
 template <int U>
 __device__ __forceinline__ void gather_row(const Dims &d, const Workspace &ws, const CallArgs &c, int j, int e,
@@ -286,9 +288,8 @@ __device__ __forceinline__ void gather_row(const Dims &d, const Workspace &ws, c
         ws.meta[row * 3 + 1] = static_cast<uint32_t>(t);
         ws.meta[row * 3 + 2] = static_cast<uint32_t>(kk);
     }
-    __syncwarp();
     if (lane == 0)
-        ptx::red_release_add(ws.arrive + row / BM, 1u);
+        atomicAdd(ws.arrive + row / BM, 1u);
 }
 
 }  // namespace route

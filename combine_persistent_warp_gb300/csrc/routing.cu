@@ -83,8 +83,12 @@ cudaError_t launch_dispatch(const Dims &d, const Workspace &ws, const CallArgs &
     Workspace ww = ws;
     CallArgs cc = c;
     void *args[] = {&dd, &ww, &cc};
-    return cudaLaunchCooperativeKernel(reinterpret_cast<void *>(dispatch_kernel), dim3(num_sms),
-                                       dim3(DISPATCH_THREADS), args, smem, s);
+    // the gather of a large batch wants every warp an SM can hold; a small batch is bound by
+    // the routing steps and the launch, which half the block does faster
+    const long long rows = static_cast<long long>(c.T) * d.K;
+    const int threads = rows >= 8LL * 1024 ? DISPATCH_THREADS : DISPATCH_THREADS / 2;
+    return cudaLaunchCooperativeKernel(reinterpret_cast<void *>(dispatch_kernel), dim3(num_sms), dim3(threads), args,
+                                       smem, s);
 }
 
 // ------------------------------------------------------------------ combine -------------

@@ -517,6 +517,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 continue;
             }
             const long long prow = static_cast<long long>(blk) * BM + row;
+            // a warp whose 32 rows are all padding of a partly filled M-block (most warps at
+            // decode) only hands each TMEM partial back: its results are never stored
+            const bool dead = q * 32 >= ws.block_rows[blk];
             const float *sfa = (phase == 1 ? ws.pool_sf : ws.act_sf) + prow;
             const float *sb0;
             const float *sb1;
@@ -527,7 +530,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 sb0 = sf2 + (static_cast<long long>(e) * (d.H / 128) + 2 * nt + wg) * NKB2;
                 sb1 = sb0;
             }
-            if (phase == 2) {
+            if (phase == 2 && !dead) {
                 // act_sf of this block is written by other CTAs in this launch: acquire the
                 // block's completion counter (as the producer does before its TMA loads)
                 // before the first scale read, and read the scales coherently (L2), not
@@ -569,6 +572,17 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 if (warp == 4 && lane == 0)
                     CPW_STAMP(3, pit);
                 ptx::tc_fence_after();
+                if (dead) {
+                    ptx::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if constexpr (PAIRED)
+                            ptx::mbar_arrive_cluster(tempty0 + buf * static_cast<uint32_t>(sizeof(uint64_t)));
+                        else
+                            ptx::mbar_arrive(&bars->tempty[buf]);
+                    }
+                    continue;
+                }
                 const uint32_t taddr = tmem + lane_base + buf * BN + wg * 128;
                 // two 32-column loads in flight per round; the partial is handed back to the
                 // UMMA issuer as soon as its last columns are in registers, before the last

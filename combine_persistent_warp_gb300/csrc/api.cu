@@ -24,9 +24,12 @@ using namespace cpw;
 struct moe_ctx {
     int dev = -1;
     int num_sms = 0;
-    Dims d{};
+    Dims d{};                    // E, K include the shared experts (experts E_routed.., slots K_routed..)
+    int E_routed = 0, K_routed = 0, S = 0;   // routed experts, routed top-k, shared experts
     bool reserved = false;
     bool have_weights = false;
+    bool routed_loaded = false, shared_loaded = false;
+    bool routed_pow2 = false, shared_pow2 = false;
     Workspace ws{};
     void *small_mem = nullptr;   // header + routing arrays (size depends on E, R only)
     void *big_mem = nullptr;     // table, pools, combine, staging (depends on max_tokens)
@@ -49,6 +52,9 @@ struct moe_ctx {
     int64_t *st_idx = nullptr;
     float *st_w = nullptr;
     uint16_t *st_out = nullptr;
+    // shared experts: every token's route extended by slots K_routed.. (expert E_routed + s, weight 1)
+    int64_t *ext_idx = nullptr;
+    float *ext_w = nullptr;
     cudaStream_t last_stream = nullptr;
     bool have_last = false;
     int last_T = 0;
@@ -182,6 +188,10 @@ size_t carve_big(moe_ctx *h, char *base, int max_tokens, Workspace &ws)
     h->st_idx = c.take<int64_t>(static_cast<size_t>(max_tokens) * d.K);
     h->st_w = c.take<float>(static_cast<size_t>(max_tokens) * d.K);
     h->st_out = c.take<uint16_t>(static_cast<size_t>(max_tokens) * d.H);
+    if (h->S > 0) {
+        h->ext_idx = c.take<int64_t>(static_cast<size_t>(max_tokens) * d.K);
+        h->ext_w = c.take<float>(static_cast<size_t>(max_tokens) * d.K);
+    }
     return align_up(c.off, 256);
 }
 
@@ -234,11 +244,16 @@ const char *moe_status_string(int s)
 
 int moe_create(int E, int H, int I, int topk, int R, moe_handle_t *out)
 {
+    return moe_create_shared(E, H, I, topk, R, 0, out);
+}
+
+int moe_create_shared(int E, int H, int I, int topk, int R, int n_shared, moe_handle_t *out)
+{
     if (!out)
         return MOE_ERR_INVALID_ARG;
     *out = nullptr;
-    if (E < 1 || E > 1024 || H < 256 || H % 256 != 0 || I < 128 || I % 128 != 0 || topk < 1 ||
-        topk > 32 || topk > E || R < 1 || R > 64 || E * R > 16384)
+    if (E < 1 || H < 256 || H % 256 != 0 || I < 128 || I % 128 != 0 || topk < 1 || topk > E || R < 1 ||
+        R > 64 || n_shared < 0 || E + n_shared > 1024 || topk + n_shared > 32 || (E + n_shared) * R > 16384)
         return MOE_ERR_INVALID_ARG;
     int dev = 0;
     CK(cudaGetDevice(&dev));
@@ -251,7 +266,10 @@ int moe_create(int E, int H, int I, int topk, int R, moe_handle_t *out)
         return MOE_ERR_INVALID_ARG;
     h->dev = dev;
     h->num_sms = prop.multiProcessorCount;
-    h->d = Dims{E, H, I, topk, R};
+    h->d = Dims{E + n_shared, H, I, topk + n_shared, R};
+    h->E_routed = E;
+    h->K_routed = topk;
+    h->S = n_shared;
     *out = h;
     return MOE_OK;
 }
@@ -313,31 +331,35 @@ int moe_reserve(moe_handle_t h, int max_tokens)
     return MOE_OK;
 }
 
-int moe_load_weights(moe_handle_t h, const uint8_t *w_gate_up, const float *sf_gate_up,
-                     const uint8_t *w_down, const float *sf_down, void *stream)
+namespace {
+
+// Weights of experts [e0, e0 + n) of the handle's expert slots (routed experts first, then
+// the shared ones): re-laid into GEMM tiles, scales copied, UE8M0 scale blocks built;
+// *pow2 = every scale of these experts is a power of two.
+int load_expert_weights(moe_ctx *h, int e0, int n, const uint8_t *w_gate_up, const float *sf_gate_up,
+                        const uint8_t *w_down, const float *sf_down, cudaStream_t s, bool *pow2)
 {
-    if (!h || !w_gate_up || !sf_gate_up || !w_down || !sf_down)
+    if (!w_gate_up || !sf_gate_up || !w_down || !sf_down)
         return MOE_ERR_INVALID_ARG;
     if (!aligned(w_gate_up, 16) || !aligned(w_down, 16) || !aligned(sf_gate_up, 4) || !aligned(sf_down, 4))
         return MOE_ERR_INVALID_ARG;
     CK(cudaSetDevice(h->dev));
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
     const Dims &d = h->d;
-    const size_t n1 = static_cast<size_t>(d.E) * 2 * d.I * d.H;
-    const size_t ns1 = static_cast<size_t>(d.E) * (2 * d.I / 128) * (d.H / 128);
-    const size_t n2 = static_cast<size_t>(d.E) * d.H * d.I;
-    const size_t ns2 = static_cast<size_t>(d.E) * (d.H / 128) * (d.I / 128);
+    const size_t w1e = static_cast<size_t>(2) * d.I * d.H, w2e = static_cast<size_t>(d.H) * d.I;
+    const size_t s1e = static_cast<size_t>(2 * d.I / 128) * (d.H / 128), s2e = static_cast<size_t>(d.H / 128) * (d.I / 128);
+    const size_t b1e = static_cast<size_t>(2 * d.I / BN) * (d.H / 128) * 1024, b2e = static_cast<size_t>(d.H / BN) * (d.I / 128) * 1024;
+    const size_t n1 = d.E * w1e, n2 = d.E * w2e;
     if (!h->w_mem) {
         Carver c{nullptr};
         auto carve = [&](char *base) {
             c = Carver{base};
             h->w1 = c.take<uint8_t>(n1);
-            h->s1 = c.take<float>(ns1);
+            h->s1 = c.take<float>(d.E * s1e);
             h->w2 = c.take<uint8_t>(n2);
-            h->s2 = c.take<float>(ns2);
+            h->s2 = c.take<float>(d.E * s2e);
             // UE8M0 scale blocks: 1 KB per weight tile (256 rows) and 128-deep K block
-            h->sfb1 = c.take<uint8_t>(static_cast<size_t>(d.E) * (2 * d.I / BN) * (d.H / 128) * 1024);
-            h->sfb2 = c.take<uint8_t>(static_cast<size_t>(d.E) * (d.H / BN) * (d.I / 128) * 1024);
+            h->sfb1 = c.take<uint8_t>(d.E * b1e);
+            h->sfb2 = c.take<uint8_t>(d.E * b2e);
             h->sfb_bad = c.take<uint32_t>(1);
             return align_up(c.off, 256);
         };
@@ -346,33 +368,66 @@ int moe_load_weights(moe_handle_t h, const uint8_t *w_gate_up, const float *sf_g
         carve(static_cast<char *>(h->w_mem));
         h->w_bytes = bytes;
     }
-    if (launch_relayout_weights(w_gate_up, h->w1, d.E, 2 * d.I, d.H, d.I, s) != cudaSuccess ||
-        launch_relayout_weights(w_down, h->w2, d.E, d.H, d.I, 0, s) != cudaSuccess)
+    if (launch_relayout_weights(w_gate_up, h->w1 + e0 * w1e, n, 2 * d.I, d.H, d.I, s) != cudaSuccess ||
+        launch_relayout_weights(w_down, h->w2 + e0 * w2e, n, d.H, d.I, 0, s) != cudaSuccess)
         return MOE_ERR_CUDA;
-    CK(cudaMemcpyAsync(h->s1, sf_gate_up, ns1 * sizeof(float), cudaMemcpyDeviceToDevice, s));
-    CK(cudaMemcpyAsync(h->s2, sf_down, ns2 * sizeof(float), cudaMemcpyDeviceToDevice, s));
+    CK(cudaMemcpyAsync(h->s1 + e0 * s1e, sf_gate_up, n * s1e * sizeof(float), cudaMemcpyDeviceToDevice, s));
+    CK(cudaMemcpyAsync(h->s2 + e0 * s2e, sf_down, n * s2e * sizeof(float), cudaMemcpyDeviceToDevice, s));
     // UE8M0 scale blocks for the block-scaled path; usable only if every scale is 2^k
     CK(cudaMemsetAsync(h->sfb_bad, 0, sizeof(uint32_t), s));
-    if (launch_build_sfb(sf_gate_up, h->sfb1, d.E, 2 * d.I, d.H, d.I, h->sfb_bad, s) != cudaSuccess ||
-        launch_build_sfb(sf_down, h->sfb2, d.E, d.H, d.I, 0, h->sfb_bad, s) != cudaSuccess)
+    if (launch_build_sfb(sf_gate_up, h->sfb1 + e0 * b1e, n, 2 * d.I, d.H, d.I, h->sfb_bad, s) != cudaSuccess ||
+        launch_build_sfb(sf_down, h->sfb2 + e0 * b2e, n, d.H, d.I, 0, h->sfb_bad, s) != cudaSuccess)
         return MOE_ERR_CUDA;
     uint32_t bad = 1;
     CK(cudaMemcpyAsync(&bad, h->sfb_bad, sizeof(uint32_t), cudaMemcpyDeviceToHost, s));
     CK(cudaStreamSynchronize(s));
-    h->weights_pow2 = bad == 0;
+    *pow2 = bad == 0;
     // weight tiles as rows of 128 bytes: tile (e, nt, kb) starts at row ((e*NT + nt)*KB + kb)*256
     if (encode_tile_map(&h->maps.b1, h->w1, n1 / 128, 128, BN) != MOE_OK ||
         encode_tile_map(&h->maps.b2, h->w2, n2 / 128, 128, BN) != MOE_OK ||
         encode_tile_map(&h->maps.b1h, h->w1, n1 / 128, 128, BN / 2) != MOE_OK ||
         encode_tile_map(&h->maps.b2h, h->w2, n2 / 128, 128, BN / 2) != MOE_OK ||
-        encode_sf_map(&h->sf_maps.sfb1, h->sfb1, static_cast<uint64_t>(d.E) * (2 * d.I / BN) * (d.H / 128) * 1024, 4) !=
-            MOE_OK ||
-        encode_sf_map(&h->sf_maps.sfb2, h->sfb2, static_cast<uint64_t>(d.E) * (d.H / BN) * (d.I / 128) * 1024, 4) !=
-            MOE_OK)
+        encode_sf_map(&h->sf_maps.sfb1, h->sfb1, static_cast<uint64_t>(d.E) * b1e, 4) != MOE_OK ||
+        encode_sf_map(&h->sf_maps.sfb2, h->sfb2, static_cast<uint64_t>(d.E) * b2e, 4) != MOE_OK)
         return MOE_ERR_CUDA;
-    h->have_weights = true;
     h->last_stream = s;
     h->have_last = true;
+    return MOE_OK;
+}
+
+void update_weight_state(moe_ctx *h)
+{
+    h->have_weights = h->routed_loaded && (h->S == 0 || h->shared_loaded);
+    h->weights_pow2 = h->routed_pow2 && (h->S == 0 || h->shared_pow2);
+}
+
+}  // namespace
+
+int moe_load_weights(moe_handle_t h, const uint8_t *w_gate_up, const float *sf_gate_up,
+                     const uint8_t *w_down, const float *sf_down, void *stream)
+{
+    if (!h)
+        return MOE_ERR_INVALID_ARG;
+    const int rc = load_expert_weights(h, 0, h->E_routed, w_gate_up, sf_gate_up, w_down, sf_down,
+                                       static_cast<cudaStream_t>(stream), &h->routed_pow2);
+    if (rc != MOE_OK)
+        return rc;
+    h->routed_loaded = true;
+    update_weight_state(h);
+    return MOE_OK;
+}
+
+int moe_load_shared_weights(moe_handle_t h, const uint8_t *w_gate_up, const float *sf_gate_up,
+                            const uint8_t *w_down, const float *sf_down, void *stream)
+{
+    if (!h || h->S == 0)
+        return MOE_ERR_INVALID_ARG;
+    const int rc = load_expert_weights(h, h->E_routed, h->S, w_gate_up, sf_gate_up, w_down, sf_down,
+                                       static_cast<cudaStream_t>(stream), &h->shared_pow2);
+    if (rc != MOE_OK)
+        return rc;
+    h->shared_loaded = true;
+    update_weight_state(h);
     return MOE_OK;
 }
 
@@ -404,6 +459,12 @@ int moe_forward(moe_handle_t h, int T, const uint8_t *x, const float *x_sf, cons
         return MOE_ERR_BAD_SCALE;
     const bool bs = h->scale_mode == 1 || (h->scale_mode == 2 && h->weights_pow2);
     CallArgs c{T, x, x_sf, topk_idx, topk_w, out, h->timeout_ns, h->debug_skip_barrier, bs ? 1 : 0};
+    if (h->S > 0) {
+        // shared experts: each token's route gains slots K_routed.. naming expert E_routed + s
+        // with weight 1, written by one small kernel ahead of the routing kernel
+        c.idx = h->ext_idx;
+        c.w = h->ext_w;
+    }
     cudaEvent_t *ev = nullptr;
     if (h->profile) {
         if (h->prof_calls < PROF_MAX_CALLS)
@@ -412,7 +473,10 @@ int moe_forward(moe_handle_t h, int T, const uint8_t *x, const float *x_sf, cons
             ++h->prof_dropped;
     }
     auto mark = [&](int i) { return ev ? cudaEventRecord(ev[i], s) : cudaSuccess; };
-    if (mark(0) != cudaSuccess || launch_dispatch(h->d, h->ws, c, h->num_sms, s) != cudaSuccess ||
+    if (mark(0) != cudaSuccess ||
+        (h->S > 0 && launch_extend_route(topk_idx, topk_w, h->ext_idx, h->ext_w, T, h->K_routed, h->S, h->E_routed,
+                                         h->num_sms, s) != cudaSuccess) ||
+        launch_dispatch(h->d, h->ws, c, h->num_sms, s) != cudaSuccess ||
         mark(1) != cudaSuccess ||
         (bs ? launch_ffn_bs(h->maps, h->sf_maps, h->d, h->ws, c, h->sfb1, h->sfb2, wave_blocks(h), h->num_sms,
                             ffn_paired(h, T), s)
@@ -464,8 +528,8 @@ static int forward_host_impl(moe_handle_t h, int T, const uint8_t *host_x, const
     const Dims &d = h->d;
     const void *src[4] = {host_x, host_x_sf, host_topk_idx, host_topk_w};
     void *dst[4] = {h->st_x, h->st_sf, h->st_idx, h->st_w};
-    const long long bytes[4] = {static_cast<long long>(T) * d.H, 4ll * T * (d.H / 128), 8ll * T * d.K,
-                                4ll * T * d.K};
+    const long long bytes[4] = {static_cast<long long>(T) * d.H, 4ll * T * (d.H / 128), 8ll * T * h->K_routed,
+                                4ll * T * h->K_routed};
     const void *dev_src[4];
     bool in_place = true;
     for (int i = 0; i < 4 && in_place; ++i) {
@@ -621,6 +685,7 @@ int moe_get_info(moe_handle_t h, moe_info *info)
     info->num_sms = h->num_sms;
     info->workspace_bytes = h->small_bytes + h->big_bytes;
     info->weight_bytes = h->w_bytes;
+    info->n_shared = h->S;
     return MOE_OK;
 }
 

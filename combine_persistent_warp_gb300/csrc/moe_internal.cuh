@@ -122,6 +122,10 @@ cudaError_t launch_build_sfb(const float *s, uint8_t *dst, int E, int N, int K, 
                              cudaStream_t st);
 cudaError_t launch_combine(const Dims &d, const Workspace &ws, const CallArgs &c, int num_sms,
                            cudaStream_t s);
+// shared experts: idx_ext / w_ext [T][K + S] = the caller's [T][K] route plus slots K + s naming
+// expert E_routed + s with weight 1
+cudaError_t launch_extend_route(const int64_t *idx, const float *w, int64_t *idx_ext, float *w_ext, int T, int K,
+                                int S, int E_routed, int num_sms, cudaStream_t s);
 cudaError_t launch_stage_inputs(const void *const src[4], void *const dst[4], const long long bytes[4], int num_sms,
                                 cudaStream_t s);
 cudaError_t launch_relayout_weights(const uint8_t *src, uint8_t *dst, int E, int N, int K, int gate_up_I,

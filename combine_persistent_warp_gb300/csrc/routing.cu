@@ -194,6 +194,39 @@ cudaError_t launch_combine(const Dims &d, const Workspace &ws, const CallArgs &c
     return cudaGetLastError();
 }
 
+// ------------------------------------------------------------------ shared experts -----
+// Every token also goes through each shared expert, whose output enters the top-k sum
+// unweighted, in a combine plane of its own after the routed slots ("DeepGEMM Mega MoE 对称内存
+// （Symmetric Memory）深度分析" §8.2: num_topk + 1 planes when shared experts exist).  Here a
+// shared expert is an expert slot after the routed ones that every token's route names in
+// slot K + s with weight 1, so routing, the grouped GEMMs and the combine need nothing else.
+__global__ void extend_route_kernel(const int64_t *__restrict__ idx, const float *__restrict__ w,
+                                    int64_t *__restrict__ idx_ext, float *__restrict__ w_ext, int T, int K, int S,
+                                    int E_routed)
+{
+    const int KS = K + S;
+    const long long n = static_cast<long long>(T) * KS;
+    for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+         i += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const long long t = i / KS;
+        const int k = static_cast<int>(i - t * KS);
+        if (k < K) {
+            idx_ext[i] = idx[t * K + k];
+            w_ext[i] = w[t * K + k];
+        } else {
+            idx_ext[i] = E_routed + (k - K);
+            w_ext[i] = 1.0f;
+        }
+    }
+}
+
+cudaError_t launch_extend_route(const int64_t *idx, const float *w, int64_t *idx_ext, float *w_ext, int T, int K,
+                                int S, int E_routed, int num_sms, cudaStream_t s)
+{
+    extend_route_kernel<<<num_sms, 256, 0, s>>>(idx, w, idx_ext, w_ext, T, K, S, E_routed);
+    return cudaGetLastError();
+}
+
 // ------------------------------------------------------------------ host inputs --------
 // Copies of the host-buffer entry point's inputs, read straight from pinned (device-mapped)
 // host memory in one launch instead of one copy-engine transfer per buffer.  Every pointer

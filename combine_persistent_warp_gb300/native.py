@@ -42,7 +42,7 @@ class MoeInfo(ctypes.Structure):
                 ("topk", ctypes.c_int), ("R", ctypes.c_int), ("max_tokens", ctypes.c_int),
                 ("pool_rows", ctypes.c_int), ("block_m", ctypes.c_int), ("block_n", ctypes.c_int),
                 ("num_sms", ctypes.c_int), ("workspace_bytes", ctypes.c_uint64),
-                ("weight_bytes", ctypes.c_uint64)]
+                ("weight_bytes", ctypes.c_uint64), ("n_shared", ctypes.c_int)]
 
 
 def header_functions() -> list[str]:
@@ -69,8 +69,10 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     H = ctypes.c_void_p
     sig = {
         "moe_create": [I, I, I, I, I, ctypes.POINTER(H)],
+        "moe_create_shared": [I, I, I, I, I, I, ctypes.POINTER(H)],
         "moe_reserve": [H, I],
         "moe_load_weights": [H, P, P, P, P, P],
+        "moe_load_shared_weights": [H, P, P, P, P, P],
         "moe_forward": [H, I, P, P, P, P, P, P],
         "moe_forward_host": [H, I, P, P, P, P, P, P],
         "moe_forward_host_async": [H, I, P, P, P, P, P, P],
@@ -108,13 +110,22 @@ def _stream_handle(stream) -> int:
 
 
 class FusedMoE:
-    """The fused FP8 MoE layer on the current CUDA device (one handle of the C ABI)."""
+    """The fused FP8 MoE layer on the current CUDA device (one handle of the C ABI).
+    `n_shared` shared experts (moe_create_shared): every token also goes through each, its
+    output added with weight 1; their weights come from load_shared_weights.  `E` and
+    `topk` are the routed counts; the debug views use the handle's expert slots
+    (E + n_shared) and combine planes (topk + n_shared)."""
 
-    def __init__(self, E: int, H: int, I: int, topk: int, R: int):
+    def __init__(self, E: int, H: int, I: int, topk: int, R: int, n_shared: int = 0):
         self.lib = load()
         self.E, self.H, self.I, self.topk, self.R = E, H, I, topk, R
+        self.n_shared = n_shared
+        self.E_slots, self.K_planes = E + n_shared, topk + n_shared
         h = ctypes.c_void_p()
-        _check(self.lib.moe_create(E, H, I, topk, R, ctypes.byref(h)), "moe_create")
+        if n_shared:
+            _check(self.lib.moe_create_shared(E, H, I, topk, R, n_shared, ctypes.byref(h)), "moe_create_shared")
+        else:
+            _check(self.lib.moe_create(E, H, I, topk, R, ctypes.byref(h)), "moe_create")
         self.h = h
         self.max_tokens = 0
 
@@ -125,16 +136,25 @@ class FusedMoE:
         return self
 
     def load_weights(self, w_gate_up, sf_gate_up, w_down, sf_down, stream=None):
+        self._load(self.lib.moe_load_weights, self.E, "moe_load_weights",
+                   w_gate_up, sf_gate_up, w_down, sf_down, stream)
+        return self
+
+    def load_shared_weights(self, w_gate_up, sf_gate_up, w_down, sf_down, stream=None):
+        # (a handle without shared experts refuses in the C call, with MOE_ERR_INVALID_ARG)
+        self._load(self.lib.moe_load_shared_weights, self.n_shared or w_gate_up.shape[0],
+                   "moe_load_shared_weights", w_gate_up, sf_gate_up, w_down, sf_down, stream)
+        return self
+
+    def _load(self, fn, E, what, w_gate_up, sf_gate_up, w_down, sf_down, stream):
         import torch
-        E, H, I = self.E, self.H, self.I
+        H, I = self.H, self.I
         _expect(w_gate_up, (E, 2 * I, H), torch.uint8, "w_gate_up")
         _expect(sf_gate_up, (E, 2 * I // 128, H // 128), torch.float32, "sf_gate_up")
         _expect(w_down, (E, H, I), torch.uint8, "w_down")
         _expect(sf_down, (E, H // 128, I // 128), torch.float32, "sf_down")
-        _check(self.lib.moe_load_weights(self.h, w_gate_up.data_ptr(), sf_gate_up.data_ptr(),
-                                         w_down.data_ptr(), sf_down.data_ptr(),
-                                         _stream_handle(stream)), "moe_load_weights")
-        return self
+        _check(fn(self.h, w_gate_up.data_ptr(), sf_gate_up.data_ptr(), w_down.data_ptr(),
+                  sf_down.data_ptr(), _stream_handle(stream)), what)
 
     def set_option(self, option: int, value: int):
         _check(self.lib.moe_set_option(self.h, option, value), "moe_set_option")
@@ -188,12 +208,12 @@ class FusedMoE:
 
     def debug_routing(self, T: int) -> dict:
         import numpy as np
-        E, R = self.E, self.R
+        E, R = self.E_slots, self.R
         inf = self.info()
         counts = np.zeros(E, np.uint32)
         recv = np.zeros((E, R), np.uint32)
         off = np.zeros(E + 1, np.int32)
-        rows_cap = (-(-T * self.topk // inf.block_m) + E) * inf.block_m
+        rows_cap = (-(-T * self.K_planes // inf.block_m) + E) * inf.block_m
         meta = np.zeros((max(rows_cap, 1), 3), np.uint32)
         P = ctypes.c_int(0)
         bm = ctypes.c_int(0)
@@ -205,19 +225,19 @@ class FusedMoE:
 
     def cumulative_expert_rows(self):
         import numpy as np
-        rows = np.zeros(self.E, np.uint64)
+        rows = np.zeros(self.E_slots, np.uint64)
         _check(self.lib.moe_cumulative_expert_rows(self.h, rows.ctypes.data), "moe_cumulative_expert_rows")
         return rows
 
     def debug_buffer(self, which: str):
         import numpy as np
         inf = self.info()
-        P, H, I, K = inf.pool_rows, self.H, self.I, self.topk
+        P, H, I, K = inf.pool_rows, self.H, self.I, self.K_planes
         shapes = {
             "pool_x": ((P, H), np.uint8), "pool_sf": ((H // 128, P), np.float32),
             "act": ((P, I), np.uint8), "act_sf": ((I // 128, P), np.float32),
             "combine": ((K, inf.max_tokens, H), np.uint16),
-            "table": ((self.E, self.R, max(1, inf.max_tokens // self.R)), np.int32),
+            "table": ((self.E_slots, self.R, max(1, inf.max_tokens // self.R)), np.int32),
         }
         shape, dt = shapes[which]
         a = np.zeros(shape, dt)

@@ -46,7 +46,7 @@ enum moe_status {
     MOE_ERR_INVALID_ARG = 1,        /* bad size, null or misaligned pointer            */
     MOE_ERR_CUDA = 2,               /* a CUDA runtime/driver call failed               */
     MOE_ERR_CAPACITY = 3,           /* T above the reserved maximum                    */
-    MOE_ERR_NO_WEIGHTS = 4,         /* forward before moe_load_weights                 */
+    MOE_ERR_NO_WEIGHTS = 4,         /* forward before the weights (routed and shared) are loaded */
     MOE_ERR_UNSUPPORTED_DEVICE = 5, /* not an sm_103 GPU, or a shape this build lacks  */
     MOE_ERR_BAD_INDEX = 6,          /* device: an expert id outside [0,E) other than -1 */
     MOE_ERR_TIMEOUT = 7,            /* device: a bounded wait gave up                  */
@@ -61,6 +61,16 @@ enum moe_status {
  * topk <= E <= 1024, 1 <= R <= 64, E*R <= 16384, on the current device, which must be
  * sm_103.  Allocates no device memory.  *out receives the handle. */
 int moe_create(int E, int H, int I, int topk, int R, moe_handle_t *out);
+
+/* As moe_create, with n_shared shared experts besides the E routed ones ("DeepGEMM Mega MoE
+ * 对称内存（Symmetric Memory）深度分析" §8.2: the combine buffer gets a plane after the top-k
+ * ones when shared experts exist, and §10.1 passes their weights separately).  Every token
+ * also goes through each shared expert (same H and I as the routed ones), whose output is
+ * added to the token's top-k sum with weight 1.  The caller's topk_idx / topk_w stay
+ * [T][topk] (routed only); the shared experts' weights come from moe_load_shared_weights.
+ * Requires E + n_shared <= 1024, topk + n_shared <= 32, (E + n_shared)*R <= 16384;
+ * n_shared = 0 is moe_create. */
+int moe_create_shared(int E, int H, int I, int topk, int R, int n_shared, moe_handle_t *out);
 
 /* Allocate the device workspace for up to max_tokens tokens per forward (the pages'
  * host pre-sizing: a larger batch is an error, not a reallocation).  May be called
@@ -77,6 +87,12 @@ int moe_reserve(moe_handle_t h, int max_tokens);
  * ("DeepGEMM Mega MoE 对称内存（Symmetric Memory）深度分析" §10.2). */
 int moe_load_weights(moe_handle_t h, const uint8_t *w_gate_up, const float *sf_gate_up,
                      const uint8_t *w_down, const float *sf_down, void *stream);
+
+/* Weights of the n_shared shared experts, layouts as moe_load_weights with n_shared in
+ * place of E.  Required before a forward of a handle made with n_shared > 0;
+ * MOE_ERR_INVALID_ARG on a handle without shared experts. */
+int moe_load_shared_weights(moe_handle_t h, const uint8_t *w_gate_up, const float *sf_gate_up,
+                            const uint8_t *w_down, const float *sf_down, void *stream);
 
 /* The layer on T tokens (0 <= T <= max_tokens, T % R == 0; source r owns tokens
  * [r*T/R, (r+1)*T/R)).  Asynchronous on `stream`.
@@ -147,6 +163,9 @@ typedef struct moe_info {
     int num_sms;          /* persistent grid size                            */
     uint64_t workspace_bytes;
     uint64_t weight_bytes;
+    int n_shared;         /* shared experts; E and topk above include them: shared expert s
+                             is expert slot E - n_shared + s and combine plane
+                             topk - n_shared + s (the debug buffers use these sizes) */
 } moe_info;
 int moe_get_info(moe_handle_t h, moe_info *info);
 

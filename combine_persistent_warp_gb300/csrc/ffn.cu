@@ -69,6 +69,12 @@ constexpr uint32_t PAIR_STAGE_BYTES = STAGE_A_BYTES + PAIR_B_BYTES;
 constexpr int PAIR_STAGES = static_cast<int>((STAGES * STAGE_BYTES) / PAIR_STAGE_BYTES);
 constexpr int MAX_STAGES = PAIR_STAGES > STAGES ? PAIR_STAGES : STAGES;
 constexpr uint32_t IDESC_PAIR = ptx::idesc_e4m3_f32(2 * BM, BN);
+// One CTA, one stage per scale block: the UMMA issuer commits once per K block (to the
+// TMEM-full barrier) and the epilogue, having seen that the MMAs are done, releases the
+// operand stage to the producer.  A second commit per K block for the stage cost ~95 cycles
+// of UMMA issue each time.
+template <bool PAIRED>
+constexpr bool EPI_RELEASES_STAGE = !PAIRED && SUBS == 1;
 static_assert(PAIR_STAGES * PAIR_STAGE_BYTES <= STAGES * STAGE_BYTES, "pair stages exceed the ring");
 
 #ifdef CPW_TRACE
@@ -450,7 +456,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                             }
                             if constexpr (PAIRED)
                                 ptx::umma_commit_pair(&bars->empty[s], static_cast<uint16_t>(0x3));
-                            else
+                            else if constexpr (!EPI_RELEASES_STAGE<PAIRED>)
                                 ptx::umma_commit(&bars->empty[s]);
                             CPW_STAMP(2, it);
                         }
@@ -568,6 +574,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 if (!__all_sync(0xFFFFFFFFu, ptx::mbar_wait(&bars->tfull[buf], bph, deadline))) {
                     ok = false;
                     break;
+                }
+                if constexpr (EPI_RELEASES_STAGE<PAIRED>) {
+                    if (warp == 4 && lane == 0)
+                        ptx::mbar_arrive(&bars->empty[pit % NST]);   // this K block's operand stage
                 }
                 if (warp == 4 && lane == 0)
                     CPW_STAMP(3, pit);

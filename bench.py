@@ -44,8 +44,8 @@ L2_BYTES = 129 * 2 ** 20
 # DRAM bytes per launch from one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum),
 # valid only while the kernel sources hash to `src_sha`; see profiles/.
 NCU_TRAFFIC = {
-    ("decode", "expert_ffn"): {"bytes": 1425209600 + 13367040, "src_sha": "b7eea1b711ed0325"},
-    ("prefill", "expert_ffn"): {"bytes": 2130786304 + 528295680, "src_sha": "b7eea1b711ed0325"},
+    ("decode", "expert_ffn"): {"bytes": 1425220352 + 14429440, "src_sha": "59a1f06def27fd31"},
+    ("prefill", "expert_ffn"): {"bytes": 1919576320 + 535503360, "src_sha": "59a1f06def27fd31"},
     ("decode-pow2", "expert_ffn"): {"bytes": 1465405952 + 3284480, "src_sha": "47ce09d331634a6c"},
     ("prefill-pow2", "expert_ffn"): {"bytes": 2202144256 + 517698304, "src_sha": "47ce09d331634a6c"},
 }

@@ -40,6 +40,7 @@ FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 FP8_OVER_BF16 = 2.0          # nominal dense FP8 / BF16 tensor-rate ratio on GB300
 L2_BYTES = 129 * 2 ** 20
+PROFILE_EVERY = 8            # timed steps per step carrying the per-kernel stage events
 
 # DRAM bytes per launch from one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum),
 # valid only while the kernel sources hash to `src_sha`; see profiles/.
@@ -333,7 +334,9 @@ def run_ours(args, dist: Dist) -> dict | None:
     sampler = ClockSampler(gpu_query_id(torch, dist.local_rank))
     sampler.start()
     time.sleep(0.3)
-    moe.profile_enable(True)
+    # per-kernel CUDA events on every PROFILE_EVERY-th step of the timed region (events
+    # between kernels serialise them, so recording them on every step would slow it)
+    moe.profile_enable(True, every=PROFILE_EVERY)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     dist.barrier()
     torch.cuda.synchronize()
@@ -407,6 +410,7 @@ def run_ours(args, dist: Dist) -> dict | None:
         "gpu_launches": 3 * args.steps,
         "roofline": roof,
         "stages_us_per_launch": stages,
+        "stage_events": {"every_nth_step": PROFILE_EVERY, "steps_with_events": prof["calls"]},
         "clocks": sampler.summary(h0, h1),
     }
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:

@@ -65,6 +65,8 @@ struct moe_ctx {
                                  // 2 block-scaled exactly when the weights' scales are 2^k
     // stage profiling (events on the forward's stream)
     bool profile = false;
+    int prof_every = 1;                // record every prof_every-th forward
+    long long prof_seen = 0;           // forwards since profiling was enabled
     std::vector<cudaEvent_t> events;   // 4 per recorded forward
     int prof_calls = 0, prof_dropped = 0;
 };
@@ -466,7 +468,7 @@ int moe_forward(moe_handle_t h, int T, const uint8_t *x, const float *x_sf, cons
         c.w = h->ext_w;
     }
     cudaEvent_t *ev = nullptr;
-    if (h->profile) {
+    if (h->profile && (h->prof_seen++ % h->prof_every) == 0) {
         if (h->prof_calls < PROF_MAX_CALLS)
             ev = &h->events[static_cast<size_t>(h->prof_calls++) * 4];
         else
@@ -719,7 +721,7 @@ int moe_set_option(moe_handle_t h, int option, int64_t value)
 
 int moe_profile_enable(moe_handle_t h, int enable)
 {
-    if (!h)
+    if (!h || enable < 0)
         return MOE_ERR_INVALID_ARG;
     CK(cudaSetDevice(h->dev));
     if (enable && h->events.empty()) {
@@ -728,6 +730,8 @@ int moe_profile_enable(moe_handle_t h, int enable)
             CK(cudaEventCreate(&e));
     }
     h->profile = enable != 0;
+    h->prof_every = enable > 0 ? enable : 1;
+    h->prof_seen = 0;
     h->prof_calls = 0;
     h->prof_dropped = 0;
     return MOE_OK;

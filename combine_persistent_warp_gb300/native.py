@@ -247,8 +247,9 @@ class FusedMoE:
 
     STAGES = ("dispatch", "expert_ffn", "combine")
 
-    def profile_enable(self, on: bool = True):
-        _check(self.lib.moe_profile_enable(self.h, 1 if on else 0), "moe_profile_enable")
+    def profile_enable(self, on=True, every: int = 1):
+        """Record stage events on every `every`-th forward (on=False stops)."""
+        _check(self.lib.moe_profile_enable(self.h, max(1, int(every)) if on else 0), "moe_profile_enable")
 
     def profile_read(self) -> dict:
         import numpy as np

@@ -194,13 +194,15 @@ enum moe_option {
 };
 int moe_set_option(moe_handle_t h, int option, int64_t value);
 
-/* Stage timing with CUDA events recorded on the forward's own stream.  While enabled,
- * every moe_forward records an event before and after each of its three kernels
- * (dispatch; expert FFN = gate_up GEMM + SwiGLU + down GEMM + weighted scatter; combine);
+/* Stage timing with CUDA events recorded on the forward's own stream.  enable = N > 0:
+ * the 1st, (N+1)-th, (2N+1)-th ... moe_forward from now records an event before and after
+ * each of its three kernels (dispatch; expert FFN = gate_up GEMM + SwiGLU + down GEMM +
+ * weighted scatter; combine) — N > 1 samples the forwards, so the events (which serialise
+ * the kernels they sit between) disturb only one step in N; enable = 0 stops.
  * moe_profile_read waits for the last stream, returns the summed milliseconds of each
  * stage over the recorded forwards in stage_ms[3] and their number in *calls, and starts
- * a new window.  At most 8192
- * forwards are recorded per window (later ones are counted in *dropped, not timed). */
+ * a new window.  At most 8192 forwards are recorded per window (later ones are counted in
+ * *dropped, not timed). */
 int moe_profile_enable(moe_handle_t h, int enable);
 int moe_profile_read(moe_handle_t h, double *stage_ms, int *calls, int *dropped);
 

@@ -47,10 +47,17 @@ struct moe_ctx {
     FfnMaps maps{};              // a1 pool x, b1 W1, a2 act, b2 W2
     SfMaps sf_maps{};            // UE8M0 scale blocks of pool / act rows and weight tiles
     // staging buffers of moe_forward_host
-    uint8_t *st_x = nullptr;
-    float *st_sf = nullptr;
-    int64_t *st_idx = nullptr;
-    float *st_w = nullptr;
+    // (two input sets: an asynchronous call fills one with the copy engines on copy_stream
+    // while the previous call's kernels still read the other)
+    uint8_t *st_x[2] = {nullptr, nullptr};
+    float *st_sf[2] = {nullptr, nullptr};
+    int64_t *st_idx[2] = {nullptr, nullptr};
+    float *st_w[2] = {nullptr, nullptr};
+    cudaStream_t copy_stream = nullptr;
+    cudaEvent_t ev_staged[2] = {nullptr, nullptr};   // copy_stream: set filled
+    cudaEvent_t ev_free[2] = {nullptr, nullptr};     // forward's stream: set no longer read
+    bool free_recorded[2] = {false, false};
+    unsigned host_calls = 0;
     uint16_t *st_out = nullptr;
     // shared experts: every token's route extended by slots K_routed.. (expert E_routed + s, weight 1)
     int64_t *ext_idx = nullptr;
@@ -152,6 +159,9 @@ bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 
 void free_big(moe_ctx *h)
 {
+    if (h->copy_stream)
+        cudaStreamSynchronize(h->copy_stream);
+    h->free_recorded[0] = h->free_recorded[1] = false;
     if (h->big_mem)
         cudaFree(h->big_mem);
     h->big_mem = nullptr;
@@ -185,10 +195,12 @@ size_t carve_big(moe_ctx *h, char *base, int max_tokens, Workspace &ws)
     ws.act_sf = c.take<float>(static_cast<size_t>(P) * (d.I / 128));
     ws.act_sfe = c.take<uint8_t>(static_cast<size_t>(P) * (d.I / 32));
     ws.combine = c.take<uint16_t>(static_cast<size_t>(d.K) * max_tokens * d.H);
-    h->st_x = c.take<uint8_t>(static_cast<size_t>(max_tokens) * d.H);
-    h->st_sf = c.take<float>(static_cast<size_t>(max_tokens) * (d.H / 128));
-    h->st_idx = c.take<int64_t>(static_cast<size_t>(max_tokens) * d.K);
-    h->st_w = c.take<float>(static_cast<size_t>(max_tokens) * d.K);
+    for (int i = 0; i < 2; ++i) {
+        h->st_x[i] = c.take<uint8_t>(static_cast<size_t>(max_tokens) * d.H);
+        h->st_sf[i] = c.take<float>(static_cast<size_t>(max_tokens) * (d.H / 128));
+        h->st_idx[i] = c.take<int64_t>(static_cast<size_t>(max_tokens) * d.K);
+        h->st_w[i] = c.take<float>(static_cast<size_t>(max_tokens) * d.K);
+    }
     h->st_out = c.take<uint16_t>(static_cast<size_t>(max_tokens) * d.H);
     if (h->S > 0) {
         h->ext_idx = c.take<int64_t>(static_cast<size_t>(max_tokens) * d.K);
@@ -505,10 +517,13 @@ static void *mapped_host(const void *p)
     return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
 }
 
-// Shared body of the host-buffer entry points.  Inputs in pinned memory are read in place by
-// one staging kernel (16-byte aligned buffers), others are copied by the copy engine; the
-// output is written in place by the combine kernel when it is pinned and 16-byte aligned,
-// else copied back from the staging buffer.
+// Shared body of the host-buffer entry points.  Asynchronous calls with pinned inputs copy
+// them with the copy engines on a side stream into one of two staging sets, so the copies of
+// call i+1 overlap the kernels of call i (the forward waits for its copies by an event, and
+// a set is refilled only after the forward that read it).  Otherwise pinned inputs are read
+// in place by one staging kernel (16-byte aligned buffers) and pageable ones copied on the
+// forward's stream.  The output is written in place by the combine kernel when it is pinned
+// and 16-byte aligned, else copied back from the staging buffer.
 static int forward_host_impl(moe_handle_t h, int T, const uint8_t *host_x, const float *host_x_sf,
                              const int64_t *host_topk_idx, const float *host_topk_w, uint16_t *host_out,
                              void *stream, bool wait)
@@ -529,27 +544,56 @@ static int forward_host_impl(moe_handle_t h, int T, const uint8_t *host_x, const
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const Dims &d = h->d;
     const void *src[4] = {host_x, host_x_sf, host_topk_idx, host_topk_w};
-    void *dst[4] = {h->st_x, h->st_sf, h->st_idx, h->st_w};
     const long long bytes[4] = {static_cast<long long>(T) * d.H, 4ll * T * (d.H / 128), 8ll * T * h->K_routed,
                                 4ll * T * h->K_routed};
     const void *dev_src[4];
-    bool in_place = true;
-    for (int i = 0; i < 4 && in_place; ++i) {
+    bool pinned = true, in_place = true;
+    for (int i = 0; i < 4; ++i) {
         dev_src[i] = mapped_host(src[i]);
-        in_place = dev_src[i] != nullptr && aligned(dev_src[i], 16);
+        pinned = pinned && dev_src[i] != nullptr;
+        in_place = in_place && dev_src[i] != nullptr && aligned(dev_src[i], 16);
     }
-    if (in_place) {
-        CK(launch_stage_inputs(dev_src, dst, bytes, h->num_sms, s));
-    } else {
+    int set = 0;
+    if (!wait && pinned) {
+        if (!h->copy_stream) {
+            CK(cudaStreamCreateWithFlags(&h->copy_stream, cudaStreamNonBlocking));
+            for (int i = 0; i < 2; ++i) {
+                CK(cudaEventCreateWithFlags(&h->ev_staged[i], cudaEventDisableTiming));
+                CK(cudaEventCreateWithFlags(&h->ev_free[i], cudaEventDisableTiming));
+            }
+        }
+        set = static_cast<int>(h->host_calls++ & 1u);
+        void *dst[4] = {h->st_x[set], h->st_sf[set], h->st_idx[set], h->st_w[set]};
+        if (h->free_recorded[set])
+            CK(cudaStreamWaitEvent(h->copy_stream, h->ev_free[set], 0));
         for (int i = 0; i < 4; ++i)
-            CK(cudaMemcpyAsync(dst[i], src[i], static_cast<size_t>(bytes[i]), cudaMemcpyHostToDevice, s));
+            CK(cudaMemcpyAsync(dst[i], src[i], static_cast<size_t>(bytes[i]), cudaMemcpyHostToDevice,
+                               h->copy_stream));
+        CK(cudaEventRecord(h->ev_staged[set], h->copy_stream));
+        CK(cudaStreamWaitEvent(s, h->ev_staged[set], 0));
+    } else {
+        // set 0: any asynchronous call that used it has been waited for by this stream order
+        // (its forward ran on a stream this call follows) or by a synchronous return
+        if (h->free_recorded[0])
+            CK(cudaStreamWaitEvent(s, h->ev_free[0], 0));
+        void *dst[4] = {h->st_x[0], h->st_sf[0], h->st_idx[0], h->st_w[0]};
+        if (in_place) {
+            CK(launch_stage_inputs(dev_src, dst, bytes, h->num_sms, s));
+        } else {
+            for (int i = 0; i < 4; ++i)
+                CK(cudaMemcpyAsync(dst[i], src[i], static_cast<size_t>(bytes[i]), cudaMemcpyHostToDevice, s));
+        }
     }
     uint16_t *out_dev = static_cast<uint16_t *>(mapped_host(host_out));
     const bool out_in_place = out_dev != nullptr && aligned(out_dev, 16);
-    int rc = moe_forward(h, T, h->st_x, h->st_sf, h->st_idx, h->st_w, out_in_place ? out_dev : h->st_out,
-                         stream);
+    int rc = moe_forward(h, T, h->st_x[set], h->st_sf[set], h->st_idx[set], h->st_w[set],
+                         out_in_place ? out_dev : h->st_out, stream);
     if (rc != MOE_OK)
         return rc;
+    if (h->ev_free[set]) {
+        CK(cudaEventRecord(h->ev_free[set], s));
+        h->free_recorded[set] = true;
+    }
     if (!out_in_place)
         CK(cudaMemcpyAsync(host_out, h->st_out, sizeof(uint16_t) * T * d.H, cudaMemcpyDeviceToHost, s));
     if (wait)
@@ -772,6 +816,14 @@ int moe_destroy(moe_handle_t h)
     for (auto &e : h->events)
         cudaEventDestroy(e);
     free_big(h);
+    for (int i = 0; i < 2; ++i) {
+        if (h->ev_staged[i])
+            cudaEventDestroy(h->ev_staged[i]);
+        if (h->ev_free[i])
+            cudaEventDestroy(h->ev_free[i]);
+    }
+    if (h->copy_stream)
+        cudaStreamDestroy(h->copy_stream);
     if (h->small_mem)
         cudaFree(h->small_mem);
     if (h->w_mem)

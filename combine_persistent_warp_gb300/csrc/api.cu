@@ -361,7 +361,9 @@ int load_expert_weights(moe_ctx *h, int e0, int n, const uint8_t *w_gate_up, con
     const Dims &d = h->d;
     const size_t w1e = static_cast<size_t>(2) * d.I * d.H, w2e = static_cast<size_t>(d.H) * d.I;
     const size_t s1e = static_cast<size_t>(2 * d.I / 128) * (d.H / 128), s2e = static_cast<size_t>(d.H / 128) * (d.I / 128);
-    const size_t b1e = static_cast<size_t>(2 * d.I / BN) * (d.H / 128) * 1024, b2e = static_cast<size_t>(d.H / BN) * (d.I / 128) * 1024;
+    // UE8M0 scale blocks: 1 KB per weight tile and group of four 128-deep K blocks
+    const size_t b1e = static_cast<size_t>(2 * d.I / BN) * ((d.H / 128 + 3) / 4) * 1024,
+                 b2e = static_cast<size_t>(d.H / BN) * ((d.I / 128 + 3) / 4) * 1024;
     const size_t n1 = d.E * w1e, n2 = d.E * w2e;
     if (!h->w_mem) {
         Carver c{nullptr};
@@ -371,7 +373,6 @@ int load_expert_weights(moe_ctx *h, int e0, int n, const uint8_t *w_gate_up, con
             h->s1 = c.take<float>(d.E * s1e);
             h->w2 = c.take<uint8_t>(n2);
             h->s2 = c.take<float>(d.E * s2e);
-            // UE8M0 scale blocks: 1 KB per weight tile (256 rows) and 128-deep K block
             h->sfb1 = c.take<uint8_t>(d.E * b1e);
             h->sfb2 = c.take<uint8_t>(d.E * b2e);
             h->sfb_bad = c.take<uint32_t>(1);

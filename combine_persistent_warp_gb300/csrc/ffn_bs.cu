@@ -13,13 +13,16 @@
 // （Symmetric Memory）深度分析" §8.1 and the UE8M0 scale format it names); with arbitrary fp32
 // scales the layer uses ffn.cu instead.
 //
-// Scale factors reach TMEM through shared memory: per stage the producer bulk-copies a
-// 512-byte A block (the 128 rows' scale words, row r at byte 16*(r%32) + 4*(r/32)) and a
-// 1 KB B block (two 512-byte halves; tile column n at 512*(n/128) + 16*(n%32) + 4*((n%128)/32)),
-// each word holding the UE8M0 byte four times (one per 32-deep K slice).  The UMMA issuer
-// copies them into TMEM with tcgen05.cp 32x128b.warpx4 (every lane quarter gets the same
-// 32 lanes), where the UMMA reads row m's scale at lane m, column base + m/32, and tile
-// column n's at lane 32*q + n%32, column base + n/32, byte = the K slice.
+// Scale factors reach TMEM through shared memory, once per group of four 128-deep K blocks:
+// with a group's first stage the producer bulk-copies a 512-byte A block (the 128 rows'
+// scale words, row r at byte 16*(r%32) + 4*(r/32)) and a 1 KB B block (two 512-byte halves;
+// tile column n at 512*(n/128) + 16*(n%32) + 4*((n%128)/32)), each word holding the UE8M0
+// bytes of the group's four K blocks (byte j = K block 4g + j).  The UMMA issuer copies them
+// into TMEM with tcgen05.cp 32x128b.warpx4 (every lane quarter gets the same 32 lanes),
+// where the UMMA reads row m's scale at lane m, column base + m/32, and tile column n's at
+// lane 32*q + n%32, column base + n/32, byte = the instruction's scale id, here K block % 4
+// for all four 32-deep UMMAs of a K block.  Copying once per group instead of once per K
+// block took the issue sequence from ~830 to ~700 cycles per K block.
 //
 // Roles (one CTA per SM, 12 warps): warp 0 TMA producer (A, B and the two scale blocks of
 // a 128-deep K block per stage, 4 stages); warp 1 UMMA issuer (scale copies + 4 block-scaled
@@ -41,7 +44,8 @@ namespace {
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int EPI_WARPS = 8;
 constexpr int TILE_RING = 4;
-constexpr uint32_t SF_COL = 256;          // scale slot s: columns SF_COL + 16*s (A: +0..3, B: +4..11)
+constexpr uint32_t SF_COL = 256;          // scale slot j: columns SF_COL + 16*j (A: +0..3, B: +4..11)
+constexpr int SF_GROUP = 4;               // K blocks per scale block (bytes of a scale word)
 constexpr uint32_t SFA_BYTES = 512, SFB_BYTES = 1024, SF_STAGE_BYTES = SFA_BYTES + SFB_BYTES;
 static_assert(BKS == BK, "the block-scaled kernel stages whole 128-deep K blocks");
 // Two-CTA mode: one M = 256 UMMA covers two M-blocks of an expert, one per CTA of a cluster
@@ -55,14 +59,14 @@ constexpr int PAIR_STAGES = static_cast<int>((STAGES * STAGE_BYTES) / PAIR_STAGE
 static_assert(PAIR_STAGES * PAIR_STAGE_BYTES <= STAGES * STAGE_BYTES, "pair stages exceed the ring");
 static_assert(SF_COL + 16 * PAIR_STAGES <= TMEM_COLS, "scale slots exceed TMEM");
 
-// block-scaled instruction descriptor: B scale slice at bits 4-5, e4m3 A/B (formats 0),
-// K-major A and B, N>>3 at 17-22, UE8M0 scales (bit 23), M>>4 at 24-28, A scale slice at
-// 29-30
+// block-scaled instruction descriptor: B scale id (byte of the scale word) at bits 4-5, e4m3
+// A/B (formats 0), K-major A and B, N>>3 at 17-22, UE8M0 scales (bit 23), M>>4 at 24-28, A
+// scale id at 29-30
 template <int M>
-__device__ __forceinline__ uint32_t idesc_bs(int k)
+__device__ __forceinline__ uint32_t idesc_bs(int sf_id)
 {
-    return (static_cast<uint32_t>(k) << 4) | (static_cast<uint32_t>(BN >> 3) << 17) | (1u << 23) |
-           (static_cast<uint32_t>(M >> 4) << 24) | (static_cast<uint32_t>(k) << 29);
+    return (static_cast<uint32_t>(sf_id) << 4) | (static_cast<uint32_t>(BN >> 3) << 17) | (1u << 23) |
+           (static_cast<uint32_t>(M >> 4) << 24) | (static_cast<uint32_t>(sf_id) << 29);
 }
 
 // one CTA: D (128 rows) (+)= A x B^T with scales from this CTA's TMEM.  Two CTAs (issued by
@@ -356,20 +360,24 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     const uint32_t a_bytes = a_stage_bytes(n_part);
                     // bytes the stage's full barrier waits for: this CTA's, plus (2-CTA mode,
                     // even CTA) the odd CTA's, whose loads count on the even CTA's barrier
-                    uint32_t tx_bytes = a_bytes + (PAIRED ? PAIR_B_BYTES : STAGE_B_BYTES) +
-                                        (tv.null_half ? 0u : SFA_BYTES) + SFB_BYTES;
+                    // (the scale blocks only with the first stage of a group of K blocks)
+                    uint32_t tx_bytes = a_bytes + (PAIRED ? PAIR_B_BYTES : STAGE_B_BYTES);
+                    uint32_t tx_sf = (tv.null_half ? 0u : SFA_BYTES) + SFB_BYTES;
                     if (PAIRED && rank == 0) {
                         const BsView ov = view_of(tile, 1);
-                        tx_bytes += a_stage_bytes(a_parts(ov)) + PAIR_B_BYTES + (ov.null_half ? 0u : SFA_BYTES) + SFB_BYTES;
+                        tx_bytes += a_stage_bytes(a_parts(ov)) + PAIR_B_BYTES;
+                        tx_sf += (ov.null_half ? 0u : SFA_BYTES) + SFB_BYTES;
                     }
                     const CUtensorMap *ta = phase == 1 ? (part ? &maps.a1p : &maps.a1) : (part ? &maps.a2p : &maps.a2);
                     const CUtensorMap *tb = PAIRED ? (phase == 1 ? &maps.b1h : &maps.b2h) : (phase == 1 ? &maps.b1 : &maps.b2);
                     const int nkb = phase == 1 ? NKB1 : NKB2;
-                    const int tile0 = (e * (phase == 1 ? tl.NT1 : tl.NT2) + nt) * nkb;
-                    // scale blocks: A per (M-block, K block), B per (weight tile, K block)
+                    const int wtile = e * (phase == 1 ? tl.NT1 : tl.NT2) + nt;
+                    const int tile0 = wtile * nkb;
+                    // scale blocks: A per (M-block, K-block group), B per (weight tile, group)
+                    const int ng = (nkb + SF_GROUP - 1) / SF_GROUP;
                     const uint8_t *sfa_src = (phase == 1 ? ws.pool_sfe : ws.act_sfe) +
-                                             static_cast<long long>(blk) * nkb * SFA_BYTES;
-                    const uint8_t *sfb_src = (phase == 1 ? sfb1 : sfb2) + static_cast<long long>(tile0) * SFB_BYTES;
+                                             static_cast<long long>(blk) * ng * SFA_BYTES;
+                    const uint8_t *sfb_src = (phase == 1 ? sfb1 : sfb2) + static_cast<long long>(wtile) * ng * SFB_BYTES;
                     if (phase == 2 && !tv.null_half) {
                         // the act rows and their scales of this block are complete: the
                         // dependency warp has acquired the block's gate_up completion count
@@ -399,8 +407,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                         }
                         uint8_t *sa = smem + s * SBYTES;
                         uint8_t *ss = sf_smem + s * SF_STAGE_BYTES;
+                        const bool sf_k = kb % SF_GROUP == 0;   // first K block of a scale group
+                        const int grp = kb / SF_GROUP;
                         if (!PAIRED || rank == 0)
-                            ptx::mbar_arrive_expect_tx(&bars->full[s], tx_bytes);
+                            ptx::mbar_arrive_expect_tx(&bars->full[s], tx_bytes + (sf_k ? tx_sf : 0u));
                         if constexpr (PAIRED) {
                             // own A rows, own half of the weight tile, own copies of the scale
                             // blocks (this block's A scales; all 256 weight rows' scales),
@@ -415,11 +425,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                             }
                             ptx::tma_load_2d_pair(sa + STAGE_A_BYTES, tb, fb, 0,
                                                   (tile0 + kb) * BN + static_cast<int>(rank) * (BN / 2), pol_b);
-                            if (!tv.null_half)
+                            if (sf_k && !tv.null_half)
                                 ptx::tma_load_2d_pair(ss, phase == 1 ? &sfm.sfa1 : &sfm.sfa2, fb, 0,
-                                                      (blk * nkb + kb) * static_cast<int>(SFA_BYTES / 256), pol_a);
-                            ptx::tma_load_2d_pair(ss + SFA_BYTES, phase == 1 ? &sfm.sfb1 : &sfm.sfb2, fb, 0,
-                                                  (tile0 + kb) * static_cast<int>(SFB_BYTES / 256), pol_b);
+                                                      (blk * ng + grp) * static_cast<int>(SFA_BYTES / 256), pol_a);
+                            if (sf_k)
+                                ptx::tma_load_2d_pair(ss + SFA_BYTES, phase == 1 ? &sfm.sfb1 : &sfm.sfb2, fb, 0,
+                                                      (wtile * ng + grp) * static_cast<int>(SFB_BYTES / 256), pol_b);
                         } else {
                             if (part) {
                                 for (int g = 0; g < n_part; ++g)
@@ -429,9 +440,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                                 ptx::tma_load_2d(sa, ta, &bars->full[s], kb * BK, blk * BM, pol_a);
                             }
                             ptx::tma_load_2d(sa + STAGE_A_BYTES, tb, &bars->full[s], 0, (tile0 + kb) * BN, pol_b);
-                            ptx::bulk_load(ss, sfa_src + kb * SFA_BYTES, SFA_BYTES, &bars->full[s]);
-                            ptx::bulk_load(ss + SFA_BYTES, sfb_src + static_cast<long long>(kb) * SFB_BYTES, SFB_BYTES,
-                                           &bars->full[s]);
+                            if (sf_k) {
+                                ptx::bulk_load(ss, sfa_src + grp * SFA_BYTES, SFA_BYTES, &bars->full[s]);
+                                ptx::bulk_load(ss + SFA_BYTES, sfb_src + static_cast<long long>(grp) * SFB_BYTES,
+                                               SFB_BYTES, &bars->full[s]);
+                            }
                         }
                     }
                     while (ok && fstep < 3)
@@ -489,6 +502,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             // the odd CTA's issuer only takes its tile slots)
             if (lane == 0) {
                 uint32_t it = 0, tcount = 0, acc_n = 0;
+                // scale groups copied so far: group g goes to TMEM slot g % NST, reused only after
+                // NST more groups, whose first stage's arrival implies (through the stage ring)
+                // that every UMMA of group g has completed
+                uint32_t gcount = 0, sfa = 0, sfb = 0;
                 bool ok = true;
                 const bool issuer = !PAIRED || rank == 0;
                 while (ok) {
@@ -521,18 +538,23 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                             break;
                         }
                         ptx::tc_fence_after();
-                        const uint32_t ss = ptx::smem_u32(sf_smem + s * SF_STAGE_BYTES);
-                        const uint32_t sfa = tmem + SF_COL + 16 * s, sfb = sfa + 4;
-                        sf_copy<PAIRED>(sfa, ss);
-                        sf_copy<PAIRED>(sfb, ss + SFA_BYTES);
-                        sf_copy<PAIRED>(sfb + 4, ss + SFA_BYTES + 512);
+                        if (kb % SF_GROUP == 0) {
+                            const uint32_t ss = ptx::smem_u32(sf_smem + s * SF_STAGE_BYTES);
+                            sfa = tmem + SF_COL + 16 * (gcount % NST);
+                            sfb = sfa + 4;
+                            ++gcount;
+                            sf_copy<PAIRED>(sfa, ss);
+                            sf_copy<PAIRED>(sfb, ss + SFA_BYTES);
+                            sf_copy<PAIRED>(sfb + 4, ss + SFA_BYTES + 512);
+                        }
                         const uint32_t a_addr = ptx::smem_u32(smem + s * SBYTES);
                         const uint64_t adesc = ptx::kmajor_swizzled_desc<BKS>(a_addr);
                         const uint64_t bdesc = ptx::kmajor_swizzled_desc<BKS>(a_addr + STAGE_A_BYTES);
 #pragma unroll
                         for (int k = 0; k < BK / 32; ++k)   // +32 bytes along K = +2 in the >>4 field
-                            umma_bs<PAIRED>(tmem, adesc + 2 * k, bdesc + 2 * k, idesc_bs<PAIRED ? 2 * BM : BM>(k), sfa,
-                                            sfb, (kb > 0 || k > 0) ? 1u : 0u);
+                            umma_bs<PAIRED>(tmem, adesc + 2 * k, bdesc + 2 * k,
+                                            idesc_bs<PAIRED ? 2 * BM : BM>(kb % SF_GROUP), sfa, sfb,
+                                            (kb > 0 || k > 0) ? 1u : 0u);
                         if constexpr (PAIRED)
                             ptx::umma_commit_pair(&bars->empty[s], static_cast<uint16_t>(0x3));
                         else
@@ -676,10 +698,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     }
                     if (wg == 0) {
                         ws.act_sf[static_cast<long long>(nt) * ws.P + prow] = sf;
-                        // UE8M0 scale word of this row in the block's 512-byte scale block
-                        const uint32_t byte = (__float_as_uint(sf) >> 23) & 0xFFu;
-                        *reinterpret_cast<uint32_t *>(ws.act_sfe + (static_cast<long long>(blk) * NKB2 + nt) * SFA_BYTES +
-                                                      16 * (row % 32) + 4 * (row / 32)) = byte * 0x01010101u;
+                        // UE8M0 byte of this row and K block nt of the down GEMM, in the block's
+                        // 512-byte scale block of group nt / 4
+                        ws.act_sfe[(static_cast<long long>(blk) * ((NKB2 + SF_GROUP - 1) / SF_GROUP) + nt / SF_GROUP) *
+                                       SFA_BYTES +
+                                   16 * (row % 32) + 4 * (row / 32) + nt % SF_GROUP] =
+                            static_cast<uint8_t>(__float_as_uint(sf) >> 23);
                     }
                 }
                 __syncwarp();
@@ -833,9 +857,9 @@ cudaError_t launch_ffn_bs(const FfnMaps &maps, const SfMaps &sf_maps, const Dims
 }
 
 // ------------------------------------------------------------------ weight scales -----
-// Load-time UE8M0 scale blocks of the weight tiles: for weight tile (e, nt) and K block kb,
-// 1 KB at ((e*NT + nt)*KB + kb)*1024 with tile column n's word at 512*(n/128) + 16*(n%32) +
-// 4*((n%128)/32).  Column n of a gate_up tile (gate_up_I > 0) is the gate row group nt if
+// Load-time UE8M0 scale blocks of the weight tiles: for weight tile (e, nt) and group g of
+// four K blocks, 1 KB at ((e*NT + nt)*G + g)*1024 (G = ceil(KB/4)) with tile column n's word
+// at 512*(n/128) + 16*(n%32) + 4*((n%128)/32), byte kb % 4 = K block kb's scale.  Column n of a gate_up tile (gate_up_I > 0) is the gate row group nt if
 // (n/8) is even, else the up group I/128 + nt (the interleave by 8); of a down tile, the row
 // group 2*nt + n/128.  Any scale that is not a positive normal power of two sets *bad.
 __global__ void build_sfb_kernel(const float *__restrict__ s, uint8_t *__restrict__ dst, int E, int N, int K,
@@ -861,8 +885,9 @@ __global__ void build_sfb_kernel(const float *__restrict__ s, uint8_t *__restric
         const uint32_t ex = (b >> 23) & 0xFFu;
         if ((b & 0x807FFFFFu) != 0u || ex == 0u || ex == 0xFFu)
             atomicOr(bad, 1u);
-        *reinterpret_cast<uint32_t *>(dst + tk * SFB_BYTES + 512 * (n / 128) + 16 * (n % 32) + 4 * ((n % 128) / 32)) =
-            ex * 0x01010101u;
+        const long long g = et * ((KB + SF_GROUP - 1) / SF_GROUP) + kb / SF_GROUP;
+        dst[g * SFB_BYTES + 512 * (n / 128) + 16 * (n % 32) + 4 * ((n % 128) / 32) + kb % SF_GROUP] =
+            static_cast<uint8_t>(ex);
     }
 }
 

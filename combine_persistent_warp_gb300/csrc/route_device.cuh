@@ -273,14 +273,15 @@ __device__ __forceinline__ void gather_row(const Dims &d, const Workspace &ws, c
         const float sf = __ldg(c.x_sf + static_cast<long long>(t) * KBH + kb);
         ws.pool_sf[static_cast<long long>(kb) * ws.P + row] = sf;
         if (c.block_scaled) {
-            // UE8M0 word of this row in its M-block's 512-byte scale block of K block kb
-            // (row r at byte 16*(r%32) + 4*(r/32)); the scale must be a power of two
+            // UE8M0 byte of this row and K block kb in its M-block's 512-byte scale block of
+            // the group of four K blocks kb / 4 (row r's word at byte 16*(r%32) + 4*(r/32),
+            // byte kb % 4); the scale must be a power of two
             const uint32_t b = __float_as_uint(sf), ex = (b >> 23) & 0xFFu;
             if ((b & 0x807FFFFFu) != 0u || ex == 0u || ex == 0xFFu)
                 record_error(ws.hdr, DEV_BAD_SCALE);
             const int rr = static_cast<int>(row % BM);
-            *reinterpret_cast<uint32_t *>(ws.pool_sfe + ((row / BM) * KBH + kb) * 512 + 16 * (rr % 32) +
-                                          4 * (rr / 32)) = ex * 0x01010101u;
+            ws.pool_sfe[((row / BM) * ((KBH + 3) / 4) + kb / 4) * 512 + 16 * (rr % 32) + 4 * (rr / 32) + kb % 4] =
+                static_cast<uint8_t>(ex);
         }
     }
     if (lane == 0) {

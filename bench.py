@@ -45,10 +45,10 @@ PROFILE_EVERY = 8            # timed steps per step carrying the per-kernel stag
 # DRAM bytes per launch from one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum),
 # valid only while the kernel sources hash to `src_sha`; see profiles/.
 NCU_TRAFFIC = {
-    ("decode", "expert_ffn"): {"bytes": 1425220352 + 14429440, "src_sha": "59a1f06def27fd31"},
-    ("prefill", "expert_ffn"): {"bytes": 1919576320 + 535503360, "src_sha": "59a1f06def27fd31"},
-    ("decode-pow2", "expert_ffn"): {"bytes": 1465405952 + 3284480, "src_sha": "47ce09d331634a6c"},
-    ("prefill-pow2", "expert_ffn"): {"bytes": 2202144256 + 517698304, "src_sha": "47ce09d331634a6c"},
+    ("decode", "expert_ffn"): {"bytes": 1425283072 + 14444800, "src_sha": "59a1f06def27fd31"},
+    ("prefill", "expert_ffn"): {"bytes": 1877737216 + 533531904, "src_sha": "59a1f06def27fd31"},
+    ("decode-pow2", "expert_ffn"): {"bytes": 1431478016 + 3511296, "src_sha": "31f7f51a2a16ad06"},
+    ("prefill-pow2", "expert_ffn"): {"bytes": 2117926912 + 514405632, "src_sha": "31f7f51a2a16ad06"},
 }
 # sources each stage's kernel is compiled from (a recorded traffic figure is used only while
 # these hash to its `src_sha`)

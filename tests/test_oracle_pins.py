@@ -335,3 +335,29 @@ def test_skipped_slots_and_empty_tokens(oracle_mod):
     assert not bad and not np.any(f32[0])
     y, _, _ = oracle_mod.expert_ffn(x[5], xs[5], w1[idx[5, 0]], s1[idx[5, 0]], w2[idx[5, 0]], s2[idx[5, 0]])
     assert np.array_equal(f32[1], (float(w[5, 0]) * y).astype(np.float32))
+
+
+def test_forward_tiny_matches_independent_numpy_restatement(oracle_mod):
+    """The whole tiny batch (64 tokens, 8 experts, top-2, 2 sources) against a second,
+    independent float64 restatement of the layer: torch's FP8 and bf16 casts, numpy matmuls
+    per (token, slot) expert FFN, and the top-k sum in fp32 in ascending slot order."""
+    from combine_persistent_warp_gb300.workloads import make_inputs
+    inp = make_inputs("tiny")
+    h = oracle_mod.HostInputs.from_inputs(inp)
+    bits, out32, bad = oracle_mod.forward_tokens(h, np.arange(h.T))
+    assert not bad
+    ref = np.zeros((h.T, h.H), np.float32)
+    for t in range(h.T):
+        acc = np.zeros(h.H, np.float32)
+        for kk in range(h.k):
+            e = int(h.idx[t, kk])
+            if e < 0:
+                continue
+            y = _dense_ffn_library(inp.x[t], inp.x_sf[t], inp.w_gate_up[e], inp.sf_gate_up[e],
+                                   inp.w_down[e], inp.sf_down[e])[0].astype(np.float32)
+            acc = (acc + np.float32(h.w[t, kk]) * y).astype(np.float32)
+        ref[t] = acc
+    ref_bits = torch.from_numpy(ref).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    rel = np.linalg.norm(out32 - ref, axis=1) / np.maximum(np.linalg.norm(ref, axis=1), 1e-30)
+    assert rel.max() <= 1e-3            # room for a rare one-step FP8 requant flip
+    assert (bits == ref_bits).mean() >= 0.99

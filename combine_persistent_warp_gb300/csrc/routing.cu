@@ -58,8 +58,9 @@ __global__ void __launch_bounds__(DISPATCH_THREADS, 1)
     route::segments(d, ws, recv_s, cum, blk);
 
     // ---- gather, one warp per received row (global order across experts) -------------------
+    // (warps numbered CTA-minor, so a small batch's rows spread over every SM)
     const int lane = threadIdx.x & 31;
-    const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, nw = (gridDim.x * blockDim.x) >> 5;
+    const int gw = (threadIdx.x >> 5) * gridDim.x + blockIdx.x, nw = (gridDim.x * blockDim.x) >> 5;
     const int total_rows = cum[E];
     for (int j = gw; j < total_rows; j += nw) {
         const int e = route::last_le(cum, E + 1, j);

@@ -215,3 +215,64 @@ def test_scale_mode_values():
     g = out.float().cpu().numpy()
     rel = np.linalg.norm(g - ref, axis=1) / np.maximum(np.linalg.norm(ref, axis=1), 1e-30)
     assert np.all(rel <= TOL), rel.max()
+
+
+# ------------------------------------------------------------------ edge cases ----------
+def _pow2_layer(T_max, E=8, H=256, I=256, k=2, R=2, seed=51):
+    torch.cuda.set_device(0)
+    wl = Workload("pow2-edge", T=T_max, H=H, I=I, E=E, topk=k, R=R, seed=seed, scales="pow2")
+    inp = make_inputs(wl, device="cuda")
+    moe = FusedMoE(E, H, I, k, R).reserve(T_max)
+    moe.load_weights(inp.w_gate_up, inp.sf_gate_up, inp.w_down, inp.sf_down)
+    return moe, inp
+
+
+def _compare_pow2(moe, inp, idx, w, T):
+    x, xs = inp.x[:T].contiguous(), inp.x_sf[:T].contiguous()
+    out = moe.forward(x, xs, idx, w)
+    torch.cuda.synchronize()
+    assert moe.get_error() == 0
+    h = oracle.HostInputs(x, xs, idx, w, inp.w_gate_up, inp.sf_gate_up, inp.w_down, inp.sf_down)
+    oracle.set_scale_rule("pow2")
+    try:
+        _, ref, _ = oracle.forward_tokens(h, np.arange(T))
+    finally:
+        oracle.set_scale_rule("fp32")
+    g = out.float().cpu().numpy()
+    den = np.linalg.norm(ref, axis=1)
+    rel = np.where(den > 0, np.linalg.norm(g - ref, axis=1) / np.maximum(den, 1e-30), np.linalg.norm(g - ref, axis=1))
+    assert np.all(rel <= TOL), rel.max()
+    return out
+
+
+def test_block_scaled_ragged_batch_and_single_hot_expert():
+    """158 tokens (79 per source, no tile multiple), expert 3 receiving every token in slot 0
+    (two M-blocks, the second partly filled), K = 256 and 256: one scale group per tile."""
+    moe, inp = _pow2_layer(T_max=160)
+    T = 158
+    idx = inp.topk_idx[:T].clone()
+    idx[:, 0] = 3
+    idx[:, 1] = torch.where(idx[:, 1] == 3, torch.full_like(idx[:, 1], -1), idx[:, 1])
+    _compare_pow2(moe, inp, idx.contiguous(), inp.topk_w[:T].contiguous(), T)
+    dbg = moe.debug_routing(T)
+    assert dbg["counts"][3] == T
+
+
+def test_block_scaled_scale_groups_span_tiles():
+    """H = 1280 (10 K blocks: scale groups of 4, 4 and 2) and I = 640 (5 K blocks: 4 and 1),
+    so K-block groups end mid-way and tiles start on every stage of the ring."""
+    moe, inp = _pow2_layer(T_max=256, E=4, H=1280, I=640, k=2, R=2, seed=53)
+    _compare_pow2(moe, inp, inp.topk_idx, inp.topk_w, 256)
+
+
+def test_block_scaled_empty_and_all_skipped():
+    moe, inp = _pow2_layer(T_max=64)
+    e = torch.empty(0, 256, dtype=torch.uint8, device="cuda")
+    out = moe.forward(e, torch.empty(0, 2, device="cuda"), torch.empty(0, 2, dtype=torch.int64, device="cuda"),
+                      torch.empty(0, 2, device="cuda"))
+    assert out.shape == (0, 256) and moe.get_error() == 0
+    idx = torch.full((64, 2), -1, dtype=torch.int64, device="cuda")
+    out = moe.forward(inp.x, inp.x_sf, idx, inp.topk_w)
+    torch.cuda.synchronize()
+    assert moe.get_error() == 0
+    assert not torch.any(out.float() != 0)

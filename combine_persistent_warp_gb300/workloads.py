@@ -1,7 +1,8 @@
 """Seeded synthetic workloads for the fused MoE layer.
 
 This module only *synthesises inputs*: routing decisions, FP8 activations with
-1x128 fp32 scales, and FP8 expert weights with 128x128 fp32 block scales.  It
+1x128 fp32 scales, and FP8 expert weights with 128x128 fp32 block scales (or
+MXFP4 expert weights: E2M1 codes with one E8M0 scale per 32 elements).  It
 holds none of the layer's own arithmetic (no GEMM, no SwiGLU, no combine).  The
 FP8 encoding of the synthetic tensors is done by PyTorch's ``float8_e4m3fn``
 cast (a library routine); both the CUDA path and the CPU oracle receive the
@@ -38,6 +39,8 @@ class Workload:
     seed: int = 0
     scales: str = "fp32"       # "fp32": sf = max(amax,1e-4)/448; "pow2": the smallest power
                                # of two >= that (UE8M0-representable, block-scaled UMMA path)
+    weights: str = "fp8"       # "fp8": e4m3 with 128x128 scales; "mxfp4": E2M1 with 1x32
+                               # E8M0 scales (needs scales == "pow2")
 
     @property
     def T_src(self) -> int:
@@ -60,8 +63,17 @@ POW2_WORKLOADS = {f"{k}-pow2": Workload(**{**asdict(v), "name": f"{k}-pow2", "sc
                   for k, v in WORKLOADS.items()}
 
 
+# the same batches with MXFP4 expert weights (and power-of-two activation scales)
+MXFP4_WORKLOADS = {f"{k}-mxfp4": Workload(**{**asdict(v), "name": f"{k}-mxfp4", "scales": "pow2",
+                                            "weights": "mxfp4"})
+                   for k, v in WORKLOADS.items()}
+
+
 def workload(name: str) -> Workload:
-    return WORKLOADS[name] if name in WORKLOADS else POW2_WORKLOADS[name]
+    for table in (WORKLOADS, POW2_WORKLOADS, MXFP4_WORKLOADS):
+        if name in table:
+            return table[name]
+    raise KeyError(name)
 
 
 def _gen(seed: int, device) -> torch.Generator:
@@ -157,6 +169,54 @@ def make_weights(E: int, H: int, I: int, *, seed: int, device="cpu", std: float 
     return w1, s1, w2, s2
 
 
+# ------------------------------------------------------ MXFP4 synthesis -----
+E2M1_MAX_EXP = 2                      # exponent of the largest E2M1 magnitude, 6 = 1.5 * 2^2
+E2M1_MAGS = (0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0)   # codes 0..7 (bit 3 = sign)
+
+
+def quantize_mxfp4(w: torch.Tensor):
+    """fp32 [N, K] -> (packed E2M1 bytes uint8 [N, K/2], E8M0 scale bytes uint8 [N, K/32]).
+
+    OCP Microscaling conversion: each run of 32 elements of a row shares the scale
+    X = 2^(floor(log2(amax)) - 2) (2 = the largest E2M1 exponent; an all-zero run takes
+    X = 2^-127), stored as the byte log2(X) + 127; each element becomes the nearest E2M1
+    value of v / X (ties to the even code), saturated to +-6.  Element 2j sits in the low
+    nibble of byte j, element 2j + 1 in the high nibble."""
+    N, K = w.shape
+    g = w.float().view(N, K // 32, 32)
+    amax = g.abs().amax(dim=2)
+    _, e = torch.frexp(amax)                       # amax = m * 2^e, m in [0.5, 1)
+    sexp = torch.where(amax > 0, e - 1 - E2M1_MAX_EXP, torch.full_like(e, -127)).clamp(-127, 127)
+    a = (g / torch.ldexp(torch.ones_like(amax), sexp)[:, :, None]).abs()
+    mags = torch.tensor(E2M1_MAGS, device=w.device)
+    mids = (mags[1:] + mags[:-1]) / 2
+    lo = torch.bucketize(a, mids, right=False)     # ties -> the smaller magnitude
+    hi = torch.bucketize(a, mids, right=True)      # ties -> the larger magnitude
+    code = torch.where(lo % 2 == 0, lo, hi).to(torch.uint8)
+    code = code | ((g < 0) & (code > 0)).to(torch.uint8) << 3
+    code = code.view(N, K)
+    packed = code[:, 0::2] | (code[:, 1::2] << 4)
+    return packed.contiguous(), (sexp + 127).to(torch.uint8).contiguous()
+
+
+def make_weights_mxfp4(E: int, H: int, I: int, *, seed: int, device="cpu", std: float = 0.02):
+    """Expert weights W ~ N(0, std) (the same draws as ``make_weights``) as MXFP4.
+
+    Returns w_gate_up uint8 [E, 2I, H/2] (rows 0..I-1 gate, I..2I-1 up), sf_gate_up uint8
+    [E, 2I, H/32], w_down uint8 [E, H, I/2], sf_down uint8 [E, H, I/32]."""
+    g = _gen(seed * 104729 + 3, device)
+    w1 = torch.empty(E, 2 * I, H // 2, dtype=torch.uint8, device=device)
+    s1 = torch.empty(E, 2 * I, H // 32, dtype=torch.uint8, device=device)
+    w2 = torch.empty(E, H, I // 2, dtype=torch.uint8, device=device)
+    s2 = torch.empty(E, H, I // 32, dtype=torch.uint8, device=device)
+    for e in range(E):
+        a = torch.randn(2 * I, H, generator=g, device=device) * std
+        w1[e], s1[e] = quantize_mxfp4(a)
+        b = torch.randn(H, I, generator=g, device=device) * std
+        w2[e], s2[e] = quantize_mxfp4(b)
+    return w1, s1, w2, s2
+
+
 def make_activations(T: int, H: int, *, seed: int, device="cpu", scales: str = "fp32"):
     """x ~ N(0,1), rounded to bf16, then FP8 e4m3 with 1x128 fp32 scales."""
     g = _gen(seed * 15485863 + 11, device)
@@ -196,7 +256,10 @@ def make_inputs(wl: Workload | str, device="cpu", *, T: int | None = None) -> In
     idx, w = make_routing(wl.T, wl.E, wl.topk, seed=wl.seed, routing=wl.routing,
                           zipf_s=wl.zipf_s, skip_frac=wl.skip_frac)
     x, x_sf = make_activations(wl.T, wl.H, seed=wl.seed, device=device, scales=wl.scales)
-    w1, s1, w2, s2 = make_weights(wl.E, wl.H, wl.I, seed=wl.seed, device=device, scales=wl.scales)
+    if wl.weights == "mxfp4":
+        w1, s1, w2, s2 = make_weights_mxfp4(wl.E, wl.H, wl.I, seed=wl.seed, device=device)
+    else:
+        w1, s1, w2, s2 = make_weights(wl.E, wl.H, wl.I, seed=wl.seed, device=device, scales=wl.scales)
     return Inputs(wl, x, x_sf, idx.to(device), w.to(device), w1, s1, w2, s2)
 
 

@@ -21,6 +21,10 @@ Pins (what ties each function to something other than itself) are in
   * power-of-two scale rule -- closed forms (exact powers, neighbours), the defining
                          inequalities sf/2 < q <= sf, and the requantised stage against
                          numpy with the rule applied by exponent arithmetic
+  * MXFP4 weights     -- all 16 E2M1 codes against the OCP MX element table, E8M0 bytes
+                         against 2^(b-127), nibble order and per-32 scale index by single-
+                         element weights, and the whole layer against its FP8 twin (the
+                         same weight values written as e4m3 codes with 128x128 scales)
 """
 from __future__ import annotations
 
@@ -64,6 +68,13 @@ def lib():
         L.orc_pow2_ceil.restype = ctypes.c_float
         L.orc_forward_tokens.restype = ctypes.c_int
         L.orc_forward_tokens.argtypes = [ctypes.c_int] * 5 + [P] * 8 + [ctypes.c_int, P, P, P]
+        L.orc_forward_tokens_fmt.restype = ctypes.c_int
+        L.orc_forward_tokens_fmt.argtypes = [ctypes.c_int] * 6 + [P] * 8 + [ctypes.c_int, P, P, P]
+        L.orc_expert_ffn_fmt.argtypes = [ctypes.c_int] * 3 + [P] * 9
+        L.orc_e2m1_decode.restype = ctypes.c_double
+        L.orc_e2m1_decode.argtypes = [ctypes.c_uint8]
+        L.orc_e8m0_decode.restype = ctypes.c_double
+        L.orc_e8m0_decode.argtypes = [ctypes.c_uint8]
         L.orc_num_threads.restype = ctypes.c_int
         L.orc_init()
         _lib = L
@@ -186,36 +197,61 @@ def pow2_ceil(v: float) -> float:
     return float(lib().orc_pow2_ceil(float(v)))
 
 
-def expert_ffn(x_row, xsf_row, w1_e, s1_e, w2_e, s2_e):
-    """One expert on one token: (y [H] float64, hq [I] uint8, hsf [I/128] float32)."""
+WEIGHT_FORMATS = {"fp8": 0, "mxfp4": 1}
+
+
+def e2m1_decode(codes) -> np.ndarray:
+    """Values of FP4 E2M1 codes (low 4 bits of each byte)."""
+    c = _np(codes, np.uint8)
+    return np.array([lib().orc_e2m1_decode(int(v) & 0xF) for v in c.ravel()], np.float64).reshape(c.shape)
+
+
+def e8m0_decode(codes) -> np.ndarray:
+    """Values of E8M0 scale bytes."""
+    c = _np(codes, np.uint8)
+    return np.array([lib().orc_e8m0_decode(int(v)) for v in c.ravel()], np.float64).reshape(c.shape)
+
+
+def expert_ffn(x_row, xsf_row, w1_e, s1_e, w2_e, s2_e, weights: str = "fp8"):
+    """One expert on one token: (y [H] float64, hq [I] uint8, hsf [I/128] float32).
+
+    weights "fp8": w1 [2I][H] e4m3, s1 [2I/128][H/128] fp32, w2 [H][I], s2 [H/128][I/128];
+    "mxfp4": w1 [2I][H/2] packed E2M1, s1 [2I][H/32] E8M0, w2 [H][I/2], s2 [H][I/32]."""
+    fmt = WEIGHT_FORMATS[weights]
+    sdt = np.uint8 if fmt else np.float32
     x = _np(x_row, np.uint8)
     xs = _np(xsf_row, np.float32)
     w1 = _np(w1_e, np.uint8)
-    s1 = _np(s1_e, np.float32)
+    s1 = _np(s1_e, sdt)
     w2 = _np(w2_e, np.uint8)
-    s2 = _np(s2_e, np.float32)
+    s2 = _np(s2_e, sdt)
     H = x.size
-    I = w2.shape[-1]
+    I = w2.shape[-1] * (2 if fmt else 1)
     y = np.empty(H, np.float64)
     hq = np.empty(I, np.uint8)
     hsf = np.empty(I // 128, np.float32)
-    lib().orc_expert_ffn(H, I, _p(x), _p(xs), _p(w1), _p(s1), _p(w2), _p(s2),
-                         _p(y), _p(hq), _p(hsf))
+    lib().orc_expert_ffn_fmt(fmt, H, I, _p(x), _p(xs), _p(w1), _p(s1), _p(w2), _p(s2),
+                             _p(y), _p(hq), _p(hsf))
     return y, hq, hsf
 
 
 class HostInputs:
-    """Host copies of one workload's inputs, in the layouts the oracle reads."""
+    """Host copies of one workload's inputs, in the layouts the oracle reads (weight
+    layouts of ``weights`` as in ``expert_ffn``)."""
 
-    def __init__(self, x, x_sf, topk_idx, topk_w, w_gate_up, sf_gate_up, w_down, sf_down):
+    def __init__(self, x, x_sf, topk_idx, topk_w, w_gate_up, sf_gate_up, w_down, sf_down,
+                 weights: str = "fp8"):
+        self.weights = weights
+        fmt = WEIGHT_FORMATS[weights]
+        sdt = np.uint8 if fmt else np.float32
         self.x = _np(x, np.uint8)
         self.x_sf = _np(x_sf, np.float32)
         self.idx = _np(topk_idx, np.int64)
         self.w = _np(topk_w, np.float32)
         self.w1 = _np(w_gate_up, np.uint8)
-        self.s1 = _np(sf_gate_up, np.float32)
+        self.s1 = _np(sf_gate_up, sdt)
         self.w2 = _np(w_down, np.uint8)
-        self.s2 = _np(sf_down, np.float32)
+        self.s2 = _np(sf_down, sdt)
         self.T, self.H = self.x.shape if self.x.ndim == 2 else (0, self.w2.shape[1])
         self.E, twoI, _ = self.w1.shape
         self.I = twoI // 2
@@ -224,7 +260,7 @@ class HostInputs:
     @classmethod
     def from_inputs(cls, inp):
         return cls(inp.x, inp.x_sf, inp.topk_idx, inp.topk_w, inp.w_gate_up, inp.sf_gate_up,
-                   inp.w_down, inp.sf_down)
+                   inp.w_down, inp.sf_down, weights=getattr(inp.wl, "weights", "fp8"))
 
 
 def forward_tokens(h: HostInputs, tokens):
@@ -233,9 +269,10 @@ def forward_tokens(h: HostInputs, tokens):
     n = tok.size
     out = np.empty((n, h.H), np.uint16)
     out32 = np.empty((n, h.H), np.float32)
-    bad = lib().orc_forward_tokens(h.T, h.H, h.I, h.E, h.k, _p(h.x), _p(h.x_sf), _p(h.idx),
-                                   _p(h.w), _p(h.w1), _p(h.s1), _p(h.w2), _p(h.s2),
-                                   n, _p(tok), _p(out), _p(out32))
+    bad = lib().orc_forward_tokens_fmt(WEIGHT_FORMATS[h.weights], h.T, h.H, h.I, h.E, h.k,
+                                       _p(h.x), _p(h.x_sf), _p(h.idx), _p(h.w), _p(h.w1),
+                                       _p(h.s1), _p(h.w2), _p(h.s2), n, _p(tok), _p(out),
+                                       _p(out32))
     return out, out32, bool(bad)
 
 

@@ -54,13 +54,40 @@ double orc_e4m3_decode(uint8_t code)
     return sign ? -mag : mag;
 }
 
+/* ------------------------------------------------------------------ MXFP4 -------- */
+
+/* Value of one FP4 E2M1 code (the element format of OCP Microscaling MXFP4): bit 3 sign,
+ * bits 2..1 exponent with bias 1, bit 0 mantissa; exponent 0 is subnormal (0.m * 2^0),
+ * and there is no infinity or NaN. */
+double orc_e2m1_decode(uint8_t code)
+{
+    int sign = (code >> 3) & 1;
+    int expo = (code >> 1) & 0x3;
+    int mant = code & 0x1;
+    double mag;
+    if (expo == 0)
+        mag = (double)mant / 2.0;                         /* subnormal: 0.m * 2^(1-bias) */
+    else
+        mag = ldexp(1.0 + (double)mant / 2.0, expo - 1);  /* normal: 1.m * 2^(e-bias) */
+    return sign ? -mag : mag;
+}
+
+/* Value of one E8M0 (UE8M0) scale byte: 2^(b - 127); 0xFF is NaN (OCP MX scale format). */
+double orc_e8m0_decode(uint8_t b)
+{
+    return b == 0xFF ? NAN : ldexp(1.0, (int)b - 127);
+}
+
 static double g_dec[256];
+static double g_dec4[16];
 static int g_dec_ready = 0;
 
 void orc_init(void)
 {
     for (int c = 0; c < 256; ++c)
         g_dec[c] = orc_e4m3_decode((uint8_t)c);
+    for (int c = 0; c < 16; ++c)
+        g_dec4[c] = orc_e2m1_decode((uint8_t)c);
     g_dec_ready = 1;
 }
 
@@ -224,9 +251,30 @@ int orc_route_counts(int T, int k, int E, int R, const int64_t *idx,
 
 /* ------------------------------------------------------------------ expert FFN ---- */
 
+/* Weight formats of the expert FFN.
+ *   ORC_W_FP8:   [N][K] e4m3 codes, fp32 scales [N/128][K/128], one per 128x128 block;
+ *   ORC_W_MXFP4: [N][K/2] bytes of packed E2M1 codes, element 2j in the low nibble of byte j
+ *                and element 2j+1 in the high nibble, with E8M0 scales [N][K/32], one per 32
+ *                consecutive elements of a row (the OCP Microscaling MXFP4 block: 32 elements
+ *                sharing one power-of-two scale).  The pages name FP8 x FP4 weights for their
+ *                SM100 kernel ("DeepGEMM Mega MoE 对称内存（Symmetric Memory）深度分析" §11
+ *                file table) without fixing the FP4 format; MXFP4 is the reading taken. */
+enum { ORC_W_FP8 = 0, ORC_W_MXFP4 = 1 };
+
+/* Element (n, c) of a row-major weight of K columns: code value times its block scale. */
+static inline double wval(int wfmt, const uint8_t *w, const void *s, int64_t n, int64_t c, int64_t K)
+{
+    if (wfmt == ORC_W_MXFP4) {
+        const uint8_t byte = w[n * (K / 2) + c / 2];
+        const uint8_t code = (c & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 0xF);
+        return g_dec4[code] * orc_e8m0_decode(((const uint8_t *)s)[n * (K / 32) + c / 32]);
+    }
+    return dec(w[n * K + c]) * (double)((const float *)s)[(n / 128) * (K / 128) + c / 128];
+}
+
 /* One expert on one token ([WT1] §六: Linear1 gate_up, SwiGLU, Linear2 down).
- *   x [H] e4m3 with xsf [H/128];  w1 [2I][H] e4m3 with s1 [2I/128][H/128];
- *   w2 [H][I] e4m3 with s2 [H/128][I/128].
+ *   x [H] e4m3 with xsf [H/128];  w1 [2I][H] with s1;  w2 [H][I] with s2, in weight format
+ *   wfmt (above).
  * Every operand is dequantised element by element (code value times its block scale),
  * products are summed in double.  Outputs: y [H] (double); optional hq [I] codes and
  * hsf [I/128] scales of the re-quantised SwiGLU output. */
@@ -244,12 +292,12 @@ float orc_pow2_ceil(float v)
     return f == 0.5f ? v : ldexpf(1.0f, e);
 }
 
-void orc_expert_ffn(int H, int I, const uint8_t *x, const float *xsf,
-                    const uint8_t *w1, const float *s1,
-                    const uint8_t *w2, const float *s2,
-                    double *y, uint8_t *hq, float *hsf)
+void orc_expert_ffn_fmt(int wfmt, int H, int I, const uint8_t *x, const float *xsf,
+                        const uint8_t *w1, const void *s1,
+                        const uint8_t *w2, const void *s2,
+                        double *y, uint8_t *hq, float *hsf)
 {
-    const int KB1 = H / 128, KB2 = I / 128;
+    const int KB2 = I / 128;
     double *dx = (double *)malloc(sizeof(double) * (size_t)H);
     float *h = (float *)malloc(sizeof(float) * (size_t)I);
     double *hd = (double *)malloc(sizeof(double) * (size_t)I);
@@ -261,13 +309,9 @@ void orc_expert_ffn(int H, int I, const uint8_t *x, const float *xsf,
 
     for (int n = 0; n < I; ++n) {
         double g = 0.0, u = 0.0;
-        const uint8_t *wg = w1 + (int64_t)n * H;
-        const uint8_t *wu = w1 + (int64_t)(I + n) * H;
-        const float *sg = s1 + (int64_t)(n / 128) * KB1;
-        const float *su = s1 + (int64_t)((I + n) / 128) * KB1;
         for (int c = 0; c < H; ++c) {
-            g += dx[c] * (dec(wg[c]) * (double)sg[c / 128]);
-            u += dx[c] * (dec(wu[c]) * (double)su[c / 128]);
+            g += dx[c] * wval(wfmt, w1, s1, n, c, H);
+            u += dx[c] * wval(wfmt, w1, s1, I + n, c, H);
         }
         double silu = g / (1.0 + exp(-g));
         h[n] = (float)(silu * u);
@@ -292,15 +336,22 @@ void orc_expert_ffn(int H, int I, const uint8_t *x, const float *xsf,
 
     for (int c = 0; c < H; ++c) {
         double acc = 0.0;
-        const uint8_t *wd = w2 + (int64_t)c * I;
-        const float *sd = s2 + (int64_t)(c / 128) * KB2;
         for (int n = 0; n < I; ++n)
-            acc += hd[n] * (dec(wd[n]) * (double)sd[n / 128]);
+            acc += hd[n] * wval(wfmt, w2, s2, c, n, I);
         y[c] = acc;
     }
     free(dx);
     free(h);
     free(hd);
+}
+
+/* The FP8-weight form of orc_expert_ffn_fmt. */
+void orc_expert_ffn(int H, int I, const uint8_t *x, const float *xsf,
+                    const uint8_t *w1, const float *s1,
+                    const uint8_t *w2, const float *s2,
+                    double *y, uint8_t *hq, float *hsf)
+{
+    orc_expert_ffn_fmt(ORC_W_FP8, H, I, x, xsf, w1, s1, w2, s2, y, hq, hsf);
 }
 
 /* ------------------------------------------------------------------ layer ---------- */
@@ -310,18 +361,25 @@ void orc_expert_ffn(int H, int I, const uint8_t *x, const float *xsf,
  * ([DC] §1: Output(T) = sum_k w_k * Expert_k(T)).  out_bf16 [ntok][H] receives the bf16
  * bits, out_f32 (optional) the fp32 value before the bf16 rounding.  Returns 1 if a
  * token names an expert outside [0, E) other than -1 (that slot is skipped). */
-int orc_forward_tokens(int T, int H, int I, int E, int k,
-                       const uint8_t *x, const float *xsf,
-                       const int64_t *idx, const float *w,
-                       const uint8_t *w1, const float *s1,
-                       const uint8_t *w2, const float *s2,
-                       int ntok, const int32_t *tokens,
-                       uint16_t *out_bf16, float *out_f32)
+int orc_forward_tokens_fmt(int wfmt, int T, int H, int I, int E, int k,
+                           const uint8_t *x, const float *xsf,
+                           const int64_t *idx, const float *w,
+                           const uint8_t *w1, const void *s1,
+                           const uint8_t *w2, const void *s2,
+                           int ntok, const int32_t *tokens,
+                           uint16_t *out_bf16, float *out_f32)
 {
     int bad = 0;
     (void)T;
     if (!g_dec_ready)
         orc_init();
+    /* per-expert strides of the weights (bytes) and scales (elements of their type) */
+    const int mx = wfmt == ORC_W_MXFP4;
+    const int64_t w1e = mx ? (int64_t)2 * I * (H / 2) : (int64_t)2 * I * H;
+    const int64_t w2e = mx ? (int64_t)H * (I / 2) : (int64_t)H * I;
+    const int64_t s1e = mx ? (int64_t)2 * I * (H / 32) : (int64_t)(2 * I / 128) * (H / 128);
+    const int64_t s2e = mx ? (int64_t)H * (I / 32) : (int64_t)(H / 128) * (I / 128);
+    const size_t ssz = mx ? sizeof(uint8_t) : sizeof(float);
 #pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
     for (int i = 0; i < ntok; ++i) {
         const int t = tokens[i];
@@ -335,10 +393,9 @@ int orc_forward_tokens(int T, int H, int I, int E, int k,
                 bad |= 1;
                 continue;
             }
-            orc_expert_ffn(H, I, x + (int64_t)t * H, xsf + (int64_t)t * (H / 128),
-                           w1 + (int64_t)e * 2 * I * H, s1 + (int64_t)e * (2 * I / 128) * (H / 128),
-                           w2 + (int64_t)e * H * I, s2 + (int64_t)e * (H / 128) * (I / 128),
-                           y, NULL, NULL);
+            orc_expert_ffn_fmt(wfmt, H, I, x + (int64_t)t * H, xsf + (int64_t)t * (H / 128),
+                               w1 + e * w1e, (const char *)s1 + e * s1e * ssz,
+                               w2 + e * w2e, (const char *)s2 + e * s2e * ssz, y, NULL, NULL);
             const double wk = (double)w[(int64_t)t * k + kk];
             for (int c = 0; c < H; ++c)
                 acc[c] += wk * y[c];
@@ -353,6 +410,19 @@ int orc_forward_tokens(int T, int H, int I, int E, int k,
         free(y);
     }
     return bad;
+}
+
+/* The FP8-weight form of orc_forward_tokens_fmt. */
+int orc_forward_tokens(int T, int H, int I, int E, int k,
+                       const uint8_t *x, const float *xsf,
+                       const int64_t *idx, const float *w,
+                       const uint8_t *w1, const float *s1,
+                       const uint8_t *w2, const float *s2,
+                       int ntok, const int32_t *tokens,
+                       uint16_t *out_bf16, float *out_f32)
+{
+    return orc_forward_tokens_fmt(ORC_W_FP8, T, H, I, E, k, x, xsf, idx, w, w1, s1, w2, s2, ntok, tokens,
+                                  out_bf16, out_f32);
 }
 
 int orc_num_threads(void)

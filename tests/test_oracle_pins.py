@@ -361,3 +361,112 @@ def test_forward_tiny_matches_independent_numpy_restatement(oracle_mod):
     rel = np.linalg.norm(out32 - ref, axis=1) / np.maximum(np.linalg.norm(ref, axis=1), 1e-30)
     assert rel.max() <= 1e-3            # room for a rare one-step FP8 requant flip
     assert (bits == ref_bits).mean() >= 0.99
+
+
+# ------------------------------------------------------------------ MXFP4 weights ----
+# OCP Microscaling Formats (MX) v1.0, FP4 E2M1 element: the eight magnitudes of codes 0..7
+# (bit 3 is the sign), and E8M0 scale bytes 2^(b-127) with 0xFF = NaN.
+OCP_E2M1 = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+
+
+def test_e2m1_decode_all_codes(oracle_mod):
+    got = oracle_mod.e2m1_decode(np.arange(16, dtype=np.uint8))
+    want = np.array(OCP_E2M1 + [-v for v in OCP_E2M1])
+    assert np.array_equal(got, want)
+    assert np.signbit(got[8]) and not np.signbit(got[0])
+
+
+def test_e8m0_decode(oracle_mod):
+    b = np.array([0, 1, 100, 126, 127, 128, 200, 254], np.uint8)
+    assert np.array_equal(oracle_mod.e8m0_decode(b), np.ldexp(1.0, b.astype(int) - 127))
+    assert np.isnan(oracle_mod.e8m0_decode(np.array([255], np.uint8))[0])
+
+
+def _fp8_twin_of_mxfp4(packed, sf):
+    """An FP8 weight with the same element values as an MXFP4 one ([N][K/2] packed, [N][K/32]
+    E8M0): per 128x128 block the scale 2^m with m the block's smallest scale exponent, and
+    e4m3 codes (torch's cast) of value / 2^m, exact while each block's exponents span <= 6."""
+    p = packed.numpy().astype(np.int64)
+    N = p.shape[0]
+    codes = np.empty((N, 2 * p.shape[1]), np.int64)
+    codes[:, 0::2] = p & 0xF
+    codes[:, 1::2] = p >> 4
+    mags = np.array(OCP_E2M1)
+    val = np.where(codes >= 8, -mags[codes & 7], mags[codes & 7])
+    ex = sf.numpy().astype(np.int64) - 127                       # [N][K/32]
+    val = val * np.ldexp(1.0, np.repeat(ex, 32, axis=1))
+    K = val.shape[1]
+    m = ex.reshape(N // 128, 128, K // 128, 4).min(axis=(1, 3))   # [N/128][K/128]
+    assert (ex.reshape(N // 128, 128, K // 128, 4).max(axis=(1, 3)) - m).max() <= 6
+    scale = np.ldexp(1.0, m).astype(np.float32)
+    q = val / np.kron(scale.astype(np.float64), np.ones((128, 128)))
+    c8 = torch.from_numpy(q).to(torch.float8_e4m3fn)
+    assert np.array_equal(c8.to(torch.float64).numpy(), q)        # exact twin
+    return c8.view(torch.uint8), torch.from_numpy(scale)
+
+
+def _mxfp4_case(E=3, H=256, I=128, seed=5, span=4):
+    """Random MXFP4 expert weights: uniform codes, per-32 scale bytes 120 + [0, span]."""
+    g = torch.Generator().manual_seed(seed)
+    def one(N, K):
+        packed = torch.randint(0, 256, (E, N, K // 2), generator=g, dtype=torch.int64).to(torch.uint8)
+        sf = (120 + torch.randint(0, span + 1, (E, N, K // 32), generator=g)).to(torch.uint8)
+        return packed, sf
+    return one(2 * I, H) + one(H, I)
+
+
+def test_mxfp4_layer_equals_its_fp8_twin(oracle_mod):
+    """Every output of the layer with MXFP4 weights (random codes, per-32 scales varying
+    within each 128x128 block) is bit-identical to the layer with the FP8 twin weights:
+    the oracle's nibble order, scale index and per-expert strides all enter."""
+    from combine_persistent_warp_gb300 import workloads as W
+    E, H, I, T, k = 3, 256, 128, 12, 2
+    w1, s1, w2, s2 = _mxfp4_case(E, H, I)
+    t1 = [_fp8_twin_of_mxfp4(w1[e], s1[e]) for e in range(E)]
+    t2 = [_fp8_twin_of_mxfp4(w2[e], s2[e]) for e in range(E)]
+    f1, g1 = torch.stack([a for a, _ in t1]), torch.stack([b for _, b in t1])
+    f2, g2 = torch.stack([a for a, _ in t2]), torch.stack([b for _, b in t2])
+    idx, w = W.make_routing(T, E, k, seed=3)
+    x, xs = W.make_activations(T, H, seed=3, scales="pow2")
+    h4 = oracle_mod.HostInputs(x, xs, idx, w, w1, s1, w2, s2, weights="mxfp4")
+    h8 = oracle_mod.HostInputs(x, xs, idx, w, f1, g1, f2, g2)
+    for rule in ("fp32", "pow2"):
+        oracle_mod.set_scale_rule(rule)
+        try:
+            b4, o4, bad4 = oracle_mod.forward_tokens(h4, np.arange(T))
+            b8, o8, bad8 = oracle_mod.forward_tokens(h8, np.arange(T))
+        finally:
+            oracle_mod.set_scale_rule("fp32")
+        assert not bad4 and not bad8
+        assert np.array_equal(o4, o8) and np.array_equal(b4, b8)
+        assert np.abs(o4).max() > 0
+
+
+def test_mxfp4_single_element_weights(oracle_mod):
+    """Gate, up and down weights each with one non-zero element: the expert output is that
+    element's closed form, so a swapped nibble or a wrong scale index moves it."""
+    H, I = 256, 128
+    x = torch.zeros(H, dtype=torch.uint8)
+    xs = torch.ones(H // 128)
+    c0 = 37                                   # odd column: the high nibble of byte 18
+    x[c0] = 0x38                              # e4m3 1.0
+    w1 = torch.zeros(2 * I, H // 2, dtype=torch.uint8)
+    s1 = torch.full((2 * I, H // 32), 127, dtype=torch.uint8)
+    n0 = 5
+    w1[n0, c0 // 2] = 0x3 << 4                # gate (n0, c0) = code 3 = 1.5
+    w1[I + n0, c0 // 2] = 0x6 << 4            # up (n0, c0) = code 6 = 4.0
+    s1[n0, c0 // 32] = 129                    # x 4
+    s1[I + n0, c0 // 32] = 126                # x 0.5
+    w2 = torch.zeros(H, I // 2, dtype=torch.uint8)
+    s2 = torch.full((H, I // 32), 127, dtype=torch.uint8)
+    r0 = 200
+    w2[r0, n0 // 2] = 0xD << 4 if n0 % 2 else 0xD   # down (r0, n0) = code 13 = -3.0
+    s2[r0, n0 // 32] = 128                    # x 2
+    y, hq, hsf = oracle_mod.expert_ffn(x, xs, w1, s1, w2, s2, weights="mxfp4")
+    g, u = 1.5 * 4.0, 4.0 * 0.5
+    hval = np.float32(g / (1.0 + np.exp(-g)) * u)
+    sf = np.float32(hval / np.float32(448.0))
+    hd = torch.tensor([float(hval / sf)]).to(torch.float8_e4m3fn).double().item() * float(sf)
+    want = np.zeros(H)
+    want[r0] = hd * -3.0 * 2.0
+    assert np.allclose(y, want, rtol=0, atol=1e-12) and y[r0] != 0

@@ -48,3 +48,30 @@ def test_make_inputs_shapes():
     assert inp.sf_down.shape == (wl.E, wl.H // 128, wl.I // 128)
     again = W.make_inputs("tiny")
     assert torch.equal(inp.x, again.x) and torch.equal(inp.topk_idx, again.topk_idx)
+
+
+def test_quantize_mxfp4_scale_rule_and_error_bound():
+    """MXFP4 synthesis: each 32-run's scale is 2^(floor(log2 amax) - 2), the decoded values
+    (oracle decoders) lie within half an E2M1 step of v (saturated runs: within 2 X), and the
+    packing puts element 2j in the low nibble."""
+    import oracle
+    from combine_persistent_warp_gb300.workloads import quantize_mxfp4
+    g = torch.Generator().manual_seed(9)
+    w = torch.randn(64, 256, generator=g) * 0.02
+    w[3, :32] = 0.0                                   # an all-zero run
+    packed, sf = quantize_mxfp4(w)
+    assert packed.shape == (64, 128) and sf.shape == (64, 8)
+    amax = w.view(64, 8, 32).abs().amax(dim=2).double().numpy()
+    ex = sf.numpy().astype(np.int64) - 127
+    nz = amax > 0
+    assert np.array_equal(ex[nz], (np.floor(np.log2(amax[nz])) - 2).astype(np.int64))
+    assert ex[3, 0] == -127
+    p = packed.numpy()
+    codes = np.stack([p & 0xF, p >> 4], axis=2).reshape(64, 256)
+    X = np.repeat(np.ldexp(1.0, ex), 32, axis=1)
+    q = oracle.e2m1_decode(codes) * X
+    err = np.abs(q - w.double().numpy())
+    # E2M1 steps: 0.5 up to 2, 1 up to 4, 2 up to 6; |v|/X < 8 always
+    a = np.abs(w.double().numpy()) / X
+    bound = np.where(a <= 2, 0.25, np.where(a <= 4, 0.5, np.where(a <= 6, 1.0, 2.0))) * X
+    assert np.all(err <= bound + 1e-18)

@@ -30,6 +30,8 @@ struct moe_ctx {
     bool have_weights = false;
     bool routed_loaded = false, shared_loaded = false;
     bool routed_pow2 = false, shared_pow2 = false;
+    int fmt_routed = MOE_WEIGHTS_FP8, fmt_shared = MOE_WEIGHTS_FP8;   // format of each loaded set
+    bool mxfp4 = false;          // the loaded weights are MXFP4 (block-scaled kernel, FP4 B tiles)
     Workspace ws{};
     void *small_mem = nullptr;   // header + routing arrays (size depends on E, R only)
     void *big_mem = nullptr;     // table, pools, combine, staging (depends on max_tokens)
@@ -46,6 +48,14 @@ struct moe_ctx {
     size_t w_bytes = 0;
     FfnMaps maps{};              // a1 pool x, b1 W1, a2 act, b2 W2
     SfMaps sf_maps{};            // UE8M0 scale blocks of pool / act rows and weight tiles
+    // MXFP4 weights (allocated by the first MXFP4 load): packed E2M1 tiles
+    // [E][N/256][K/128][256][64] and UE8M0 scale blocks of 1 KB per weight tile and K block
+    uint8_t *w41 = nullptr, *w42 = nullptr, *sfb41 = nullptr, *sfb42 = nullptr;
+    uint32_t *sfb4_bad = nullptr;
+    void *w4_mem = nullptr;
+    size_t w4_bytes = 0;
+    CUtensorMap b41{}, b42{}, b41h{}, b42h{};   // 16U4_ALIGN16B maps of the E2M1 tiles
+    CUtensorMap sfb41_map{}, sfb42_map{};
     // staging buffers of moe_forward_host
     // (two input sets: an asynchronous call fills one with the copy engines on copy_stream
     // while the previous call's kernels still read the other)
@@ -113,6 +123,24 @@ int encode_tile_map(CUtensorMap *m, void *base, uint64_t rows, uint64_t cols, ui
                                               : CU_TENSOR_MAP_SWIZZLE_32B;
     CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
+}
+
+// Packed E2M1 weight tiles as rows of 64 bytes (128 four-bit values), element type
+// 16U4_ALIGN16B: a box of 128 values x box_rows lands in shared memory as 128-byte rows (each
+// 8 packed bytes followed by an 8-byte gap), swizzled at 128 bytes like an e4m3 tile; the
+// transaction count is the packed bytes.  Needs a 32-byte aligned base.
+int encode_fp4_tile_map(CUtensorMap *m, void *base, uint64_t rows, uint32_t box_rows)
+{
+    if (get_encoder() != MOE_OK || reinterpret_cast<uintptr_t>(base) % 32 != 0)
+        return MOE_ERR_CUDA;
+    cuuint64_t dims[2] = {128, rows};
+    cuuint64_t strides[1] = {64};
+    cuuint32_t box[2] = {128, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, base, dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
 }
@@ -383,8 +411,8 @@ int load_expert_weights(moe_ctx *h, int e0, int n, const uint8_t *w_gate_up, con
         carve(static_cast<char *>(h->w_mem));
         h->w_bytes = bytes;
     }
-    if (launch_relayout_weights(w_gate_up, h->w1 + e0 * w1e, n, 2 * d.I, d.H, d.I, s) != cudaSuccess ||
-        launch_relayout_weights(w_down, h->w2 + e0 * w2e, n, d.H, d.I, 0, s) != cudaSuccess)
+    if (launch_relayout_weights(w_gate_up, h->w1 + e0 * w1e, n, 2 * d.I, d.H, d.I, 128, s) != cudaSuccess ||
+        launch_relayout_weights(w_down, h->w2 + e0 * w2e, n, d.H, d.I, 0, 128, s) != cudaSuccess)
         return MOE_ERR_CUDA;
     CK(cudaMemcpyAsync(h->s1 + e0 * s1e, sf_gate_up, n * s1e * sizeof(float), cudaMemcpyDeviceToDevice, s));
     CK(cudaMemcpyAsync(h->s2 + e0 * s2e, sf_down, n * s2e * sizeof(float), cudaMemcpyDeviceToDevice, s));
@@ -410,10 +438,67 @@ int load_expert_weights(moe_ctx *h, int e0, int n, const uint8_t *w_gate_up, con
     return MOE_OK;
 }
 
+// MXFP4 weights of experts [e0, e0 + n): packed E2M1 rows re-laid into 16 KB GEMM tiles,
+// UE8M0 scales into per-(tile, K block) scale blocks.  MOE_ERR_BAD_SCALE if a scale byte is
+// 0xFF (NaN).
+int load_expert_weights_mxfp4(moe_ctx *h, int e0, int n, const uint8_t *w_gate_up, const uint8_t *sf_gate_up,
+                              const uint8_t *w_down, const uint8_t *sf_down, cudaStream_t s)
+{
+    if (!w_gate_up || !sf_gate_up || !w_down || !sf_down)
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned(w_gate_up, 16) || !aligned(w_down, 16) || !aligned(sf_gate_up, 4) || !aligned(sf_down, 4))
+        return MOE_ERR_INVALID_ARG;
+    CK(cudaSetDevice(h->dev));
+    const Dims &d = h->d;
+    const size_t w1e = static_cast<size_t>(2) * d.I * (d.H / 2), w2e = static_cast<size_t>(d.H) * (d.I / 2);
+    const size_t b1e = static_cast<size_t>(2 * d.I / BN) * (d.H / 128) * 1024,
+                 b2e = static_cast<size_t>(d.H / BN) * (d.I / 128) * 1024;
+    const size_t n1 = d.E * w1e, n2 = d.E * w2e;
+    if (!h->w4_mem) {
+        Carver c{nullptr};
+        auto carve = [&](char *base) {
+            c = Carver{base};
+            h->w41 = c.take<uint8_t>(n1);
+            h->w42 = c.take<uint8_t>(n2);
+            h->sfb41 = c.take<uint8_t>(d.E * b1e);
+            h->sfb42 = c.take<uint8_t>(d.E * b2e);
+            h->sfb4_bad = c.take<uint32_t>(1);
+            return align_up(c.off, 256);
+        };
+        const size_t bytes = carve(nullptr);
+        CK(cudaMalloc(&h->w4_mem, bytes));
+        carve(static_cast<char *>(h->w4_mem));
+        h->w4_bytes = bytes;
+    }
+    if (launch_relayout_weights(w_gate_up, h->w41 + e0 * w1e, n, 2 * d.I, d.H, d.I, 64, s) != cudaSuccess ||
+        launch_relayout_weights(w_down, h->w42 + e0 * w2e, n, d.H, d.I, 0, 64, s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    CK(cudaMemsetAsync(h->sfb4_bad, 0, sizeof(uint32_t), s));
+    if (launch_build_sfb4(sf_gate_up, h->sfb41 + e0 * b1e, n, 2 * d.I, d.H, d.I, h->sfb4_bad, s) != cudaSuccess ||
+        launch_build_sfb4(sf_down, h->sfb42 + e0 * b2e, n, d.H, d.I, 0, h->sfb4_bad, s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    uint32_t bad = 1;
+    CK(cudaMemcpyAsync(&bad, h->sfb4_bad, sizeof(uint32_t), cudaMemcpyDeviceToHost, s));
+    CK(cudaStreamSynchronize(s));
+    // tile (e, nt, kb) starts at 64-byte row ((e*NT + nt)*KB + kb)*256
+    if (encode_fp4_tile_map(&h->b41, h->w41, n1 / 64, BN) != MOE_OK ||
+        encode_fp4_tile_map(&h->b42, h->w42, n2 / 64, BN) != MOE_OK ||
+        encode_fp4_tile_map(&h->b41h, h->w41, n1 / 64, BN / 2) != MOE_OK ||
+        encode_fp4_tile_map(&h->b42h, h->w42, n2 / 64, BN / 2) != MOE_OK ||
+        encode_sf_map(&h->sfb41_map, h->sfb41, static_cast<uint64_t>(d.E) * b1e, 4) != MOE_OK ||
+        encode_sf_map(&h->sfb42_map, h->sfb42, static_cast<uint64_t>(d.E) * b2e, 4) != MOE_OK)
+        return MOE_ERR_CUDA;
+    h->last_stream = s;
+    h->have_last = true;
+    return bad ? MOE_ERR_BAD_SCALE : MOE_OK;
+}
+
 void update_weight_state(moe_ctx *h)
 {
-    h->have_weights = h->routed_loaded && (h->S == 0 || h->shared_loaded);
+    // routed and shared experts run in one kernel: both sets in one format
+    h->have_weights = h->routed_loaded && (h->S == 0 || (h->shared_loaded && h->fmt_shared == h->fmt_routed));
     h->weights_pow2 = h->routed_pow2 && (h->S == 0 || h->shared_pow2);
+    h->mxfp4 = h->fmt_routed == MOE_WEIGHTS_MXFP4;
 }
 
 }  // namespace
@@ -423,13 +508,15 @@ int moe_load_weights(moe_handle_t h, const uint8_t *w_gate_up, const float *sf_g
 {
     if (!h)
         return MOE_ERR_INVALID_ARG;
+    h->routed_loaded = false;
     const int rc = load_expert_weights(h, 0, h->E_routed, w_gate_up, sf_gate_up, w_down, sf_down,
                                        static_cast<cudaStream_t>(stream), &h->routed_pow2);
-    if (rc != MOE_OK)
-        return rc;
-    h->routed_loaded = true;
+    if (rc == MOE_OK) {
+        h->routed_loaded = true;
+        h->fmt_routed = MOE_WEIGHTS_FP8;
+    }
     update_weight_state(h);
-    return MOE_OK;
+    return rc;
 }
 
 int moe_load_shared_weights(moe_handle_t h, const uint8_t *w_gate_up, const float *sf_gate_up,
@@ -437,13 +524,49 @@ int moe_load_shared_weights(moe_handle_t h, const uint8_t *w_gate_up, const floa
 {
     if (!h || h->S == 0)
         return MOE_ERR_INVALID_ARG;
+    h->shared_loaded = false;
     const int rc = load_expert_weights(h, h->E_routed, h->S, w_gate_up, sf_gate_up, w_down, sf_down,
                                        static_cast<cudaStream_t>(stream), &h->shared_pow2);
-    if (rc != MOE_OK)
-        return rc;
-    h->shared_loaded = true;
+    if (rc == MOE_OK) {
+        h->shared_loaded = true;
+        h->fmt_shared = MOE_WEIGHTS_FP8;
+    }
     update_weight_state(h);
-    return MOE_OK;
+    return rc;
+}
+
+int moe_load_weights_mxfp4(moe_handle_t h, const uint8_t *w_gate_up, const uint8_t *sf_gate_up,
+                           const uint8_t *w_down, const uint8_t *sf_down, void *stream)
+{
+    if (!h)
+        return MOE_ERR_INVALID_ARG;
+    h->routed_loaded = false;
+    const int rc = load_expert_weights_mxfp4(h, 0, h->E_routed, w_gate_up, sf_gate_up, w_down, sf_down,
+                                             static_cast<cudaStream_t>(stream));
+    if (rc == MOE_OK) {
+        h->routed_loaded = true;
+        h->fmt_routed = MOE_WEIGHTS_MXFP4;
+        h->routed_pow2 = true;
+    }
+    update_weight_state(h);
+    return rc;
+}
+
+int moe_load_shared_weights_mxfp4(moe_handle_t h, const uint8_t *w_gate_up, const uint8_t *sf_gate_up,
+                                  const uint8_t *w_down, const uint8_t *sf_down, void *stream)
+{
+    if (!h || h->S == 0)
+        return MOE_ERR_INVALID_ARG;
+    h->shared_loaded = false;
+    const int rc = load_expert_weights_mxfp4(h, h->E_routed, h->S, w_gate_up, sf_gate_up, w_down, sf_down,
+                                             static_cast<cudaStream_t>(stream));
+    if (rc == MOE_OK) {
+        h->shared_loaded = true;
+        h->fmt_shared = MOE_WEIGHTS_MXFP4;
+        h->shared_pow2 = true;
+    }
+    update_weight_state(h);
+    return rc;
 }
 
 int moe_forward(moe_handle_t h, int T, const uint8_t *x, const float *x_sf, const int64_t *topk_idx,
@@ -469,10 +592,11 @@ int moe_forward(moe_handle_t h, int T, const uint8_t *x, const float *x_sf, cons
     CK(cudaSetDevice(h->dev));
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     // power-of-two scales: the block-scaled kernel (the weights were checked at load time,
-    // the activation scales are checked by the routing kernel's gather)
-    if (h->scale_mode == 1 && !h->weights_pow2)
+    // the activation scales are checked by the routing kernel's gather); MXFP4 weights run
+    // only there
+    if ((h->scale_mode == 1 && !h->weights_pow2) || (h->scale_mode == 0 && h->mxfp4))
         return MOE_ERR_BAD_SCALE;
-    const bool bs = h->scale_mode == 1 || (h->scale_mode == 2 && h->weights_pow2);
+    const bool bs = h->mxfp4 || h->scale_mode == 1 || (h->scale_mode == 2 && h->weights_pow2);
     CallArgs c{T, x, x_sf, topk_idx, topk_w, out, h->timeout_ns, h->debug_skip_barrier, bs ? 1 : 0};
     if (h->S > 0) {
         // shared experts: each token's route gains slots K_routed.. naming expert E_routed + s
@@ -488,13 +612,25 @@ int moe_forward(moe_handle_t h, int T, const uint8_t *x, const float *x_sf, cons
             ++h->prof_dropped;
     }
     auto mark = [&](int i) { return ev ? cudaEventRecord(ev[i], s) : cudaSuccess; };
+    // MXFP4: the weight-tile and weight-scale maps of the E2M1 tiles
+    FfnMaps maps4 = h->maps;
+    SfMaps sf_maps4 = h->sf_maps;
+    if (h->mxfp4) {
+        maps4.b1 = h->b41;
+        maps4.b2 = h->b42;
+        maps4.b1h = h->b41h;
+        maps4.b2h = h->b42h;
+        sf_maps4.sfb1 = h->sfb41_map;
+        sf_maps4.sfb2 = h->sfb42_map;
+    }
     if (mark(0) != cudaSuccess ||
         (h->S > 0 && launch_extend_route(topk_idx, topk_w, h->ext_idx, h->ext_w, T, h->K_routed, h->S, h->E_routed,
                                          h->num_sms, s) != cudaSuccess) ||
         launch_dispatch(h->d, h->ws, c, h->num_sms, s) != cudaSuccess ||
         mark(1) != cudaSuccess ||
-        (bs ? launch_ffn_bs(h->maps, h->sf_maps, h->d, h->ws, c, h->sfb1, h->sfb2, wave_blocks(h), h->num_sms,
-                            ffn_paired(h, T), s)
+        (bs ? launch_ffn_bs(h->mxfp4 ? maps4 : h->maps, h->mxfp4 ? sf_maps4 : h->sf_maps, h->d, h->ws, c,
+                            h->mxfp4 ? h->sfb41 : h->sfb1, h->mxfp4 ? h->sfb42 : h->sfb2, wave_blocks(h),
+                            h->num_sms, ffn_paired(h, T), h->mxfp4, s)
             : launch_ffn(h->maps, h->d, h->ws, c, h->s1, h->s2, wave_blocks(h), h->num_sms, ffn_paired(h, T), s)) !=
             cudaSuccess ||
         mark(2) != cudaSuccess || launch_combine(h->d, h->ws, c, h->num_sms, s) != cudaSuccess ||
@@ -731,8 +867,9 @@ int moe_get_info(moe_handle_t h, moe_info *info)
     info->block_n = BN;
     info->num_sms = h->num_sms;
     info->workspace_bytes = h->small_bytes + h->big_bytes;
-    info->weight_bytes = h->w_bytes;
+    info->weight_bytes = h->w_bytes + h->w4_bytes;
     info->n_shared = h->S;
+    info->weight_format = h->fmt_routed;
     return MOE_OK;
 }
 
@@ -829,6 +966,8 @@ int moe_destroy(moe_handle_t h)
         cudaFree(h->small_mem);
     if (h->w_mem)
         cudaFree(h->w_mem);
+    if (h->w4_mem)
+        cudaFree(h->w4_mem);
     delete h;
     return MOE_OK;
 }

@@ -24,6 +24,17 @@
 // for all four 32-deep UMMAs of a K block.  Copying once per group instead of once per K
 // block took the issue sequence from ~830 to ~700 cycles per K block.
 //
+// MXFP4 weights (FP4 = true): the weight tiles are packed E2M1 (64 bytes per row and 128-deep
+// K block) with one UE8M0 scale per row and 32-deep K slice (the OCP Microscaling block).  TMA
+// loads them with the 16U4_ALIGN16B element type, which widens every 8 bytes (16 values) to a
+// 16-byte slot in shared memory: the 128-byte-row image the UMMA reads for a 4-bit operand of
+// kind::mxf8f6f4 (B format E2M1), at the same swizzle and descriptor as an e4m3 tile, while
+// only the packed 16 KB per stage comes from memory.  The B scale words then change every K
+// block (byte j = the scale of the block's j-th 32-deep slice, instruction B scale id = j),
+// so the producer stages a 1 KB B scale block with every stage and the issuer copies it to
+// TMEM per K block, into the slot of the stage (reused only after the stage's next fill,
+// i.e. after the UMMAs that read it); the A scales keep their once-per-group copy.
+//
 // Roles (one CTA per SM, 12 warps): warp 0 TMA producer (A, B and the two scale blocks of
 // a 128-deep K block per stage, 4 stages); warp 1 UMMA issuer (scale copies + 4 block-scaled
 // UMMAs per stage into one 256-column TMEM accumulator); warps 4-11 epilogue (two
@@ -59,14 +70,14 @@ constexpr int PAIR_STAGES = static_cast<int>((STAGES * STAGE_BYTES) / PAIR_STAGE
 static_assert(PAIR_STAGES * PAIR_STAGE_BYTES <= STAGES * STAGE_BYTES, "pair stages exceed the ring");
 static_assert(SF_COL + 16 * PAIR_STAGES <= TMEM_COLS, "scale slots exceed TMEM");
 
-// block-scaled instruction descriptor: B scale id (byte of the scale word) at bits 4-5, e4m3
-// A/B (formats 0), K-major A and B, N>>3 at 17-22, UE8M0 scales (bit 23), M>>4 at 24-28, A
-// scale id at 29-30
-template <int M>
-__device__ __forceinline__ uint32_t idesc_bs(int sf_id)
+// block-scaled instruction descriptor: B scale id (byte of the scale word) at bits 4-5, A
+// format e4m3 (0) at bits 7-9, B format at bits 10-12 (e4m3 = 0, E2M1 = 5), K-major A and B,
+// N>>3 at 17-22, UE8M0 scales (bit 23), M>>4 at 24-28, A scale id at 29-30
+template <int M, bool FP4>
+__device__ __forceinline__ uint32_t idesc_bs(int a_sf_id, int b_sf_id)
 {
-    return (static_cast<uint32_t>(sf_id) << 4) | (static_cast<uint32_t>(BN >> 3) << 17) | (1u << 23) |
-           (static_cast<uint32_t>(M >> 4) << 24) | (static_cast<uint32_t>(sf_id) << 29);
+    return (static_cast<uint32_t>(b_sf_id) << 4) | ((FP4 ? 5u : 0u) << 10) | (static_cast<uint32_t>(BN >> 3) << 17) |
+           (1u << 23) | (static_cast<uint32_t>(M >> 4) << 24) | (static_cast<uint32_t>(a_sf_id) << 29);
 }
 
 // one CTA: D (128 rows) (+)= A x B^T with scales from this CTA's TMEM.  Two CTAs (issued by
@@ -162,7 +173,7 @@ struct BsView {
 
 }  // namespace
 
-template <bool PAIRED>
+template <bool PAIRED, bool FP4>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     ffn_bs_kernel(const __grid_constant__ FfnMaps maps, const __grid_constant__ SfMaps sfm, const Dims d,
                   const Workspace ws, const CallArgs c, const uint8_t *__restrict__ sfb1,
@@ -170,6 +181,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 {
     constexpr int NST = PAIRED ? PAIR_STAGES : STAGES;                     // stages in the ring
     constexpr uint32_t SBYTES = PAIRED ? PAIR_STAGE_BYTES : STAGE_BYTES;   // operand bytes per stage
+    // weight bytes a stage's TMA brings from memory for this CTA (packed E2M1: half the
+    // shared-memory image)
+    constexpr uint32_t B_TX = (PAIRED ? PAIR_B_BYTES : STAGE_B_BYTES) / (FP4 ? 2u : 1u);
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
@@ -361,23 +375,26 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     // bytes the stage's full barrier waits for: this CTA's, plus (2-CTA mode,
                     // even CTA) the odd CTA's, whose loads count on the even CTA's barrier
                     // (the scale blocks only with the first stage of a group of K blocks)
-                    uint32_t tx_bytes = a_bytes + (PAIRED ? PAIR_B_BYTES : STAGE_B_BYTES);
-                    uint32_t tx_sf = (tv.null_half ? 0u : SFA_BYTES) + SFB_BYTES;
+                    uint32_t tx_bytes = a_bytes + B_TX;
+                    uint32_t tx_sfa = tv.null_half ? 0u : SFA_BYTES, tx_sfb = SFB_BYTES;
                     if (PAIRED && rank == 0) {
                         const BsView ov = view_of(tile, 1);
-                        tx_bytes += a_stage_bytes(a_parts(ov)) + PAIR_B_BYTES;
-                        tx_sf += (ov.null_half ? 0u : SFA_BYTES) + SFB_BYTES;
+                        tx_bytes += a_stage_bytes(a_parts(ov)) + B_TX;
+                        tx_sfa += ov.null_half ? 0u : SFA_BYTES;
+                        tx_sfb += SFB_BYTES;
                     }
                     const CUtensorMap *ta = phase == 1 ? (part ? &maps.a1p : &maps.a1) : (part ? &maps.a2p : &maps.a2);
                     const CUtensorMap *tb = PAIRED ? (phase == 1 ? &maps.b1h : &maps.b2h) : (phase == 1 ? &maps.b1 : &maps.b2);
                     const int nkb = phase == 1 ? NKB1 : NKB2;
                     const int wtile = e * (phase == 1 ? tl.NT1 : tl.NT2) + nt;
                     const int tile0 = wtile * nkb;
-                    // scale blocks: A per (M-block, K-block group), B per (weight tile, group)
+                    // scale blocks: A per (M-block, K-block group), B per (weight tile, group), or
+                    // with MXFP4 weights per (weight tile, K block)
                     const int ng = (nkb + SF_GROUP - 1) / SF_GROUP;
+                    const int nbb = FP4 ? nkb : ng;   // B scale blocks per weight tile
                     const uint8_t *sfa_src = (phase == 1 ? ws.pool_sfe : ws.act_sfe) +
                                              static_cast<long long>(blk) * ng * SFA_BYTES;
-                    const uint8_t *sfb_src = (phase == 1 ? sfb1 : sfb2) + static_cast<long long>(wtile) * ng * SFB_BYTES;
+                    const uint8_t *sfb_src = (phase == 1 ? sfb1 : sfb2) + static_cast<long long>(wtile) * nbb * SFB_BYTES;
                     if (phase == 2 && !tv.null_half) {
                         // the act rows and their scales of this block are complete: the
                         // dependency warp has acquired the block's gate_up completion count
@@ -409,8 +426,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                         uint8_t *ss = sf_smem + s * SF_STAGE_BYTES;
                         const bool sf_k = kb % SF_GROUP == 0;   // first K block of a scale group
                         const int grp = kb / SF_GROUP;
+                        const bool sfb_k = FP4 || sf_k;         // a B scale block with this stage
+                        const int bb = FP4 ? kb : grp;          // its index within the tile
                         if (!PAIRED || rank == 0)
-                            ptx::mbar_arrive_expect_tx(&bars->full[s], tx_bytes + (sf_k ? tx_sf : 0u));
+                            ptx::mbar_arrive_expect_tx(&bars->full[s],
+                                                       tx_bytes + (sf_k ? tx_sfa : 0u) + (sfb_k ? tx_sfb : 0u));
                         if constexpr (PAIRED) {
                             // own A rows, own half of the weight tile, own copies of the scale
                             // blocks (this block's A scales; all 256 weight rows' scales),
@@ -428,9 +448,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                             if (sf_k && !tv.null_half)
                                 ptx::tma_load_2d_pair(ss, phase == 1 ? &sfm.sfa1 : &sfm.sfa2, fb, 0,
                                                       (blk * ng + grp) * static_cast<int>(SFA_BYTES / 256), pol_a);
-                            if (sf_k)
+                            if (sfb_k)
                                 ptx::tma_load_2d_pair(ss + SFA_BYTES, phase == 1 ? &sfm.sfb1 : &sfm.sfb2, fb, 0,
-                                                      (wtile * ng + grp) * static_cast<int>(SFB_BYTES / 256), pol_b);
+                                                      (wtile * nbb + bb) * static_cast<int>(SFB_BYTES / 256), pol_b);
                         } else {
                             if (part) {
                                 for (int g = 0; g < n_part; ++g)
@@ -440,11 +460,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                                 ptx::tma_load_2d(sa, ta, &bars->full[s], kb * BK, blk * BM, pol_a);
                             }
                             ptx::tma_load_2d(sa + STAGE_A_BYTES, tb, &bars->full[s], 0, (tile0 + kb) * BN, pol_b);
-                            if (sf_k) {
+                            if (sf_k)
                                 ptx::bulk_load(ss, sfa_src + grp * SFA_BYTES, SFA_BYTES, &bars->full[s]);
-                                ptx::bulk_load(ss + SFA_BYTES, sfb_src + static_cast<long long>(grp) * SFB_BYTES,
+                            if (sfb_k)
+                                ptx::bulk_load(ss + SFA_BYTES, sfb_src + static_cast<long long>(bb) * SFB_BYTES,
                                                SFB_BYTES, &bars->full[s]);
-                            }
                         }
                     }
                     while (ok && fstep < 3)
@@ -504,7 +524,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 uint32_t it = 0, tcount = 0, acc_n = 0;
                 // scale groups copied so far: group g goes to TMEM slot g % NST, reused only after
                 // NST more groups, whose first stage's arrival implies (through the stage ring)
-                // that every UMMA of group g has completed
+                // that every UMMA of group g has completed (MXFP4: the per-K-block B scales go
+                // to the B columns of the stage's slot, reused after the stage's next fill)
                 uint32_t gcount = 0, sfa = 0, sfb = 0;
                 bool ok = true;
                 const bool issuer = !PAIRED || rank == 0;
@@ -538,12 +559,19 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                             break;
                         }
                         ptx::tc_fence_after();
+                        const uint32_t ss = ptx::smem_u32(sf_smem + s * SF_STAGE_BYTES);
                         if (kb % SF_GROUP == 0) {
-                            const uint32_t ss = ptx::smem_u32(sf_smem + s * SF_STAGE_BYTES);
                             sfa = tmem + SF_COL + 16 * (gcount % NST);
-                            sfb = sfa + 4;
                             ++gcount;
                             sf_copy<PAIRED>(sfa, ss);
+                            if constexpr (!FP4) {
+                                sfb = sfa + 4;
+                                sf_copy<PAIRED>(sfb, ss + SFA_BYTES);
+                                sf_copy<PAIRED>(sfb + 4, ss + SFA_BYTES + 512);
+                            }
+                        }
+                        if constexpr (FP4) {
+                            sfb = tmem + SF_COL + 16 * s + 4;
                             sf_copy<PAIRED>(sfb, ss + SFA_BYTES);
                             sf_copy<PAIRED>(sfb + 4, ss + SFA_BYTES + 512);
                         }
@@ -553,8 +581,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 #pragma unroll
                         for (int k = 0; k < BK / 32; ++k)   // +32 bytes along K = +2 in the >>4 field
                             umma_bs<PAIRED>(tmem, adesc + 2 * k, bdesc + 2 * k,
-                                            idesc_bs<PAIRED ? 2 * BM : BM>(kb % SF_GROUP), sfa, sfb,
-                                            (kb > 0 || k > 0) ? 1u : 0u);
+                                            idesc_bs<PAIRED ? 2 * BM : BM, FP4>(kb % SF_GROUP, FP4 ? k : kb % SF_GROUP),
+                                            sfa, sfb, (kb > 0 || k > 0) ? 1u : 0u);
                         if constexpr (PAIRED)
                             ptx::umma_commit_pair(&bars->empty[s], static_cast<uint16_t>(0x3));
                         else
@@ -790,9 +818,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 
 cudaError_t launch_ffn_bs(const FfnMaps &maps, const SfMaps &sf_maps, const Dims &d, const Workspace &ws,
                           const CallArgs &c, const uint8_t *sfb1, const uint8_t *sfb2, int wave_blocks, int num_sms,
-                          bool paired, cudaStream_t s)
+                          bool paired, bool fp4, cudaStream_t s)
 {
-    static bool configured[2] = {false, false};
+    static bool configured[4] = {false, false, false, false};
     static int paired_grid = 0;
     static int paired_coop = 1;   // cooperative attribute accepted together with clusters
     constexpr int SMEM1 = 1024 + STAGES * STAGE_BYTES + 8192 + STAGES * SF_STAGE_BYTES;
@@ -800,12 +828,16 @@ cudaError_t launch_ffn_bs(const FfnMaps &maps, const SfMaps &sf_maps, const Dims
     static_assert(sizeof(BsBars) <= 8192, "barrier block");
     static_assert(SMEM2 <= 227 * 1024, "shared memory per CTA");
     const int smem = paired ? SMEM2 : SMEM1;
-    void *kern = paired ? reinterpret_cast<void *>(ffn_bs_kernel<true>) : reinterpret_cast<void *>(ffn_bs_kernel<false>);
-    if (!configured[paired]) {
+    void *kern = paired ? (fp4 ? reinterpret_cast<void *>(ffn_bs_kernel<true, true>)
+                               : reinterpret_cast<void *>(ffn_bs_kernel<true, false>))
+                        : (fp4 ? reinterpret_cast<void *>(ffn_bs_kernel<false, true>)
+                               : reinterpret_cast<void *>(ffn_bs_kernel<false, false>));
+    const int variant = (paired ? 2 : 0) + (fp4 ? 1 : 0);
+    if (!configured[variant]) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess)
             return e;
-        configured[paired] = true;
+        configured[variant] = true;
     }
     FfnMaps m = maps;
     SfMaps sm = sf_maps;
@@ -895,6 +927,46 @@ cudaError_t launch_build_sfb(const float *s, uint8_t *dst, int E, int N, int K, 
                              cudaStream_t st)
 {
     build_sfb_kernel<<<1024, 256, 0, st>>>(s, dst, E, N, K, gate_up_I, bad);
+    return cudaGetLastError();
+}
+
+// MXFP4 weights: scale blocks per weight tile and K block.  s = [E][N][K/32] UE8M0 bytes in
+// the caller's row order; for weight tile (e, nt) and K block kb, 1 KB at
+// ((e*NT + nt)*KB + kb)*1024 with tile column n's word at 512*(n/128) + 16*(n%32) +
+// 4*((n%128)/32), byte j = the scale of the row's 32-deep slice 4*kb + j.  Tile column n is
+// weight row nt*256 + n, through the gate/up interleave by 8 for the gate_up weight (the
+// row order of the re-laid weight tiles).  A byte 0xFF (NaN in the UE8M0 format) sets *bad.
+__global__ void build_sfb4_kernel(const uint8_t *__restrict__ s, uint8_t *__restrict__ dst, int E, int N, int K,
+                                  int gate_up_I, uint32_t *bad)
+{
+    const int KB = K / 128, NT = N / BN;
+    const long long words = static_cast<long long>(E) * NT * KB * BN;
+    for (long long q = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; q < words;
+         q += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const int n = static_cast<int>(q % BN);
+        const long long tk = q / BN;   // (e*NT + nt)*KB + kb
+        const int kb = static_cast<int>(tk % KB);
+        const long long et = tk / KB;
+        const int nt = static_cast<int>(et % NT);
+        const long long e = et / NT;
+        const int row = nt * BN + n;
+        int srow = row;
+        if (gate_up_I > 0) {
+            const int j = row / 16, i = row % 16;
+            srow = i < 8 ? 8 * j + i : gate_up_I + 8 * j + (i - 8);
+        }
+        // K/32 is a multiple of 4: the four bytes of K block kb are one aligned word
+        const uint32_t w = *reinterpret_cast<const uint32_t *>(s + (e * N + srow) * (K / 32) + 4 * kb);
+        if (((w & 0xFFu) == 0xFFu) || ((w >> 8 & 0xFFu) == 0xFFu) || ((w >> 16 & 0xFFu) == 0xFFu) || ((w >> 24) == 0xFFu))
+            atomicOr(bad, 1u);
+        *reinterpret_cast<uint32_t *>(dst + tk * SFB_BYTES + 512 * (n / 128) + 16 * (n % 32) + 4 * ((n % 128) / 32)) = w;
+    }
+}
+
+cudaError_t launch_build_sfb4(const uint8_t *s, uint8_t *dst, int E, int N, int K, int gate_up_I, uint32_t *bad,
+                              cudaStream_t st)
+{
+    build_sfb4_kernel<<<1024, 256, 0, st>>>(s, dst, E, N, K, gate_up_I, bad);
     return cudaGetLastError();
 }
 

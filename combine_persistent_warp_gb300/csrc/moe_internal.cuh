@@ -114,12 +114,16 @@ struct SfMaps {
     CUtensorMap sfa1, sfa2, sfb1, sfb2;
 };
 // power-of-two scales: the block-scaled FFN kernel (ffn_bs.cu) and the load-time UE8M0
-// scale blocks of the weight tiles; paired: 2-CTA clusters (one M = 256 UMMA per block pair)
+// scale blocks of the weight tiles; paired: 2-CTA clusters (one M = 256 UMMA per block pair);
+// fp4: MXFP4 weight tiles (packed E2M1, maps of the 16U4_ALIGN16B type) with per-K-block
+// scale blocks
 cudaError_t launch_ffn_bs(const FfnMaps &maps, const SfMaps &sf_maps, const Dims &d, const Workspace &ws,
                           const CallArgs &c, const uint8_t *sfb1, const uint8_t *sfb2, int wave_blocks, int num_sms,
-                          bool paired, cudaStream_t s);
+                          bool paired, bool fp4, cudaStream_t s);
 cudaError_t launch_build_sfb(const float *s, uint8_t *dst, int E, int N, int K, int gate_up_I, uint32_t *bad,
                              cudaStream_t st);
+cudaError_t launch_build_sfb4(const uint8_t *s, uint8_t *dst, int E, int N, int K, int gate_up_I, uint32_t *bad,
+                              cudaStream_t st);
 cudaError_t launch_combine(const Dims &d, const Workspace &ws, const CallArgs &c, int num_sms,
                            cudaStream_t s);
 // shared experts: idx_ext / w_ext [T][K + S] = the caller's [T][K] route plus slots K + s naming
@@ -128,7 +132,8 @@ cudaError_t launch_extend_route(const int64_t *idx, const float *w, int64_t *idx
                                 int S, int E_routed, int num_sms, cudaStream_t s);
 cudaError_t launch_stage_inputs(const void *const src[4], void *const dst[4], const long long bytes[4], int num_sms,
                                 cudaStream_t s);
+// kb_bytes: bytes of a 128-element K block of a weight row (128 e4m3, 64 packed E2M1)
 cudaError_t launch_relayout_weights(const uint8_t *src, uint8_t *dst, int E, int N, int K, int gate_up_I,
-                                    cudaStream_t s);
+                                    int kb_bytes, cudaStream_t s);
 
 }  // namespace cpw

@@ -269,23 +269,26 @@ cudaError_t launch_stage_inputs(const void *const src[4], void *const dst[4], co
 }
 
 // ------------------------------------------------------------------ weights -------------
-// Load-time weight re-layout into GEMM tiles.  dst = [E][N/256][K/128][256][128] bytes: every
-// 256-row x 128-byte tile the FFN kernel loads per 128-deep K block is one contiguous 32 KB
-// block, so each weight load streams whole DRAM pages instead of 256 rows 7 KB apart.
+// Load-time weight re-layout into GEMM tiles.  A weight row of K elements is K/128 blocks of
+// kb_bytes bytes (128 for e4m3; 64 for packed 4-bit E2M1, two elements per byte).  dst =
+// [E][N/256][K/128][256][kb_bytes] bytes: every 256-row tile the FFN kernel loads per 128-deep
+// K block is one contiguous block (32 KB / 16 KB), so each weight load streams whole DRAM
+// pages instead of 256 rows several KB apart.
 // With gate_up_I > 0 (the gate_up weight, N = 2I) the rows are also gate/up interleaved:
 // within each group of 16 rows, rows 0..7 are gate rows 8j..8j+7 and rows 8..15 are up rows
 // I+8j..I+8j+7 (granularity 8, the layout of "DeepGEMM Mega MoE 对称内存（Symmetric Memory）
 // 深度分析" §10.2), so one 256-row tile holds 128 gate rows and the 128 matching up rows.
 __global__ void relayout_weights_kernel(const uint8_t *__restrict__ src, uint8_t *__restrict__ dst, int E,
-                                        int N, int K, int gate_up_I)
+                                        int N, int K, int gate_up_I, int kb_bytes)
 {
-    const int KB = K / 128, NT = N / BN;
-    const long long chunks = static_cast<long long>(E) * N * (K / 16);
+    const int KB = K / 128, NT = N / BN, C16 = kb_bytes / 16;
+    const long long row_bytes = static_cast<long long>(KB) * kb_bytes;
+    const long long chunks = static_cast<long long>(E) * N * KB * C16;
     for (long long q = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; q < chunks;
          q += static_cast<long long>(gridDim.x) * blockDim.x) {
         long long t = q;
-        const int c16 = static_cast<int>(t % 8);
-        t /= 8;
+        const int c16 = static_cast<int>(t % C16);
+        t /= C16;
         const int r = static_cast<int>(t % BN);
         t /= BN;
         const int kb = static_cast<int>(t % KB);
@@ -298,16 +301,17 @@ __global__ void relayout_weights_kernel(const uint8_t *__restrict__ src, uint8_t
             const int j = n / 16, i = n % 16;
             srow = i < 8 ? 8 * j + i : gate_up_I + 8 * j + (i - 8);
         }
-        const uint4 *sp = reinterpret_cast<const uint4 *>(src + (e * N + srow) * static_cast<long long>(K) +
-                                                          kb * 128 + c16 * 16);
+        const uint4 *sp = reinterpret_cast<const uint4 *>(src + (e * N + srow) * row_bytes + kb * kb_bytes + c16 * 16);
         reinterpret_cast<uint4 *>(dst)[q] = *sp;
     }
 }
 
 cudaError_t launch_relayout_weights(const uint8_t *src, uint8_t *dst, int E, int N, int K, int gate_up_I,
-                                    cudaStream_t s)
+                                    int kb_bytes, cudaStream_t s)
 {
-    relayout_weights_kernel<<<2048, 256, 0, s>>>(src, dst, E, N, K, gate_up_I);
+    if (kb_bytes != 128 && kb_bytes != 64)
+        return cudaErrorInvalidValue;
+    relayout_weights_kernel<<<2048, 256, 0, s>>>(src, dst, E, N, K, gate_up_I, kb_bytes);
     return cudaGetLastError();
 }
 

@@ -29,6 +29,7 @@ OPT_DEBUG_SKIP_BARRIER = 1
 OPT_FFN_MODE = 2
 OPT_SCALE_MODE = 3
 SCALE_FP32, SCALE_POW2, SCALE_AUTO = 0, 1, 2   # values of OPT_SCALE_MODE (default SCALE_AUTO)
+WEIGHTS_FP8, WEIGHTS_MXFP4 = 0, 1              # values of MoeInfo.weight_format
 
 
 class MoeError(RuntimeError):
@@ -42,7 +43,8 @@ class MoeInfo(ctypes.Structure):
                 ("topk", ctypes.c_int), ("R", ctypes.c_int), ("max_tokens", ctypes.c_int),
                 ("pool_rows", ctypes.c_int), ("block_m", ctypes.c_int), ("block_n", ctypes.c_int),
                 ("num_sms", ctypes.c_int), ("workspace_bytes", ctypes.c_uint64),
-                ("weight_bytes", ctypes.c_uint64), ("n_shared", ctypes.c_int)]
+                ("weight_bytes", ctypes.c_uint64), ("n_shared", ctypes.c_int),
+                ("weight_format", ctypes.c_int)]
 
 
 def header_functions() -> list[str]:
@@ -73,6 +75,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         "moe_reserve": [H, I],
         "moe_load_weights": [H, P, P, P, P, P],
         "moe_load_shared_weights": [H, P, P, P, P, P],
+        "moe_load_weights_mxfp4": [H, P, P, P, P, P],
+        "moe_load_shared_weights_mxfp4": [H, P, P, P, P, P],
         "moe_forward": [H, I, P, P, P, P, P, P],
         "moe_forward_host": [H, I, P, P, P, P, P, P],
         "moe_forward_host_async": [H, I, P, P, P, P, P, P],
@@ -146,15 +150,40 @@ class FusedMoE:
                    "moe_load_shared_weights", w_gate_up, sf_gate_up, w_down, sf_down, stream)
         return self
 
-    def _load(self, fn, E, what, w_gate_up, sf_gate_up, w_down, sf_down, stream):
+    def load_weights_mxfp4(self, w_gate_up, sf_gate_up, w_down, sf_down, stream=None):
+        """MXFP4 weights: packed E2M1 uint8 [E, 2I, H/2] / [E, H, I/2] (element 2j in the low
+        nibble) with UE8M0 uint8 scales [E, 2I, H/32] / [E, H, I/32] (one per 32 elements)."""
+        self._load(self.lib.moe_load_weights_mxfp4, self.E, "moe_load_weights_mxfp4",
+                   w_gate_up, sf_gate_up, w_down, sf_down, stream, mxfp4=True)
+        return self
+
+    def load_shared_weights_mxfp4(self, w_gate_up, sf_gate_up, w_down, sf_down, stream=None):
+        self._load(self.lib.moe_load_shared_weights_mxfp4, self.n_shared or w_gate_up.shape[0],
+                   "moe_load_shared_weights_mxfp4", w_gate_up, sf_gate_up, w_down, sf_down, stream,
+                   mxfp4=True)
+        return self
+
+    def _load(self, fn, E, what, w_gate_up, sf_gate_up, w_down, sf_down, stream, mxfp4=False):
         import torch
         H, I = self.H, self.I
-        _expect(w_gate_up, (E, 2 * I, H), torch.uint8, "w_gate_up")
-        _expect(sf_gate_up, (E, 2 * I // 128, H // 128), torch.float32, "sf_gate_up")
-        _expect(w_down, (E, H, I), torch.uint8, "w_down")
-        _expect(sf_down, (E, H // 128, I // 128), torch.float32, "sf_down")
+        if mxfp4:
+            _expect(w_gate_up, (E, 2 * I, H // 2), torch.uint8, "w_gate_up")
+            _expect(sf_gate_up, (E, 2 * I, H // 32), torch.uint8, "sf_gate_up")
+            _expect(w_down, (E, H, I // 2), torch.uint8, "w_down")
+            _expect(sf_down, (E, H, I // 32), torch.uint8, "sf_down")
+        else:
+            _expect(w_gate_up, (E, 2 * I, H), torch.uint8, "w_gate_up")
+            _expect(sf_gate_up, (E, 2 * I // 128, H // 128), torch.float32, "sf_gate_up")
+            _expect(w_down, (E, H, I), torch.uint8, "w_down")
+            _expect(sf_down, (E, H // 128, I // 128), torch.float32, "sf_down")
         _check(fn(self.h, w_gate_up.data_ptr(), sf_gate_up.data_ptr(), w_down.data_ptr(),
                   sf_down.data_ptr(), _stream_handle(stream)), what)
+
+    def load(self, inp, stream=None):
+        """Weights of a workloads.Inputs in its format (FP8 or MXFP4)."""
+        if getattr(inp.wl, "weights", "fp8") == "mxfp4":
+            return self.load_weights_mxfp4(inp.w_gate_up, inp.sf_gate_up, inp.w_down, inp.sf_down, stream)
+        return self.load_weights(inp.w_gate_up, inp.sf_gate_up, inp.w_down, inp.sf_down, stream)
 
     def set_option(self, option: int, value: int):
         _check(self.lib.moe_set_option(self.h, option, value), "moe_set_option")

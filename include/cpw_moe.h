@@ -94,6 +94,34 @@ int moe_load_weights(moe_handle_t h, const uint8_t *w_gate_up, const float *sf_g
 int moe_load_shared_weights(moe_handle_t h, const uint8_t *w_gate_up, const float *sf_gate_up,
                             const uint8_t *w_down, const float *sf_down, void *stream);
 
+/* Weight formats (moe_info.weight_format). */
+enum moe_weight_format {
+    MOE_WEIGHTS_FP8 = 0,    /* e4m3 with fp32 128x128 block scales (moe_load_weights)     */
+    MOE_WEIGHTS_MXFP4 = 1   /* E2M1 with UE8M0 1x32 scales (moe_load_weights_mxfp4)       */
+};
+
+/* MXFP4 expert weights (FP8 activations x FP4 weights: the pages name an FP8 x FP4 variant
+ * of the SM100 kernel, "DeepGEMM Mega MoE 对称内存（Symmetric Memory）深度分析" §11, without
+ * its format; this is the OCP Microscaling MXFP4 block: 32 consecutive elements of a row
+ * share one power-of-two scale).
+ *   w_gate_up  [E][2I][H/2] bytes of packed E2M1 codes (element 2j in the low nibble of byte
+ *              j, element 2j+1 in the high nibble), rows 0..I-1 = gate, I..2I-1 = up
+ *   sf_gate_up [E][2I][H/32] UE8M0 bytes (scale 2^(b-127) of elements 32j..32j+31 of a row)
+ *   w_down     [E][H][I/2] packed E2M1
+ *   sf_down    [E][H][I/32] UE8M0
+ * Weight pointers 16-byte aligned, scale pointers 4-byte aligned.  The forward then runs the
+ * block-scaled UMMA with E2M1 weight operands; the activation scales (x_sf) must be powers of
+ * two, and MOE_OPT_SCALE_MODE 0 makes moe_forward return MOE_ERR_BAD_SCALE.  A scale byte
+ * 0xFF (NaN) makes this call return MOE_ERR_BAD_SCALE and leaves the weights unloaded.
+ * Routed and shared weights must be loaded in one format: until they are, moe_forward
+ * returns MOE_ERR_NO_WEIGHTS. */
+int moe_load_weights_mxfp4(moe_handle_t h, const uint8_t *w_gate_up, const uint8_t *sf_gate_up,
+                           const uint8_t *w_down, const uint8_t *sf_down, void *stream);
+
+/* The n_shared shared experts' weights as MXFP4, layouts as moe_load_weights_mxfp4. */
+int moe_load_shared_weights_mxfp4(moe_handle_t h, const uint8_t *w_gate_up, const uint8_t *sf_gate_up,
+                                  const uint8_t *w_down, const uint8_t *sf_down, void *stream);
+
 /* The layer on T tokens (0 <= T <= max_tokens, T % R == 0; source r owns tokens
  * [r*T/R, (r+1)*T/R)).  Asynchronous on `stream`.
  *   x        [T][H] e4m3            x_sf [T][H/128] fp32 (1x128 activation scales)
@@ -166,6 +194,7 @@ typedef struct moe_info {
     int n_shared;         /* shared experts; E and topk above include them: shared expert s
                              is expert slot E - n_shared + s and combine plane
                              topk - n_shared + s (the debug buffers use these sizes) */
+    int weight_format;    /* moe_weight_format of the routed weights last loaded          */
 } moe_info;
 int moe_get_info(moe_handle_t h, moe_info *info);
 

@@ -1,6 +1,9 @@
 import os
 import sys
 
+import numpy as np
+import torch
+
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -30,3 +33,31 @@ def oracle_mod():
     import oracle
     oracle.lib()
     return oracle
+
+
+# OCP Microscaling Formats (MX) v1.0, FP4 E2M1 element: the eight magnitudes of codes 0..7
+# (bit 3 is the sign); E8M0 scale bytes are 2^(b-127) with 0xFF = NaN.
+OCP_E2M1 = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+
+
+def fp8_twin_of_mxfp4(packed, sf):
+    """An FP8 weight with the same element values as an MXFP4 one ([N][K/2] packed, [N][K/32]
+    E8M0): per 128x128 block the scale 2^m with m the block's smallest scale exponent, and
+    e4m3 codes (torch's cast) of value / 2^m, exact while each block's exponents span <= 6."""
+    p = packed.numpy().astype(np.int64)
+    N = p.shape[0]
+    codes = np.empty((N, 2 * p.shape[1]), np.int64)
+    codes[:, 0::2] = p & 0xF
+    codes[:, 1::2] = p >> 4
+    mags = np.array(OCP_E2M1)
+    val = np.where(codes >= 8, -mags[codes & 7], mags[codes & 7])
+    ex = sf.numpy().astype(np.int64) - 127                       # [N][K/32]
+    val = val * np.ldexp(1.0, np.repeat(ex, 32, axis=1))
+    K = val.shape[1]
+    m = ex.reshape(N // 128, 128, K // 128, 4).min(axis=(1, 3))   # [N/128][K/128]
+    assert (ex.reshape(N // 128, 128, K // 128, 4).max(axis=(1, 3)) - m).max() <= 6
+    scale = np.ldexp(1.0, m).astype(np.float32)
+    q = val / np.kron(scale.astype(np.float64), np.ones((128, 128)))
+    c8 = torch.from_numpy(q).to(torch.float8_e4m3fn)
+    assert np.array_equal(c8.to(torch.float64).numpy(), q)        # exact twin
+    return c8.view(torch.uint8), torch.from_numpy(scale)

@@ -11,7 +11,7 @@ import numpy as np
 import pytest
 import torch
 
-from conftest import golden
+from conftest import OCP_E2M1, fp8_twin_of_mxfp4, golden
 
 pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
 
@@ -364,9 +364,6 @@ def test_forward_tiny_matches_independent_numpy_restatement(oracle_mod):
 
 
 # ------------------------------------------------------------------ MXFP4 weights ----
-# OCP Microscaling Formats (MX) v1.0, FP4 E2M1 element: the eight magnitudes of codes 0..7
-# (bit 3 is the sign), and E8M0 scale bytes 2^(b-127) with 0xFF = NaN.
-OCP_E2M1 = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
 
 
 def test_e2m1_decode_all_codes(oracle_mod):
@@ -380,29 +377,6 @@ def test_e8m0_decode(oracle_mod):
     b = np.array([0, 1, 100, 126, 127, 128, 200, 254], np.uint8)
     assert np.array_equal(oracle_mod.e8m0_decode(b), np.ldexp(1.0, b.astype(int) - 127))
     assert np.isnan(oracle_mod.e8m0_decode(np.array([255], np.uint8))[0])
-
-
-def _fp8_twin_of_mxfp4(packed, sf):
-    """An FP8 weight with the same element values as an MXFP4 one ([N][K/2] packed, [N][K/32]
-    E8M0): per 128x128 block the scale 2^m with m the block's smallest scale exponent, and
-    e4m3 codes (torch's cast) of value / 2^m, exact while each block's exponents span <= 6."""
-    p = packed.numpy().astype(np.int64)
-    N = p.shape[0]
-    codes = np.empty((N, 2 * p.shape[1]), np.int64)
-    codes[:, 0::2] = p & 0xF
-    codes[:, 1::2] = p >> 4
-    mags = np.array(OCP_E2M1)
-    val = np.where(codes >= 8, -mags[codes & 7], mags[codes & 7])
-    ex = sf.numpy().astype(np.int64) - 127                       # [N][K/32]
-    val = val * np.ldexp(1.0, np.repeat(ex, 32, axis=1))
-    K = val.shape[1]
-    m = ex.reshape(N // 128, 128, K // 128, 4).min(axis=(1, 3))   # [N/128][K/128]
-    assert (ex.reshape(N // 128, 128, K // 128, 4).max(axis=(1, 3)) - m).max() <= 6
-    scale = np.ldexp(1.0, m).astype(np.float32)
-    q = val / np.kron(scale.astype(np.float64), np.ones((128, 128)))
-    c8 = torch.from_numpy(q).to(torch.float8_e4m3fn)
-    assert np.array_equal(c8.to(torch.float64).numpy(), q)        # exact twin
-    return c8.view(torch.uint8), torch.from_numpy(scale)
 
 
 def _mxfp4_case(E=3, H=256, I=128, seed=5, span=4):
@@ -422,8 +396,8 @@ def test_mxfp4_layer_equals_its_fp8_twin(oracle_mod):
     from combine_persistent_warp_gb300 import workloads as W
     E, H, I, T, k = 3, 256, 128, 12, 2
     w1, s1, w2, s2 = _mxfp4_case(E, H, I)
-    t1 = [_fp8_twin_of_mxfp4(w1[e], s1[e]) for e in range(E)]
-    t2 = [_fp8_twin_of_mxfp4(w2[e], s2[e]) for e in range(E)]
+    t1 = [fp8_twin_of_mxfp4(w1[e], s1[e]) for e in range(E)]
+    t2 = [fp8_twin_of_mxfp4(w2[e], s2[e]) for e in range(E)]
     f1, g1 = torch.stack([a for a, _ in t1]), torch.stack([b for _, b in t1])
     f2, g2 = torch.stack([a for a, _ in t2]), torch.stack([b for _, b in t2])
     idx, w = W.make_routing(T, E, k, seed=3)

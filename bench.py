@@ -45,10 +45,12 @@ PROFILE_EVERY = 8            # timed steps per step carrying the per-kernel stag
 # DRAM bytes per launch from one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum),
 # valid only while the kernel sources hash to `src_sha`; see profiles/.
 NCU_TRAFFIC = {
-    ("decode", "expert_ffn"): {"bytes": 1425283072 + 14444800, "src_sha": "59a1f06def27fd31"},
-    ("prefill", "expert_ffn"): {"bytes": 1877737216 + 533531904, "src_sha": "59a1f06def27fd31"},
-    ("decode-pow2", "expert_ffn"): {"bytes": 1431478016 + 3511296, "src_sha": "31f7f51a2a16ad06"},
-    ("prefill-pow2", "expert_ffn"): {"bytes": 2117926912 + 514405632, "src_sha": "31f7f51a2a16ad06"},
+    ("decode", "expert_ffn"): {"bytes": 1425256448 + 14529792, "src_sha": "fbc87d810249e61e"},
+    ("prefill", "expert_ffn"): {"bytes": 1892651264 + 534686208, "src_sha": "fbc87d810249e61e"},
+    ("decode-pow2", "expert_ffn"): {"bytes": 1431475200 + 3602944, "src_sha": "471a697d4cd814f3"},
+    ("prefill-pow2", "expert_ffn"): {"bytes": 2108371200 + 514178816, "src_sha": "471a697d4cd814f3"},
+    ("decode-mxfp4", "expert_ffn"): {"bytes": 759860224 + 3274752, "src_sha": "471a697d4cd814f3"},
+    ("prefill-mxfp4", "expert_ffn"): {"bytes": 1060229888 + 511471872, "src_sha": "471a697d4cd814f3"},
 }
 # sources each stage's kernel is compiled from (a recorded traffic figure is used only while
 # these hash to its `src_sha`)
@@ -212,8 +214,13 @@ def work_model(inp) -> dict:
     idx = inp.topk_idx
     M = int((idx >= 0).sum().item())
     touched = int(torch.unique(idx[idx >= 0]).numel())
-    w1 = touched * (2 * I * H + (2 * I // 128) * (H // 128) * 4)
-    w2 = touched * (H * I + (H // 128) * (I // 128) * 4)
+    if getattr(wl, "weights", "fp8") == "mxfp4":
+        # packed E2M1 (half a byte per element) + one UE8M0 byte per 32 elements
+        w1 = touched * (2 * I * H // 2 + 2 * I * H // 32)
+        w2 = touched * (H * I // 2 + H * I // 32)
+    else:
+        w1 = touched * (2 * I * H + (2 * I // 128) * (H // 128) * 4)
+        w2 = touched * (H * I + (H // 128) * (I // 128) * 4)
     x_rows = M * (H + (H // 128) * 4)            # gathered activation rows + scales
     act_rows = M * (I + (I // 128) * 4)
     # expert_ffn = gate_up GEMM (W1, gathered rows in, SwiGLU rows out) + down GEMM (W2,
@@ -249,7 +256,8 @@ def roofline_for(stage: str, avg_s: float, model: dict, workload: str) -> dict:
     fp8_peak = pk["bf16_tflops"] * FP8_OVER_BF16
     t_tensor = flops / (fp8_peak * 1e12) if flops else 0.0
     traffic = None
-    src_key = "expert_ffn_bs" if stage == "expert_ffn" and workload.endswith("-pow2") else stage
+    block_scaled = workload.endswith("-pow2") or workload.endswith("-mxfp4")
+    src_key = "expert_ffn_bs" if stage == "expert_ffn" and block_scaled else stage
     rec = NCU_TRAFFIC.get((workload, stage))
     if rec and rec.get("src_sha") == kernel_sources_sha(src_key):
         traffic = rec["bytes"]
@@ -316,7 +324,7 @@ def run_ours(args, dist: Dist) -> dict | None:
     model = work_model(inp)
     M = model["M"]
     moe = FusedMoE(wl.E, wl.H, wl.I, wl.topk, wl.R).reserve(wl.T)
-    moe.load_weights(inp.w_gate_up, inp.sf_gate_up, inp.w_down, inp.sf_down)
+    moe.load(inp)   # FP8 or MXFP4 weights, by the workload
     from combine_persistent_warp_gb300 import native
     if args.ffn_mode:
         moe.set_option(native.OPT_FFN_MODE, args.ffn_mode)
@@ -396,9 +404,11 @@ def run_ours(args, dist: Dist) -> dict | None:
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": dist.world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_max / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "fp8e4m3 (fp32 accumulate, bf16 out)", "data": "synthetic",
+        "dtype": ("fp8e4m3 x e2m1 (MXFP4 weights; fp32 accumulate, bf16 out)" if wl.weights == "mxfp4"
+                  else "fp8e4m3 (fp32 accumulate, bf16 out)"), "data": "synthetic",
         "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E,
                    "topk": wl.topk, "R": wl.R, "routing": wl.routing, "scales": wl.scales,
+                   "weights": wl.weights,
                    "routed_rows_per_step": M, "parallelism": f"replicas x{dist.world}",
                    "l2": ("inputs larger than L2: %.2f GB of expert weights streamed per step, "
                           "no flush" % (model["weight_bytes"] / 1e9))},
@@ -491,7 +501,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--workload", default="decode",
                     help="tiny, decode, prefill, skewed, large, or one of them with -pow2 "
-                         "(power-of-two scales: the block-scaled UMMA path)")
+                         "(power-of-two scales: the block-scaled UMMA path) or -mxfp4 (MXFP4 "
+                         "weights on the block-scaled path)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=300)
     ap.add_argument("--cpu-tokens", type=int, default=128)

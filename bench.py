@@ -486,7 +486,9 @@ def run_reference(args, dist: Dist) -> dict | None:
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "impl": "reference",
         "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E,
-                   "topk": wl.topk, "R": wl.R, "routing": wl.routing, "parallelism": "host cores"},
+                   "topk": wl.topk, "R": wl.R, "routing": wl.routing, "scales": wl.scales,
+                   "weights": wl.weights, "routed_rows_per_step": int(len(valid)),
+                   "parallelism": "host cores"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},

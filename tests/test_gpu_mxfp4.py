@@ -72,6 +72,9 @@ CASES = {
                         weights="mxfp4"), 16),
     "prefill": (Workload("mx-prefill", T=4096, H=7168, I=2048, E=32, topk=8, R=8, seed=2, scales="pow2",
                          weights="mxfp4"), 10),
+    # the skewed (Zipf, 5% skipped slots, 64 experts) and large (128 experts) batches
+    "skewed": ("skewed-mxfp4", 10),
+    "large": ("large-mxfp4", 10),
 }
 
 
@@ -79,6 +82,7 @@ CASES = {
 def test_mxfp4_matches_oracle(case):
     wl, n = CASES[case]
     moe, inp = mx_layer(wl)
+    wl = inp.wl
     out = moe.forward(inp.x, inp.x_sf, inp.topk_idx, inp.topk_w)
     torch.cuda.synchronize()
     assert moe.get_error() == 0

@@ -17,7 +17,8 @@ Pins (what ties each function to something other than itself) are in
   * expert FFN        -- single expert, k=1, w=1 reduces to a dense FFN checked against
                          numpy matmuls + torch FP8 casts; zero down weights; identical
                          experts; linearity in the gate weights
-  * combine           -- closed form 0.73*E2(T0) + 0.27*E7(T0)
+  * combine           -- closed form 0.73*E2(T0) + 0.27*E7(T0); the bf16-plane diagnostic
+                         mode against numpy (bf16 casts by torch) on the per-slot outputs
   * power-of-two scale rule -- closed forms (exact powers, neighbours), the defining
                          inequalities sf/2 < q <= sf, and the requantised stage against
                          numpy with the rule applied by exponent arithmetic
@@ -64,6 +65,8 @@ def lib():
         L.orc_expert_ffn.argtypes = [ctypes.c_int, ctypes.c_int] + [P] * 9
         L.orc_set_scale_rule.argtypes = [ctypes.c_int]
         L.orc_set_scale_rule.restype = None
+        L.orc_set_plane_bf16.argtypes = [ctypes.c_int]
+        L.orc_set_plane_bf16.restype = None
         L.orc_pow2_ceil.argtypes = [ctypes.c_float]
         L.orc_pow2_ceil.restype = ctypes.c_float
         L.orc_forward_tokens.restype = ctypes.c_int
@@ -190,6 +193,13 @@ def set_scale_rule(rule: str):
     if rule not in ("fp32", "pow2"):
         raise ValueError(rule)
     lib().orc_set_scale_rule(1 if rule == "pow2" else 0)
+
+
+def set_plane_bf16(on: bool):
+    """Diagnostic combine: each slot's weighted output rounded to a bf16 plane value, planes
+    summed in fp32 ascending k (as the bf16 combine buffer + fp32 reduce do); default off:
+    the top-k sum kept in double."""
+    lib().orc_set_plane_bf16(1 if on else 0)
 
 
 def pow2_ceil(v: float) -> float:

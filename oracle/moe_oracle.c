@@ -356,6 +356,22 @@ void orc_expert_ffn(int H, int I, const uint8_t *x, const float *xsf,
 
 /* ------------------------------------------------------------------ layer ---------- */
 
+/* Diagnostic combine mode ([SYM] §8.2 keeps the per-slot combine planes in bf16): when set,
+ * each slot's weighted expert output is rounded to fp32 and then to bf16 (one plane value),
+ * and the planes are summed in fp32 in ascending k, as a bf16 combine buffer followed by an
+ * fp32 reduce computes it.  Off (default): the sum of w_k * y_k is kept in double.  Set
+ * before calling the numerics (not thread-safe). */
+static int g_plane_bf16 = 0;
+void orc_set_plane_bf16(int on) { g_plane_bf16 = on != 0; }
+
+static inline float bf16_bits_value(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return f;
+}
+
 /* The layer on a list of tokens: out[t] = bf16( sum over k ascending of w[t,k] *
  * Expert_{idx[t,k]}(x[t]) ), skipping idx == -1; a token with no valid slot gives 0
  * ([DC] §1: Output(T) = sum_k w_k * Expert_k(T)).  out_bf16 [ntok][H] receives the bf16
@@ -384,6 +400,7 @@ int orc_forward_tokens_fmt(int wfmt, int T, int H, int I, int E, int k,
     for (int i = 0; i < ntok; ++i) {
         const int t = tokens[i];
         double *acc = (double *)calloc((size_t)H, sizeof(double));
+        float *accf = (float *)calloc((size_t)H, sizeof(float));
         double *y = (double *)malloc(sizeof(double) * (size_t)H);
         for (int kk = 0; kk < k; ++kk) {
             int64_t e = idx[(int64_t)t * k + kk];
@@ -397,16 +414,22 @@ int orc_forward_tokens_fmt(int wfmt, int T, int H, int I, int E, int k,
                                w1 + e * w1e, (const char *)s1 + e * s1e * ssz,
                                w2 + e * w2e, (const char *)s2 + e * s2e * ssz, y, NULL, NULL);
             const double wk = (double)w[(int64_t)t * k + kk];
-            for (int c = 0; c < H; ++c)
-                acc[c] += wk * y[c];
+            if (g_plane_bf16) {
+                for (int c = 0; c < H; ++c)
+                    accf[c] += bf16_bits_value(orc_bf16_rne((float)(wk * y[c])));
+            } else {
+                for (int c = 0; c < H; ++c)
+                    acc[c] += wk * y[c];
+            }
         }
         for (int c = 0; c < H; ++c) {
-            float f = (float)acc[c];
+            float f = g_plane_bf16 ? accf[c] : (float)acc[c];
             out_bf16[(int64_t)i * H + c] = orc_bf16_rne(f);
             if (out_f32)
                 out_f32[(int64_t)i * H + c] = f;
         }
         free(acc);
+        free(accf);
         free(y);
     }
     return bad;

@@ -444,3 +444,32 @@ def test_mxfp4_single_element_weights(oracle_mod):
     want = np.zeros(H)
     want[r0] = hd * -3.0 * 2.0
     assert np.allclose(y, want, rtol=0, atol=1e-12) and y[r0] != 0
+
+
+def test_bf16_plane_mode_matches_numpy_restatement(oracle_mod):
+    """Diagnostic combine mode: out[t] = bf16(fp32 sum over ascending k of bf16(fp32(w_k y_k)))
+    with y_k the (pinned) expert outputs; restated with torch's bf16 casts and numpy fp32
+    adds, bit for bit, on the tiny batch (skipped slots included)."""
+    from combine_persistent_warp_gb300.workloads import Workload, make_inputs
+    inp = make_inputs(Workload("plane", T=16, H=256, I=128, E=4, topk=3, R=2, seed=21, skip_frac=0.1))
+    h = oracle_mod.HostInputs.from_inputs(inp)
+    oracle_mod.set_plane_bf16(True)
+    try:
+        bits, out32, _ = oracle_mod.forward_tokens(h, np.arange(h.T))
+    finally:
+        oracle_mod.set_plane_bf16(False)
+    to_bf16 = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(torch.bfloat16).float().numpy()
+    for t in range(h.T):
+        acc = np.zeros(h.H, np.float32)
+        for kk in range(h.k):
+            e = int(h.idx[t, kk])
+            if e < 0:
+                continue
+            y, _, _ = oracle_mod.expert_ffn(h.x[t], h.x_sf[t], h.w1[e], h.s1[e], h.w2[e], h.s2[e])
+            acc = (acc + to_bf16((np.float64(h.w[t, kk]) * y).astype(np.float32))).astype(np.float32)
+        want = torch.from_numpy(acc).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+        assert np.array_equal(bits[t], want), t
+        assert np.array_equal(out32[t], acc), t
+    # default mode unchanged: the double sum
+    b2, o2, _ = oracle_mod.forward_tokens(h, np.arange(h.T))
+    assert not np.array_equal(o2, out32)

@@ -53,7 +53,9 @@ enum moe_status {
     MOE_ERR_SLOT_OVERFLOW = 8,      /* device: > T/R rows of one source for one expert */
     MOE_ERR_NOT_RESERVED = 9,       /* forward before moe_reserve                      */
     MOE_ERR_BAD_SCALE = 10          /* block-scaled mode: a weight scale (at the forward) or
-                                       an activation scale (device) is not a power of two */
+                                       an activation scale (device) is not a power of two;
+                                       MXFP4 weights: a NaN scale byte (at load), or a forward
+                                       forced to the fp32-scale kernel */
 };
 
 /* Create a layer for E experts, hidden size H, expert intermediate size I, top-k, and R

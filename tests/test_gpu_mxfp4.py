@@ -228,3 +228,21 @@ def test_mxfp4_errors():
     # shape checks of the binding
     with pytest.raises(ValueError):
         moe.load_weights_mxfp4(inp.w_gate_up[:, :, :-16].contiguous(), inp.sf_gate_up, inp.w_down, inp.sf_down)
+
+
+def test_mxfp4_host_buffers_match_device_forward():
+    """The host-buffer entry points (pinned inputs, synchronous and asynchronous) give the same
+    bits as the device-pointer forward with MXFP4 weights."""
+    wl = Workload("mx-host", T=256, H=512, I=256, E=8, topk=4, R=4, seed=69, scales="pow2", weights="mxfp4")
+    moe, inp = mx_layer(wl)
+    dev = moe.forward(inp.x, inp.x_sf, inp.topk_idx, inp.topk_w).clone()
+    torch.cuda.synchronize()
+    pin = lambda t: t.cpu().pin_memory()
+    px, psf, pidx, pw = pin(inp.x), pin(inp.x_sf), pin(inp.topk_idx), pin(inp.topk_w)
+    host = moe.forward_host(px, psf, pidx, pw)
+    o_async = torch.empty(wl.T, wl.H, dtype=torch.bfloat16).pin_memory()
+    moe.forward_host(px, psf, pidx, pw, out=o_async, wait=False)
+    torch.cuda.synchronize()
+    assert moe.get_error() == 0
+    assert torch.equal(host.view(torch.int16), dev.cpu().view(torch.int16))
+    assert torch.equal(o_async.view(torch.int16), dev.cpu().view(torch.int16))

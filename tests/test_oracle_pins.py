@@ -473,3 +473,50 @@ def test_bf16_plane_mode_matches_numpy_restatement(oracle_mod):
     # default mode unchanged: the double sum
     b2, o2, _ = oracle_mod.forward_tokens(h, np.arange(h.T))
     assert not np.array_equal(o2, out32)
+
+
+def _mxfp4_dequant(packed, sf):
+    """[N][K/2] packed E2M1 + [N][K/32] E8M0 -> float64 [N][K] from the OCP element table."""
+    p = packed.numpy().astype(np.int64)
+    codes = np.empty((p.shape[0], 2 * p.shape[1]), np.int64)
+    codes[:, 0::2], codes[:, 1::2] = p & 0xF, p >> 4
+    mags = np.array(OCP_E2M1)
+    v = np.where(codes >= 8, -mags[codes & 7], mags[codes & 7])
+    return v * np.ldexp(1.0, np.repeat(sf.numpy().astype(np.int64) - 127, 32, axis=1))
+
+
+def test_forward_tiny_mxfp4_matches_independent_numpy_restatement(oracle_mod):
+    """The tiny batch with MXFP4 weights (generator's OCP conversion) against a second
+    restatement: OCP-table dequantisation, numpy fp64 matmuls, torch FP8 casts for the
+    power-of-two requant, the top-k sum in fp32 ascending k."""
+    from combine_persistent_warp_gb300.workloads import make_inputs
+    inp = make_inputs("tiny-mxfp4")
+    h = oracle_mod.HostInputs.from_inputs(inp)
+    assert h.weights == "mxfp4"
+    oracle_mod.set_scale_rule("pow2")
+    try:
+        bits, out32, bad = oracle_mod.forward_tokens(h, np.arange(h.T))
+    finally:
+        oracle_mod.set_scale_rule("fp32")
+    assert not bad
+    I = h.I
+    W1 = [_mxfp4_dequant(inp.w_gate_up[e], inp.sf_gate_up[e]) for e in range(h.E)]
+    W2 = [_mxfp4_dequant(inp.w_down[e], inp.sf_down[e]) for e in range(h.E)]
+    ref = np.zeros((h.T, h.H), np.float32)
+    for t in range(h.T):
+        dx = _dequant(inp.x[t][None, :], inp.x_sf[t][None, :], 1, 128)[0]
+        acc = np.zeros(h.H, np.float32)
+        for kk in range(h.k):
+            e = int(h.idx[t, kk])
+            if e < 0:
+                continue
+            gu = W1[e] @ dx
+            hv = (gu[:I] / (1.0 + np.exp(-gu[:I])) * gu[I:]).astype(np.float32).reshape(-1, 128)
+            sf = _np_pow2_ceil(np.maximum(np.abs(hv).max(axis=1), np.float32(1e-4)) / np.float32(448.0))
+            q = torch_e4m3_encode(hv / sf[:, None])
+            hd = (torch_e4m3_value(q) * sf[:, None].astype(np.float64)).reshape(-1)
+            y = (W2[e] @ hd).astype(np.float32)
+            acc = (acc + np.float32(h.w[t, kk]) * y).astype(np.float32)
+        ref[t] = acc
+    rel = np.linalg.norm(out32 - ref, axis=1) / np.maximum(np.linalg.norm(ref, axis=1), 1e-30)
+    assert rel.max() <= 1e-3

@@ -48,3 +48,30 @@ def test_host_side_argument_checks_need_no_gpu():
     st = ctypes.c_int()
     assert lib.moe_get_error(None, ctypes.byref(st)) == 1
     assert lib.moe_destroy(None) == 1
+
+
+def _header_enum_values():
+    """NAME = value pairs of the header's enums (comments stripped)."""
+    import re
+    text = open(native.HEADER, encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return {m.group(1): int(m.group(2)) for m in re.finditer(r"\b(MOE_[A-Z0-9_]+)\s*=\s*(\d+)", text)}
+
+
+def test_binding_constants_match_the_header():
+    v = _header_enum_values()
+    for code, name in native.STATUS.items():
+        assert v[name] == code, name
+    assert v["MOE_OPT_TIMEOUT_NS"] == native.OPT_TIMEOUT_NS
+    assert v["MOE_OPT_DEBUG_SKIP_BARRIER"] == native.OPT_DEBUG_SKIP_BARRIER
+    assert v["MOE_OPT_FFN_MODE"] == native.OPT_FFN_MODE
+    assert v["MOE_OPT_SCALE_MODE"] == native.OPT_SCALE_MODE
+    assert v["MOE_WEIGHTS_FP8"] == native.WEIGHTS_FP8 and v["MOE_WEIGHTS_MXFP4"] == native.WEIGHTS_MXFP4
+    for name, idx in native.BUFFERS.items():
+        assert v["MOE_BUF_" + name.upper()] == idx
+
+
+def test_mxfp4_loaders_refuse_null_handles_without_a_gpu():
+    lib = native.load()
+    assert lib.moe_load_weights_mxfp4(None, None, None, None, None, None) == 1
+    assert lib.moe_load_shared_weights_mxfp4(None, None, None, None, None, None) == 1

@@ -2,18 +2,22 @@
 """Benchmark of the fused FP8 MoE layer on GB300.
 
 One step = one forward of the whole layer (routing, gather, gate_up GEMM + SwiGLU +
-requant, down GEMM + weighted scatter, combine) over one synthetic batch.  The default
-workload is the decode batch: T=128 tokens, H=7168, I=2048, E=32, topk=8, R=8, uniform
-routing, FP8 e4m3 activations and weights with fp32 block scales.
+requant, down GEMM + weighted scatter, combine) over one synthetic batch.  The headline
+workload is the largest single-GPU batch: T=16384 tokens, H=4096, I=1536, E=128, topk=8,
+R=8, uniform routing, FP8 e4m3 activations and weights with fp32 block scales.  The same
+run also times the other batch shapes (tiny, decode, prefill, skewed) and reports them
+under ``per_config``.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
 Prints ONE JSON line.  ``value`` is routed (token, slot) rows per second of the whole
 job with inputs resident in HBM, timed with CUDA events on the forward's stream; ``e2e``
-is the same metric through ``moe_forward_host`` (pinned host buffers, copies inside the
-timed region).  ``roofline`` covers the dominant kernel, timed live with CUDA events the
-library records around each of its kernels.  ``--impl reference`` times the plain CPU
-oracle on a bounded sample of the same workload instead (the reference arm).
+is the same metric through ``moe_forward_host_async`` (pinned host buffers, copies inside
+the timed region).  ``roofline`` covers the dominant kernel, timed live with CUDA events the
+library records around each of its kernels; its tensor peak is the larger of a dense FP8
+GEMM measured at the start of the run and the measured bf16 peak times the nominal FP8/bf16
+ratio.  ``--impl reference`` times the plain CPU oracle on a bounded sample of the same
+workload instead (the reference arm).
 Several GPUs run independent replicas (the layer is single-GPU): ``value`` sums the rows
 of all ranks over the slowest rank's time.
 """
@@ -207,7 +211,12 @@ def gpu_query_id(torch, dev: int) -> str:
 
 # ------------------------------------------------------------------ work model ----
 def work_model(inp) -> dict:
-    """Algorithmic bytes and FLOPs of each stage for one forward (valid rows only)."""
+    """Algorithmic bytes and FLOPs of one forward (valid rows only).
+
+    compulsory_bytes: what the layer must move at least once (the expert weights and scales
+    of the experts the batch touches, x and its scales, the routing ids and gate weights, the
+    bf16 output); intermediate_bytes: what this design writes and reads back on the way (the
+    gathered pool, the SwiGLU rows, the bf16 combine planes)."""
     import torch
     wl = inp.wl
     T, H, I, E, K = wl.T, wl.H, wl.I, wl.E, wl.topk
@@ -223,17 +232,18 @@ def work_model(inp) -> dict:
         w2 = touched * (H * I + (H // 128) * (I // 128) * 4)
     x_rows = M * (H + (H // 128) * 4)            # gathered activation rows + scales
     act_rows = M * (I + (I // 128) * 4)
-    # expert_ffn = gate_up GEMM (W1, gathered rows in, SwiGLU rows out) + down GEMM (W2,
-    # SwiGLU rows in, weighted bf16 rows out); one kernel
+    compulsory = w1 + w2 + T * (H + (H // 128) * 4) + T * K * 12 + T * H * 2
+    intermediate = 2 * x_rows + 2 * act_rows + 2 * M * H * 2 + M * 12
     st = {
         "dispatch": {"bytes": T * K * 8 + 2 * x_rows + M * (12 + 8), "flops": 0},
+        # gate_up GEMM + SwiGLU + down GEMM + weighted scatter (one kernel): weights, the
+        # gathered rows in, the SwiGLU rows out and back in, the bf16 planes out
         "expert_ffn": {"bytes": w1 + w2 + x_rows + 2 * act_rows + M * H * 2 + M * 16,
                        "flops": 2 * M * H * 2 * I + 2 * M * I * H},
         "combine": {"bytes": M * H * 2 + T * H * 2 + T * K * 8, "flops": M * H},
     }
-    compulsory = (w1 + w2 + T * (H + (H // 128) * 4) + T * K * 12 + T * H * 2)
     return {"M": M, "touched_experts": touched, "stages": st, "compulsory_bytes": compulsory,
-            "flops": 6 * M * H * I, "weight_bytes": w1 + w2}
+            "intermediate_bytes": intermediate, "flops": 6 * M * H * I, "weight_bytes": w1 + w2}
 
 
 def peaks() -> tuple[dict, str]:
@@ -247,13 +257,53 @@ def peaks() -> tuple[dict, str]:
                 "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
-def roofline_for(stage: str, avg_s: float, model: dict, workload: str) -> dict:
+def measure_fp8_gemm_tflops(dev, n: int = 8192, reps: int = 10) -> float | None:
+    """Dense FP8 e4m3 GEMM n x n x n through cuBLAS (torch._scaled_mm, bf16 out), best of
+    `reps` CUDA-event-timed calls after a warm-up; TFLOP/s, or None where unavailable."""
+    import torch
+    try:
+        a = torch.randn(n, n, device=dev).to(torch.float8_e4m3fn)
+        b = torch.randn(n, n, device=dev).to(torch.float8_e4m3fn).t()   # column-major operand
+        one = torch.ones((), device=dev)
+        mm = lambda: torch._scaled_mm(a, b, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+        for _ in range(3):
+            mm()
+        torch.cuda.synchronize(dev)
+        best = float("inf")
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            mm()
+            e1.record()
+            e1.synchronize()
+            best = min(best, e0.elapsed_time(e1) / 1e3)
+        del a, b
+        torch.cuda.empty_cache()
+        return 2.0 * n ** 3 / best / 1e12
+    except Exception:
+        return None
+
+
+def tensor_peak(fp8_measured: float | None) -> tuple[float, str]:
+    """FP8 tensor denominator: the larger of the measured dense FP8 GEMM and the measured bf16
+    burst peak times the nominal FP8/bf16 ratio (the larger one never flatters a fraction)."""
+    pk, src = peaks()
+    via_bf16 = pk["bf16_tflops"] * FP8_OVER_BF16
+    if fp8_measured is not None and fp8_measured > via_bf16:
+        return fp8_measured, "measured dense FP8 GEMM (torch._scaled_mm 8192^3, best of 10)"
+    return via_bf16, f"{src} bf16 burst x {FP8_OVER_BF16} (nominal fp8/bf16)"
+
+
+def roofline_for(stage: str, avg_s: float, model: dict, workload: str, fp8_measured: float | None) -> dict:
+    """Roofline of the dominant kernel.  HBM-bound shapes count the layer's compulsory bytes
+    (all of them pass through this kernel or its neighbours once; the intermediates of the
+    design are reported beside them, not counted); tensor-bound shapes count 6*M*H*I."""
     pk, src = peaks()
     st = model["stages"][stage]
-    bytes_ = st["bytes"]
     flops = st["flops"]
+    bytes_ = model["compulsory_bytes"] if stage == "expert_ffn" else st["bytes"]
+    fp8_peak, fp8_src = tensor_peak(fp8_measured)
     t_hbm = bytes_ / (pk["hbm_gbs"] * 1e9)
-    fp8_peak = pk["bf16_tflops"] * FP8_OVER_BF16
     t_tensor = flops / (fp8_peak * 1e12) if flops else 0.0
     traffic = None
     block_scaled = workload.endswith("-pow2") or workload.endswith("-mxfp4")
@@ -261,17 +311,31 @@ def roofline_for(stage: str, avg_s: float, model: dict, workload: str) -> dict:
     rec = NCU_TRAFFIC.get((workload, stage))
     if rec and rec.get("src_sha") == kernel_sources_sha(src_key):
         traffic = rec["bytes"]
+    common = {"kernel": stage, "kernel_fn": KERNEL_FN.get(src_key, stage), "traffic": traffic,
+              "avg_launch_us": avg_s * 1e6}
     if t_tensor > t_hbm and flops:
         achieved = flops / avg_s / 1e12
-        return {"bound": "tensor", "kernel": stage, "kernel_fn": KERNEL_FN.get(src_key, stage),
-                "achieved": achieved, "peak": fp8_peak,
-                "unit": "TFLOP/s", "frac": achieved / fp8_peak, "traffic": traffic,
-                "algorithmic_flops": flops, "peak_source": f"{src} bf16 x {FP8_OVER_BF16} (fp8/bf16 nominal)"}
+        return {"bound": "tensor", "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
+                "frac": achieved / fp8_peak, "algorithmic_flops": flops, "peak_source": fp8_src,
+                "fp8_gemm_measured_tflops": fp8_measured,
+                "bf16_x2_tflops": pk["bf16_tflops"] * FP8_OVER_BF16, "nominal_fp8_tflops": 4500.0,
+                **common}
     achieved = bytes_ / avg_s / 1e9
-    return {"bound": "hbm", "kernel": stage, "kernel_fn": KERNEL_FN.get(src_key, stage),
-            "achieved": achieved, "peak": pk["hbm_gbs"],
-            "unit": "GB/s", "frac": achieved / pk["hbm_gbs"], "traffic": traffic,
-            "algorithmic_bytes": bytes_, "peak_source": f"{src} (hbm_gbs, copy bandwidth)"}
+    return {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+            "frac": achieved / pk["hbm_gbs"], "algorithmic_bytes": bytes_,
+            "kernel_bytes_with_intermediates": st["bytes"],
+            "peak_source": f"{src} (hbm_gbs, copy bandwidth)", **common}
+
+
+def layer_roofline(model: dict, step_s: float, fp8_measured: float | None) -> dict:
+    """The whole step against t_roof = max(FLOPs / FP8 peak, compulsory bytes / HBM)."""
+    pk, _ = peaks()
+    fp8_peak, _ = tensor_peak(fp8_measured)
+    t_t = model["flops"] / (fp8_peak * 1e12)
+    t_b = model["compulsory_bytes"] / (pk["hbm_gbs"] * 1e9)
+    return {"t_roof_us": max(t_t, t_b) * 1e6, "bound": "tensor" if t_t > t_b else "hbm",
+            "frac": max(t_t, t_b) / step_s, "compulsory_bytes": model["compulsory_bytes"],
+            "intermediate_bytes": model["intermediate_bytes"], "flops": model["flops"]}
 
 
 # ------------------------------------------------------------------ CPU oracle ----
@@ -301,131 +365,197 @@ def cpu_baseline(inp, n_tokens: int, min_seconds: float = 10.0) -> dict:
     oracle.set_scale_rule(inp.wl.scales)
     host = oracle.HostInputs.from_inputs(inp)
     total_rows, total_dt, passes = 0, 0.0, 0
-    while passes == 0 or (total_dt < min_seconds and passes < 50):
-        _, dt, rows = oracle_rows_per_s(host, toks)
-        total_rows += rows
-        total_dt += dt
-        passes += 1
+    try:
+        while passes == 0 or (total_dt < min_seconds and passes < 50):
+            _, dt, rows = oracle_rows_per_s(host, toks)
+            total_rows += rows
+            total_dt += dt
+            passes += 1
+    finally:
+        oracle.set_scale_rule("fp32")
     return {"value": total_rows / total_dt, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
             "sample": f"{toks.size} tokens ({total_rows // passes} routed rows) of the {inp.wl.name} batch, "
                       f"{passes} passes, {total_dt:.1f} s wall"}
 
 
 # ------------------------------------------------------------------ arms -----------
-def run_ours(args, dist: Dist) -> dict | None:
+def _l2_flush_buffer(torch, dev):
+    return torch.empty(2 * L2_BYTES // 4, dtype=torch.int32, device=dev)
+
+
+def needs_l2_flush(model: dict) -> bool:
+    """A batch whose weights and intermediate buffers fit in twice the L2 gets an L2 flush
+    before every timed step; larger ones stream more than the L2 every step."""
+    return model["weight_bytes"] + model["intermediate_bytes"] < 2 * L2_BYTES
+
+
+def config_of(wl, model: dict, world: int, flush: bool) -> dict:
+    return {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E,
+            "topk": wl.topk, "R": wl.R, "routing": wl.routing, "scales": wl.scales,
+            "weights": wl.weights, "routed_rows_per_step": model["M"],
+            "parallelism": f"replicas x{world}",
+            "l2": ("L2 flushed (%d MB written) before every timed step, steps timed one by one"
+                   % (2 * L2_BYTES >> 20) if flush else
+                   "inputs larger than L2: %.2f GB of expert weights streamed per step, no flush"
+                   % (model["weight_bytes"] / 1e9))}
+
+
+def bench_config(name: str, args, dist: Dist, steps: int, warmup: int, *, e2e_steps: int,
+                 cpu_seconds: float | None, fp8_measured: float | None, sampler=None) -> dict:
+    """Time `steps` forwards of one workload (after `warmup` untimed ones) and describe them.
+
+    Workloads whose weights and buffers fit in twice the L2 get an L2 flush (a write of twice
+    its size) before every timed forward, and each forward is timed alone; larger ones stream
+    more than the L2 every step and run back to back."""
     import torch
-    from combine_persistent_warp_gb300 import FusedMoE
+    from combine_persistent_warp_gb300 import FusedMoE, native
     from combine_persistent_warp_gb300.workloads import make_inputs
 
-    torch.cuda.set_device(dist.local_rank)
     dev = torch.device("cuda", dist.local_rank)
-    inp = make_inputs(args.workload, device=dev)
+    inp = make_inputs(name, device=dev)
     wl = inp.wl
     model = work_model(inp)
     M = model["M"]
     moe = FusedMoE(wl.E, wl.H, wl.I, wl.topk, wl.R).reserve(wl.T)
     moe.load(inp)   # FP8 or MXFP4 weights, by the workload
-    from combine_persistent_warp_gb300 import native
     if args.ffn_mode:
         moe.set_option(native.OPT_FFN_MODE, args.ffn_mode)
     if wl.scales == "pow2":   # power-of-two scales: the hardware block-scaled path
         moe.set_option(native.OPT_SCALE_MODE, 1)
     out = torch.empty(wl.T, wl.H, dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream(dev)
+    flush = needs_l2_flush(model)
+    scratch = _l2_flush_buffer(torch, dev) if flush else None
 
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         moe.forward(inp.x, inp.x_sf, inp.topk_idx, inp.topk_w, out=out)
     torch.cuda.synchronize()
     if moe.get_error() != 0:
-        raise RuntimeError("device error during warm-up")
+        raise RuntimeError(f"{name}: device error during warm-up")
 
-    sampler = ClockSampler(gpu_query_id(torch, dist.local_rank))
-    sampler.start()
-    time.sleep(0.3)
     # per-kernel CUDA events on every PROFILE_EVERY-th step of the timed region (events
     # between kernels serialise them, so recording them on every step would slow it)
-    moe.profile_enable(True, every=PROFILE_EVERY)
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    moe.profile_enable(True, every=1 if flush else PROFILE_EVERY)
     dist.barrier()
     torch.cuda.synchronize()
     h0 = time.time()
-    ev0.record(stream)
-    for _ in range(args.steps):
-        moe.forward(inp.x, inp.x_sf, inp.topk_idx, inp.topk_w, out=out)
-    ev1.record(stream)
-    torch.cuda.synchronize()
+    if flush:
+        local_s = 0.0
+        for _ in range(steps):
+            scratch.fill_(1)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            moe.forward(inp.x, inp.x_sf, inp.topk_idx, inp.topk_w, out=out)
+            e1.record(stream)
+            e1.synchronize()
+            local_s += e0.elapsed_time(e1) / 1e3
+    else:
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for _ in range(steps):
+            moe.forward(inp.x, inp.x_sf, inp.topk_idx, inp.topk_w, out=out)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        local_s = ev0.elapsed_time(ev1) / 1e3
     h1 = time.time()
     dist.barrier()
     prof = moe.profile_read()
     moe.profile_enable(False)
-    time.sleep(0.15)
-    sampler.stop()
     if moe.get_error() != 0:
-        raise RuntimeError("device error during the timed region")
-    local_s = ev0.elapsed_time(ev1) / 1e3
-    value, t_max = aggregate(M * args.steps, local_s, dist)
+        raise RuntimeError(f"{name}: device error during the timed region")
+    value, t_max = aggregate(M * steps, local_s, dist)
+    stage_ms = prof["stage_ms"]
+    calls = max(1, prof["calls"])
+    dominant = max(stage_ms, key=stage_ms.get)
+    res = {
+        "value": value, "unit": UNIT, "steps": steps, "warmup": warmup,
+        "ms_per_step": t_max / steps * 1e3,
+        "config": config_of(wl, model, dist.world, flush),
+        "roofline": roofline_for(dominant, stage_ms[dominant] / calls / 1e3, model, wl.name, fp8_measured),
+        "layer_roofline": layer_roofline(model, t_max / steps, fp8_measured),
+        "stages_us_per_launch": {k: v / calls * 1e3 for k, v in stage_ms.items()},
+        "stage_events": {"every_nth_step": 1 if flush else PROFILE_EVERY, "steps_with_events": prof["calls"]},
+        "gpu_launches": 3 * steps,
+        "dtype": ("fp8e4m3 x e2m1 (MXFP4 weights; fp32 accumulate, bf16 out)" if wl.weights == "mxfp4"
+                  else "fp8e4m3 (fp32 accumulate, bf16 out)"),
+    }
+    if sampler is not None:
+        res["clocks"] = sampler.summary(h0, h1)
 
-    # end to end through the host-buffer entry points (pinned host inputs read and the
-    # result written back every step inside the timed region): the asynchronous one, which
-    # lets the host enqueue step i+1 while step i runs, and the synchronous one
-    pin = lambda t: t.cpu().pin_memory()
-    hx, hsf, hidx, hw = pin(inp.x), pin(inp.x_sf), pin(inp.topk_idx), pin(inp.topk_w)
-    hout = torch.empty(wl.T, wl.H, dtype=torch.bfloat16).pin_memory()
-    e2e_steps = max(1, min(args.steps, args.e2e_steps))
-
-    def host_loop(wait: bool) -> float:
-        for _ in range(max(3, min(args.warmup, 20))):
-            moe.forward_host(hx, hsf, hidx, hw, out=hout, wait=wait)
+    if e2e_steps > 0:
+        # end to end through the host-buffer entry point: pinned host inputs read and the
+        # result written back every step inside the timed region (moe_forward_host_async,
+        # which lets the host enqueue step i+1 while step i runs)
+        pin = lambda t: t.cpu().pin_memory()
+        hx, hsf, hidx, hw = pin(inp.x), pin(inp.x_sf), pin(inp.topk_idx), pin(inp.topk_w)
+        hout = torch.empty(wl.T, wl.H, dtype=torch.bfloat16).pin_memory()
+        for _ in range(max(3, min(warmup, 20))):
+            moe.forward_host(hx, hsf, hidx, hw, out=hout, wait=False)
         dist.barrier()
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for _ in range(e2e_steps):
-            moe.forward_host(hx, hsf, hidx, hw, out=hout, wait=wait)
+            moe.forward_host(hx, hsf, hidx, hw, out=hout, wait=False)
         e1.record(stream)
         torch.cuda.synchronize()
         dist.barrier()
         if moe.get_error() != 0:
-            raise RuntimeError("device error in the end-to-end loop")
-        return aggregate(M * e2e_steps, e0.elapsed_time(e1) / 1e3, dist)[0]
-
-    e2e_value = host_loop(wait=False)
-    e2e_sync_value = host_loop(wait=True)
-    h2d = sum(t.numel() * t.element_size() for t in (hx, hsf, hidx, hw))
-    d2h = hout.numel() * hout.element_size()
-
-    stage_ms = prof["stage_ms"]
-    calls = max(1, prof["calls"])
-    dominant = max(stage_ms, key=stage_ms.get)
-    roof = roofline_for(dominant, stage_ms[dominant] / calls / 1e3, model, wl.name)
-    stages = {k: v / calls * 1e3 for k, v in stage_ms.items()}   # us per launch
-
-    res = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": dist.world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_max / args.steps * 1e3,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": ("fp8e4m3 x e2m1 (MXFP4 weights; fp32 accumulate, bf16 out)" if wl.weights == "mxfp4"
-                  else "fp8e4m3 (fp32 accumulate, bf16 out)"), "data": "synthetic",
-        "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E,
-                   "topk": wl.topk, "R": wl.R, "routing": wl.routing, "scales": wl.scales,
-                   "weights": wl.weights,
-                   "routed_rows_per_step": M, "parallelism": f"replicas x{dist.world}",
-                   "l2": ("inputs larger than L2: %.2f GB of expert weights streamed per step, "
-                          "no flush" % (model["weight_bytes"] / 1e9))},
-        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-                "entry_point": "moe_forward_host_async (one stream, synchronized after the last step)",
-                "sync_value": e2e_sync_value,
-                "sync_entry_point": "moe_forward_host (returns after each step)"},
-        "gpu_launches": 3 * args.steps,
-        "roofline": roof,
-        "stages_us_per_launch": stages,
-        "stage_events": {"every_nth_step": PROFILE_EVERY, "steps_with_events": prof["calls"]},
-        "clocks": sampler.summary(h0, h1),
-    }
-    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
-        res["cpu_baseline"] = cpu_baseline(inp, args.cpu_tokens, args.cpu_seconds)
+            raise RuntimeError(f"{name}: device error in the end-to-end loop")
+        e2e_value = aggregate(M * e2e_steps, e0.elapsed_time(e1) / 1e3, dist)[0]
+        res["e2e"] = {"value": e2e_value, "unit": UNIT,
+                      "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in (hx, hsf, hidx, hw)),
+                      "d2h_bytes_per_step": hout.numel() * hout.element_size(), "steps": e2e_steps,
+                      "entry_point": "moe_forward_host_async (one stream, synchronized after the last step)"}
+        del hx, hsf, hidx, hw, hout
+    if cpu_seconds is not None and dist.rank == 0 and dist.world == 1:
+        res["cpu_baseline"] = cpu_baseline(inp, args.cpu_tokens, cpu_seconds)
     moe.close()
+    del inp, out, scratch
+    torch.cuda.empty_cache()
+    return res
+
+
+def run_ours(args, dist: Dist) -> dict | None:
+    import torch
+
+    torch.cuda.set_device(dist.local_rank)
+    dev = torch.device("cuda", dist.local_rank)
+    fp8_tflops = measure_fp8_gemm_tflops(dev) if not args.no_fp8_peak else None
+    sampler = ClockSampler(gpu_query_id(torch, dist.local_rank))
+    sampler.start()
+    time.sleep(0.3)
+    try:
+        head = bench_config(args.workload, args, dist, args.steps, args.warmup,
+                            e2e_steps=max(1, min(args.steps, args.e2e_steps)),
+                            cpu_seconds=None if args.no_cpu_baseline else args.cpu_seconds,
+                            fp8_measured=fp8_tflops, sampler=sampler)
+        per = {}
+        for name in [n for n in args.per_config.split(",") if n and n != args.workload]:
+            small = name.split("-")[0] in ("tiny", "decode")
+            per[name] = bench_config(name, args, dist, max(args.steps, 200) if small else args.steps,
+                                     max(args.warmup, 5),
+                                     e2e_steps=max(1, min(args.steps, args.e2e_steps)),
+                                     cpu_seconds=None if args.no_cpu_baseline else args.per_config_cpu_seconds,
+                                     fp8_measured=fp8_tflops, sampler=sampler)
+    finally:
+        time.sleep(0.15)
+        sampler.stop()
+    res = {
+        "metric": METRIC, "value": head["value"], "unit": UNIT, "n_gpus": dist.world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": head["dtype"], "data": "synthetic", "config": head["config"],
+        "e2e": head["e2e"], "gpu_launches": head["gpu_launches"], "roofline": head["roofline"],
+        "layer_roofline": head["layer_roofline"], "stages_us_per_launch": head["stages_us_per_launch"],
+        "stage_events": head["stage_events"], "clocks": head.get("clocks"),
+        "fp8_gemm_tflops_measured": fp8_tflops,
+    }
+    if "cpu_baseline" in head:
+        res["cpu_baseline"] = head["cpu_baseline"]
+    if per:
+        res["per_config"] = per
+        res["clocks_whole_run"] = sampler.summary(0.0, time.time())
     return res if dist.rank == 0 else None
 
 
@@ -437,9 +567,17 @@ def run_reference(args, dist: Dist) -> dict | None:
 
     if dist.rank != 0:
         return None
-    inp = make_inputs(args.workload, device="cpu")
+    import torch
+    # the inputs are synthesised where the other arm makes them (the device generator draws
+    # other numbers than the CPU one), then copied to the host
+    if torch.cuda.is_available():
+        inp = make_inputs(args.workload, device=torch.device("cuda", dist.local_rank)).to("cpu")
+        torch.cuda.empty_cache()
+    else:
+        inp = make_inputs(args.workload, device="cpu")
     oracle.set_scale_rule(inp.wl.scales)
     wl = inp.wl
+    model = work_model(inp)
     host = oracle.HostInputs.from_inputs(inp)
     h_idx = host.idx
     cores = oracle.num_threads()
@@ -485,10 +623,9 @@ def run_reference(args, dist: Dist) -> dict | None:
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_s / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "impl": "reference",
-        "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E,
-                   "topk": wl.topk, "R": wl.R, "routing": wl.routing, "scales": wl.scales,
-                   "weights": wl.weights, "routed_rows_per_step": int(len(valid)),
-                   "parallelism": "host cores"},
+        # the workload's description as the other arm prints it (the CPU steps each take a
+        # bounded sample of this batch: see cpu_baseline.sample)
+        "config": config_of(wl, model, dist.world, needs_l2_flush(model)),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -499,21 +636,26 @@ def run_reference(args, dist: Dist) -> dict | None:
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=50)
-    ap.add_argument("--workload", default="decode",
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="large",
                     help="tiny, decode, prefill, skewed, large, or one of them with -pow2 "
                          "(power-of-two scales: the block-scaled UMMA path) or -mxfp4 (MXFP4 "
                          "weights on the block-scaled path)")
+    ap.add_argument("--per-config", default="tiny,decode,prefill,skewed",
+                    help="comma-separated workloads also timed in the same run (reported under "
+                         "per_config; empty for none)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=300)
     ap.add_argument("--cpu-tokens", type=int, default=128)
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="minimum wall time of the oracle baseline sample (repeated passes)")
+    ap.add_argument("--per-config-cpu-seconds", type=float, default=3.0)
     ap.add_argument("--ref-budget-s", type=float, default=120.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-fp8-peak", action="store_true")
     ap.add_argument("--ffn-mode", type=int, default=0,
-                    help="expert FFN kernel mode: 0 automatic, 1 one CTA per tile, 2 CTA pairs")
+                    help="expert FFN kernel mode: 0 automatic, 1 one CTA per tile")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -13,13 +13,34 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <map>
+#include <mutex>
 #include <new>
+#include <utility>
 #include <vector>
 
 #include "../../include/cpw_moe.h"
 #include "moe_internal.cuh"
 
 using namespace cpw;
+
+cudaError_t cpw::ensure_max_dynamic_smem(const void *kernel, int bytes)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    static std::mutex mu;
+    static std::map<std::pair<const void *, int>, int> set_to;
+    std::lock_guard<std::mutex> lock(mu);
+    int &cur = set_to[{kernel, dev}];
+    if (bytes <= cur)
+        return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess)
+        cur = bytes;
+    return e;
+}
 
 struct moe_ctx {
     int dev = -1;

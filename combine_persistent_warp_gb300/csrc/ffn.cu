@@ -795,16 +795,12 @@ cudaError_t launch_ffn(const FfnMaps &maps, const Dims &d, const Workspace &ws, 
                        const float *sf1, const float *sf2, int wave_blocks, int num_sms, bool paired,
                        cudaStream_t s)
 {
-    static bool configured[2] = {false, false};
     static int paired_grid = 0;
     static int paired_coop = 1;   // cooperative attribute accepted together with clusters
     void *kern = paired ? reinterpret_cast<void *>(ffn_kernel<true>) : reinterpret_cast<void *>(ffn_kernel<false>);
-    if (!configured[paired]) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM_BYTES);
-        if (e != cudaSuccess)
-            return e;
-        configured[paired] = true;
-    }
+    cudaError_t e0 = ensure_max_dynamic_smem(kern, GEMM_SMEM_BYTES);
+    if (e0 != cudaSuccess)
+        return e0;
     FfnMaps m = maps;
     Dims dd = d;
     Workspace ww = ws;

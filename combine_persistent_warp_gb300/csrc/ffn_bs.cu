@@ -820,7 +820,6 @@ cudaError_t launch_ffn_bs(const FfnMaps &maps, const SfMaps &sf_maps, const Dims
                           const CallArgs &c, const uint8_t *sfb1, const uint8_t *sfb2, int wave_blocks, int num_sms,
                           bool paired, bool fp4, cudaStream_t s)
 {
-    static bool configured[4] = {false, false, false, false};
     static int paired_grid = 0;
     static int paired_coop = 1;   // cooperative attribute accepted together with clusters
     constexpr int SMEM1 = 1024 + STAGES * STAGE_BYTES + 8192 + STAGES * SF_STAGE_BYTES;
@@ -832,13 +831,9 @@ cudaError_t launch_ffn_bs(const FfnMaps &maps, const SfMaps &sf_maps, const Dims
                                : reinterpret_cast<void *>(ffn_bs_kernel<true, false>))
                         : (fp4 ? reinterpret_cast<void *>(ffn_bs_kernel<false, true>)
                                : reinterpret_cast<void *>(ffn_bs_kernel<false, false>));
-    const int variant = (paired ? 2 : 0) + (fp4 ? 1 : 0);
-    if (!configured[variant]) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess)
-            return e;
-        configured[variant] = true;
-    }
+    cudaError_t e0 = ensure_max_dynamic_smem(kern, smem);
+    if (e0 != cudaSuccess)
+        return e0;
     FfnMaps m = maps;
     SfMaps sm = sf_maps;
     Dims dd = d;

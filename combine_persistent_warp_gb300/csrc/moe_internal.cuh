@@ -88,6 +88,11 @@ __device__ __forceinline__ void record_error(uint32_t *hdr, uint32_t code)
     atomicCAS(hdr + HDR_ERR_CALL, 0u, code);
 }
 
+// cudaFuncSetAttribute(MaxDynamicSharedMemorySize) holds per device: raises a kernel's limit
+// to `bytes` on the current device unless a call for that (kernel, device) already has
+// (thread-safe; defined in api.cu).
+cudaError_t ensure_max_dynamic_smem(const void *kernel, int bytes);
+
 // Launchers (one per translation unit).
 size_t dispatch_smem_bytes(const Dims &d);
 cudaError_t launch_dispatch(const Dims &d, const Workspace &ws, const CallArgs &c, int num_sms,
@@ -98,8 +103,9 @@ struct FfnMaps {
     CUtensorMap a1p, a2p;         // pool x / act with 32-row boxes (partly filled M-blocks)
     CUtensorMap b1h, b2h;         // W1 / W2 tiles with 128-row boxes (half tiles, 2-CTA mode)
 };
-// paired: 2-CTA clusters sharing each weight tile by TMA multicast (shapes with several
-// M-blocks per expert); otherwise one CTA per tile with a dynamic tile counter.
+// paired: 2-CTA clusters, one cta_group::2 UMMA over two M-blocks of an expert, each CTA
+// loading its own A rows and one half of the weight tile; otherwise one CTA per tile with a
+// dynamic tile counter.
 cudaError_t launch_ffn(const FfnMaps &maps, const Dims &d, const Workspace &ws, const CallArgs &c,
                        const float *sf1, const float *sf2, int wave_blocks, int num_sms, bool paired,
                        cudaStream_t s);

@@ -11,7 +11,9 @@
 //
 // The array's name is only a host-side stand-in in host code, so the real device address
 // is looked up once per device with cudaGetSymbolAddress (with that device current) and
-// passed to the kernels.  Every call shares the array and leaves its contents behind: the
+// passed to the kernels.  The address is kept for the life of the process: a device reset
+// (cudaDeviceReset, which unloads the module) makes it stale, so the entry point must not be
+// called on a device after a reset of that device.  Every call shares the array and leaves its contents behind: the
 // counters are cleared on the caller's stream at the start of each call, the table needs
 // no clearing (every entry read is written first by the same call).  Calls that overlap on
 // the GPU (different streams, or different host threads on one device) race on the array.
@@ -199,19 +201,67 @@ __global__ void __launch_bounds__(NA_THREADS)
         recv_s[i] = static_cast<uint32_t>(send[r * E + e]);
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
+    {
+        // expert row and M-block prefixes: each thread sums a run of at most two experts,
+        // then a block-wide scan (warp shuffles, then the warp totals)
+        __shared__ int wtot[2][NA_THREADS / 32];
+        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+        const int per = (E + NA_THREADS - 1) / NA_THREADS;
+        const int e0 = min(E, static_cast<int>(threadIdx.x) * per), e1 = min(E, e0 + per);
         int rows = 0, blocks = 0;
-        for (int e = 0; e < E; ++e) {
+        for (int e = e0; e < e1; ++e) {
             int n = 0;
             for (int r = 0; r < R; ++r)
                 n += static_cast<int>(recv_s[e * R + r]);
-            cum[e] = rows;
-            blk[e] = blocks;
             rows += n;
             blocks += (n + BM - 1) / BM;
         }
-        cum[E] = rows;
-        blk[E] = blocks;
+        int inc_rows = rows, inc_blocks = blocks;
+        for (int o = 1; o < 32; o <<= 1) {
+            const int a = __shfl_up_sync(0xFFFFFFFFu, inc_rows, o);
+            const int b = __shfl_up_sync(0xFFFFFFFFu, inc_blocks, o);
+            if (lane >= o) {
+                inc_rows += a;
+                inc_blocks += b;
+            }
+        }
+        if (lane == 31) {
+            wtot[0][warp] = inc_rows;
+            wtot[1][warp] = inc_blocks;
+        }
+        __syncthreads();
+        if (warp == 0) {
+            int wr = lane < NA_THREADS / 32 ? wtot[0][lane] : 0;
+            int wb = lane < NA_THREADS / 32 ? wtot[1][lane] : 0;
+            for (int o = 1; o < 32; o <<= 1) {
+                const int a = __shfl_up_sync(0xFFFFFFFFu, wr, o);
+                const int b = __shfl_up_sync(0xFFFFFFFFu, wb, o);
+                if (lane >= o) {
+                    wr += a;
+                    wb += b;
+                }
+            }
+            if (lane < NA_THREADS / 32) {
+                wtot[0][lane] = wr;   // inclusive prefix over warps
+                wtot[1][lane] = wb;
+            }
+        }
+        __syncthreads();
+        int base_rows = inc_rows - rows + (warp > 0 ? wtot[0][warp - 1] : 0);
+        int base_blocks = inc_blocks - blocks + (warp > 0 ? wtot[1][warp - 1] : 0);
+        for (int e = e0; e < e1; ++e) {
+            int n = 0;
+            for (int r = 0; r < R; ++r)
+                n += static_cast<int>(recv_s[e * R + r]);
+            cum[e] = base_rows;
+            blk[e] = base_blocks;
+            base_rows += n;
+            base_blocks += (n + BM - 1) / BM;
+        }
+        if (threadIdx.x == NA_THREADS - 1) {
+            cum[E] = wtot[0][NA_THREADS / 32 - 1];
+            blk[E] = wtot[1][NA_THREADS / 32 - 1];
+        }
     }
     __syncthreads();
     if (blockIdx.x == 0) {
@@ -260,6 +310,12 @@ extern "C" int moe_route_noalloc(int T, int E, int topk, int R, const int64_t *t
     if (rc != MOE_OK)
         return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // the scratch address is the current device's: the stream must belong to that device
+    int cur = 0, sdev = 0;
+    if (cudaGetDevice(&cur) != cudaSuccess || cudaStreamGetDevice(s, &sdev) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (sdev != cur)
+        return MOE_ERR_INVALID_ARG;
     auto *send = reinterpret_cast<unsigned long long *>(scratch);
     auto *table = reinterpret_cast<int32_t *>(scratch + NA_SEND_BYTES);
     if (cudaMemsetAsync(send, 0, sizeof(unsigned long long) * E * R, s) != cudaSuccess ||

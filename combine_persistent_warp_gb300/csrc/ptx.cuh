@@ -107,20 +107,6 @@ __device__ __forceinline__ void red_release_add(uint32_t *p, uint32_t v)
     asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
-// 2-D tiled load into the same shared-memory offset of every CTA in `cta_mask` (cluster
-// multicast); each destination CTA's mbarrier at `bar`'s offset gets the bytes it received.
-__device__ __forceinline__ void tma_load_2d_multicast(void *smem_dst, const CUtensorMap *map, uint64_t *bar,
-                                                      int32_t x, int32_t y, uint16_t cta_mask,
-                                                      uint64_t cache_hint)
-{
-    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-                 ".multicast::cluster.L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5, %6;" ::"r"(
-                     smem_u32(smem_dst)),
-                 "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "h"(cta_mask),
-                 "l"(cache_hint)
-                 : "memory");
-}
-
 // 2-D tiled load into this CTA's shared memory whose completion is counted on an mbarrier
 // of either CTA of the pair (`bar_cluster` is a shared::cluster address, e.g. the leader
 // CTA's barrier from map_cluster), for the two-CTA UMMA.

@@ -72,14 +72,9 @@ cudaError_t launch_dispatch(const Dims &d, const Workspace &ws, const CallArgs &
                             cudaStream_t s)
 {
     const size_t smem = dispatch_smem_bytes(d);
-    static size_t configured = 0;
-    if (smem > configured) {
-        cudaError_t e = cudaFuncSetAttribute(dispatch_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(smem));
-        if (e != cudaSuccess)
-            return e;
-        configured = smem;
-    }
+    cudaError_t e = ensure_max_dynamic_smem(reinterpret_cast<const void *>(dispatch_kernel), static_cast<int>(smem));
+    if (e != cudaSuccess)
+        return e;
     Dims dd = d;
     Workspace ww = ws;
     CallArgs cc = c;

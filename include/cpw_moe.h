@@ -59,7 +59,8 @@ enum moe_status {
 };
 
 /* Create a layer for E experts, hidden size H, expert intermediate size I, top-k, and R
- * logical source partitions.  Requires H % 256 == 0, I % 128 == 0, 1 <= topk <= 32,
+ * logical source partitions (the layer object the pages' Python API builds before its
+ * forward: "DeepGEMM Mega MoE 对称内存（Symmetric Memory）深度分析" §10.1).  Requires H % 256 == 0, I % 128 == 0, 1 <= topk <= 32,
  * topk <= E <= 1024, 1 <= R <= 64, E*R <= 16384, on the current device, which must be
  * sm_103.  Allocates no device memory.  *out receives the handle. */
 int moe_create(int E, int H, int I, int topk, int R, moe_handle_t *out);
@@ -125,7 +126,9 @@ int moe_load_shared_weights_mxfp4(moe_handle_t h, const uint8_t *w_gate_up, cons
                                   const uint8_t *w_down, const uint8_t *sf_down, void *stream);
 
 /* The layer on T tokens (0 <= T <= max_tokens, T % R == 0; source r owns tokens
- * [r*T/R, (r+1)*T/R)).  Asynchronous on `stream`.
+ * [r*T/R, (r+1)*T/R)): Output(T) = sum_k w_k Expert_k(T) ("Dispatch/Combine: 博客理论 ↔
+ * DeepEP 源码 ↔ DeepGEMM Mega MoE 三方对比分析" §1), by the fused call sequence of "DeepGEMM
+ * Mega MoE 对称内存（Symmetric Memory）深度分析" §10.1.  Asynchronous on `stream`.
  *   x        [T][H] e4m3            x_sf [T][H/128] fp32 (1x128 activation scales)
  *   topk_idx [T][topk] int64, -1 = skip this slot
  *   topk_w   [T][topk] fp32 gate weights
@@ -152,11 +155,15 @@ int moe_forward_host_async(moe_handle_t h, int T, const uint8_t *host_x, const f
                            uint16_t *host_out, void *stream);
 
 /* Wait for the handle's last stream, then return (and clear) the sticky device status in
- * *device_status (a moe_status value; MOE_OK if none).  Clearing also resets the
+ * *device_status (a moe_status value; MOE_OK if none).  The pages' kernel stops with an
+ * assertion when a bounded wait runs out ("DeepGEMM Mega MoE 对称内存（Symmetric Memory）深度
+ * 分析" §6.2); here the kernels record the failure and this call reports it.  Clearing also resets the
  * workspace counters so the next forward starts clean. */
 int moe_get_error(moe_handle_t h, int *device_status);
 
-/* Routing results of the last forward (host copies, after syncing its stream):
+/* Routing results of the last forward (host copies, after syncing its stream), i.e. the
+ * per-expert counts, expert segments and pool metadata of "Mega-MoE walkthrough part 2"
+ * (kwkr.cn/news/1317662) §2.4-2.6:
  *   counts [E] rows per expert, recv [E][R] rows per (expert, source),
  *   block_offset [E+1] first M-block of each expert in the pool (last = total blocks),
  *   meta [P][3] {source, token, topk slot} of every pool row (rows past an expert's
@@ -252,13 +259,17 @@ int moe_profile_read(moe_handle_t h, double *stage_ms, int *calls, int *dropped)
  * GPU, kept until the process exits; sizes beyond it return MOE_ERR_CAPACITY: at most
  * E*R <= 4096, T*topk <= 131072 and E*T <= 1048576 (plus the moe_create limits on E, topk
  * and R, and T % R == 0).  The first call on a device looks up that array's device
- * address and should come before any stream capture.  Asynchronous on `stream`; calls
- * that overlap on the GPU share the scratch and race. */
+ * address and should come before any stream capture; the address is kept until the process
+ * exits, so the entry point must not be used on a device after that device was reset
+ * (cudaDeviceReset).  Asynchronous on `stream`, which must belong to the current device
+ * (MOE_ERR_INVALID_ARG otherwise); calls that overlap on the GPU share the scratch and race. */
 int moe_route_noalloc(int T, int E, int topk, int R, const int64_t *topk_idx, uint32_t *counts,
                       uint32_t *recv, int32_t *block_offset, uint32_t *meta, int32_t *status,
                       void *stream);
 
-/* Release every device buffer of the handle (after syncing its last stream). */
+/* Release every device buffer of the handle (after syncing its last stream): the teardown
+ * of the buffers the layer object of "DeepGEMM Mega MoE 对称内存（Symmetric Memory）深度分析"
+ * §10.1 allocates. */
 int moe_destroy(moe_handle_t h);
 
 /* Static description of a status code. */

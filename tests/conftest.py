@@ -61,3 +61,52 @@ def fp8_twin_of_mxfp4(packed, sf):
     c8 = torch.from_numpy(q).to(torch.float8_e4m3fn)
     assert np.array_equal(c8.to(torch.float64).numpy(), q)        # exact twin
     return c8.view(torch.uint8), torch.from_numpy(scale)
+
+
+def _rows_by_token(dbg):
+    """(token, M-block) of every valid pool row of the last forward (padding rows left out)."""
+    BM, off, counts, meta = dbg["block_m"], dbg["block_offset"], dbg["counts"], dbg["meta"]
+    toks, blks = [np.zeros(0, np.int64)], [np.zeros(0, np.int64)]
+    for e in range(counts.size):
+        n = int(counts[e])
+        if n:
+            r = int(off[e]) * BM + np.arange(n)
+            toks.append(meta[r, 1].astype(np.int64))
+            blks.append(r // BM)
+    return np.concatenate(toks), np.concatenate(blks)
+
+
+def block_cover_tokens(dbg, extra=()):
+    """Tokens whose routed rows, together, fall in every M-block of the pool of the last
+    forward (dbg = FusedMoE.debug_routing()): every M-block of every expert, the last partly
+    filled block of each and the blocks of the last wave included, holds at least one row of
+    a returned token.  Greedy: for each block not yet covered, the token among its rows that
+    covers the most uncovered blocks.  The `extra` tokens are part of the result (sorted)."""
+    tok, blk = _rows_by_token(dbg)
+    nblk = int(dbg["block_offset"][-1])
+    by_tok = {}
+    for t, b in zip(tok.tolist(), blk.tolist()):
+        by_tok.setdefault(t, []).append(b)
+    by_tok = {t: np.array(v, np.int64) for t, v in by_tok.items()}
+    by_blk = {}
+    for t, b in zip(tok.tolist(), blk.tolist()):
+        by_blk.setdefault(b, set()).add(t)
+    covered = np.zeros(nblk, bool)
+    chosen = set(int(t) for t in extra)
+    for t in chosen:
+        if t in by_tok:
+            covered[by_tok[t]] = True
+    for b in range(nblk):
+        if covered[b]:
+            continue
+        best = max(sorted(by_blk[b]), key=lambda t: int((~covered[by_tok[t]]).sum()))
+        covered[by_tok[best]] = True
+        chosen.add(best)
+    assert covered.all()
+    return np.array(sorted(chosen), np.int64)
+
+
+def blocks_of_tokens(dbg, tokens):
+    """M-blocks holding at least one valid row of `tokens` (to check a cover)."""
+    tok, blk = _rows_by_token(dbg)
+    return set(blk[np.isin(tok, np.asarray(tokens, np.int64))].tolist())

@@ -14,11 +14,13 @@ import oracle
 from combine_persistent_warp_gb300 import FusedMoE, MoeError
 from combine_persistent_warp_gb300 import native
 from combine_persistent_warp_gb300.workloads import Workload, make_inputs
+from conftest import block_cover_tokens, blocks_of_tokens
 
 pytestmark = pytest.mark.gpu
 
 TOL = 2e-2
-SAMPLES = {"tiny-pow2": None, "decode-pow2": 24, "prefill-pow2": 12, "skewed-pow2": 12, "large-pow2": 12}
+# compared tokens: all (tiny, decode), else a seeded sample plus a cover of every M-block
+SAMPLES = {"tiny-pow2": None, "decode-pow2": None, "prefill-pow2": 12, "skewed-pow2": 12, "large-pow2": 12}
 
 
 def layer(name):
@@ -47,7 +49,9 @@ def test_block_scaled_output_and_stage_parity(name):
     torch.cuda.synchronize()
     assert moe.get_error() == 0
     h = oracle.HostInputs.from_inputs(inp)
-    toks = sample(wl.T, SAMPLES[name], h.idx)
+    dbg = moe.debug_routing(wl.T)
+    toks = block_cover_tokens(dbg, extra=sample(wl.T, SAMPLES[name], h.idx).tolist())
+    assert blocks_of_tokens(dbg, toks) == set(range(int(dbg["block_offset"][-1])))
     oracle.set_scale_rule("pow2")
     try:
         _, ref, bad = oracle.forward_tokens(h, toks)

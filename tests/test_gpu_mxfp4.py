@@ -11,7 +11,7 @@ import pytest
 import torch
 
 import oracle
-from conftest import fp8_twin_of_mxfp4
+from conftest import block_cover_tokens, blocks_of_tokens, fp8_twin_of_mxfp4
 from combine_persistent_warp_gb300 import FusedMoE, MoeError
 from combine_persistent_warp_gb300 import native
 from combine_persistent_warp_gb300.workloads import Workload, make_inputs, make_weights, make_weights_mxfp4
@@ -69,7 +69,7 @@ CASES = {
                         weights="mxfp4"), None),
     # the decode and prefill shapes (hidden 7168, intermediate 2048, 32 experts, top-8)
     "decode": (Workload("mx-decode", T=128, H=7168, I=2048, E=32, topk=8, R=8, seed=1, scales="pow2",
-                        weights="mxfp4"), 16),
+                        weights="mxfp4"), None),
     "prefill": (Workload("mx-prefill", T=4096, H=7168, I=2048, E=32, topk=8, R=8, seed=2, scales="pow2",
                          weights="mxfp4"), 10),
     # the skewed (Zipf, 5% skipped slots, 64 experts) and large (128 experts) batches
@@ -87,7 +87,11 @@ def test_mxfp4_matches_oracle(case):
     torch.cuda.synchronize()
     assert moe.get_error() == 0
     assert moe.info().weight_format == native.WEIGHTS_MXFP4
-    toks = sample(wl.T, n)
+    # a seeded sample plus a cover of the pool: every M-block of every expert holds a row of
+    # a compared token
+    dbg = moe.debug_routing(wl.T)
+    toks = block_cover_tokens(dbg, extra=sample(wl.T, n).tolist())
+    assert blocks_of_tokens(dbg, toks) == set(range(int(dbg["block_offset"][-1])))
     ref = oracle_out(inp, toks)
     rel = rel_l2(out[torch.as_tensor(toks, device=out.device)], ref)
     assert np.all(rel <= TOL), f"max per-token rel L2 {rel.max():.3e}"

@@ -15,12 +15,14 @@ import oracle
 from combine_persistent_warp_gb300 import FusedMoE, MoeError
 from combine_persistent_warp_gb300 import native
 from combine_persistent_warp_gb300.workloads import WORKLOADS, Workload, make_inputs
+from conftest import block_cover_tokens, blocks_of_tokens
 
 pytestmark = pytest.mark.gpu
 
 TOL = 2e-2
-# tokens compared against the oracle per workload (all for tiny, a seeded sample else)
-SAMPLES = {"tiny": None, "decode": 24, "prefill": 12, "skewed": 12, "large": 12}
+# tokens compared against the oracle per workload: all of them (tiny, decode), else a seeded
+# sample plus a cover of the pool (at least one row in every M-block of every expert)
+SAMPLES = {"tiny": None, "decode": None, "prefill": 12, "skewed": 12, "large": 12}
 
 
 def rel_l2(got_bf16: torch.Tensor, ref: np.ndarray) -> np.ndarray:
@@ -98,9 +100,9 @@ def check_routing(c: Case):
         assert np.array_equal(pool_sf[:, rows], h.x_sf[m[:, 1]].T)
         gpu_keys.append(((e * R + m[:, 0]) * T + m[:, 1]) * K + m[:, 2])
     gpu_keys = np.sort(np.concatenate(gpu_keys)) if gpu_keys else np.zeros(0, np.int64)
-    t_idx, k_idx = np.nonzero(h.idx >= 0)
-    e_idx = h.idx[t_idx, k_idx]
-    ref_keys = np.sort(((e_idx * R + t_idx // Tsrc) * T + t_idx) * K + k_idx)
+    ref = oracle.route_multiset(h.idx, E, R)
+    ref_keys = np.sort(np.array([((e * R + r) * T + t) * K + kk for (e, r), v in ref.items() for t, kk in v],
+                                np.int64))
     assert np.array_equal(gpu_keys, ref_keys)
     return dbg
 
@@ -116,7 +118,9 @@ def test_routing_bit_exact(name):
 def test_output_parity(name):
     c = case(name)
     assert c.status == 0
-    toks = c.sample_tokens(SAMPLES[name])
+    dbg = c.moe.debug_routing(c.wl.T)
+    toks = block_cover_tokens(dbg, extra=c.sample_tokens(SAMPLES[name]).tolist())
+    assert blocks_of_tokens(dbg, toks) == set(range(int(dbg["block_offset"][-1])))
     _, ref, bad = oracle.forward_tokens(c.host, toks)
     assert not bad
     rel = rel_l2(c.out[torch.as_tensor(toks, device=c.out.device)], ref)

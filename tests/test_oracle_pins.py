@@ -177,6 +177,35 @@ def test_route_counts_vs_bincount(oracle_mod):
     assert oracle_mod.route_counts(bad_idx, E, R)[2]
 
 
+def test_route_multiset_hand_example(oracle_mod):
+    """Index-table grouping ("Mega-MoE 内核代码导读：从 Dispatch 到 WGMMA 的融合流水线" §4.3: an
+    entry of token t's slot k goes to table[expert][source of t]) on a batch small enough to
+    write out: T=4 tokens in R=2 sources of 2, top-2 over E=3 experts, -1 skipped."""
+    idx = np.array([[0, 2], [2, -1], [1, 0], [-1, 2]], np.int64)
+    got = oracle_mod.route_multiset(idx, 3, 2)
+    want = {(0, 0): [(0, 0)], (0, 1): [(2, 1)], (1, 0): [], (1, 1): [(2, 0)],
+            (2, 0): [(0, 1), (1, 0)], (2, 1): [(3, 1)]}
+    assert got == want
+
+
+def test_route_multiset_brute_force(oracle_mod):
+    """Every valid (token, slot) appears exactly once, under its own expert and its token's
+    source, and the group sizes equal the C oracle's per-(expert, source) counts."""
+    from combine_persistent_warp_gb300.workloads import make_routing
+    T, E, k, R = 96, 7, 3, 4
+    idx, _ = make_routing(T, E, k, seed=8, skip_frac=0.15)
+    a = idx.numpy()
+    got = oracle_mod.route_multiset(idx, E, R)
+    _, recv, _ = oracle_mod.route_counts(idx, E, R)
+    seen = []
+    for (e, r), v in got.items():
+        assert len(v) == recv[e, r]
+        for t, kk in v:
+            assert a[t, kk] == e and t // (T // R) == r
+            seen.append((t, kk))
+    assert sorted(seen) == [(t, kk) for t in range(T) for kk in range(k) if a[t, kk] >= 0]
+
+
 # ------------------------------------------------------------------ numerics ------
 def _tiny_inputs(E=4, H=256, I=128, T=8, k=2, seed=11):
     from combine_persistent_warp_gb300 import workloads as W

@@ -1,4 +1,5 @@
-"""The allocation-free routing entry point, checked against the regular forward path.
+"""The allocation-free routing entry point, checked against the regular forward path and
+against the CPU oracle's routing.
 
 moe_route_noalloc exists for callers that may not allocate device memory -- code that
 runs under another framework's memory pool or a fixed memory budget, or a loop that must
@@ -15,6 +16,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from combine_persistent_warp_gb300 import FusedMoE, native
 from combine_persistent_warp_gb300.workloads import make_inputs
 
@@ -55,6 +57,29 @@ def _check_same(ref, got, wl):
             assert sa == sb
 
 
+def _check_oracle(got, idx, wl):
+    """The same outputs against the CPU oracle's routing: counts and per-source counts by
+    direct counting, block offsets by ceil_div prefix, the round-robin source order of every
+    expert, and the (token, slot) multiset of every (expert, source)."""
+    torch.cuda.synchronize()
+    assert int(got["status"].item()) == 0
+    counts, recv, bad = oracle.route_counts(idx, wl.E, wl.R)
+    assert not bad
+    assert np.array_equal(got["counts"].cpu().numpy().astype(np.uint32), counts)
+    assert np.array_equal(got["recv"].cpu().numpy().astype(np.uint32), recv)
+    off = oracle.block_offsets(counts, 128)
+    assert np.array_equal(got["block_offset"].cpu().numpy(), off)
+    meta = got["meta"].cpu().numpy().astype(np.int64)
+    groups = oracle.route_multiset(idx, wl.E, wl.R)
+    for e in range(wl.E):
+        rows = off[e] * 128 + np.arange(int(counts[e]))
+        src, _ = oracle.round_robin(recv[e])
+        assert np.array_equal(meta[rows, 0], src)
+        for r in range(wl.R):
+            m = meta[rows][meta[rows, 0] == r]
+            assert sorted(map(tuple, m[:, 1:].tolist())) == groups[(e, r)]
+
+
 @pytest.mark.gpu
 @pytest.mark.parametrize("name", ["tiny", "decode", "skewed"])
 def test_noalloc_routing_matches_forward_twice(name):
@@ -64,6 +89,7 @@ def test_noalloc_routing_matches_forward_twice(name):
     for _ in range(2):
         got = native.route_noalloc(inp.topk_idx, inp.wl.E, inp.wl.R)
         _check_same(ref, got, inp.wl)
+        _check_oracle(got, inp.topk_idx, inp.wl)
 
 
 @pytest.mark.gpu

@@ -184,6 +184,10 @@ int encode_sf_map(CUtensorMap *m, void *base, uint64_t bytes, uint32_t box_rows)
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
+// 256-row tiles of the down weight (H rows; the last tile is half zero rows when H is an odd
+// multiple of 128)
+inline int h_tiles(const Dims &d) { return (d.H + BN - 1) / BN; }
+
 // Bump allocator over one cudaMalloc'd block.
 struct Carver {
     char *base;
@@ -315,7 +319,7 @@ int moe_create_shared(int E, int H, int I, int topk, int R, int n_shared, moe_ha
     if (!out)
         return MOE_ERR_INVALID_ARG;
     *out = nullptr;
-    if (E < 1 || H < 256 || H % 256 != 0 || I < 128 || I % 128 != 0 || topk < 1 || topk > E || R < 1 ||
+    if (E < 1 || H < 128 || H % 128 != 0 || I < 128 || I % 128 != 0 || topk < 1 || topk > E || R < 1 ||
         R > 64 || n_shared < 0 || E + n_shared > 1024 || topk + n_shared > 32 || (E + n_shared) * R > 16384)
         return MOE_ERR_INVALID_ARG;
     int dev = 0;
@@ -408,11 +412,12 @@ int load_expert_weights(moe_ctx *h, int e0, int n, const uint8_t *w_gate_up, con
         return MOE_ERR_INVALID_ARG;
     CK(cudaSetDevice(h->dev));
     const Dims &d = h->d;
-    const size_t w1e = static_cast<size_t>(2) * d.I * d.H, w2e = static_cast<size_t>(d.H) * d.I;
+    // down-weight tiles cover H rounded up to the 256-row tile (zero rows past H)
+    const size_t w1e = static_cast<size_t>(2) * d.I * d.H, w2e = static_cast<size_t>(h_tiles(d)) * BN * d.I;
     const size_t s1e = static_cast<size_t>(2 * d.I / 128) * (d.H / 128), s2e = static_cast<size_t>(d.H / 128) * (d.I / 128);
     // UE8M0 scale blocks: 1 KB per weight tile and group of four 128-deep K blocks
     const size_t b1e = static_cast<size_t>(2 * d.I / BN) * ((d.H / 128 + 3) / 4) * 1024,
-                 b2e = static_cast<size_t>(d.H / BN) * ((d.I / 128 + 3) / 4) * 1024;
+                 b2e = static_cast<size_t>(h_tiles(d)) * ((d.I / 128 + 3) / 4) * 1024;
     const size_t n1 = d.E * w1e, n2 = d.E * w2e;
     if (!h->w_mem) {
         Carver c{nullptr};
@@ -471,9 +476,9 @@ int load_expert_weights_mxfp4(moe_ctx *h, int e0, int n, const uint8_t *w_gate_u
         return MOE_ERR_INVALID_ARG;
     CK(cudaSetDevice(h->dev));
     const Dims &d = h->d;
-    const size_t w1e = static_cast<size_t>(2) * d.I * (d.H / 2), w2e = static_cast<size_t>(d.H) * (d.I / 2);
+    const size_t w1e = static_cast<size_t>(2) * d.I * (d.H / 2), w2e = static_cast<size_t>(h_tiles(d)) * BN * (d.I / 2);
     const size_t b1e = static_cast<size_t>(2 * d.I / BN) * (d.H / 128) * 1024,
-                 b2e = static_cast<size_t>(d.H / BN) * (d.I / 128) * 1024;
+                 b2e = static_cast<size_t>(h_tiles(d)) * (d.I / 128) * 1024;
     const size_t n1 = d.E * w1e, n2 = d.E * w2e;
     if (!h->w4_mem) {
         Carver c{nullptr};

@@ -82,9 +82,11 @@ static_assert(PAIR_STAGES * PAIR_STAGE_BYTES <= STAGES * STAGE_BYTES, "pair stag
 // pipeline stage for the producer (0: load issue) and the UMMA issuer (1: stage full,
 // 2: MMAs issued), per scale block for one epilogue warp (3: TMEM full, 4: promoted,
 // 5: tile epilogue start).
-// 6: producer tile start, 7: producer done waiting for a down tile's gate_up blocks.
+// 6: producer tile start, 7: producer done waiting for a down tile's gate_up blocks,
+// 8: UMMA issuer done waiting for an empty TMEM partial (per scale block), 9: the epilogue
+// warp's TMEM-empty arrival (per scale block).
 // g_cta_span: global-timer ns at every CTA's start and end (cross-SM comparable).
-constexpr int TRACE_CTAS = 2, TRACE_EVENTS = 8, TRACE_ITERS = 4096, TRACE_MAX_GRID = 1024;
+constexpr int TRACE_CTAS = 2, TRACE_EVENTS = 10, TRACE_ITERS = 4096, TRACE_MAX_GRID = 1024;
 __device__ unsigned long long g_trace[TRACE_CTAS][TRACE_EVENTS][TRACE_ITERS];
 __device__ unsigned long long g_cta_span[2][TRACE_MAX_GRID];
 __device__ __forceinline__ int trace_slot()
@@ -234,7 +236,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     ptx::tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
 
-    const TileList tl{(2 * d.I) / BN, d.H / BN, PAIRED ? bars->pair_off[d.E] : ws.blk_off[d.E],
+    const TileList tl{(2 * d.I) / BN, (d.H + BN - 1) / BN, PAIRED ? bars->pair_off[d.E] : ws.blk_off[d.E],
                       PAIRED ? max(1, wave_blocks / 2) : wave_blocks};
     const int ntiles = tl.total();
     const int nclusters = static_cast<int>(gridDim.x) / 2, cluster_id = static_cast<int>(blockIdx.x) / 2;
@@ -432,6 +434,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                             ok = false;
                             break;
                         }
+                        CPW_STAMP(8, pit);
                         const uint32_t dt = tmem + buf * BN;
                         // the SUBS stages of one scale block accumulate into one TMEM partial
                         for (int j = 0; j < SUBS; ++j, ++it) {
@@ -524,8 +527,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             }
             const long long prow = static_cast<long long>(blk) * BM + row;
             // a warp whose 32 rows are all padding of a partly filled M-block (most warps at
-            // decode) only hands each TMEM partial back: its results are never stored
-            const bool dead = q * 32 >= ws.block_rows[blk];
+            // decode) only hands each TMEM partial back: its results are never stored; so does
+            // the second column half of the last down tile when H is an odd multiple of 128
+            // (its weight rows are zero and lie past H)
+            const bool dead = q * 32 >= ws.block_rows[blk] || (phase == 2 && nt * BN + wg * 128 >= d.H);
             const float *sfa = (phase == 1 ? ws.pool_sf : ws.act_sf) + prow;
             const float *sb0;
             const float *sb1;
@@ -559,11 +564,15 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 #pragma unroll
             for (int j = 0; j < 128; ++j)
                 acc[j] = 0.0f;
-            float a_nx = phase == 1 ? __ldg(sfa) : __ldcg(sfa);
-            float b0_nx = __ldg(sb0), b1_nx = __ldg(sb1);
+            float a_nx = 0.0f, b0_nx = 0.0f, b1_nx = 0.0f;
+            if (!dead) {
+                a_nx = phase == 1 ? __ldg(sfa) : __ldcg(sfa);
+                b0_nx = __ldg(sb0);
+                b1_nx = __ldg(sb1);
+            }
             for (int kb = 0; kb < nkb; ++kb, ++pit) {
                 const float s0 = a_nx * b0_nx, s1 = a_nx * b1_nx;
-                if (kb + 1 < nkb) {
+                if (kb + 1 < nkb && !dead) {
                     const float *na = sfa + static_cast<long long>(kb + 1) * ws.P;
                     a_nx = phase == 1 ? __ldg(na) : __ldcg(na);
                     b0_nx = __ldg(sb0 + kb + 1);
@@ -621,6 +630,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     else
                         ptx::mbar_arrive(&bars->tempty[buf]);
                 }
+                if (warp == 4 && lane == 0)
+                    CPW_STAMP(9, pit);
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
                     const float sj = ((j >> 3) & 1) ? s1 : s0;
@@ -701,7 +712,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 // xor-shuffle stages; then store (h, i) has the group write row i's half h as
                 // one full 128-byte line, four lines per instruction.
                 const int rows = ws.block_rows[blk];
-                if (q * 32 < rows) {
+                if (!dead) {
                     float gw = 0.0f;
                     uint32_t roff = 0;   // combine row: slot * max_tokens + token
                     if (row < rows) {

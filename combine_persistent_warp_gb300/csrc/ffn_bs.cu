@@ -255,7 +255,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     ptx::tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
 
-    const BsTiles tl{(2 * d.I) / BN, d.H / BN, PAIRED ? bars->pair_off[d.E] : ws.blk_off[d.E],
+    const BsTiles tl{(2 * d.I) / BN, (d.H + BN - 1) / BN, PAIRED ? bars->pair_off[d.E] : ws.blk_off[d.E],
                      PAIRED ? max(1, wave_blocks / 2) : wave_blocks};
     const int ntiles = tl.total();
     const int nclusters = static_cast<int>(gridDim.x) / 2, cluster_id = static_cast<int>(blockIdx.x) / 2;
@@ -747,7 +747,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 // transposes its 8 rows x 8 16-byte chunks (per 128-byte half) with three
                 // xor-shuffle stages; then store (h, i) has the group write row i's half h as
                 // one full 128-byte line, four lines per instruction.
-                if (q * 32 < rows) {
+                // (with H an odd multiple of 128 the last down tile's second column half lies
+                // past H: its weight rows are zero and nothing is stored)
+                if (q * 32 < rows && nt * BN + wg * 128 < d.H) {
                     float gw = 0.0f;
                     uint32_t roff = 0;   // combine row: slot * max_tokens + token
                     if (row < rows) {
@@ -888,11 +890,13 @@ cudaError_t launch_ffn_bs(const FfnMaps &maps, const SfMaps &sf_maps, const Dims
 // four K blocks, 1 KB at ((e*NT + nt)*G + g)*1024 (G = ceil(KB/4)) with tile column n's word
 // at 512*(n/128) + 16*(n%32) + 4*((n%128)/32), byte kb % 4 = K block kb's scale.  Column n of a gate_up tile (gate_up_I > 0) is the gate row group nt if
 // (n/8) is even, else the up group I/128 + nt (the interleave by 8); of a down tile, the row
-// group 2*nt + n/128.  Any scale that is not a positive normal power of two sets *bad.
+// group 2*nt + n/128.  Any scale that is not a positive normal power of two sets *bad.  A
+// last tile that covers fewer than 256 rows (N an odd multiple of 128) gets the byte 127
+// (scale 1) for its missing rows, whose re-laid weights are zero.
 __global__ void build_sfb_kernel(const float *__restrict__ s, uint8_t *__restrict__ dst, int E, int N, int K,
                                  int gate_up_I, uint32_t *bad)
 {
-    const int KB = K / 128, NT = N / BN;
+    const int KB = K / 128, NT = (N + BN - 1) / BN;
     const long long words = static_cast<long long>(E) * NT * KB * BN;
     for (long long q = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; q < words;
          q += static_cast<long long>(gridDim.x) * blockDim.x) {
@@ -907,11 +911,14 @@ __global__ void build_sfb_kernel(const float *__restrict__ s, uint8_t *__restric
             group = ((n >> 3) & 1) ? gate_up_I / 128 + nt : nt;
         else
             group = 2 * nt + n / 128;
-        const float v = s[(static_cast<long long>(e) * (N / 128) + group) * KB + kb];
-        const uint32_t b = __float_as_uint(v);
-        const uint32_t ex = (b >> 23) & 0xFFu;
-        if ((b & 0x807FFFFFu) != 0u || ex == 0u || ex == 0xFFu)
-            atomicOr(bad, 1u);
+        uint32_t ex = 127u;
+        if (nt * BN + n < N) {
+            const float v = s[(static_cast<long long>(e) * (N / 128) + group) * KB + kb];
+            const uint32_t b = __float_as_uint(v);
+            ex = (b >> 23) & 0xFFu;
+            if ((b & 0x807FFFFFu) != 0u || ex == 0u || ex == 0xFFu)
+                atomicOr(bad, 1u);
+        }
         const long long g = et * ((KB + SF_GROUP - 1) / SF_GROUP) + kb / SF_GROUP;
         dst[g * SFB_BYTES + 512 * (n / 128) + 16 * (n % 32) + 4 * ((n % 128) / 32) + kb % SF_GROUP] =
             static_cast<uint8_t>(ex);
@@ -931,10 +938,11 @@ cudaError_t launch_build_sfb(const float *s, uint8_t *dst, int E, int N, int K, 
 // 4*((n%128)/32), byte j = the scale of the row's 32-deep slice 4*kb + j.  Tile column n is
 // weight row nt*256 + n, through the gate/up interleave by 8 for the gate_up weight (the
 // row order of the re-laid weight tiles).  A byte 0xFF (NaN in the UE8M0 format) sets *bad.
+// Rows past N of a last tile that covers fewer than 256 rows get the bytes 127 (zero weights).
 __global__ void build_sfb4_kernel(const uint8_t *__restrict__ s, uint8_t *__restrict__ dst, int E, int N, int K,
                                   int gate_up_I, uint32_t *bad)
 {
-    const int KB = K / 128, NT = N / BN;
+    const int KB = K / 128, NT = (N + BN - 1) / BN;
     const long long words = static_cast<long long>(E) * NT * KB * BN;
     for (long long q = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; q < words;
          q += static_cast<long long>(gridDim.x) * blockDim.x) {
@@ -951,7 +959,8 @@ __global__ void build_sfb4_kernel(const uint8_t *__restrict__ s, uint8_t *__rest
             srow = i < 8 ? 8 * j + i : gate_up_I + 8 * j + (i - 8);
         }
         // K/32 is a multiple of 4: the four bytes of K block kb are one aligned word
-        const uint32_t w = *reinterpret_cast<const uint32_t *>(s + (e * N + srow) * (K / 32) + 4 * kb);
+        const uint32_t w = row < N ? *reinterpret_cast<const uint32_t *>(s + (e * N + srow) * (K / 32) + 4 * kb)
+                                   : 0x7F7F7F7Fu;
         if (((w & 0xFFu) == 0xFFu) || ((w >> 8 & 0xFFu) == 0xFFu) || ((w >> 16 & 0xFFu) == 0xFFu) || ((w >> 24) == 0xFFu))
             atomicOr(bad, 1u);
         *reinterpret_cast<uint32_t *>(dst + tk * SFB_BYTES + 512 * (n / 128) + 16 * (n % 32) + 4 * ((n % 128) / 32)) = w;

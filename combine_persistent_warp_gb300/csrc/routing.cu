@@ -269,6 +269,8 @@ cudaError_t launch_stage_inputs(const void *const src[4], void *const dst[4], co
 // [E][N/256][K/128][256][kb_bytes] bytes: every 256-row tile the FFN kernel loads per 128-deep
 // K block is one contiguous block (32 KB / 16 KB), so each weight load streams whole DRAM
 // pages instead of 256 rows several KB apart.
+// N need not be a multiple of 256: the last tile's rows past N are written as zeros (the
+// down weight with H an odd multiple of 128).
 // With gate_up_I > 0 (the gate_up weight, N = 2I) the rows are also gate/up interleaved:
 // within each group of 16 rows, rows 0..7 are gate rows 8j..8j+7 and rows 8..15 are up rows
 // I+8j..I+8j+7 (granularity 8, the layout of "DeepGEMM Mega MoE 对称内存（Symmetric Memory）
@@ -276,9 +278,9 @@ cudaError_t launch_stage_inputs(const void *const src[4], void *const dst[4], co
 __global__ void relayout_weights_kernel(const uint8_t *__restrict__ src, uint8_t *__restrict__ dst, int E,
                                         int N, int K, int gate_up_I, int kb_bytes)
 {
-    const int KB = K / 128, NT = N / BN, C16 = kb_bytes / 16;
+    const int KB = K / 128, NT = (N + BN - 1) / BN, C16 = kb_bytes / 16;
     const long long row_bytes = static_cast<long long>(KB) * kb_bytes;
-    const long long chunks = static_cast<long long>(E) * N * KB * C16;
+    const long long chunks = static_cast<long long>(E) * NT * BN * KB * C16;
     for (long long q = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; q < chunks;
          q += static_cast<long long>(gridDim.x) * blockDim.x) {
         long long t = q;
@@ -291,6 +293,10 @@ __global__ void relayout_weights_kernel(const uint8_t *__restrict__ src, uint8_t
         const int nt = static_cast<int>(t % NT);
         const long long e = t / NT;
         const int n = nt * BN + r;
+        if (n >= N) {
+            reinterpret_cast<uint4 *>(dst)[q] = make_uint4(0u, 0u, 0u, 0u);
+            continue;
+        }
         int srow = n;
         if (gate_up_I > 0) {
             const int j = n / 16, i = n % 16;

@@ -36,7 +36,13 @@ def test_host_side_argument_checks_need_no_gpu():
     h = ctypes.c_void_p()
     assert lib.moe_create(8, 256, 128, 2, 2, None) == 1
     assert lib.moe_create(0, 256, 128, 2, 2, ctypes.byref(h)) == 1      # E
-    assert lib.moe_create(8, 384, 128, 2, 2, ctypes.byref(h)) == 1      # H % 256
+    assert lib.moe_create(8, 320, 128, 2, 2, ctypes.byref(h)) == 1      # H % 128
+    assert lib.moe_create(8, 0, 128, 2, 2, ctypes.byref(h)) == 1        # H
+    # H an odd multiple of 128 passes the shape checks (without a GPU it then fails later)
+    rc = lib.moe_create(8, 384, 128, 2, 2, ctypes.byref(h))
+    assert rc != 1
+    if rc == 0:
+        lib.moe_destroy(h)
     assert lib.moe_create(8, 256, 96, 2, 2, ctypes.byref(h)) == 1       # I % 128
     assert lib.moe_create(8, 256, 128, 9, 2, ctypes.byref(h)) == 1      # topk > E
     assert lib.moe_create(8, 256, 128, 33, 2, ctypes.byref(h)) == 1     # topk > 32

@@ -269,6 +269,15 @@ def test_block_scaled_scale_groups_span_tiles():
     _compare_pow2(moe, inp, inp.topk_idx, inp.topk_w, 256)
 
 
+@pytest.mark.parametrize("H", [384, 640])
+def test_block_scaled_hidden_size_odd_multiple_of_128(H):
+    """H = 3 or 5 x 128: the last down tile's second column half runs on zero weight rows
+    whose UE8M0 scale bytes are 127, and stores nothing; every token against the oracle."""
+    moe, inp = _pow2_layer(T_max=256, E=4, H=H, I=256, k=2, R=2, seed=54 + H)
+    out = _compare_pow2(moe, inp, inp.topk_idx, inp.topk_w, 256)
+    assert out.shape == (256, H)
+
+
 def test_block_scaled_empty_and_all_skipped():
     moe, inp = _pow2_layer(T_max=64)
     e = torch.empty(0, 256, dtype=torch.uint8, device="cuda")

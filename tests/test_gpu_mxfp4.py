@@ -67,6 +67,9 @@ CASES = {
     # 10 and 5 K blocks: A scale groups end mid-way through tiles
     "groups": (Workload("mx-groups", T=256, H=1280, I=640, E=4, topk=2, R=2, seed=63, scales="pow2",
                         weights="mxfp4"), None),
+    # H = 5 x 128: the last down tile's second column half lies past H (zero weight rows)
+    "odd-h": (Workload("mx-odd-h", T=256, H=640, I=256, E=4, topk=2, R=2, seed=65, scales="pow2",
+                       weights="mxfp4"), None),
     # the decode and prefill shapes (hidden 7168, intermediate 2048, 32 experts, top-8)
     "decode": (Workload("mx-decode", T=128, H=7168, I=2048, E=32, topk=8, R=8, seed=1, scales="pow2",
                         weights="mxfp4"), None),

@@ -172,6 +172,22 @@ def run_and_compare(moe, inp, idx, w, T):
     return out, ref
 
 
+@pytest.mark.parametrize("H", [384, 640])
+def test_hidden_size_odd_multiple_of_128(H):
+    """H = 3 or 5 x 128: the down GEMM's last 256-column tile covers 128 real columns (its
+    other half runs on zero weight rows and stores nothing); every token against the oracle,
+    with a Zipf-skewed routing so experts hold several M-blocks and a partly filled last one."""
+    T = 384
+    wl = Workload("odd-h", T=T, H=H, I=256, E=6, topk=3, R=4, routing="zipf", zipf_s=1.1, skip_frac=0.05,
+                  seed=70 + H)
+    inp = make_inputs(wl, device="cuda")
+    moe = FusedMoE(wl.E, H, wl.I, wl.topk, wl.R).reserve(T)
+    moe.load_weights(inp.w_gate_up, inp.sf_gate_up, inp.w_down, inp.sf_down)
+    assert moe.info().H == H
+    out, _ = run_and_compare(moe, inp, inp.topk_idx, inp.topk_w, T)
+    assert out.shape == (T, H)
+
+
 def test_empty_batch():
     moe, inp = tiny_layer()
     e = torch.empty(0, 256, dtype=torch.uint8, device="cuda")

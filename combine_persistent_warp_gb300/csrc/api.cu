@@ -68,15 +68,13 @@ struct moe_ctx {
     void *w_mem = nullptr;
     size_t w_bytes = 0;
     FfnMaps maps{};              // a1 pool x, b1 W1, a2 act, b2 W2
-    SfMaps sf_maps{};            // UE8M0 scale blocks of pool / act rows and weight tiles
     // MXFP4 weights (allocated by the first MXFP4 load): packed E2M1 tiles
     // [E][N/256][K/128][256][64] and UE8M0 scale blocks of 1 KB per weight tile and K block
     uint8_t *w41 = nullptr, *w42 = nullptr, *sfb41 = nullptr, *sfb42 = nullptr;
     uint32_t *sfb4_bad = nullptr;
     void *w4_mem = nullptr;
     size_t w4_bytes = 0;
-    CUtensorMap b41{}, b42{}, b41h{}, b42h{};   // 16U4_ALIGN16B maps of the E2M1 tiles
-    CUtensorMap sfb41_map{}, sfb42_map{};
+    CUtensorMap b41{}, b42{};    // 16U4_ALIGN16B maps of the E2M1 tiles
     // staging buffers of moe_forward_host
     // (two input sets: an asynchronous call fills one with the copy engines on copy_stream
     // while the previous call's kernels still read the other)
@@ -98,7 +96,7 @@ struct moe_ctx {
     int last_T = 0;
     long long timeout_ns = 2000000000LL;
     int debug_skip_barrier = 0;
-    int ffn_mode = 0;            // 0 auto, 1 one CTA per tile, 2 two-CTA clusters
+    int ffn_mode = 0;            // 0 automatic, 1 one CTA per tile (the same kernel)
     int scale_mode = 2;          // 0 fp32 scales, 1 power-of-two scales (block-scaled UMMA),
                                  // 2 block-scaled exactly when the weights' scales are 2^k
     // stage profiling (events on the forward's stream)
@@ -162,22 +160,6 @@ int encode_fp4_tile_map(CUtensorMap *m, void *base, uint64_t rows, uint32_t box_
     cuuint32_t estr[2] = {1, 1};
     CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, base, dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
-}
-
-// 2-D byte matrix of `bytes` / 256 rows of 256 bytes, boxes of box_rows whole rows, no
-// swizzle (the UE8M0 scale blocks the 2-CTA block-scaled kernel stages by TMA)
-int encode_sf_map(CUtensorMap *m, void *base, uint64_t bytes, uint32_t box_rows)
-{
-    if (get_encoder() != MOE_OK || bytes % 256 != 0)
-        return MOE_ERR_CUDA;
-    cuuint64_t dims[2] = {256, bytes / 256};
-    cuuint64_t strides[1] = {256};
-    cuuint32_t box[2] = {256, box_rows};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, strides, box, estr,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
 }
@@ -272,14 +254,6 @@ int wave_blocks(const moe_ctx *h)
     return static_cast<int>(std::max(1ll, half_l2 / per_block));
 }
 
-// One CTA per tile by default (measured faster on GB300 for every workload shape tried);
-// MOE_OPT_FFN_MODE = 2 selects the 2-CTA cluster mode.
-bool ffn_paired(const moe_ctx *h, int T)
-{
-    (void)T;
-    return h->ffn_mode == 2;
-}
-
 int sync_last(moe_ctx *h)
 {
     if (h->have_last)
@@ -319,7 +293,7 @@ int moe_create_shared(int E, int H, int I, int topk, int R, int n_shared, moe_ha
     if (!out)
         return MOE_ERR_INVALID_ARG;
     *out = nullptr;
-    if (E < 1 || H < 128 || H % 128 != 0 || I < 128 || I % 128 != 0 || topk < 1 || topk > E || R < 1 ||
+    if (E < 1 || H < 128 || H % 128 != 0 || H / 128 > MAX_KB || I / 128 > MAX_KB || I < 128 || I % 128 != 0 || topk < 1 || topk > E || R < 1 ||
         R > 64 || n_shared < 0 || E + n_shared > 1024 || topk + n_shared > 32 || (E + n_shared) * R > 16384)
         return MOE_ERR_INVALID_ARG;
     int dev = 0;
@@ -389,9 +363,7 @@ int moe_reserve(moe_handle_t h, int max_tokens)
     if (encode_tile_map(&h->maps.a1, ws.pool_x, ws.P, d.H, BM) != MOE_OK ||
         encode_tile_map(&h->maps.a2, ws.act, ws.P, d.I, BM) != MOE_OK ||
         encode_tile_map(&h->maps.a1p, ws.pool_x, ws.P, d.H, A_ROWS_PART) != MOE_OK ||
-        encode_tile_map(&h->maps.a2p, ws.act, ws.P, d.I, A_ROWS_PART) != MOE_OK ||
-        encode_sf_map(&h->sf_maps.sfa1, ws.pool_sfe, static_cast<uint64_t>(ws.P) * (d.H / 32), 2) != MOE_OK ||
-        encode_sf_map(&h->sf_maps.sfa2, ws.act_sfe, static_cast<uint64_t>(ws.P) * (d.I / 32), 2) != MOE_OK)
+        encode_tile_map(&h->maps.a2p, ws.act, ws.P, d.I, A_ROWS_PART) != MOE_OK)
         return MOE_ERR_CUDA;
     CK(cudaDeviceSynchronize());
     h->reserved = true;
@@ -453,11 +425,7 @@ int load_expert_weights(moe_ctx *h, int e0, int n, const uint8_t *w_gate_up, con
     *pow2 = bad == 0;
     // weight tiles as rows of 128 bytes: tile (e, nt, kb) starts at row ((e*NT + nt)*KB + kb)*256
     if (encode_tile_map(&h->maps.b1, h->w1, n1 / 128, 128, BN) != MOE_OK ||
-        encode_tile_map(&h->maps.b2, h->w2, n2 / 128, 128, BN) != MOE_OK ||
-        encode_tile_map(&h->maps.b1h, h->w1, n1 / 128, 128, BN / 2) != MOE_OK ||
-        encode_tile_map(&h->maps.b2h, h->w2, n2 / 128, 128, BN / 2) != MOE_OK ||
-        encode_sf_map(&h->sf_maps.sfb1, h->sfb1, static_cast<uint64_t>(d.E) * b1e, 4) != MOE_OK ||
-        encode_sf_map(&h->sf_maps.sfb2, h->sfb2, static_cast<uint64_t>(d.E) * b2e, 4) != MOE_OK)
+        encode_tile_map(&h->maps.b2, h->w2, n2 / 128, 128, BN) != MOE_OK)
         return MOE_ERR_CUDA;
     h->last_stream = s;
     h->have_last = true;
@@ -508,11 +476,7 @@ int load_expert_weights_mxfp4(moe_ctx *h, int e0, int n, const uint8_t *w_gate_u
     CK(cudaStreamSynchronize(s));
     // tile (e, nt, kb) starts at 64-byte row ((e*NT + nt)*KB + kb)*256
     if (encode_fp4_tile_map(&h->b41, h->w41, n1 / 64, BN) != MOE_OK ||
-        encode_fp4_tile_map(&h->b42, h->w42, n2 / 64, BN) != MOE_OK ||
-        encode_fp4_tile_map(&h->b41h, h->w41, n1 / 64, BN / 2) != MOE_OK ||
-        encode_fp4_tile_map(&h->b42h, h->w42, n2 / 64, BN / 2) != MOE_OK ||
-        encode_sf_map(&h->sfb41_map, h->sfb41, static_cast<uint64_t>(d.E) * b1e, 4) != MOE_OK ||
-        encode_sf_map(&h->sfb42_map, h->sfb42, static_cast<uint64_t>(d.E) * b2e, 4) != MOE_OK)
+        encode_fp4_tile_map(&h->b42, h->w42, n2 / 64, BN) != MOE_OK)
         return MOE_ERR_CUDA;
     h->last_stream = s;
     h->have_last = true;
@@ -638,26 +602,20 @@ int moe_forward(moe_handle_t h, int T, const uint8_t *x, const float *x_sf, cons
             ++h->prof_dropped;
     }
     auto mark = [&](int i) { return ev ? cudaEventRecord(ev[i], s) : cudaSuccess; };
-    // MXFP4: the weight-tile and weight-scale maps of the E2M1 tiles
+    // MXFP4: the weight-tile maps of the E2M1 tiles
     FfnMaps maps4 = h->maps;
-    SfMaps sf_maps4 = h->sf_maps;
     if (h->mxfp4) {
         maps4.b1 = h->b41;
         maps4.b2 = h->b42;
-        maps4.b1h = h->b41h;
-        maps4.b2h = h->b42h;
-        sf_maps4.sfb1 = h->sfb41_map;
-        sf_maps4.sfb2 = h->sfb42_map;
     }
     if (mark(0) != cudaSuccess ||
         (h->S > 0 && launch_extend_route(topk_idx, topk_w, h->ext_idx, h->ext_w, T, h->K_routed, h->S, h->E_routed,
                                          h->num_sms, s) != cudaSuccess) ||
         launch_dispatch(h->d, h->ws, c, h->num_sms, s) != cudaSuccess ||
         mark(1) != cudaSuccess ||
-        (bs ? launch_ffn_bs(h->mxfp4 ? maps4 : h->maps, h->mxfp4 ? sf_maps4 : h->sf_maps, h->d, h->ws, c,
-                            h->mxfp4 ? h->sfb41 : h->sfb1, h->mxfp4 ? h->sfb42 : h->sfb2, wave_blocks(h),
-                            h->num_sms, ffn_paired(h, T), h->mxfp4, s)
-            : launch_ffn(h->maps, h->d, h->ws, c, h->s1, h->s2, wave_blocks(h), h->num_sms, ffn_paired(h, T), s)) !=
+        (bs ? launch_ffn_bs(maps4, h->d, h->ws, c, h->mxfp4 ? h->sfb41 : h->sfb1, h->mxfp4 ? h->sfb42 : h->sfb2,
+                            wave_blocks(h), h->num_sms, h->mxfp4, s)
+            : launch_ffn(h->maps, h->d, h->ws, c, h->s1, h->s2, wave_blocks(h), h->num_sms, s)) !=
             cudaSuccess ||
         mark(2) != cudaSuccess || launch_combine(h->d, h->ws, c, h->num_sms, s) != cudaSuccess ||
         mark(3) != cudaSuccess)
@@ -913,7 +871,7 @@ int moe_set_option(moe_handle_t h, int option, int64_t value)
         h->debug_skip_barrier = value != 0;
         return MOE_OK;
     case MOE_OPT_FFN_MODE:
-        if (value < 0 || value > 2)
+        if (value < 0 || value > 1)
             return MOE_ERR_INVALID_ARG;
         h->ffn_mode = static_cast<int>(value);
         return MOE_OK;

@@ -59,16 +59,7 @@ constexpr uint32_t SF_COL = 256;          // scale slot j: columns SF_COL + 16*j
 constexpr int SF_GROUP = 4;               // K blocks per scale block (bytes of a scale word)
 constexpr uint32_t SFA_BYTES = 512, SFB_BYTES = 1024, SF_STAGE_BYTES = SFA_BYTES + SFB_BYTES;
 static_assert(BKS == BK, "the block-scaled kernel stages whole 128-deep K blocks");
-// Two-CTA mode: one M = 256 UMMA covers two M-blocks of an expert, one per CTA of a cluster
-// pair; each CTA stages its 128 A rows, one 128-row half of the weight tile and its own copy
-// of the tile's scale blocks, so an operand stage is 32 KB instead of 48 KB and the same
-// 192 KB ring holds six stages.  Per K block each SM's shared memory then takes 33.5 KB of
-// TMA writes and serves 32 KB of UMMA reads, against 49.5 KB and 48 KB with one CTA per tile.
-constexpr uint32_t PAIR_B_BYTES = STAGE_B_BYTES / 2;
-constexpr uint32_t PAIR_STAGE_BYTES = STAGE_A_BYTES + PAIR_B_BYTES;
-constexpr int PAIR_STAGES = static_cast<int>((STAGES * STAGE_BYTES) / PAIR_STAGE_BYTES);
-static_assert(PAIR_STAGES * PAIR_STAGE_BYTES <= STAGES * STAGE_BYTES, "pair stages exceed the ring");
-static_assert(SF_COL + 16 * PAIR_STAGES <= TMEM_COLS, "scale slots exceed TMEM");
+static_assert(SF_COL + 16 * STAGES <= TMEM_COLS, "scale slots exceed TMEM");
 
 // block-scaled instruction descriptor: B scale id (byte of the scale word) at bits 4-5, A
 // format e4m3 (0) at bits 7-9, B format at bits 10-12 (e4m3 = 0, E2M1 = 5), K-major A and B,
@@ -80,38 +71,23 @@ __device__ __forceinline__ uint32_t idesc_bs(int a_sf_id, int b_sf_id)
            (1u << 23) | (static_cast<uint32_t>(M >> 4) << 24) | (static_cast<uint32_t>(a_sf_id) << 29);
 }
 
-// one CTA: D (128 rows) (+)= A x B^T with scales from this CTA's TMEM.  Two CTAs (issued by
-// the even CTA of the pair): D (256 rows, 128 in each CTA's TMEM at the same address), each
-// CTA holding 128 rows of A and half of B's N rows at the same shared-memory offsets, and
-// each CTA's own TMEM holding the scales of its A rows and of all 256 B rows
-template <bool PAIR>
+// D (128 rows) (+)= A x B^T with the A and B scale factors read from this CTA's TMEM
 __device__ __forceinline__ void umma_bs(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
                                         uint32_t sfb, uint32_t accumulate)
 {
-    if constexpr (PAIR)
-        asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
-                     "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d),
-                     "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
-                     : "memory");
-    else
-        asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
-                     "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d),
-                     "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
-                     : "memory");
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d),
+                 "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+                 : "memory");
 }
 
 // shared -> TMEM copy of 32 rows x 16 bytes (no swizzle, 8-row groups 128 B apart) into
-// four columns of every lane quarter; the two-CTA form, issued by the even CTA, copies each
-// CTA's shared memory at that offset into its own TMEM
-template <bool PAIR>
+// four columns of every lane quarter
 __device__ __forceinline__ void sf_copy(uint32_t taddr, uint32_t smem_addr)
 {
     const uint64_t desc = static_cast<uint64_t>((smem_addr >> 4) & 0x3FFF) | (static_cast<uint64_t>(8) << 16) |
                           (static_cast<uint64_t>(128 >> 4) << 32) | (static_cast<uint64_t>(1) << 46);
-    if constexpr (PAIR)
-        asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
-    else
-        asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
 }
 
 // the smallest power of two >= v for a positive normal fp32 v (exact)
@@ -122,8 +98,8 @@ __device__ __forceinline__ float pow2_ceil(float v)
 }
 
 struct __align__(8) BsBars {
-    uint64_t full[PAIR_STAGES];
-    uint64_t empty[PAIR_STAGES];
+    uint64_t full[STAGES];
+    uint64_t empty[STAGES];
     uint64_t tfull;
     uint64_t tempty;
     uint64_t xbar;
@@ -134,7 +110,6 @@ struct __align__(8) BsBars {
     uint32_t tmem_base;
     int abort;
     float amax[2][2][BM];
-    int32_t pair_off[1025];   // 2-CTA mode: first block pair of each expert (E <= 1024)
 };
 
 struct BsTiles {
@@ -162,28 +137,23 @@ struct BsTiles {
     }
 };
 
-// Tile of the list as one CTA sees it.  In 2-CTA mode a list entry is a pair of
-// consecutive M-blocks of one expert; CTA rank r takes the r-th block, and an expert with an
-// odd block count leaves rank 1 a null half (it loads no A rows and no A scales, only its
-// half of the weight tile and the tile's scales, and stores nothing).
+// Tile of the list: phase, n-tile, M-block and its expert.
 struct BsView {
     int phase, nt, blk, e;
-    bool null_half;
 };
 
 }  // namespace
 
-template <bool PAIRED, bool FP4>
+template <bool FP4>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
-    ffn_bs_kernel(const __grid_constant__ FfnMaps maps, const __grid_constant__ SfMaps sfm, const Dims d,
+    ffn_bs_kernel(const __grid_constant__ FfnMaps maps, const Dims d,
                   const Workspace ws, const CallArgs c, const uint8_t *__restrict__ sfb1,
                   const uint8_t *__restrict__ sfb2, const int wave_blocks)
 {
-    constexpr int NST = PAIRED ? PAIR_STAGES : STAGES;                     // stages in the ring
-    constexpr uint32_t SBYTES = PAIRED ? PAIR_STAGE_BYTES : STAGE_BYTES;   // operand bytes per stage
-    // weight bytes a stage's TMA brings from memory for this CTA (packed E2M1: half the
-    // shared-memory image)
-    constexpr uint32_t B_TX = (PAIRED ? PAIR_B_BYTES : STAGE_B_BYTES) / (FP4 ? 2u : 1u);
+    constexpr int NST = STAGES;                  // stages in the ring
+    constexpr uint32_t SBYTES = STAGE_BYTES;     // operand bytes per stage
+    // weight bytes a stage's TMA brings from memory (packed E2M1: half the shared-memory image)
+    constexpr uint32_t B_TX = STAGE_B_BYTES / (FP4 ? 2u : 1u);
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
@@ -196,15 +166,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                              *reinterpret_cast<volatile uint32_t *>(ws.hdr + HDR_ERR_STICKY);
         bars->abort = err != 0;
         if (!err) {
-            // 2-CTA mode: only the even CTA's full and TMEM-empty barriers are used; both
-            // CTAs' loads count on its full barrier, both CTAs' epilogue warps arrive on its
-            // TMEM-empty barrier, and its UMMA commits arrive on both CTAs' empty / TMEM-full
             for (int s = 0; s < NST; ++s) {
                 ptx::mbar_init(&bars->full[s], 1);
                 ptx::mbar_init(&bars->empty[s], 1);
             }
             ptx::mbar_init(&bars->tfull, 1);
-            ptx::mbar_init(&bars->tempty, (PAIRED ? 2 : 1) * EPI_WARPS);
+            ptx::mbar_init(&bars->tempty, EPI_WARPS);
             ptx::mbar_init(&bars->xbar, 32 * EPI_WARPS);
             for (int i = 0; i < TILE_RING; ++i) {
                 ptx::mbar_init(&bars->tile_full[i], 1);
@@ -215,80 +182,27 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         }
     }
     __syncthreads();
-    uint32_t rank = 0;
-    if constexpr (PAIRED) {
-        // both CTAs' barriers are initialised before any remote load, commit or arrive, and
-        // both take the same abort decision (a CTA must not leave while its peer may still
-        // write into its shared memory)
-        ptx::cluster_sync();
-        rank = ptx::cluster_ctarank();
-        const int peer_abort = ptx::ld_cluster_s32(ptx::map_cluster(&bars->abort, rank ^ 1u));
-        const bool stop = bars->abort || peer_abort;
-        ptx::cluster_sync();
-        if (stop)
-            return;
-        if (threadIdx.x == 0) {
-            int acc = 0;
-            for (int e = 0; e < d.E; ++e) {
-                bars->pair_off[e] = acc;
-                acc += (ws.blk_off[e + 1] - ws.blk_off[e] + 1) / 2;
-            }
-            bars->pair_off[d.E] = acc;
-        }
-    } else {
-        if (bars->abort)
-            return;
-    }
+    if (bars->abort)
+        return;
     if (warp == 1) {
-        if constexpr (PAIRED) {
-            ptx::tmem_alloc_pair(&bars->tmem_base, TMEM_COLS);
-            ptx::tmem_relinquish_pair();
-        } else {
-            ptx::tmem_alloc(&bars->tmem_base, TMEM_COLS);
-            ptx::tmem_relinquish();
-        }
+        ptx::tmem_alloc(&bars->tmem_base, TMEM_COLS);
+        ptx::tmem_relinquish();
     }
     ptx::tc_fence_before();
     __syncthreads();
-    if constexpr (PAIRED)
-        ptx::cluster_sync();   // both CTAs hold their TMEM before the even CTA's first copy or UMMA
     ptx::tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
 
-    const BsTiles tl{(2 * d.I) / BN, (d.H + BN - 1) / BN, PAIRED ? bars->pair_off[d.E] : ws.blk_off[d.E],
-                     PAIRED ? max(1, wave_blocks / 2) : wave_blocks};
+    const BsTiles tl{(2 * d.I) / BN, (d.H + BN - 1) / BN, ws.blk_off[d.E], wave_blocks};
     const int ntiles = tl.total();
-    const int nclusters = static_cast<int>(gridDim.x) / 2, cluster_id = static_cast<int>(blockIdx.x) / 2;
-    auto view_of = [&](int tile, uint32_t r) {
+    auto view = [&](int tile) {
         BsView v;
-        int unit;
-        tl.at(tile, v.phase, unit, v.nt);
-        if constexpr (PAIRED) {
-            int lo = 0, hi = d.E - 1;   // expert of pair `unit`: last e with pair_off[e] <= unit
-            while (lo < hi) {
-                const int mid = (lo + hi + 1) >> 1;
-                if (bars->pair_off[mid] <= unit)
-                    lo = mid;
-                else
-                    hi = mid - 1;
-            }
-            v.e = lo;
-            const int b = ws.blk_off[lo] + 2 * (unit - bars->pair_off[lo]) + static_cast<int>(r);
-            v.null_half = b >= ws.blk_off[lo + 1];
-            v.blk = v.null_half ? b - 1 : b;
-        } else {
-            v.blk = unit;
-            v.e = ws.block_expert[unit];
-            v.null_half = false;
-        }
+        tl.at(tile, v.phase, v.blk, v.nt);
+        v.e = ws.block_expert[v.blk];
         return v;
     };
-    auto view = [&](int tile) { return view_of(tile, rank); };
     // A bytes a CTA stages per K block for a tile (a partly filled M-block loads only the
-    // 32-row groups that hold valid rows; a null half loads none), plus the scale blocks
-    auto a_parts = [&](const BsView &v) {
-        return v.null_half ? 0 : (ws.block_rows[v.blk] + A_ROWS_PART - 1) / A_ROWS_PART;
-    };
+    // 32-row groups that hold valid rows), plus the scale blocks
     auto a_stage_bytes = [&](int n_part) {
         return n_part < BM / A_ROWS_PART ? static_cast<uint32_t>(n_part * A_ROWS_PART * BKS) : STAGE_A_BYTES;
     };
@@ -313,13 +227,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 const uint64_t pol_b_shared = ptx::policy_evict_normal();
                 uint32_t it = 0, tcount = 0;
                 bool ok = true;
-                // One CTA per tile: tiles are claimed from the global counter one ahead (a CTA
-                // holds at most one claimed, unstarted tile; the smallest unfinished tile is
-                // always being worked on).  2-CTA mode: round-robin over clusters in list order
-                // (both CTAs of a pair see the same tiles).
-                auto claim_after = [&](int t) {
-                    return PAIRED ? t + nclusters : static_cast<int>(atomicAdd(ws.hdr + HDR_TILE_NEXT, 1u));
-                };
+                // Tiles are claimed from the global counter one ahead (a CTA holds at most one
+                // claimed, unstarted tile; the smallest unfinished tile is always being worked on).
+                auto claim_after = [&](int) { return static_cast<int>(atomicAdd(ws.hdr + HDR_TILE_NEXT, 1u)); };
                 // The next tile is claimed, published to the ring (so the issuer, the epilogue
                 // and the dependency warp see it a tile ahead), and its metadata (its M-block's
                 // expert and valid rows, the expert's M-block count) read, in three steps taken
@@ -337,7 +247,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     ++pcount;
                     return true;
                 };
-                int m_tile = PAIRED ? cluster_id : static_cast<int>(atomicAdd(ws.hdr + HDR_TILE_NEXT, 1u));
+                int m_tile = static_cast<int>(atomicAdd(ws.hdr + HDR_TILE_NEXT, 1u));
                 BsView m_v{};
                 int m_rows = 0, m_eblocks = 0;
                 auto fetch = [&](int step, int cur) {
@@ -369,22 +279,15 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     int fstep = 0, fkb = -2;   // next tile's steps done; K block of the last one
                     const int phase = tv.phase, blk = tv.blk, nt = tv.nt, e = tv.e;
                     const uint64_t pol_b = tv_eblocks > 1 ? pol_b_shared : pol_b_once;
-                    const int n_part = tv.null_half ? 0 : (tv_rows + A_ROWS_PART - 1) / A_ROWS_PART;
+                    const int n_part = (tv_rows + A_ROWS_PART - 1) / A_ROWS_PART;
                     const bool part = n_part < BM / A_ROWS_PART;
                     const uint32_t a_bytes = a_stage_bytes(n_part);
-                    // bytes the stage's full barrier waits for: this CTA's, plus (2-CTA mode,
-                    // even CTA) the odd CTA's, whose loads count on the even CTA's barrier
-                    // (the scale blocks only with the first stage of a group of K blocks)
-                    uint32_t tx_bytes = a_bytes + B_TX;
-                    uint32_t tx_sfa = tv.null_half ? 0u : SFA_BYTES, tx_sfb = SFB_BYTES;
-                    if (PAIRED && rank == 0) {
-                        const BsView ov = view_of(tile, 1);
-                        tx_bytes += a_stage_bytes(a_parts(ov)) + B_TX;
-                        tx_sfa += ov.null_half ? 0u : SFA_BYTES;
-                        tx_sfb += SFB_BYTES;
-                    }
+                    // bytes the stage's full barrier waits for (the scale blocks only with the
+                    // first stage of a group of K blocks)
+                    const uint32_t tx_bytes = a_bytes + B_TX;
+                    const uint32_t tx_sfa = SFA_BYTES, tx_sfb = SFB_BYTES;
                     const CUtensorMap *ta = phase == 1 ? (part ? &maps.a1p : &maps.a1) : (part ? &maps.a2p : &maps.a2);
-                    const CUtensorMap *tb = PAIRED ? (phase == 1 ? &maps.b1h : &maps.b2h) : (phase == 1 ? &maps.b1 : &maps.b2);
+                    const CUtensorMap *tb = phase == 1 ? &maps.b1 : &maps.b2;
                     const int nkb = phase == 1 ? NKB1 : NKB2;
                     const int wtile = e * (phase == 1 ? tl.NT1 : tl.NT2) + nt;
                     const int tile0 = wtile * nkb;
@@ -395,7 +298,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     const uint8_t *sfa_src = (phase == 1 ? ws.pool_sfe : ws.act_sfe) +
                                              static_cast<long long>(blk) * ng * SFA_BYTES;
                     const uint8_t *sfb_src = (phase == 1 ? sfb1 : sfb2) + static_cast<long long>(wtile) * nbb * SFB_BYTES;
-                    if (phase == 2 && !tv.null_half) {
+                    if (phase == 2) {
                         // the act rows and their scales of this block are complete: the
                         // dependency warp has acquired the block's gate_up completion count
                         // (a GPU-scope acquire here would also wait for this thread's loads in
@@ -428,30 +331,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                         const int grp = kb / SF_GROUP;
                         const bool sfb_k = FP4 || sf_k;         // a B scale block with this stage
                         const int bb = FP4 ? kb : grp;          // its index within the tile
-                        if (!PAIRED || rank == 0)
-                            ptx::mbar_arrive_expect_tx(&bars->full[s],
-                                                       tx_bytes + (sf_k ? tx_sfa : 0u) + (sfb_k ? tx_sfb : 0u));
-                        if constexpr (PAIRED) {
-                            // own A rows, own half of the weight tile, own copies of the scale
-                            // blocks (this block's A scales; all 256 weight rows' scales),
-                            // counted on the even CTA's full barrier
-                            const uint32_t fb = ptx::map_cluster(&bars->full[s], 0);
-                            if (part) {
-                                for (int g = 0; g < n_part; ++g)
-                                    ptx::tma_load_2d_pair(sa + g * A_ROWS_PART * BKS, ta, fb, kb * BK,
-                                                          blk * BM + g * A_ROWS_PART, pol_a);
-                            } else {
-                                ptx::tma_load_2d_pair(sa, ta, fb, kb * BK, blk * BM, pol_a);
-                            }
-                            ptx::tma_load_2d_pair(sa + STAGE_A_BYTES, tb, fb, 0,
-                                                  (tile0 + kb) * BN + static_cast<int>(rank) * (BN / 2), pol_b);
-                            if (sf_k && !tv.null_half)
-                                ptx::tma_load_2d_pair(ss, phase == 1 ? &sfm.sfa1 : &sfm.sfa2, fb, 0,
-                                                      (blk * ng + grp) * static_cast<int>(SFA_BYTES / 256), pol_a);
-                            if (sfb_k)
-                                ptx::tma_load_2d_pair(ss + SFA_BYTES, phase == 1 ? &sfm.sfb1 : &sfm.sfb2, fb, 0,
-                                                      (wtile * nbb + bb) * static_cast<int>(SFB_BYTES / 256), pol_b);
-                        } else {
+                        ptx::mbar_arrive_expect_tx(&bars->full[s],
+                                                   tx_bytes + (sf_k ? tx_sfa : 0u) + (sfb_k ? tx_sfb : 0u));
+                        {
                             if (part) {
                                 for (int g = 0; g < n_part; ++g)
                                     ptx::tma_load_2d(sa + g * A_ROWS_PART * BKS, ta, &bars->full[s], kb * BK,
@@ -472,11 +354,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 }
                 if (!ok)
                     record_error(ws.hdr, DEV_TIMEOUT);
-                // drain: every issued load has landed before the CTA may exit (2-CTA mode:
-                // has been consumed by the UMMA, whose commit reaches both CTAs)
+                // drain: every issued load has landed before the CTA may exit
                 const uint64_t dl = ptx::globaltimer() + static_cast<uint64_t>(c.timeout_ns);
                 for (uint32_t i = it > NST ? it - NST : 0; i < it; ++i)
-                    ptx::mbar_wait(PAIRED ? &bars->empty[i % NST] : &bars->full[i % NST], (i / NST) & 1u, dl);
+                    ptx::mbar_wait(&bars->full[i % NST], (i / NST) & 1u, dl);
             }
         } else if (warp == 2) {
             // -------------------------------------------------------- dependency warp --
@@ -499,7 +380,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     if (tile < 0)
                         break;
                     const BsView v = view(tile);
-                    if (v.phase == 2 && !v.null_half) {
+                    if (v.phase == 2) {
                         for (uint32_t i = 0;; ++i) {
                             if (ptx::ld_acquire_gpu(ws.l1_done + v.blk) >= l1_target)
                                 break;
@@ -518,8 +399,6 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             }
         } else if (warp == 1) {
             // -------------------------------------------------------- UMMA issuer -----
-            // (2-CTA mode: the even CTA issues every scale copy, UMMA and commit of the pair;
-            // the odd CTA's issuer only takes its tile slots)
             if (lane == 0) {
                 uint32_t it = 0, tcount = 0, acc_n = 0;
                 // scale groups copied so far: group g goes to TMEM slot g % NST, reused only after
@@ -528,7 +407,6 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 // to the B columns of the stage's slot, reused after the stage's next fill)
                 uint32_t gcount = 0, sfa = 0, sfb = 0;
                 bool ok = true;
-                const bool issuer = !PAIRED || rank == 0;
                 while (ok) {
                     const uint32_t slot = tcount % TILE_RING, sph = (tcount / TILE_RING) & 1u;
                     if (!ptx::mbar_wait(&bars->tile_full[slot], sph, deadline)) {
@@ -540,13 +418,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     ++tcount;
                     if (tile < 0)
                         break;
-                    if (!issuer)
-                        continue;
                     int phase, unit, nt;
                     tl.at(tile, phase, unit, nt);
                     const int nkb = phase == 1 ? NKB1 : NKB2;
                     // the previous tile's accumulator has been read by every epilogue warp
-                    // (of both CTAs in 2-CTA mode)
                     if (!ptx::mbar_wait(&bars->tempty, (acc_n & 1u) ^ 1u, deadline)) {
                         ok = false;
                         break;
@@ -563,37 +438,31 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                         if (kb % SF_GROUP == 0) {
                             sfa = tmem + SF_COL + 16 * (gcount % NST);
                             ++gcount;
-                            sf_copy<PAIRED>(sfa, ss);
+                            sf_copy(sfa, ss);
                             if constexpr (!FP4) {
                                 sfb = sfa + 4;
-                                sf_copy<PAIRED>(sfb, ss + SFA_BYTES);
-                                sf_copy<PAIRED>(sfb + 4, ss + SFA_BYTES + 512);
+                                sf_copy(sfb, ss + SFA_BYTES);
+                                sf_copy(sfb + 4, ss + SFA_BYTES + 512);
                             }
                         }
                         if constexpr (FP4) {
                             sfb = tmem + SF_COL + 16 * s + 4;
-                            sf_copy<PAIRED>(sfb, ss + SFA_BYTES);
-                            sf_copy<PAIRED>(sfb + 4, ss + SFA_BYTES + 512);
+                            sf_copy(sfb, ss + SFA_BYTES);
+                            sf_copy(sfb + 4, ss + SFA_BYTES + 512);
                         }
                         const uint32_t a_addr = ptx::smem_u32(smem + s * SBYTES);
                         const uint64_t adesc = ptx::kmajor_swizzled_desc<BKS>(a_addr);
                         const uint64_t bdesc = ptx::kmajor_swizzled_desc<BKS>(a_addr + STAGE_A_BYTES);
 #pragma unroll
                         for (int k = 0; k < BK / 32; ++k)   // +32 bytes along K = +2 in the >>4 field
-                            umma_bs<PAIRED>(tmem, adesc + 2 * k, bdesc + 2 * k,
-                                            idesc_bs<PAIRED ? 2 * BM : BM, FP4>(kb % SF_GROUP, FP4 ? k : kb % SF_GROUP),
-                                            sfa, sfb, (kb > 0 || k > 0) ? 1u : 0u);
-                        if constexpr (PAIRED)
-                            ptx::umma_commit_pair(&bars->empty[s], static_cast<uint16_t>(0x3));
-                        else
-                            ptx::umma_commit(&bars->empty[s]);
+                            umma_bs(tmem, adesc + 2 * k, bdesc + 2 * k,
+                                    idesc_bs<BM, FP4>(kb % SF_GROUP, FP4 ? k : kb % SF_GROUP), sfa, sfb,
+                                    (kb > 0 || k > 0) ? 1u : 0u);
+                        ptx::umma_commit(&bars->empty[s]);
                     }
                     if (!ok)
                         break;
-                    if constexpr (PAIRED)
-                        ptx::umma_commit_pair(&bars->tfull, static_cast<uint16_t>(0x3));
-                    else
-                        ptx::umma_commit(&bars->tfull);
+                    ptx::umma_commit(&bars->tfull);
                     ++acc_n;
                 }
                 if (!ok)
@@ -614,8 +483,6 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         const int row = q * 32 + lane;           // tile row = TMEM lane
         const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
         uint32_t tcount = 0, xcount = 0, acc_n = 0;
-        // TMEM-empty arrivals go to the even CTA's barrier in 2-CTA mode
-        const uint32_t tempty0 = PAIRED ? ptx::map_cluster(&bars->tempty, 0) : 0u;
         bool ok = true;
         while (ok) {
             const uint32_t slot = tcount % TILE_RING, sph = (tcount / TILE_RING) & 1u;
@@ -631,16 +498,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             if (tile < 0)
                 break;
             int phase, blk, nt;
-            bool null_half = false;
-            if constexpr (PAIRED) {
-                const BsView tv = view(tile);
-                phase = tv.phase;
-                blk = tv.blk;
-                nt = tv.nt;
-                null_half = tv.null_half;
-            } else {
-                tl.at(tile, phase, blk, nt);
-            }
+            tl.at(tile, phase, blk, nt);
             const long long prow = static_cast<long long>(blk) * BM + row;
             // the whole tile, already scaled, in one read of this warp's 32 rows x 128 columns
             if (!__all_sync(0xFFFFFFFFu, ptx::mbar_wait(&bars->tfull, acc_n & 1u, deadline))) {
@@ -649,16 +507,6 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             }
             ++acc_n;
             ptx::tc_fence_after();
-            if (null_half) {
-                // no rows of this CTA in this tile: the UMMA still wrote its accumulator, so
-                // hand it back unread (after the TMEM-full wait, which keeps both CTAs' arrivals
-                // for one tile in one phase of the even CTA's TMEM-empty barrier)
-                ptx::tc_fence_before();
-                __syncwarp();
-                if (lane == 0)
-                    ptx::mbar_arrive_cluster(tempty0);
-                continue;
-            }
             float acc[128];
             const uint32_t taddr = tmem + lane_base + wg * 128;
 #pragma unroll
@@ -676,12 +524,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             }
             ptx::tc_fence_before();
             __syncwarp();
-            if (lane == 0) {
-                if constexpr (PAIRED)
-                    ptx::mbar_arrive_cluster(tempty0);
-                else
-                    ptx::mbar_arrive(&bars->tempty);
-            }
+            if (lane == 0)
+                ptx::mbar_arrive(&bars->tempty);
             const int rows = ws.block_rows[blk];
             if (phase == 1) {
                 // SwiGLU on the 64 (gate, up) pairs of this row and column half, then 1x128
@@ -807,82 +651,30 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 
     ptx::tc_fence_before();
     __syncthreads();
-    if constexpr (PAIRED)
-        ptx::cluster_sync();   // the peer neither reads this CTA's stages nor writes its TMEM any more
     if (warp == 1) {
         ptx::tc_fence_after();
-        if constexpr (PAIRED)
-            ptx::tmem_dealloc_pair(tmem, TMEM_COLS);
-        else
-            ptx::tmem_dealloc(tmem, TMEM_COLS);
+        ptx::tmem_dealloc(tmem, TMEM_COLS);
     }
 }
 
-cudaError_t launch_ffn_bs(const FfnMaps &maps, const SfMaps &sf_maps, const Dims &d, const Workspace &ws,
-                          const CallArgs &c, const uint8_t *sfb1, const uint8_t *sfb2, int wave_blocks, int num_sms,
-                          bool paired, bool fp4, cudaStream_t s)
+cudaError_t launch_ffn_bs(const FfnMaps &maps, const Dims &d, const Workspace &ws, const CallArgs &c,
+                          const uint8_t *sfb1, const uint8_t *sfb2, int wave_blocks, int num_sms, bool fp4,
+                          cudaStream_t s)
 {
-    static int paired_grid = 0;
-    static int paired_coop = 1;   // cooperative attribute accepted together with clusters
-    constexpr int SMEM1 = 1024 + STAGES * STAGE_BYTES + 8192 + STAGES * SF_STAGE_BYTES;
-    constexpr int SMEM2 = 1024 + STAGES * STAGE_BYTES + 8192 + PAIR_STAGES * SF_STAGE_BYTES;
+    constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + 8192 + STAGES * SF_STAGE_BYTES;
     static_assert(sizeof(BsBars) <= 8192, "barrier block");
-    static_assert(SMEM2 <= 227 * 1024, "shared memory per CTA");
-    const int smem = paired ? SMEM2 : SMEM1;
-    void *kern = paired ? (fp4 ? reinterpret_cast<void *>(ffn_bs_kernel<true, true>)
-                               : reinterpret_cast<void *>(ffn_bs_kernel<true, false>))
-                        : (fp4 ? reinterpret_cast<void *>(ffn_bs_kernel<false, true>)
-                               : reinterpret_cast<void *>(ffn_bs_kernel<false, false>));
-    cudaError_t e0 = ensure_max_dynamic_smem(kern, smem);
+    static_assert(SMEM <= 227 * 1024, "shared memory per CTA");
+    void *kern = fp4 ? reinterpret_cast<void *>(ffn_bs_kernel<true>) : reinterpret_cast<void *>(ffn_bs_kernel<false>);
+    cudaError_t e0 = ensure_max_dynamic_smem(kern, SMEM);
     if (e0 != cudaSuccess)
         return e0;
-    FfnMaps m = maps;
-    SfMaps sm = sf_maps;
-    Dims dd = d;
-    Workspace ww = ws;
-    CallArgs cc = c;
-    const uint8_t *p1 = sfb1;
-    const uint8_t *p2 = sfb2;
-    int wb = wave_blocks;
-    void *args[] = {&m, &sm, &dd, &ww, &cc, &p1, &p2, &wb};
-    // down tiles wait on gate_up tiles of other CTAs: all CTAs must be resident at once
-    if (!paired)
-        return cudaLaunchCooperativeKernel(kern, dim3(num_sms), dim3(GEMM_THREADS), args, smem, s);
-
-    cudaLaunchAttribute attrs[2];
-    attrs[0].id = cudaLaunchAttributeClusterDimension;
-    attrs[0].val.clusterDim.x = 2;
-    attrs[0].val.clusterDim.y = 1;
-    attrs[0].val.clusterDim.z = 1;
-    attrs[1].id = cudaLaunchAttributeCooperative;
-    attrs[1].val.cooperative = 1;
-    cudaLaunchConfig_t cfg = {};
-    cfg.blockDim = dim3(GEMM_THREADS);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
-    cfg.attrs = attrs;
-    if (paired_grid == 0) {
-        // every cluster resident at once: as many clusters as can be active together
-        cfg.gridDim = dim3(num_sms);
-        cfg.numAttrs = 1;
-        int clusters = 0;
-        cudaError_t e = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
-        if (e != cudaSuccess)
-            return e;
-        if (clusters < 1)
-            return cudaErrorInvalidConfiguration;
-        paired_grid = 2 * std::min(clusters, num_sms / 2);
-    }
-    cfg.gridDim = dim3(paired_grid);
-    if (paired_coop) {
-        cfg.numAttrs = 2;
-        if (cudaLaunchKernelExC(&cfg, kern, args) == cudaSuccess)
-            return cudaSuccess;
-        cudaGetLastError();   // this runtime rejects cooperative + cluster: clusters alone
-        paired_coop = 0;
-    }
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelExC(&cfg, kern, args);
+    // Tiles are claimed in list order by running CTAs only, so the launch needs no
+    // co-residency guarantee: a down tile waits only on gate_up tiles claimed before it.
+    if (fp4)
+        ffn_bs_kernel<true><<<num_sms, GEMM_THREADS, SMEM, s>>>(maps, d, ws, c, sfb1, sfb2, wave_blocks);
+    else
+        ffn_bs_kernel<false><<<num_sms, GEMM_THREADS, SMEM, s>>>(maps, d, ws, c, sfb1, sfb2, wave_blocks);
+    return cudaGetLastError();
 }
 
 // ------------------------------------------------------------------ weight scales -----

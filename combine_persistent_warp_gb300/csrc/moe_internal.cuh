@@ -18,6 +18,7 @@ constexpr int BK = 128;            // K of one fp32 scale block = one TMEM parti
 constexpr int BKS = CPW_BKS;       // K (bytes of an FP8 operand row) per pipeline stage
 constexpr int SUBS = BK / BKS;     // pipeline stages per scale block
 constexpr int STAGES = 4 * BK / BKS;   // TMA -> UMMA ring depth (192 KB of operand tiles)
+constexpr int MAX_KB = 128;        // 128-deep K blocks of H and of I at most (H, I <= 16384)
 constexpr int GEMM_THREADS = 384;  // 4 producer/issuer warps + 2 epilogue warpgroups
 constexpr int DISPATCH_THREADS = 1024;
 constexpr int COMBINE_THREADS = 256;
@@ -26,7 +27,6 @@ static_assert(BKS == 32 || BKS == 64 || BKS == 128, "stage depth must match a sw
 constexpr int STAGE_A_BYTES = BM * BKS;                // 16 KB at BKS = 128
 constexpr int STAGE_B_BYTES = BN * BKS;                // 32 KB at BKS = 128
 constexpr int STAGE_BYTES = STAGE_A_BYTES + STAGE_B_BYTES;
-constexpr int GEMM_SMEM_BYTES = 1024 /*align slack*/ + STAGES * STAGE_BYTES + 8192 /*bars etc*/;
 
 // 32-bit words of the workspace header; hot words sit on separate 128-byte lines.
 enum HdrWord : int {
@@ -101,31 +101,20 @@ constexpr int A_ROWS_PART = 32;   // row granularity of partial A-tile loads
 struct FfnMaps {
     CUtensorMap a1, b1, a2, b2;   // pool x / W1 tiles (gate_up), act / W2 tiles (down)
     CUtensorMap a1p, a2p;         // pool x / act with 32-row boxes (partly filled M-blocks)
-    CUtensorMap b1h, b2h;         // W1 / W2 tiles with 128-row boxes (half tiles, 2-CTA mode)
 };
-// paired: 2-CTA clusters, one cta_group::2 UMMA over two M-blocks of an expert, each CTA
-// loading its own A rows and one half of the weight tile; otherwise one CTA per tile with a
-// dynamic tile counter.
+// the fp32-scale FFN kernel (ffn.cu): one CTA per SM, tiles claimed in list order
 cudaError_t launch_ffn(const FfnMaps &maps, const Dims &d, const Workspace &ws, const CallArgs &c,
-                       const float *sf1, const float *sf2, int wave_blocks, int num_sms, bool paired,
-                       cudaStream_t s);
+                       const float *sf1, const float *sf2, int wave_blocks, int num_sms, cudaStream_t s);
 #ifdef CPW_TRACE
 cudaError_t trace_read(void *dst, size_t bytes);
 cudaError_t trace_clear();
 #endif
-// UE8M0 scale blocks as 2-D byte maps of 256-byte rows (no swizzle): sfa1 / sfa2 over the
-// pool / act scale blocks with 2-row boxes (512 B, one M-block and K block), sfb1 / sfb2 over
-// the weight tiles' scale blocks with 4-row boxes (1 KB, one weight tile and K block)
-struct SfMaps {
-    CUtensorMap sfa1, sfa2, sfb1, sfb2;
-};
 // power-of-two scales: the block-scaled FFN kernel (ffn_bs.cu) and the load-time UE8M0
-// scale blocks of the weight tiles; paired: 2-CTA clusters (one M = 256 UMMA per block pair);
-// fp4: MXFP4 weight tiles (packed E2M1, maps of the 16U4_ALIGN16B type) with per-K-block
-// scale blocks
-cudaError_t launch_ffn_bs(const FfnMaps &maps, const SfMaps &sf_maps, const Dims &d, const Workspace &ws,
-                          const CallArgs &c, const uint8_t *sfb1, const uint8_t *sfb2, int wave_blocks, int num_sms,
-                          bool paired, bool fp4, cudaStream_t s);
+// scale blocks of the weight tiles; fp4: MXFP4 weight tiles (packed E2M1, maps of the
+// 16U4_ALIGN16B type) with per-K-block scale blocks
+cudaError_t launch_ffn_bs(const FfnMaps &maps, const Dims &d, const Workspace &ws, const CallArgs &c,
+                          const uint8_t *sfb1, const uint8_t *sfb2, int wave_blocks, int num_sms, bool fp4,
+                          cudaStream_t s);
 cudaError_t launch_build_sfb(const float *s, uint8_t *dst, int E, int N, int K, int gate_up_I, uint32_t *bad,
                              cudaStream_t st);
 cudaError_t launch_build_sfb4(const uint8_t *s, uint8_t *dst, int E, int N, int K, int gate_up_I, uint32_t *bad,

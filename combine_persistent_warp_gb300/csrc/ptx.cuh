@@ -107,18 +107,6 @@ __device__ __forceinline__ void red_release_add(uint32_t *p, uint32_t v)
     asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
-// 2-D tiled load into this CTA's shared memory whose completion is counted on an mbarrier
-// of either CTA of the pair (`bar_cluster` is a shared::cluster address, e.g. the leader
-// CTA's barrier from map_cluster), for the two-CTA UMMA.
-__device__ __forceinline__ void tma_load_2d_pair(void *smem_dst, const CUtensorMap *map, uint32_t bar_cluster,
-                                                 int32_t x, int32_t y, uint64_t cache_hint)
-{
-    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-                 ".cta_group::2.L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(smem_dst)),
-                 "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y), "l"(cache_hint)
-                 : "memory");
-}
-
 // Untiled bulk copy global -> this CTA's shared memory, counted on `bar` (both addresses
 // 16-byte aligned, size a multiple of 16 bytes).
 __device__ __forceinline__ void bulk_load(void *smem_dst, const void *gsrc, uint32_t bytes, uint64_t *bar)
@@ -127,43 +115,6 @@ __device__ __forceinline__ void bulk_load(void *smem_dst, const void *gsrc, uint
                      smem_u32(smem_dst)),
                  "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(smem_u32(bar))
                  : "memory");
-}
-
-__device__ __forceinline__ uint32_t cluster_ctarank()
-{
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
-// Shared-memory address of the same variable in CTA `rank` of the cluster.
-__device__ __forceinline__ uint32_t map_cluster(const void *p, uint32_t rank)
-{
-    uint32_t a;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_u32(p)), "r"(rank));
-    return a;
-}
-__device__ __forceinline__ int ld_cluster_s32(uint32_t cluster_addr)
-{
-    int v;
-    asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
-    return v;
-}
-
-// Arrive on an mbarrier given by its shared::cluster address (e.g. the peer CTA's), with
-// the default semantics.  Used where the arrival only signals that TMEM columns have been
-// read (tcgen05.wait::ld + tcgen05.fence::before_thread_sync order those reads before it),
-// so no cluster-scope release fence is paid per arrival.
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster)
-{
-    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
-}
-
-// Every thread of every CTA of the cluster arrives and waits (release / acquire).
-__device__ __forceinline__ void cluster_sync()
-{
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
-                     : "memory");
 }
 
 // L2 cache policies (createpolicy): keep re-read operands, stream once-read ones.
@@ -203,24 +154,6 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
                  : "memory");
 }
-// Two-CTA (cta_group::2) forms: one warp of EACH CTA of the pair executes alloc,
-// relinquish and dealloc together; the allocation is made in both CTAs' TMEM.
-__device__ __forceinline__ void tmem_alloc_pair(uint32_t *dst_smem, uint32_t ncols)
-{
-    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                     smem_u32(dst_smem)),
-                 "r"(ncols)
-                 : "memory");
-}
-__device__ __forceinline__ void tmem_relinquish_pair()
-{
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols)
-{
-    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-                 : "memory");
-}
 __device__ __forceinline__ void tc_fence_before()
 {
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -248,38 +181,6 @@ __device__ __forceinline__ void umma_commit(uint64_t *bar)
         "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
             smem_u32(bar))
         : "memory");
-}
-
-// As umma_commit, arriving on the mbarrier at `bar`'s offset in every CTA of `cta_mask`.
-__device__ __forceinline__ void umma_commit_multicast(uint64_t *bar, uint16_t cta_mask)
-{
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-                 " [%0], %1;" ::"r"(smem_u32(bar)),
-                 "h"(cta_mask)
-                 : "memory");
-}
-
-// Two-CTA UMMA, issued by the even CTA of the pair: D (M = 256 rows, 128 in each CTA's
-// TMEM at the same address) (+)= A x B^T, where each CTA holds 128 rows of A and half of
-// B's N rows at the same shared-memory offsets the descriptors give.
-__device__ __forceinline__ void umma_f8_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                             uint32_t idesc, uint32_t accumulate)
-{
-    asm volatile("{\n\t.reg .pred p;\n\t"
-                 "setp.ne.b32 p, %4, 0;\n\t"
-                 "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-                 "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-                 : "memory");
-}
-
-// Arrive once on the mbarrier at `bar`'s offset in every CTA of `cta_mask` when every
-// two-CTA tcgen05 operation issued so far by this thread is done.
-__device__ __forceinline__ void umma_commit_pair(uint64_t *bar, uint16_t cta_mask)
-{
-    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-                 " [%0], %1;" ::"r"(smem_u32(bar)),
-                 "h"(cta_mask)
-                 : "memory");
 }
 
 // Shared-memory matrix descriptor of a K-major operand whose rows are ROW_BYTES (32, 64 or

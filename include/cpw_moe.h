@@ -60,9 +60,10 @@ enum moe_status {
 
 /* Create a layer for E experts, hidden size H, expert intermediate size I, top-k, and R
  * logical source partitions (the layer object the pages' Python API builds before its
- * forward: "DeepGEMM Mega MoE 对称内存（Symmetric Memory）深度分析" §10.1).  Requires H % 256 == 0, I % 128 == 0, 1 <= topk <= 32,
- * topk <= E <= 1024, 1 <= R <= 64, E*R <= 16384, on the current device, which must be
- * sm_103.  Allocates no device memory.  *out receives the handle. */
+ * forward: "DeepGEMM Mega MoE 对称内存（Symmetric Memory）深度分析" §10.1).  Requires
+ * H % 128 == 0, I % 128 == 0, H <= 16384, I <= 16384, 1 <= topk <= 32, topk <= E <= 1024,
+ * 1 <= R <= 64, E*R <= 16384, on the current device, which must be sm_103.  Allocates no
+ * device memory.  *out receives the handle. */
 int moe_create(int E, int H, int I, int topk, int R, moe_handle_t *out);
 
 /* As moe_create, with n_shared shared experts besides the E routed ones ("DeepGEMM Mega MoE
@@ -211,9 +212,8 @@ int moe_get_info(moe_handle_t h, moe_info *info);
  * MOE_OPT_DEBUG_SKIP_BARRIER: when 1, one CTA of the routing kernel skips its arrival
  * at the grid barrier, so the others give up after the time limit and the forward
  * ends with MOE_ERR_TIMEOUT (failure-path test; never on in normal use);
- * MOE_OPT_FFN_MODE: how the expert FFN kernel covers its tiles: 0 = automatic (default),
- * 1 = one CTA per 128-row tile, 2 = pairs of CTAs (a cluster) on two M-blocks of one expert
- * with one 256-row two-CTA UMMA.  All modes compute the same result;
+ * MOE_OPT_FFN_MODE: how the expert FFN kernel covers its tiles: 0 = automatic (default) and
+ * 1 = one CTA per 128-row tile, which are the same kernel; other values are refused;
  * MOE_OPT_SCALE_MODE: 0 = arbitrary fp32 block scales (the UMMA accumulates each 128-deep
  * K block in TMEM and the scales are applied on the CUDA cores); 1 = every scale (x_sf, both
  * weight scale tensors) is a power of two: the UMMA applies them itself as UE8M0 scale

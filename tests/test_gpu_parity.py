@@ -308,28 +308,23 @@ def test_barrier_timeout_is_reported_then_recovers():
     run_and_compare(moe, inp, inp.topk_idx, inp.topk_w, 64)
 
 
-# ----------------------------------------------------------------- FFN kernel modes -----
-def test_ffn_modes_agree_and_match_oracle():
-    """One CTA per tile vs. 2-CTA clusters (one 256-row cta_group::2 UMMA over two
-    M-blocks): same bits, within tolerance of the oracle, including experts with an odd
-    M-block count (the second CTA of their last pair has no rows and only supplies its
-    weight half)."""
+# ----------------------------------------------------------------- FFN kernel mode -----
+def test_multi_block_experts_and_mode_values():
+    """Experts with 1-3 M-blocks (odd counts among them), every token against the oracle;
+    MOE_OPT_FFN_MODE takes 0 (automatic) and 1 (one CTA per tile), the same kernel, and
+    refuses anything else."""
     T = 1024
     moe, inp = tiny_layer(T_max=T, E=8, H=256, I=256, k=2, R=2, seed=33)
     counts, _, _ = oracle.route_counts(inp.topk_idx, 8, 2)
     blocks = -(-counts.astype(np.int64) // 128)
     assert np.any(blocks % 2 == 1) and np.any(blocks >= 2)
     outs = []
-    for mode in (1, 2):
+    for mode in (0, 1):
         moe.set_option(native.OPT_FFN_MODE, mode)
         out, _ = run_and_compare(moe, inp, inp.topk_idx, inp.topk_w, T)
         outs.append(out.clone())
     assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
-
-
-def test_paired_mode_with_single_block_experts():
-    """2-CTA mode forced on a batch where every expert has one M-block: every pair has a
-    null half."""
-    moe, inp = tiny_layer()
-    moe.set_option(native.OPT_FFN_MODE, 2)
-    run_and_compare(moe, inp, inp.topk_idx, inp.topk_w, 64)
+    for bad in (-1, 2):
+        with pytest.raises(MoeError) as ei:
+            moe.set_option(native.OPT_FFN_MODE, bad)
+        assert ei.value.code == 1

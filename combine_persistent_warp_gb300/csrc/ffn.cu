@@ -158,40 +158,50 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     FfnBars *bars = reinterpret_cast<FfnBars *>(smem + STAGES * STAGE_BYTES);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+    // prologue (barriers, TMEM, tensor maps) while the routing kernel may still run
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            ptx::mbar_init(&bars->full[s], 1);
+            ptx::mbar_init(&bars->empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(&bars->tfull[b], 1);
+            ptx::mbar_init(&bars->tempty[b], EPI_WARPS);
+        }
+        ptx::mbar_init(&bars->xbar, 32 * EPI_WARPS);       // every epilogue thread
+        for (int i = 0; i < TILE_RING; ++i) {
+            ptx::mbar_init(&bars->tile_full[i], 1);
+            ptx::mbar_init(&bars->tile_empty[i], 3 + EPI_WARPS);
+            ptx::mbar_init(&bars->meta_ready[i], 1);
+            ptx::mbar_init(&bars->act_done[i], EPI_WARPS);
+        }
+        ptx::fence_mbar_init();
+    } else if (threadIdx.x == 32) {
+        ptx::prefetch_tmap(&maps.a1);
+        ptx::prefetch_tmap(&maps.b1);
+        ptx::prefetch_tmap(&maps.a2);
+        ptx::prefetch_tmap(&maps.b2);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(&bars->tmem_base, TMEM_COLS);
+        ptx::tmem_relinquish();
+    }
+    // the routing kernel's results are complete and visible past this point
+    ptx::grid_dependency_wait();
     if (threadIdx.x == 0) {
         const uint32_t err = *reinterpret_cast<volatile uint32_t *>(ws.hdr + HDR_ERR_CALL) |
                              *reinterpret_cast<volatile uint32_t *>(ws.hdr + HDR_ERR_STICKY);
         bars->abort = err != 0;
-        if (!err) {
-            for (int s = 0; s < STAGES; ++s) {
-                ptx::mbar_init(&bars->full[s], 1);
-                ptx::mbar_init(&bars->empty[s], 1);
-            }
-            for (int b = 0; b < 2; ++b) {
-                ptx::mbar_init(&bars->tfull[b], 1);
-                ptx::mbar_init(&bars->tempty[b], EPI_WARPS);
-            }
-            ptx::mbar_init(&bars->xbar, 32 * EPI_WARPS);       // every epilogue thread
-            for (int i = 0; i < TILE_RING; ++i) {
-                ptx::mbar_init(&bars->tile_full[i], 1);
-                ptx::mbar_init(&bars->tile_empty[i], 3 + EPI_WARPS);
-                ptx::mbar_init(&bars->meta_ready[i], 1);
-                ptx::mbar_init(&bars->act_done[i], EPI_WARPS);
-            }
-            ptx::fence_mbar_init();
-        }
-    }
-    __syncthreads();
-    if (bars->abort)
-        return;
-    if (warp == 1) {
-        ptx::tmem_alloc(&bars->tmem_base, TMEM_COLS);
-        ptx::tmem_relinquish();
     }
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
+    if (bars->abort) {   // a device error earlier in this forward: nothing to do
+        if (warp == 1)
+            ptx::tmem_dealloc(tmem, TMEM_COLS);
+        return;
+    }
 
     const TileList tl{(2 * d.I) / BN, (d.H + BN - 1) / BN, ws.blk_off[d.E], wave_blocks};
     const int ntiles = tl.total();
@@ -210,10 +220,6 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         if (warp == 0) {
             // -------------------------------------------------------- TMA producer ----
             if (lane == 0) {
-                ptx::prefetch_tmap(&maps.a1);
-                ptx::prefetch_tmap(&maps.b1);
-                ptx::prefetch_tmap(&maps.a2);
-                ptx::prefetch_tmap(&maps.b2);
                 const uint64_t pol_a = ptx::policy_evict_last();
                 const uint64_t pol_b_once = ptx::policy_evict_first();    // read by one block
                 const uint64_t pol_b_shared = ptx::policy_evict_normal(); // read by several
@@ -779,8 +785,8 @@ cudaError_t launch_ffn(const FfnMaps &maps, const Dims &d, const Workspace &ws, 
     cudaError_t e0 = ensure_max_dynamic_smem(reinterpret_cast<const void *>(ffn_kernel), FFN_SMEM_BYTES);
     if (e0 != cudaSuccess)
         return e0;
-    ffn_kernel<<<num_sms, GEMM_THREADS, FFN_SMEM_BYTES, s>>>(maps, d, ws, c, sf1, sf2, wave_blocks);
-    return cudaGetLastError();
+    return launch_programmatic(ffn_kernel, num_sms, GEMM_THREADS, FFN_SMEM_BYTES, s, maps, d, ws, c, sf1, sf2,
+                               wave_blocks);
 }
 
 }  // namespace cpw

@@ -161,37 +161,47 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     uint8_t *sf_smem = smem + STAGES * STAGE_BYTES + 8192;   // [NST][A 512 | B 1024]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+    // prologue (barriers, TMEM, tensor maps) while the routing kernel may still run
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NST; ++s) {
+            ptx::mbar_init(&bars->full[s], 1);
+            ptx::mbar_init(&bars->empty[s], 1);
+        }
+        ptx::mbar_init(&bars->tfull, 1);
+        ptx::mbar_init(&bars->tempty, EPI_WARPS);
+        ptx::mbar_init(&bars->xbar, 32 * EPI_WARPS);
+        for (int i = 0; i < TILE_RING; ++i) {
+            ptx::mbar_init(&bars->tile_full[i], 1);
+            ptx::mbar_init(&bars->tile_empty[i], 2 + EPI_WARPS);   // issuer, dependency warp, epilogue
+            ptx::mbar_init(&bars->dep[i], 1);
+        }
+        ptx::fence_mbar_init();
+    } else if (threadIdx.x == 32) {
+        ptx::prefetch_tmap(&maps.a1);
+        ptx::prefetch_tmap(&maps.b1);
+        ptx::prefetch_tmap(&maps.a2);
+        ptx::prefetch_tmap(&maps.b2);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(&bars->tmem_base, TMEM_COLS);
+        ptx::tmem_relinquish();
+    }
+    // the routing kernel's results are complete and visible past this point
+    ptx::grid_dependency_wait();
     if (threadIdx.x == 0) {
         const uint32_t err = *reinterpret_cast<volatile uint32_t *>(ws.hdr + HDR_ERR_CALL) |
                              *reinterpret_cast<volatile uint32_t *>(ws.hdr + HDR_ERR_STICKY);
         bars->abort = err != 0;
-        if (!err) {
-            for (int s = 0; s < NST; ++s) {
-                ptx::mbar_init(&bars->full[s], 1);
-                ptx::mbar_init(&bars->empty[s], 1);
-            }
-            ptx::mbar_init(&bars->tfull, 1);
-            ptx::mbar_init(&bars->tempty, EPI_WARPS);
-            ptx::mbar_init(&bars->xbar, 32 * EPI_WARPS);
-            for (int i = 0; i < TILE_RING; ++i) {
-                ptx::mbar_init(&bars->tile_full[i], 1);
-                ptx::mbar_init(&bars->tile_empty[i], 2 + EPI_WARPS);   // issuer, dependency warp, epilogue
-                ptx::mbar_init(&bars->dep[i], 1);
-            }
-            ptx::fence_mbar_init();
-        }
-    }
-    __syncthreads();
-    if (bars->abort)
-        return;
-    if (warp == 1) {
-        ptx::tmem_alloc(&bars->tmem_base, TMEM_COLS);
-        ptx::tmem_relinquish();
     }
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
+    if (bars->abort) {   // a device error earlier in this forward: nothing to do
+        if (warp == 1)
+            ptx::tmem_dealloc(tmem, TMEM_COLS);
+        return;
+    }
 
     const BsTiles tl{(2 * d.I) / BN, (d.H + BN - 1) / BN, ws.blk_off[d.E], wave_blocks};
     const int ntiles = tl.total();
@@ -218,10 +228,6 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         if (warp == 0) {
             // -------------------------------------------------------- TMA producer ----
             if (lane == 0) {
-                ptx::prefetch_tmap(&maps.a1);
-                ptx::prefetch_tmap(&maps.b1);
-                ptx::prefetch_tmap(&maps.a2);
-                ptx::prefetch_tmap(&maps.b2);
                 const uint64_t pol_a = ptx::policy_evict_last();
                 const uint64_t pol_b_once = ptx::policy_evict_first();
                 const uint64_t pol_b_shared = ptx::policy_evict_normal();
@@ -670,11 +676,10 @@ cudaError_t launch_ffn_bs(const FfnMaps &maps, const Dims &d, const Workspace &w
         return e0;
     // Tiles are claimed in list order by running CTAs only, so the launch needs no
     // co-residency guarantee: a down tile waits only on gate_up tiles claimed before it.
-    if (fp4)
-        ffn_bs_kernel<true><<<num_sms, GEMM_THREADS, SMEM, s>>>(maps, d, ws, c, sfb1, sfb2, wave_blocks);
-    else
-        ffn_bs_kernel<false><<<num_sms, GEMM_THREADS, SMEM, s>>>(maps, d, ws, c, sfb1, sfb2, wave_blocks);
-    return cudaGetLastError();
+    return fp4 ? launch_programmatic(ffn_bs_kernel<true>, num_sms, GEMM_THREADS, SMEM, s, maps, d, ws, c, sfb1, sfb2,
+                                     wave_blocks)
+               : launch_programmatic(ffn_bs_kernel<false>, num_sms, GEMM_THREADS, SMEM, s, maps, d, ws, c, sfb1,
+                                     sfb2, wave_blocks);
 }
 
 // ------------------------------------------------------------------ weight scales -----

@@ -93,6 +93,25 @@ __device__ __forceinline__ void record_error(uint32_t *hdr, uint32_t code)
 // (thread-safe; defined in api.cu).
 cudaError_t ensure_max_dynamic_smem(const void *kernel, int bytes);
 
+// Launch with programmatic stream serialization: the kernel may start while the previous
+// kernel of the stream still runs, and must call ptx::grid_dependency_wait() before it reads
+// anything that kernel writes.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_programmatic(void (*kern)(KArgs...), int grid, int block, int smem, cudaStream_t s, Args... args)
+{
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(static_cast<unsigned>(block));
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 // Launchers (one per translation unit).
 size_t dispatch_smem_bytes(const Dims &d);
 cudaError_t launch_dispatch(const Dims &d, const Workspace &ws, const CallArgs &c, int num_sms,

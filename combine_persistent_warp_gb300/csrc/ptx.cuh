@@ -96,6 +96,21 @@ __device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap *map, int32
                  : "memory");
 }
 
+// Programmatic dependent launch: a kernel launched with the programmatic-serialization
+// attribute may start while the previous kernel of its stream still runs; it waits here until
+// that kernel has completed and its memory operations are visible (a no-op in a kernel launched
+// without the attribute).  launch_dependents lets the next such kernel start once every CTA of
+// this grid has executed it or exited.
+__device__ __forceinline__ void grid_dependency_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Order this thread's generic-proxy global accesses with its async-proxy (TMA) ones.
 __device__ __forceinline__ void fence_proxy_async_global()
 {

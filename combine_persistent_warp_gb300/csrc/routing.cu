@@ -38,6 +38,9 @@ __global__ void __launch_bounds__(DISPATCH_THREADS, 1)
     int32_t *blk = cum + (E + 1);
     volatile int *s_ok = reinterpret_cast<volatile int *>(blk + (E + 1));
 
+    // the expert FFN kernel may be scheduled at once: its CTAs run their prologue as this
+    // kernel's CTAs leave and then wait for the whole grid
+    ptx::launch_dependents();
     // A forward after an unreported device error does nothing (every CTA sees the same
     // sticky word: nothing writes it while this kernel runs).
     if (*reinterpret_cast<volatile uint32_t *>(ws.hdr + HDR_ERR_STICKY) != 0)
@@ -186,6 +189,8 @@ cudaError_t launch_combine(const Dims &d, const Workspace &ws, const CallArgs &c
                            cudaStream_t s)
 {
     // two CTAs per SM (128 registers a thread keep 16 plane loads in flight), all resident
+    // an ordinary launch: letting it start during the FFN kernel's last tiles (programmatic
+    // launch) measured 1.3% slower on the large batch and about 1 us faster at decode
     combine_kernel<<<num_sms * 2, COMBINE_THREADS, 0, s>>>(d, ws, c);
     return cudaGetLastError();
 }

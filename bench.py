@@ -49,12 +49,9 @@ PROFILE_EVERY = 8            # timed steps per step carrying the per-kernel stag
 # DRAM bytes per launch from one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum),
 # valid only while the kernel sources hash to `src_sha`; see profiles/.
 NCU_TRAFFIC = {
-    ("decode", "expert_ffn"): {"bytes": 1425256448 + 14529792, "src_sha": "fbc87d810249e61e"},
-    ("prefill", "expert_ffn"): {"bytes": 1892651264 + 534686208, "src_sha": "fbc87d810249e61e"},
-    ("decode-pow2", "expert_ffn"): {"bytes": 1431475200 + 3602944, "src_sha": "471a697d4cd814f3"},
-    ("prefill-pow2", "expert_ffn"): {"bytes": 2108371200 + 514178816, "src_sha": "471a697d4cd814f3"},
-    ("decode-mxfp4", "expert_ffn"): {"bytes": 759860224 + 3274752, "src_sha": "471a697d4cd814f3"},
-    ("prefill-mxfp4", "expert_ffn"): {"bytes": 1060229888 + 511471872, "src_sha": "471a697d4cd814f3"},
+    ("large", "expert_ffn"): {"bytes": 3243730432 + 1251801856, "src_sha": "6fe2a4bbcd371c1c"},
+    ("prefill", "expert_ffn"): {"bytes": 2015524096 + 517387008, "src_sha": "6fe2a4bbcd371c1c"},
+    ("decode", "expert_ffn"): {"bytes": 1420979712 + 4059136, "src_sha": "6fe2a4bbcd371c1c"},
 }
 # sources each stage's kernel is compiled from (a recorded traffic figure is used only while
 # these hash to its `src_sha`)

@@ -49,9 +49,9 @@ PROFILE_EVERY = 8            # timed steps per step carrying the per-kernel stag
 # DRAM bytes per launch from one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum),
 # valid only while the kernel sources hash to `src_sha`; see profiles/.
 NCU_TRAFFIC = {
-    ("large", "expert_ffn"): {"bytes": 3243730432 + 1251801856, "src_sha": "6fe2a4bbcd371c1c"},
-    ("prefill", "expert_ffn"): {"bytes": 2015524096 + 517387008, "src_sha": "6fe2a4bbcd371c1c"},
-    ("decode", "expert_ffn"): {"bytes": 1420979712 + 4059136, "src_sha": "6fe2a4bbcd371c1c"},
+    ("large", "expert_ffn"): {"bytes": 3244002304 + 1255044352, "src_sha": "082697d8f8939f39"},
+    ("prefill", "expert_ffn"): {"bytes": 2001494272 + 520432640, "src_sha": "082697d8f8939f39"},
+    ("decode", "expert_ffn"): {"bytes": 1420967168 + 5966592, "src_sha": "082697d8f8939f39"},
 }
 # sources each stage's kernel is compiled from (a recorded traffic figure is used only while
 # these hash to its `src_sha`)

@@ -457,6 +457,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                         }
                         // the other lanes' reads below are ordered after lane 0's acquire by the
                         // warp barrier
+                        __syncwarp();
                         if (!__shfl_sync(0xFFFFFFFFu, ready, 0)) {
                             ok = false;
                             break;

@@ -49,26 +49,30 @@ PROFILE_EVERY = 8            # timed steps per step carrying the per-kernel stag
 # DRAM bytes per launch from one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum),
 # valid only while the kernel sources hash to `src_sha`; see profiles/.
 NCU_TRAFFIC = {
-    ("large", "expert_ffn"): {"bytes": 3244002304 + 1255044352, "src_sha": "082697d8f8939f39"},
-    ("prefill", "expert_ffn"): {"bytes": 2001494272 + 520432640, "src_sha": "082697d8f8939f39"},
-    ("decode", "expert_ffn"): {"bytes": 1420967168 + 5966592, "src_sha": "082697d8f8939f39"},
+    ("large", "expert_ffn"): {"bytes": 3243558400 + 1255286016, "src_sha": "13d73c603fb41646"},
+    ("decode", "expert_ffn"): {"bytes": 1421092864 + 5978880, "src_sha": "13d73c603fb41646"},
+    ("prefill", "expert_ffn"): {"bytes": 1981654528 + 520409344, "src_sha": "13d73c603fb41646"},
 }
 # sources each stage's kernel is compiled from (a recorded traffic figure is used only while
 # these hash to its `src_sha`)
 KERNEL_SOURCES = {
     "expert_ffn": ["combine_persistent_warp_gb300/csrc/ffn.cu",
                    "combine_persistent_warp_gb300/csrc/ptx.cuh",
-                   "combine_persistent_warp_gb300/csrc/moe_internal.cuh"],
+                   "combine_persistent_warp_gb300/csrc/moe_internal.cuh",
+                   "combine_persistent_warp_gb300/csrc/topk_combine.cuh"],
     # power-of-two scales: the expert FFN stage runs the block-scaled kernel
     "expert_ffn_bs": ["combine_persistent_warp_gb300/csrc/ffn_bs.cu",
                       "combine_persistent_warp_gb300/csrc/ptx.cuh",
-                      "combine_persistent_warp_gb300/csrc/moe_internal.cuh"],
+                      "combine_persistent_warp_gb300/csrc/moe_internal.cuh",
+                      "combine_persistent_warp_gb300/csrc/topk_combine.cuh"],
     "dispatch": ["combine_persistent_warp_gb300/csrc/routing.cu",
                  "combine_persistent_warp_gb300/csrc/route_device.cuh",
                  "combine_persistent_warp_gb300/csrc/ptx.cuh",
-                 "combine_persistent_warp_gb300/csrc/moe_internal.cuh"],
+                 "combine_persistent_warp_gb300/csrc/moe_internal.cuh",
+                 "combine_persistent_warp_gb300/csrc/topk_combine.cuh"],
     "combine": ["combine_persistent_warp_gb300/csrc/routing.cu",
-                "combine_persistent_warp_gb300/csrc/moe_internal.cuh"],
+                "combine_persistent_warp_gb300/csrc/moe_internal.cuh",
+                "combine_persistent_warp_gb300/csrc/topk_combine.cuh"],
 }
 
 KERNEL_FN = {"expert_ffn": "ffn_kernel", "expert_ffn_bs": "ffn_bs_kernel", "dispatch": "dispatch_kernel",
@@ -419,6 +423,15 @@ def bench_config(name: str, args, dist: Dist, steps: int, warmup: int, *, e2e_st
         moe.set_option(native.OPT_FFN_MODE, args.ffn_mode)
     if wl.scales == "pow2":   # power-of-two scales: the hardware block-scaled path
         moe.set_option(native.OPT_SCALE_MODE, 1)
+    # the automatic mode runs the combine inside the FFN kernel only for an output in pinned host
+    # memory: the end-to-end loop below, not the device-buffer loop
+    in_ffn = args.combine == "in-ffn"
+    moe.set_option(native.OPT_COMBINE_MODE, {"kernel": native.COMBINE_KERNEL, "in-ffn": native.COMBINE_IN_FFN,
+                                             "auto": native.COMBINE_AUTO}[args.combine])
+    if in_ffn:
+        # the FFN kernel also reads the bf16 planes back and writes the output
+        model["stages"]["expert_ffn"]["bytes"] += model["stages"]["combine"]["bytes"]
+        model["stages"]["expert_ffn"]["flops"] += model["stages"]["combine"]["flops"]
     out = torch.empty(wl.T, wl.H, dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream(dev)
     flush = needs_l2_flush(model)
@@ -461,18 +474,23 @@ def bench_config(name: str, args, dist: Dist, steps: int, warmup: int, *, e2e_st
     if moe.get_error() != 0:
         raise RuntimeError(f"{name}: device error during the timed region")
     value, t_max = aggregate(M * steps, local_s, dist)
-    stage_ms = prof["stage_ms"]
+    stage_ms = dict(prof["stage_ms"])
+    if in_ffn:
+        stage_ms.pop("combine", None)   # no combine launch: its events only bracket nothing
     calls = max(1, prof["calls"])
     dominant = max(stage_ms, key=stage_ms.get)
     res = {
         "value": value, "unit": UNIT, "steps": steps, "warmup": warmup,
         "ms_per_step": t_max / steps * 1e3,
         "config": config_of(wl, model, dist.world, flush),
+        "combine": {"device_buffers": "inside the expert FFN kernel" if in_ffn else "separate kernel",
+                    "host_buffers": ("separate kernel" if args.combine == "kernel"
+                                     else "inside the expert FFN kernel")},
         "roofline": roofline_for(dominant, stage_ms[dominant] / calls / 1e3, model, wl.name, fp8_measured),
         "layer_roofline": layer_roofline(model, t_max / steps, fp8_measured),
         "stages_us_per_launch": {k: v / calls * 1e3 for k, v in stage_ms.items()},
         "stage_events": {"every_nth_step": 1 if flush else PROFILE_EVERY, "steps_with_events": prof["calls"]},
-        "gpu_launches": 3 * steps,
+        "gpu_launches": (2 if in_ffn else 3) * steps,
         "dtype": ("fp8e4m3 x e2m1 (MXFP4 weights; fp32 accumulate, bf16 out)" if wl.weights == "mxfp4"
                   else "fp8e4m3 (fp32 accumulate, bf16 out)"),
     }
@@ -545,7 +563,7 @@ def run_ours(args, dist: Dist) -> dict | None:
         "dtype": head["dtype"], "data": "synthetic", "config": head["config"],
         "e2e": head["e2e"], "gpu_launches": head["gpu_launches"], "roofline": head["roofline"],
         "layer_roofline": head["layer_roofline"], "stages_us_per_launch": head["stages_us_per_launch"],
-        "stage_events": head["stage_events"], "clocks": head.get("clocks"),
+        "stage_events": head["stage_events"], "clocks": head.get("clocks"), "combine": head["combine"],
         "fp8_gemm_tflops_measured": fp8_tflops,
     }
     if "cpu_baseline" in head:
@@ -653,6 +671,9 @@ def main(argv=None):
     ap.add_argument("--no-fp8-peak", action="store_true")
     ap.add_argument("--ffn-mode", type=int, default=0,
                     help="expert FFN kernel mode: 0 automatic, 1 one CTA per tile")
+    ap.add_argument("--combine", choices=["auto", "kernel", "in-ffn"], default="auto",
+                    help="top-k combine: a separate kernel, inside the expert FFN kernel, or automatic "
+                         "(inside it for an output in pinned host memory)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

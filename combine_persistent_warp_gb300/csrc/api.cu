@@ -97,6 +97,7 @@ struct moe_ctx {
     long long timeout_ns = 2000000000LL;
     int debug_skip_barrier = 0;
     int ffn_mode = 0;            // 0 automatic, 1 one CTA per tile (the same kernel)
+    int combine_mode = 2;        // 0 separate combine kernel, 1 inside the FFN kernel, 2 automatic
     int scale_mode = 2;          // 0 fp32 scales, 1 power-of-two scales (block-scaled UMMA),
                                  // 2 block-scaled exactly when the weights' scales are 2^k
     // stage profiling (events on the forward's stream)
@@ -221,6 +222,8 @@ size_t carve_big(moe_ctx *h, char *base, int max_tokens, Workspace &ws)
     ws.block_rows = c.take<int32_t>(max_blocks);
     ws.arrive = c.take<uint32_t>(max_blocks);
     ws.l1_done = c.take<uint32_t>(max_blocks);
+    ws.tok_mask = c.take<uint32_t>(max_tokens);
+    ws.tok_cnt = c.take<uint32_t>(static_cast<size_t>(max_tokens) * ((d.H + BN - 1) / BN));
     ws.table = c.take<int32_t>(static_cast<size_t>(d.E) * d.R * tsrc_cap);
     ws.meta = c.take<uint32_t>(static_cast<size_t>(P) * 3);
     ws.pool_x = c.take<uint8_t>(static_cast<size_t>(P) * d.H);
@@ -356,6 +359,7 @@ int moe_reserve(moe_handle_t h, int max_tokens)
     h->big_bytes = bytes;
     CK(cudaMemset(ws.arrive, 0, sizeof(uint32_t) * ws.max_blocks));
     CK(cudaMemset(ws.l1_done, 0, sizeof(uint32_t) * ws.max_blocks));
+    CK(cudaMemset(ws.tok_cnt, 0, sizeof(uint32_t) * static_cast<size_t>(max_tokens) * ((d.H + BN - 1) / BN)));
     CK(cudaMemset(ws.pool_sf, 0, sizeof(float) * static_cast<size_t>(ws.P) * (d.H / 128)));
     CK(cudaMemset(ws.act_sf, 0, sizeof(float) * static_cast<size_t>(ws.P) * (d.I / 128)));
     CK(cudaMemset(ws.pool_x, 0, static_cast<size_t>(ws.P) * d.H));
@@ -559,8 +563,11 @@ int moe_load_shared_weights_mxfp4(moe_handle_t h, const uint8_t *w_gate_up, cons
     return rc;
 }
 
-int moe_forward(moe_handle_t h, int T, const uint8_t *x, const float *x_sf, const int64_t *topk_idx,
-                const float *topk_w, uint16_t *out, void *stream)
+// out_is_host: the output is pinned host memory the kernels write in place (host-buffer entry
+// points); the automatic combine mode then runs the combine inside the FFN kernel, so the
+// output rows cross to the host while the GEMMs still run instead of in one burst at the end.
+static int forward_impl(moe_handle_t h, int T, const uint8_t *x, const float *x_sf, const int64_t *topk_idx,
+                        const float *topk_w, uint16_t *out, void *stream, bool out_is_host)
 {
     if (!h || T < 0)
         return MOE_ERR_INVALID_ARG;
@@ -587,7 +594,8 @@ int moe_forward(moe_handle_t h, int T, const uint8_t *x, const float *x_sf, cons
     if ((h->scale_mode == 1 && !h->weights_pow2) || (h->scale_mode == 0 && h->mxfp4))
         return MOE_ERR_BAD_SCALE;
     const bool bs = h->mxfp4 || h->scale_mode == 1 || (h->scale_mode == 2 && h->weights_pow2);
-    CallArgs c{T, x, x_sf, topk_idx, topk_w, out, h->timeout_ns, h->debug_skip_barrier, bs ? 1 : 0};
+    const int fused = h->combine_mode == 2 ? (out_is_host ? 1 : 0) : h->combine_mode;
+    CallArgs c{T, x, x_sf, topk_idx, topk_w, out, h->timeout_ns, h->debug_skip_barrier, bs ? 1 : 0, fused};
     if (h->S > 0) {
         // shared experts: each token's route gains slots K_routed.. naming expert E_routed + s
         // with weight 1, written by one small kernel ahead of the routing kernel
@@ -617,13 +625,19 @@ int moe_forward(moe_handle_t h, int T, const uint8_t *x, const float *x_sf, cons
                             wave_blocks(h), h->num_sms, h->mxfp4, s)
             : launch_ffn(h->maps, h->d, h->ws, c, h->s1, h->s2, wave_blocks(h), h->num_sms, s)) !=
             cudaSuccess ||
-        mark(2) != cudaSuccess || launch_combine(h->d, h->ws, c, h->num_sms, s) != cudaSuccess ||
+        mark(2) != cudaSuccess || (!c.fused_combine && launch_combine(h->d, h->ws, c, h->num_sms, s) != cudaSuccess) ||
         mark(3) != cudaSuccess)
         return MOE_ERR_CUDA;
     h->last_stream = s;
     h->have_last = true;
     h->last_T = T;
     return MOE_OK;
+}
+
+int moe_forward(moe_handle_t h, int T, const uint8_t *x, const float *x_sf, const int64_t *topk_idx,
+                const float *topk_w, uint16_t *out, void *stream)
+{
+    return forward_impl(h, T, x, x_sf, topk_idx, topk_w, out, stream, false);
 }
 
 // Device address of a host buffer the GPU can access in place (pinned, mapped into the
@@ -707,8 +721,8 @@ static int forward_host_impl(moe_handle_t h, int T, const uint8_t *host_x, const
     }
     uint16_t *out_dev = static_cast<uint16_t *>(mapped_host(host_out));
     const bool out_in_place = out_dev != nullptr && aligned(out_dev, 16);
-    int rc = moe_forward(h, T, h->st_x[set], h->st_sf[set], h->st_idx[set], h->st_w[set],
-                         out_in_place ? out_dev : h->st_out, stream);
+    int rc = forward_impl(h, T, h->st_x[set], h->st_sf[set], h->st_idx[set], h->st_w[set],
+                          out_in_place ? out_dev : h->st_out, stream, out_in_place);
     if (rc != MOE_OK)
         return rc;
     if (h->ev_free[set]) {
@@ -755,6 +769,8 @@ int moe_get_error(moe_handle_t h, int *device_status)
         if (h->reserved) {
             CK(cudaMemset(h->ws.arrive, 0, sizeof(uint32_t) * h->ws.max_blocks));
             CK(cudaMemset(h->ws.l1_done, 0, sizeof(uint32_t) * h->ws.max_blocks));
+            CK(cudaMemset(h->ws.tok_cnt, 0,
+                          sizeof(uint32_t) * static_cast<size_t>(h->ws.max_tokens) * ((h->d.H + BN - 1) / BN)));
         }
         CK(cudaDeviceSynchronize());
     }
@@ -879,6 +895,11 @@ int moe_set_option(moe_handle_t h, int option, int64_t value)
         if (value < 0 || value > 2)
             return MOE_ERR_INVALID_ARG;
         h->scale_mode = static_cast<int>(value);
+        return MOE_OK;
+    case MOE_OPT_COMBINE_MODE:
+        if (value < 0 || value > 2)
+            return MOE_ERR_INVALID_ARG;
+        h->combine_mode = static_cast<int>(value);
         return MOE_OK;
     default:
         return MOE_ERR_INVALID_ARG;

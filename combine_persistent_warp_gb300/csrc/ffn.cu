@@ -38,8 +38,12 @@
 //              into the tile's ring slot, so a tile starts without a dependent global load
 //   warp 3     release warp: publishes a gate_up tile's stored SwiGLU rows to the down tiles
 //              of every CTA (proxy fence + GPU-scope release add on l1_done), so no epilogue
-//              warp waits for its own stores to drain
-//   warps 4-11 two epilogue warpgroups, columns [0,128) and [128,256) of the tile
+//              warp waits for its own stores to drain; with the top-k combine inside this
+//              kernel it also counts each stored down tile's rows per (token, n-tile) and
+//              lists the (token, n-tile) pairs the tile completed (topk_combine.cuh)
+//   warps 4-11 two epilogue warpgroups, columns [0,128) and [128,256) of the tile; with the
+//              in-kernel combine they reduce the previous tile's completed pairs after each
+//              tile
 // All waits carry a deadline; on expiry the CTA records MOE_ERR_TIMEOUT and leaves after
 // draining the copies and MMAs it has in flight.
 #include <cuda_bf16.h>
@@ -48,6 +52,7 @@
 
 #include "moe_internal.cuh"
 #include "ptx.cuh"
+#include "topk_combine.cuh"
 
 namespace cpw {
 
@@ -109,6 +114,8 @@ struct __align__(16) FfnBars {
     float sb[TILE_RING][2][MAX_KB];    // weight scales of a tile: gate | up, or down row group 2nt | 2nt+1
     float gw[TILE_RING][BM];           // down tile: gate weight of each row
     uint32_t roff[TILE_RING][BM];      // down tile: combine row (slot * max_tokens + token)
+    topk::Lists<TILE_RING> tk;         // in-kernel combine: pairs completed by a down tile
+    int exit_flag;
 };
 constexpr int FFN_SMEM_BYTES = 1024 /*align slack*/ + STAGES * STAGE_BYTES + static_cast<int>(sizeof(FfnBars));
 static_assert(FFN_SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
@@ -148,6 +155,9 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, uint64
 
 }  // namespace
 
+// FUSED: the top-k combine runs inside this kernel (topk_combine.cuh); a separate
+// instantiation, so the other one carries none of its code.
+template <bool FUSED>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     ffn_kernel(const __grid_constant__ FfnMaps maps, const Dims d, const Workspace ws, const CallArgs c,
                const float *__restrict__ sf1, const float *__restrict__ sf2, const int wave_blocks)
@@ -174,6 +184,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             ptx::mbar_init(&bars->tile_empty[i], 3 + EPI_WARPS);
             ptx::mbar_init(&bars->meta_ready[i], 1);
             ptx::mbar_init(&bars->act_done[i], EPI_WARPS);
+            ptx::mbar_init(&bars->tk.ready[i], 1);
         }
         ptx::fence_mbar_init();
     } else if (threadIdx.x == 32) {
@@ -200,6 +211,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     if (bars->abort) {   // a device error earlier in this forward: nothing to do
         if (warp == 1)
             ptx::tmem_dealloc(tmem, TMEM_COLS);
+        if (FUSED)
+            ffn_cta_exit(d, ws, &bars->exit_flag);
         return;
     }
 
@@ -486,41 +499,60 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             // -------------------------------------------------------- release warp ----
             // The epilogue warps arrive on the slot's act_done barrier when they are done with
             // a tile; for a gate_up tile that means its SwiGLU rows and scales are stored, and
-            // this lane publishes them for the down tiles of every CTA: the CTA-scope barrier
+            // lane 0 publishes them for the down tiles of every CTA: the CTA-scope barrier
             // orders the epilogue's stores before this thread's GPU-scope release (release is
-            // cumulative), and the proxy fence covers the TMA loads that read them.
-            if (lane == 0) {
-                uint32_t tcount = 0;
-                bool ok = true;
-                while (ok) {
-                    const uint32_t slot = tcount % TILE_RING, sph = (tcount / TILE_RING) & 1u;
-                    ++tcount;
-                    if (!ptx::mbar_wait(&bars->tile_full[slot], sph, deadline)) {
-                        ok = false;
-                        break;
-                    }
-                    const int tile = bars->tile_ring[slot];
-                    if (tile < 0) {
+            // cumulative), and the proxy fence covers the TMA loads that read them.  With the
+            // combine inside this kernel the warp also counts every stored down tile's rows per
+            // (token, n-tile) and lists the pairs the tile completed for the epilogue warps,
+            // which reduce them at the end of their next tile (topk_combine.cuh).
+            uint32_t tcount = 0;
+            bool ok = true;
+            while (ok) {
+                const uint32_t slot = tcount % TILE_RING, sph = (tcount / TILE_RING) & 1u;
+                ++tcount;
+                if (!warp_wait(&bars->tile_full[slot], sph, deadline)) {
+                    ok = false;
+                    break;
+                }
+                const int tile = bars->tile_ring[slot];
+                if (tile < 0) {
+                    __syncwarp();
+                    if (lane == 0)
                         ptx::mbar_arrive(&bars->tile_empty[slot]);
-                        break;
-                    }
-                    if (!ptx::mbar_wait(&bars->act_done[slot], sph, deadline)) {
-                        ok = false;
-                        break;
-                    }
+                    break;
+                }
+                if (!warp_wait(&bars->act_done[slot], sph, deadline)) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0)
                     CPW_STAMP(12, tcount - 1);
-                    int phase, blk, nt;
-                    tl.at(tile, phase, blk, nt);
-                    if (phase == 1) {
-                        ptx::fence_proxy_async_global();
-                        ptx::red_release_add(ws.l1_done + blk, static_cast<uint32_t>(EPI_WARPS));
+                int phase, blk, nt;
+                tl.at(tile, phase, blk, nt);
+                if (phase == 1 && lane == 0) {
+                    ptx::fence_proxy_async_global();
+                    ptx::red_release_add(ws.l1_done + blk, static_cast<uint32_t>(EPI_WARPS));
+                }
+                if (FUSED) {
+                    const int n = phase == 2 ? topk::count_rows(d, ws, static_cast<long long>(blk) * BM,
+                                                                bars->tile_rows[slot], nt, bars->tk.tok[slot],
+                                                                bars->tk.mask[slot], lane)
+                                             : 0;
+                    __syncwarp();
+                    if (lane == 0) {
+                        bars->tk.n[slot] = n;
+                        bars->tk.nt[slot] = nt;
+                        ptx::mbar_arrive(&bars->tk.ready[slot]);
                     }
+                }
+                __syncwarp();
+                if (lane == 0) {
                     CPW_STAMP(13, tcount - 1);
                     ptx::mbar_arrive(&bars->tile_empty[slot]);
                 }
-                if (!ok)
-                    record_error(ws.hdr, DEV_TIMEOUT);
             }
+            if (!ok && lane == 0)
+                record_error(ws.hdr, DEV_TIMEOUT);
         }
     } else {
         // ------------------------------------------------------------ epilogue --------
@@ -531,6 +563,19 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
         uint32_t it = 0, xcount = 0, tcount = 0;
         bool ok = true;
+        // in-kernel combine: the (token, n-tile) pairs the release warp listed for the previous
+        // tile are reduced by the eight epilogue warps at the end of the next one
+        int prev = -1;   // ring slot of the previous tile, -1 before the first
+        uint32_t prev_ph = 0;
+        auto reduce_listed = [&](int sl, uint32_t ph) {
+            if (!warp_wait(&bars->tk.ready[sl], ph, deadline))
+                return false;
+            const int n = bars->tk.n[sl];
+            if (n > 0)
+                topk::reduce(d, ws, c, bars->tk.tok[sl], bars->tk.mask[sl], n, bars->tk.nt[sl], warp - 4, EPI_WARPS,
+                             lane);
+            return true;
+        };
         while (ok) {
             const uint32_t slot = tcount % TILE_RING, sph = (tcount / TILE_RING) & 1u;
             ++tcount;
@@ -544,6 +589,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 __syncwarp();
                 if (lane == 0)
                     ptx::mbar_arrive(&bars->tile_empty[slot]);
+                if (FUSED && prev >= 0 && !reduce_listed(prev, prev_ph))
+                    ok = false;
                 break;
             }
             int phase, blk, nt;
@@ -746,6 +793,14 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 ptx::mbar_arrive(&bars->act_done[slot]);
                 ptx::mbar_arrive(&bars->tile_empty[slot]);
             }
+            if (FUSED) {
+                if (prev >= 0 && !reduce_listed(prev, prev_ph)) {
+                    ok = false;
+                    break;
+                }
+                prev = static_cast<int>(slot);
+                prev_ph = sph;
+            }
         }
         if (!ok)
             record_error(ws.hdr, DEV_TIMEOUT);
@@ -761,6 +816,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, TMEM_COLS);
     }
+    if (FUSED)
+        ffn_cta_exit(d, ws, &bars->exit_flag);
 }
 
 #ifdef CPW_TRACE
@@ -783,11 +840,15 @@ cudaError_t trace_clear()
 cudaError_t launch_ffn(const FfnMaps &maps, const Dims &d, const Workspace &ws, const CallArgs &c,
                        const float *sf1, const float *sf2, int wave_blocks, int num_sms, cudaStream_t s)
 {
-    cudaError_t e0 = ensure_max_dynamic_smem(reinterpret_cast<const void *>(ffn_kernel), FFN_SMEM_BYTES);
+    const void *kern = c.fused_combine ? reinterpret_cast<const void *>(ffn_kernel<true>)
+                                       : reinterpret_cast<const void *>(ffn_kernel<false>);
+    cudaError_t e0 = ensure_max_dynamic_smem(kern, FFN_SMEM_BYTES);
     if (e0 != cudaSuccess)
         return e0;
-    return launch_programmatic(ffn_kernel, num_sms, GEMM_THREADS, FFN_SMEM_BYTES, s, maps, d, ws, c, sf1, sf2,
-                               wave_blocks);
+    return c.fused_combine ? launch_programmatic(ffn_kernel<true>, num_sms, GEMM_THREADS, FFN_SMEM_BYTES, s, maps, d,
+                                                 ws, c, sf1, sf2, wave_blocks)
+                           : launch_programmatic(ffn_kernel<false>, num_sms, GEMM_THREADS, FFN_SMEM_BYTES, s, maps, d,
+                                                 ws, c, sf1, sf2, wave_blocks);
 }
 
 }  // namespace cpw

@@ -37,16 +37,21 @@
 //
 // Roles (one CTA per SM, 12 warps): warp 0 TMA producer (A, B and the two scale blocks of
 // a 128-deep K block per stage, 4 stages); warp 1 UMMA issuer (scale copies + 4 block-scaled
-// UMMAs per stage into one 256-column TMEM accumulator); warps 4-11 epilogue (two
-// warpgroups, columns [0,128) / [128,256)): one TMEM read per tile, then SwiGLU + UE8M0
-// requant (phase 1) or the weighted scatter (phase 2).  TMEM: accumulator columns 0-255,
-// scale slots 256 + 16*s.  All waits carry a deadline (MOE_ERR_TIMEOUT).
+// UMMAs per stage into one 256-column TMEM accumulator); warp 2 dependency warp (a down
+// tile's gate_up completion count); warp 3, with the top-k combine inside this kernel, counts
+// each stored down tile's rows per (token, n-tile) and lists the pairs it completed
+// (topk_combine.cuh); warps 4-11 epilogue (two warpgroups, columns [0,128) / [128,256)): one
+// TMEM read per tile, then SwiGLU + UE8M0 requant (phase 1) or the weighted scatter (phase 2),
+// and with the in-kernel combine the reduce of the previous tile's completed pairs.  TMEM:
+// accumulator columns 0-255, scale slots 256 + 16*s.  All waits carry a deadline
+// (MOE_ERR_TIMEOUT).
 #include <cuda_bf16.h>
 
 #include <algorithm>
 
 #include "moe_internal.cuh"
 #include "ptx.cuh"
+#include "topk_combine.cuh"
 
 namespace cpw {
 
@@ -106,10 +111,13 @@ struct __align__(8) BsBars {
     uint64_t tile_full[TILE_RING];
     uint64_t tile_empty[TILE_RING];
     uint64_t dep[TILE_RING];   // dependency warp -> producer: this slot's tile may be loaded
+    uint64_t act_done[TILE_RING];   // in-kernel combine: epilogue -> counting warp, tile stored
     int tile_ring[TILE_RING];
     uint32_t tmem_base;
     int abort;
+    int exit_flag;
     float amax[2][2][BM];
+    topk::Lists<TILE_RING> tk;   // in-kernel combine: pairs completed by a down tile
 };
 
 struct BsTiles {
@@ -144,7 +152,9 @@ struct BsView {
 
 }  // namespace
 
-template <bool FP4>
+// FUSED: the top-k combine runs inside this kernel (topk_combine.cuh); a separate
+// instantiation, so the other one carries none of its code.
+template <bool FP4, bool FUSED>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     ffn_bs_kernel(const __grid_constant__ FfnMaps maps, const Dims d,
                   const Workspace ws, const CallArgs c, const uint8_t *__restrict__ sfb1,
@@ -172,8 +182,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         ptx::mbar_init(&bars->xbar, 32 * EPI_WARPS);
         for (int i = 0; i < TILE_RING; ++i) {
             ptx::mbar_init(&bars->tile_full[i], 1);
-            ptx::mbar_init(&bars->tile_empty[i], 2 + EPI_WARPS);   // issuer, dependency warp, epilogue
+            // issuer, dependency warp, epilogue (and the counting warp with the in-kernel combine)
+            ptx::mbar_init(&bars->tile_empty[i], 2 + EPI_WARPS + (FUSED ? 1 : 0));
             ptx::mbar_init(&bars->dep[i], 1);
+            ptx::mbar_init(&bars->act_done[i], EPI_WARPS);
+            ptx::mbar_init(&bars->tk.ready[i], 1);
         }
         ptx::fence_mbar_init();
     } else if (threadIdx.x == 32) {
@@ -200,6 +213,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     if (bars->abort) {   // a device error earlier in this forward: nothing to do
         if (warp == 1)
             ptx::tmem_dealloc(tmem, TMEM_COLS);
+        if (FUSED)
+            ffn_cta_exit(d, ws, &bars->exit_flag);
         return;
     }
 
@@ -480,6 +495,47 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     ptx::mbar_wait(&bars->empty[i % NST], (i / NST) & 1u, dl);
                 }
             }
+        } else if (FUSED) {
+            // -------------------------------------------------------- counting warp ---
+            // In-kernel combine: once the epilogue warps have stored a down tile (act_done),
+            // count its rows per (token, n-tile) and list the pairs it completed for the
+            // epilogue warps, which reduce them at the end of their next tile
+            // (topk_combine.cuh); every tile gets its list barrier arrival.
+            uint32_t tcount = 0;
+            bool ok = true;
+            while (ok) {
+                const uint32_t slot = tcount % TILE_RING, sph = (tcount / TILE_RING) & 1u;
+                ++tcount;
+                if (!__all_sync(0xFFFFFFFFu, ptx::mbar_wait(&bars->tile_full[slot], sph, deadline))) {
+                    ok = false;
+                    break;
+                }
+                const int tile = bars->tile_ring[slot];
+                if (tile < 0) {
+                    __syncwarp();
+                    if (lane == 0)
+                        ptx::mbar_arrive(&bars->tile_empty[slot]);
+                    break;
+                }
+                if (!__all_sync(0xFFFFFFFFu, ptx::mbar_wait(&bars->act_done[slot], sph, deadline))) {
+                    ok = false;
+                    break;
+                }
+                int phase, blk, nt;
+                tl.at(tile, phase, blk, nt);
+                const int n = phase == 2 ? topk::count_rows(d, ws, static_cast<long long>(blk) * BM, ws.block_rows[blk],
+                                                            nt, bars->tk.tok[slot], bars->tk.mask[slot], lane)
+                                         : 0;
+                __syncwarp();
+                if (lane == 0) {
+                    bars->tk.n[slot] = n;
+                    bars->tk.nt[slot] = nt;
+                    ptx::mbar_arrive(&bars->tk.ready[slot]);
+                    ptx::mbar_arrive(&bars->tile_empty[slot]);
+                }
+            }
+            if (!ok && lane == 0)
+                record_error(ws.hdr, DEV_TIMEOUT);
         }
     } else {
         // ------------------------------------------------------------ epilogue --------
@@ -490,6 +546,19 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
         uint32_t tcount = 0, xcount = 0, acc_n = 0;
         bool ok = true;
+        // in-kernel combine: the (token, n-tile) pairs the counting warp listed for the previous
+        // tile are reduced by the eight epilogue warps at the end of the next one
+        int prev = -1;   // ring slot of the previous tile, -1 before the first
+        uint32_t prev_ph = 0;
+        auto reduce_listed = [&](int sl, uint32_t ph) {
+            if (!__all_sync(0xFFFFFFFFu, ptx::mbar_wait(&bars->tk.ready[sl], ph, deadline)))
+                return false;
+            const int n = bars->tk.n[sl];
+            if (n > 0)
+                topk::reduce(d, ws, c, bars->tk.tok[sl], bars->tk.mask[sl], n, bars->tk.nt[sl], warp - 4, EPI_WARPS,
+                             lane);
+            return true;
+        };
         while (ok) {
             const uint32_t slot = tcount % TILE_RING, sph = (tcount / TILE_RING) & 1u;
             if (!__all_sync(0xFFFFFFFFu, ptx::mbar_wait(&bars->tile_full[slot], sph, deadline))) {
@@ -501,8 +570,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             if (lane == 0)
                 ptx::mbar_arrive(&bars->tile_empty[slot]);
             ++tcount;
-            if (tile < 0)
+            if (tile < 0) {
+                if (FUSED && prev >= 0 && !reduce_listed(prev, prev_ph))
+                    ok = false;
                 break;
+            }
             int phase, blk, nt;
             tl.at(tile, phase, blk, nt);
             const long long prow = static_cast<long long>(blk) * BM + row;
@@ -650,6 +722,19 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     }
                 }
             }
+            if (FUSED) {
+                // the tile is stored: the counting warp may count it; then the previous tile's
+                // completed pairs
+                __syncwarp();
+                if (lane == 0)
+                    ptx::mbar_arrive(&bars->act_done[slot]);
+                if (prev >= 0 && !reduce_listed(prev, prev_ph)) {
+                    ok = false;
+                    break;
+                }
+                prev = static_cast<int>(slot);
+                prev_ph = sph;
+            }
         }
         if (!ok)
             record_error(ws.hdr, DEV_TIMEOUT);
@@ -661,6 +746,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, TMEM_COLS);
     }
+    if (FUSED)
+        ffn_cta_exit(d, ws, &bars->exit_flag);
 }
 
 cudaError_t launch_ffn_bs(const FfnMaps &maps, const Dims &d, const Workspace &ws, const CallArgs &c,
@@ -670,16 +757,25 @@ cudaError_t launch_ffn_bs(const FfnMaps &maps, const Dims &d, const Workspace &w
     constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + 8192 + STAGES * SF_STAGE_BYTES;
     static_assert(sizeof(BsBars) <= 8192, "barrier block");
     static_assert(SMEM <= 227 * 1024, "shared memory per CTA");
-    void *kern = fp4 ? reinterpret_cast<void *>(ffn_bs_kernel<true>) : reinterpret_cast<void *>(ffn_bs_kernel<false>);
+    const bool fu = c.fused_combine != 0;
+    void *kern = fp4 ? (fu ? reinterpret_cast<void *>(ffn_bs_kernel<true, true>)
+                           : reinterpret_cast<void *>(ffn_bs_kernel<true, false>))
+                     : (fu ? reinterpret_cast<void *>(ffn_bs_kernel<false, true>)
+                           : reinterpret_cast<void *>(ffn_bs_kernel<false, false>));
     cudaError_t e0 = ensure_max_dynamic_smem(kern, SMEM);
     if (e0 != cudaSuccess)
         return e0;
     // Tiles are claimed in list order by running CTAs only, so the launch needs no
     // co-residency guarantee: a down tile waits only on gate_up tiles claimed before it.
-    return fp4 ? launch_programmatic(ffn_bs_kernel<true>, num_sms, GEMM_THREADS, SMEM, s, maps, d, ws, c, sfb1, sfb2,
-                                     wave_blocks)
-               : launch_programmatic(ffn_bs_kernel<false>, num_sms, GEMM_THREADS, SMEM, s, maps, d, ws, c, sfb1,
-                                     sfb2, wave_blocks);
+    if (fp4)
+        return fu ? launch_programmatic(ffn_bs_kernel<true, true>, num_sms, GEMM_THREADS, SMEM, s, maps, d, ws, c, sfb1,
+                                        sfb2, wave_blocks)
+                  : launch_programmatic(ffn_bs_kernel<true, false>, num_sms, GEMM_THREADS, SMEM, s, maps, d, ws, c, sfb1,
+                                        sfb2, wave_blocks);
+    return fu ? launch_programmatic(ffn_bs_kernel<false, true>, num_sms, GEMM_THREADS, SMEM, s, maps, d, ws, c, sfb1,
+                                    sfb2, wave_blocks)
+              : launch_programmatic(ffn_bs_kernel<false, false>, num_sms, GEMM_THREADS, SMEM, s, maps, d, ws, c, sfb1,
+                                    sfb2, wave_blocks);
 }
 
 // ------------------------------------------------------------------ weight scales -----

@@ -34,7 +34,8 @@ enum HdrWord : int {
     HDR_ERR_CALL = 32,     // first device error of the forward in flight
     HDR_ERR_STICKY = 64,   // errors of finished forwards, until moe_get_error
     HDR_TILE_NEXT = 96,    // next tile of the FFN kernel's dynamic tile list
-    HDR_WORDS = 128
+    HDR_FFN_EXIT = 128,    // FFN CTAs finished (in-kernel combine: the last one resets)
+    HDR_WORDS = 160
 };
 
 // Device workspace of one handle.  Sizes: P = pool row capacity, MB = P / BM.
@@ -58,6 +59,8 @@ struct Workspace {
     uint16_t *combine;             // [topk][max_tokens][H] bf16 weighted expert outputs
     uint32_t *arrive;              // [MB] rows gathered per M-block
     uint32_t *l1_done;             // [MB] finished gate_up (tile, epilogue warp) pairs
+    uint32_t *tok_mask;            // [max_tokens] routed top-k slots of each token (bit k)
+    uint32_t *tok_cnt;             // [max_tokens][ceil(H/256)] scattered rows per (token, n-tile)
     int tsrc_cap;                  // max_tokens / R
     int P;                         // pool rows
     int max_blocks;                // P / BM
@@ -78,6 +81,7 @@ struct CallArgs {
     long long timeout_ns;
     int debug_skip_barrier;
     int block_scaled;   // 1: power-of-two scales, hardware block-scaled UMMA (ffn_bs.cu)
+    int fused_combine;  // 1: the top-k combine runs inside the FFN kernel (topk_combine.cuh)
 };
 
 // Device error codes (same values as the public moe_status).

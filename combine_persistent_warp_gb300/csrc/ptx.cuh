@@ -87,15 +87,6 @@ __device__ __forceinline__ void tma_load_2d(void *smem_dst, const CUtensorMap *m
                  : "memory");
 }
 
-// Prefetch one tile of a 2-D tensor map into L2 (no shared memory, no completion).
-__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap *map, int32_t x, int32_t y)
-{
-    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
-                     reinterpret_cast<uint64_t>(map)),
-                 "r"(x), "r"(y)
-                 : "memory");
-}
-
 // Programmatic dependent launch: a kernel launched with the programmatic-serialization
 // attribute may start while the previous kernel of its stream still runs; it waits here until
 // that kernel has completed and its memory operations are visible (a no-op in a kernel launched
@@ -296,11 +287,6 @@ template <uint32_t N>
 __device__ __forceinline__ void setmaxnreg_inc()
 {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
-}
-
-__device__ __forceinline__ void named_barrier(uint32_t id, uint32_t nthreads)
-{
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 }  // namespace ptx

@@ -17,6 +17,7 @@
 #include "moe_internal.cuh"
 #include "ptx.cuh"
 #include "route_device.cuh"
+#include "topk_combine.cuh"
 
 namespace cpw {
 
@@ -49,6 +50,9 @@ __global__ void __launch_bounds__(DISPATCH_THREADS, 1)
 
     // ---- count, packed claim, index table ------------------------------------------------
     route::count_claim_table(d, ws, c, cnt);
+    // in-kernel combine: each token's routed slots, and the zero rows of unrouted tokens
+    if (c.fused_combine)
+        route::token_masks(d, ws, c);
 
     // ---- grid barrier: every claim and table entry is visible past this point -----------
     const bool skip = c.debug_skip_barrier != 0 && blockIdx.x == 0;
@@ -92,9 +96,8 @@ cudaError_t launch_dispatch(const Dims &d, const Workspace &ws, const CallArgs &
 
 // ------------------------------------------------------------------ combine -------------
 // out[t] = bf16( sum over valid k, ascending, of combine[k][t] ) in fp32; no valid k -> 0.
-// Then the workspace reset of the pages' cleanup step: send counts and arrival counters go
-// back to zero; a device error of this forward moves into the sticky word and the grid
-// barrier counter is cleared (an aborted barrier leaves it mid-phase).
+// Then the workspace reset of the pages' cleanup step (reset_after_forward).  With the
+// in-kernel combine (topk_combine.cuh) this kernel is not launched.
 __global__ void __launch_bounds__(COMBINE_THREADS, 2)
     combine_kernel(const Dims d, const Workspace ws, const CallArgs c)
 {
@@ -165,24 +168,7 @@ __global__ void __launch_bounds__(COMBINE_THREADS, 2)
         }
     }
     // reset for the next forward
-    const int gtid = blockIdx.x * blockDim.x + threadIdx.x;
-    const int gthreads = gridDim.x * blockDim.x;
-    for (int i = gtid; i < d.R * d.E; i += gthreads)
-        ws.send[i] = 0ull;
-    for (int i = gtid; i < ws.max_blocks; i += gthreads) {
-        ws.arrive[i] = 0u;
-        ws.l1_done[i] = 0u;
-    }
-    if (gtid == 0) {
-        ws.hdr[HDR_TILE_NEXT] = 0u;
-        const uint32_t call = *reinterpret_cast<volatile uint32_t *>(ws.hdr + HDR_ERR_CALL);
-        if (call != 0) {
-            if (ws.hdr[HDR_ERR_STICKY] == 0)
-                ws.hdr[HDR_ERR_STICKY] = call;
-            ws.hdr[HDR_GRID_SYNC] = 0u;
-            ws.hdr[HDR_ERR_CALL] = 0u;
-        }
-    }
+    reset_after_forward(d, ws, blockIdx.x * blockDim.x + threadIdx.x, gridDim.x * blockDim.x);
 }
 
 cudaError_t launch_combine(const Dims &d, const Workspace &ws, const CallArgs &c, int num_sms,

@@ -28,6 +28,8 @@ OPT_TIMEOUT_NS = 0
 OPT_DEBUG_SKIP_BARRIER = 1
 OPT_FFN_MODE = 2
 OPT_SCALE_MODE = 3
+OPT_COMBINE_MODE = 4
+COMBINE_KERNEL, COMBINE_IN_FFN, COMBINE_AUTO = 0, 1, 2   # values of OPT_COMBINE_MODE (default COMBINE_AUTO)
 SCALE_FP32, SCALE_POW2, SCALE_AUTO = 0, 1, 2   # values of OPT_SCALE_MODE (default SCALE_AUTO)
 WEIGHTS_FP8, WEIGHTS_MXFP4 = 0, 1              # values of MoeInfo.weight_format
 

@@ -223,12 +223,22 @@ int moe_get_info(moe_handle_t h, moe_info *info);
  * loaded weights is a power of two (checked by moe_load_weights), else mode 0.  In mode 1
  * weights that are not all powers of two make moe_forward return MOE_ERR_BAD_SCALE; in
  * modes 1 and 2 an activation scale that is not, on the block-scaled path, is reported by
- * the device the same way (sticky). */
+ * the device the same way (sticky);
+ * MOE_OPT_COMBINE_MODE: where the top-k combine runs ("DeepGEMM Mega MoE 对称内存（Symmetric
+ * Memory）深度分析" §9: the per-token fp32 reduce of the top-k expert outputs).  0 = a
+ * separate kernel after the expert FFN kernel; 1 = inside the expert FFN kernel: a down tile's
+ * scattered rows are counted per (token, 256-column n-tile), and the epilogue warps reduce every
+ * (token, n-tile) whose routed rows are all scattered while other tiles are still being
+ * computed (the forward is then two kernels, three with shared experts); 2 = automatic
+ * (default): 1 when a host-buffer entry point writes the output into pinned host memory in
+ * place (its rows then cross to the host while the GEMMs still run), else 0.  All modes give
+ * the same output bits.  Other values are refused. */
 enum moe_option {
     MOE_OPT_TIMEOUT_NS = 0,
     MOE_OPT_DEBUG_SKIP_BARRIER = 1,
     MOE_OPT_FFN_MODE = 2,
-    MOE_OPT_SCALE_MODE = 3
+    MOE_OPT_SCALE_MODE = 3,
+    MOE_OPT_COMBINE_MODE = 4
 };
 int moe_set_option(moe_handle_t h, int option, int64_t value);
 

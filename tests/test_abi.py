@@ -72,6 +72,7 @@ def test_binding_constants_match_the_header():
     assert v["MOE_OPT_DEBUG_SKIP_BARRIER"] == native.OPT_DEBUG_SKIP_BARRIER
     assert v["MOE_OPT_FFN_MODE"] == native.OPT_FFN_MODE
     assert v["MOE_OPT_SCALE_MODE"] == native.OPT_SCALE_MODE
+    assert v["MOE_OPT_COMBINE_MODE"] == native.OPT_COMBINE_MODE
     assert v["MOE_WEIGHTS_FP8"] == native.WEIGHTS_FP8 and v["MOE_WEIGHTS_MXFP4"] == native.WEIGHTS_MXFP4
     for name, idx in native.BUFFERS.items():
         assert v["MOE_BUF_" + name.upper()] == idx

@@ -64,7 +64,20 @@ constexpr uint32_t SF_COL = 256;          // scale slot j: columns SF_COL + 16*j
 constexpr int SF_GROUP = 4;               // K blocks per scale block (bytes of a scale word)
 constexpr uint32_t SFA_BYTES = 512, SFB_BYTES = 1024, SF_STAGE_BYTES = SFA_BYTES + SFB_BYTES;
 static_assert(BKS == BK, "the block-scaled kernel stages whole 128-deep K blocks");
-static_assert(SF_COL + 16 * STAGES <= TMEM_COLS, "scale slots exceed TMEM");
+// Stage ring layouts.  Standard: STAGES stages of [A 16 KB | B 32 KB].  Compact, when no M-block
+// of the forward holds more than 64 rows (decode-sized batches): NST_MAX stages of [A 8 KB |
+// B 32 KB] in about the same space, i.e. one more weight tile in flight per SM.  The UMMA
+// still reads 128 A rows from the stage base; rows 64-127 then lie in the stage's own B tile
+// and only feed padding rows of the accumulator, which are never stored.
+constexpr int NST_MAX = 5;
+constexpr uint32_t COMPACT_A_BYTES = 2 * A_ROWS_PART * BKS;
+constexpr uint32_t COMPACT_STAGE_BYTES = COMPACT_A_BYTES + STAGE_B_BYTES;
+constexpr int RING_BYTES = STAGES * STAGE_BYTES > NST_MAX * static_cast<int>(COMPACT_STAGE_BYTES)
+                               ? STAGES * STAGE_BYTES
+                               : NST_MAX * static_cast<int>(COMPACT_STAGE_BYTES);
+static_assert(NST_MAX >= STAGES, "the compact ring has at least as many stages");
+static_assert(COMPACT_STAGE_BYTES % 1024 == 0 && COMPACT_A_BYTES % 1024 == 0, "128-byte swizzle atoms");
+static_assert(SF_COL + 16 * NST_MAX <= TMEM_COLS, "scale slots exceed TMEM");
 
 // block-scaled instruction descriptor: B scale id (byte of the scale word) at bits 4-5, A
 // format e4m3 (0) at bits 7-9, B format at bits 10-12 (e4m3 = 0, E2M1 = 5), K-major A and B,
@@ -103,8 +116,8 @@ __device__ __forceinline__ float pow2_ceil(float v)
 }
 
 struct __align__(8) BsBars {
-    uint64_t full[STAGES];
-    uint64_t empty[STAGES];
+    uint64_t full[NST_MAX];
+    uint64_t empty[NST_MAX];
     uint64_t tfull;
     uint64_t tempty;
     uint64_t xbar;
@@ -116,6 +129,7 @@ struct __align__(8) BsBars {
     uint32_t tmem_base;
     int abort;
     int exit_flag;
+    int max_rows;   // valid rows of the fullest M-block of the forward
     float amax[2][2][BM];
     topk::Lists<TILE_RING> tk;   // in-kernel combine: pairs completed by a down tile
 };
@@ -160,23 +174,22 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                   const Workspace ws, const CallArgs c, const uint8_t *__restrict__ sfb1,
                   const uint8_t *__restrict__ sfb2, const int wave_blocks)
 {
-    constexpr int NST = STAGES;                  // stages in the ring
-    constexpr uint32_t SBYTES = STAGE_BYTES;     // operand bytes per stage
     // weight bytes a stage's TMA brings from memory (packed E2M1: half the shared-memory image)
     constexpr uint32_t B_TX = STAGE_B_BYTES / (FP4 ? 2u : 1u);
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
-    BsBars *bars = reinterpret_cast<BsBars *>(smem + STAGES * STAGE_BYTES);
-    uint8_t *sf_smem = smem + STAGES * STAGE_BYTES + 8192;   // [NST][A 512 | B 1024]
+    BsBars *bars = reinterpret_cast<BsBars *>(smem + RING_BYTES);
+    uint8_t *sf_smem = smem + RING_BYTES + 8192;   // [stage][A 512 | B 1024]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     // prologue (barriers, TMEM, tensor maps) while the routing kernel may still run
     if (threadIdx.x == 0) {
-        for (int s = 0; s < NST; ++s) {
+        for (int s = 0; s < NST_MAX; ++s) {
             ptx::mbar_init(&bars->full[s], 1);
             ptx::mbar_init(&bars->empty[s], 1);
         }
+        bars->max_rows = 0;
         ptx::mbar_init(&bars->tfull, 1);
         ptx::mbar_init(&bars->tempty, EPI_WARPS);
         ptx::mbar_init(&bars->xbar, 32 * EPI_WARPS);
@@ -217,6 +230,21 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             ffn_cta_exit(d, ws, &bars->exit_flag);
         return;
     }
+    // the fullest M-block of the forward decides the stage layout (the same in every CTA)
+    {
+        const int nblocks = min(ws.blk_off[d.E], ws.max_blocks);
+        int mr = 0;
+        for (int b = threadIdx.x; b < nblocks; b += blockDim.x)
+            mr = max(mr, ws.block_rows[b]);
+        mr = __reduce_max_sync(0xFFFFFFFFu, mr);
+        if (lane == 0 && mr > 0)
+            atomicMax(&bars->max_rows, mr);
+        __syncthreads();
+    }
+    const bool compact = bars->max_rows <= 2 * A_ROWS_PART;
+    const uint32_t nst = compact ? NST_MAX : STAGES;                    // stages in the ring
+    const uint32_t sbytes = compact ? COMPACT_STAGE_BYTES : STAGE_BYTES;   // bytes per stage
+    const uint32_t a_reg = compact ? COMPACT_A_BYTES : STAGE_A_BYTES;      // B tile offset in a stage
 
     const BsTiles tl{(2 * d.I) / BN, (d.H + BN - 1) / BN, ws.blk_off[d.E], wave_blocks};
     const int ntiles = tl.total();
@@ -247,6 +275,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 const uint64_t pol_b_once = ptx::policy_evict_first();
                 const uint64_t pol_b_shared = ptx::policy_evict_normal();
                 uint32_t it = 0, tcount = 0;
+                uint32_t s = 0, ph = 0;   // stage of K block `it` and its ring pass parity
                 bool ok = true;
                 // Tiles are claimed from the global counter one ahead (a CTA holds at most one
                 // claimed, unstarted tile; the smallest unfinished tile is always being worked on).
@@ -330,8 +359,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                         }
                         ptx::fence_proxy_async_global();
                     }
-                    for (int kb = 0; kb < nkb; ++kb, ++it) {
-                        const uint32_t s = it % NST, ph = (it / NST) & 1u;
+                    for (int kb = 0; kb < nkb; ++kb, ++it, s = s + 1 == nst ? 0u : s + 1, ph ^= s == 0 ? 1u : 0u) {
                         // a step of the next tile's claim / publication / metadata, only when the
                         // stage is not free yet (the loads of a starving pipe are never held back)
                         // and two K blocks after the step before (whose reads it uses)
@@ -346,7 +374,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                             ok = false;
                             break;
                         }
-                        uint8_t *sa = smem + s * SBYTES;
+                        uint8_t *sa = smem + s * sbytes;
                         uint8_t *ss = sf_smem + s * SF_STAGE_BYTES;
                         const bool sf_k = kb % SF_GROUP == 0;   // first K block of a scale group
                         const int grp = kb / SF_GROUP;
@@ -362,7 +390,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                             } else {
                                 ptx::tma_load_2d(sa, ta, &bars->full[s], kb * BK, blk * BM, pol_a);
                             }
-                            ptx::tma_load_2d(sa + STAGE_A_BYTES, tb, &bars->full[s], 0, (tile0 + kb) * BN, pol_b);
+                            ptx::tma_load_2d(sa + a_reg, tb, &bars->full[s], 0, (tile0 + kb) * BN, pol_b);
                             if (sf_k)
                                 ptx::bulk_load(ss, sfa_src + grp * SFA_BYTES, SFA_BYTES, &bars->full[s]);
                             if (sfb_k)
@@ -377,8 +405,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     record_error(ws.hdr, DEV_TIMEOUT);
                 // drain: every issued load has landed before the CTA may exit
                 const uint64_t dl = ptx::globaltimer() + static_cast<uint64_t>(c.timeout_ns);
-                for (uint32_t i = it > NST ? it - NST : 0; i < it; ++i)
-                    ptx::mbar_wait(&bars->full[i % NST], (i / NST) & 1u, dl);
+                for (uint32_t i = it > nst ? it - nst : 0; i < it; ++i)
+                    ptx::mbar_wait(&bars->full[i % nst], (i / nst) & 1u, dl);
             }
         } else if (warp == 2) {
             // -------------------------------------------------------- dependency warp --
@@ -422,11 +450,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             // -------------------------------------------------------- UMMA issuer -----
             if (lane == 0) {
                 uint32_t it = 0, tcount = 0, acc_n = 0;
-                // scale groups copied so far: group g goes to TMEM slot g % NST, reused only after
-                // NST more groups, whose first stage's arrival implies (through the stage ring)
+                uint32_t s = 0, ph = 0, gslot = 0;   // stage of K block `it`, its pass parity; next scale slot
+                // scale groups copied so far: group g goes to TMEM slot g % nst, reused only after
+                // nst more groups, whose first stage's arrival implies (through the stage ring)
                 // that every UMMA of group g has completed (MXFP4: the per-K-block B scales go
                 // to the B columns of the stage's slot, reused after the stage's next fill)
-                uint32_t gcount = 0, sfa = 0, sfb = 0;
+                uint32_t sfa = 0, sfb = 0;
                 bool ok = true;
                 while (ok) {
                     const uint32_t slot = tcount % TILE_RING, sph = (tcount / TILE_RING) & 1u;
@@ -448,8 +477,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                         break;
                     }
                     ptx::tc_fence_after();
-                    for (int kb = 0; kb < nkb; ++kb, ++it) {
-                        const uint32_t s = it % NST, ph = (it / NST) & 1u;
+                    for (int kb = 0; kb < nkb; ++kb, ++it, s = s + 1 == nst ? 0u : s + 1, ph ^= s == 0 ? 1u : 0u) {
                         if (!ptx::mbar_wait(&bars->full[s], ph, deadline)) {
                             ok = false;
                             break;
@@ -457,8 +485,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                         ptx::tc_fence_after();
                         const uint32_t ss = ptx::smem_u32(sf_smem + s * SF_STAGE_BYTES);
                         if (kb % SF_GROUP == 0) {
-                            sfa = tmem + SF_COL + 16 * (gcount % NST);
-                            ++gcount;
+                            sfa = tmem + SF_COL + 16 * gslot;
+                            gslot = gslot + 1 == nst ? 0u : gslot + 1;
                             sf_copy(sfa, ss);
                             if constexpr (!FP4) {
                                 sfb = sfa + 4;
@@ -471,9 +499,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                             sf_copy(sfb, ss + SFA_BYTES);
                             sf_copy(sfb + 4, ss + SFA_BYTES + 512);
                         }
-                        const uint32_t a_addr = ptx::smem_u32(smem + s * SBYTES);
+                        const uint32_t a_addr = ptx::smem_u32(smem + s * sbytes);
                         const uint64_t adesc = ptx::kmajor_swizzled_desc<BKS>(a_addr);
-                        const uint64_t bdesc = ptx::kmajor_swizzled_desc<BKS>(a_addr + STAGE_A_BYTES);
+                        const uint64_t bdesc = ptx::kmajor_swizzled_desc<BKS>(a_addr + a_reg);
 #pragma unroll
                         for (int k = 0; k < BK / 32; ++k)   // +32 bytes along K = +2 in the >>4 field
                             umma_bs(tmem, adesc + 2 * k, bdesc + 2 * k,
@@ -492,7 +520,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 if (it > 0) {
                     const uint64_t dl = ptx::globaltimer() + static_cast<uint64_t>(c.timeout_ns);
                     const uint32_t i = it - 1;
-                    ptx::mbar_wait(&bars->empty[i % NST], (i / NST) & 1u, dl);
+                    ptx::mbar_wait(&bars->empty[i % nst], (i / nst) & 1u, dl);
                 }
             }
         } else if (FUSED) {
@@ -754,7 +782,7 @@ cudaError_t launch_ffn_bs(const FfnMaps &maps, const Dims &d, const Workspace &w
                           const uint8_t *sfb1, const uint8_t *sfb2, int wave_blocks, int num_sms, bool fp4,
                           cudaStream_t s)
 {
-    constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + 8192 + STAGES * SF_STAGE_BYTES;
+    constexpr int SMEM = 1024 + RING_BYTES + 8192 + NST_MAX * SF_STAGE_BYTES;
     static_assert(sizeof(BsBars) <= 8192, "barrier block");
     static_assert(SMEM <= 227 * 1024, "shared memory per CTA");
     const bool fu = c.fused_combine != 0;

@@ -249,3 +249,40 @@ def test_mxfp4_host_buffers_match_device_forward():
     assert moe.get_error() == 0
     assert torch.equal(host.view(torch.int16), dev.cpu().view(torch.int16))
     assert torch.equal(o_async.view(torch.int16), dev.cpu().view(torch.int16))
+
+
+@pytest.mark.parametrize("hot", [64, 65])
+@pytest.mark.parametrize("weights", ["mxfp4", "fp8"])
+def test_block_scaled_stage_layout_at_the_64_row_boundary(hot, weights):
+    """The block-scaled kernel stages 8 KB of A rows per K block (one more stage in flight)
+    when no M-block of the forward holds more than 64 rows, else 16 KB: expert 0 receives
+    exactly 64 rows (compact layout; the UMMA's padding rows 64-127 then read the stage's weight
+    tile) or 65 (standard layout); every token against the oracle, both weight formats."""
+    T = 256
+    wl = Workload(f"mx-edge-{weights}", T=T, H=512, I=256, E=6, topk=1, R=2, seed=66, scales="pow2",
+                  weights=weights)
+    torch.cuda.set_device(0)
+    inp = make_inputs(wl, device="cuda")
+    moe = FusedMoE(wl.E, wl.H, wl.I, wl.topk, wl.R).reserve(T)
+    moe.load(inp)
+    moe.set_option(native.OPT_SCALE_MODE, 1)
+    idx = (1 + torch.arange(T, device="cuda") % 5).view(T, 1)     # 5 experts x <= 52 rows
+    sel = torch.randperm(T, generator=torch.Generator().manual_seed(hot))[:hot].cuda()
+    idx[sel] = 0                                                  # expert 0: `hot` rows
+    idx = idx.contiguous()
+    counts = torch.bincount(idx.view(-1), minlength=wl.E)
+    assert int(counts.max()) == hot
+    out = moe.forward(inp.x, inp.x_sf, idx, inp.topk_w)
+    torch.cuda.synchronize()
+    assert moe.get_error() == 0
+    h = oracle.HostInputs(inp.x, inp.x_sf, idx, inp.topk_w, inp.w_gate_up, inp.sf_gate_up, inp.w_down,
+                          inp.sf_down, weights=weights)
+    oracle.set_scale_rule("pow2")
+    try:
+        _, ref, bad = oracle.forward_tokens(h, np.arange(T))
+    finally:
+        oracle.set_scale_rule("fp32")
+    assert not bad
+    rel = rel_l2(out, ref)
+    assert np.all(rel <= TOL), rel.max()
+    moe.close()

@@ -117,7 +117,6 @@ cudaError_t launch_programmatic(void (*kern)(KArgs...), int grid, int block, int
 }
 
 // Launchers (one per translation unit).
-size_t dispatch_smem_bytes(const Dims &d);
 cudaError_t launch_dispatch(const Dims &d, const Workspace &ws, const CallArgs &c, int num_sms,
                             cudaStream_t s);
 constexpr int A_ROWS_PART = 32;   // row granularity of partial A-tile loads

@@ -123,6 +123,31 @@ __device__ __forceinline__ void bulk_load(void *smem_dst, const void *gsrc, uint
                  : "memory");
 }
 
+// Untiled bulk copy this CTA's shared memory -> global, in the issuing thread's current bulk
+// group (both addresses 16-byte aligned, size a multiple of 16 bytes); bulk_commit closes the
+// group, bulk_wait_read<N> waits until at most N of the thread's groups still read shared
+// memory, bulk_wait<N> until at most N are incomplete.
+__device__ __forceinline__ void bulk_store(void *gdst, const void *smem_src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(reinterpret_cast<uint64_t>(gdst)),
+                 "r"(smem_u32(smem_src)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit()
+{
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void bulk_wait_read()
+{
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+template <int N>
+__device__ __forceinline__ void bulk_wait()
+{
+    asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // L2 cache policies (createpolicy): keep re-read operands, stream once-read ones.
 __device__ __forceinline__ uint64_t policy_evict_last()
 {

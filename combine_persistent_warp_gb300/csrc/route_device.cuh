@@ -256,45 +256,44 @@ __device__ inline void segments(const Dims &d, const Workspace &ws, uint32_t *re
     }
 }
 
-// Step a5 for pool row j (rows in expert order; e = its expert, recv_e = rows of expert e per
-// source): the round robin picks (source, slot), the table gives (token, k); one warp copies
-// the token's H bytes and H/128 scales into the pool row, writes {source, token, k} and adds
-// one to the M-block's arrival count.  The FFN kernel that reads the pool is a later launch
-// on the same stream, which already orders these stores before its loads, so the count is
-// a plain (relaxed) increment: a GPU-scope release per row stalled every warp until its
-// row's stores had reached L2.
-// U = 16-byte loads in flight per lane.
-template <int U>
-__device__ __forceinline__ void gather_row(const Dims &d, const Workspace &ws, const CallArgs &c, int j, int e,
-                                           const int32_t *cum, const int32_t *blk, const uint32_t *recv_e,
-                                           int lane)
+// Step a5: the gather of the expert-major pool, one warp per pool row at a time (rows in
+// expert order).  For pool row j of expert e (recv_e = rows of expert e per source) the round
+// robin picks (source, slot) and the index table gives (token, k); the token's H bytes move
+// global -> shared -> global by two bulk (TMA) copies through a double buffer of the warp, the
+// next row's load issued before the current row's store, while the lanes write the row's H/128
+// scales (and, on the block-scaled path, their UE8M0 bytes), its {source, token, k} and add one
+// to the M-block's arrival count.  The FFN kernel that reads the pool is a later launch on the
+// same stream, which orders all of these stores before its loads, so the count is a plain
+// (relaxed) increment.
+struct PoolRow {
+    long long row;   // pool row
+    int t, kk;       // token, top-k slot
+    uint32_t r;      // source
+};
+
+__device__ __forceinline__ PoolRow resolve_row(const Dims &d, const Workspace &ws, const CallArgs &c, int j,
+                                               const int32_t *cum, const int32_t *blk, const uint32_t *recv_s)
 {
-    const int R = d.R, K = d.K, H = d.H;
-    const int Tsrc = c.T / R;
+    const int e = last_le(cum, d.E + 1, j);
     const uint32_t i = static_cast<uint32_t>(j - cum[e]);
-    uint32_t r, slot;
-    round_robin(recv_e, R, i, r, slot);
-    const int v = __ldcg(&ws.table[(static_cast<long long>(e) * R + r) * ws.tsrc_cap + slot]);
-    const int t = static_cast<int>(r) * Tsrc + v / K;
-    const int kk = v % K;
-    const long long row = static_cast<long long>(blk[e]) * BM + i;
-    const uint4 *__restrict__ src = reinterpret_cast<const uint4 *>(c.x + static_cast<long long>(t) * H);
-    uint4 *__restrict__ dst = reinterpret_cast<uint4 *>(ws.pool_x + row * H);
-    const int H16 = H / 16, KBH = H / 128;
-    for (int q0 = lane; q0 < H16; q0 += 32 * U) {
-        uint4 buf[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u)
-            if (q0 + u * 32 < H16)
-                buf[u] = __ldg(src + q0 + u * 32);
-#pragma unroll
-        for (int u = 0; u < U; ++u)
-            if (q0 + u * 32 < H16)
-                dst[q0 + u * 32] = buf[u];
-    }
+    PoolRow x;
+    uint32_t slot;
+    round_robin(recv_s + e * d.R, d.R, i, x.r, slot);
+    const int v = __ldcg(&ws.table[(static_cast<long long>(e) * d.R + x.r) * ws.tsrc_cap + slot]);
+    x.t = static_cast<int>(x.r) * (c.T / d.R) + v / d.K;
+    x.kk = v % d.K;
+    x.row = static_cast<long long>(blk[e]) * BM + i;
+    return x;
+}
+
+// the row's scales, UE8M0 bytes, metadata and arrival (all lanes of the warp)
+__device__ __forceinline__ void row_side_data(const Dims &d, const Workspace &ws, const CallArgs &c, const PoolRow &x,
+                                              int lane)
+{
+    const int KBH = d.H / 128;
     for (int kb = lane; kb < KBH; kb += 32) {
-        const float sf = __ldg(c.x_sf + static_cast<long long>(t) * KBH + kb);
-        ws.pool_sf[static_cast<long long>(kb) * ws.P + row] = sf;
+        const float sf = __ldg(c.x_sf + static_cast<long long>(x.t) * KBH + kb);
+        ws.pool_sf[static_cast<long long>(kb) * ws.P + x.row] = sf;
         if (c.block_scaled) {
             // UE8M0 byte of this row and K block kb in its M-block's 512-byte scale block of
             // the group of four K blocks kb / 4 (row r's word at byte 16*(r%32) + 4*(r/32),
@@ -302,18 +301,75 @@ __device__ __forceinline__ void gather_row(const Dims &d, const Workspace &ws, c
             const uint32_t b = __float_as_uint(sf), ex = (b >> 23) & 0xFFu;
             if ((b & 0x807FFFFFu) != 0u || ex == 0u || ex == 0xFFu)
                 record_error(ws.hdr, DEV_BAD_SCALE);
-            const int rr = static_cast<int>(row % BM);
-            ws.pool_sfe[((row / BM) * ((KBH + 3) / 4) + kb / 4) * 512 + 16 * (rr % 32) + 4 * (rr / 32) + kb % 4] =
+            const int rr = static_cast<int>(x.row % BM);
+            ws.pool_sfe[((x.row / BM) * ((KBH + 3) / 4) + kb / 4) * 512 + 16 * (rr % 32) + 4 * (rr / 32) + kb % 4] =
                 static_cast<uint8_t>(ex);
         }
     }
     if (lane == 0) {
-        ws.meta[row * 3 + 0] = r;
-        ws.meta[row * 3 + 1] = static_cast<uint32_t>(t);
-        ws.meta[row * 3 + 2] = static_cast<uint32_t>(kk);
+        ws.meta[x.row * 3 + 0] = x.r;
+        ws.meta[x.row * 3 + 1] = static_cast<uint32_t>(x.t);
+        ws.meta[x.row * 3 + 2] = static_cast<uint32_t>(x.kk);
+        atomicAdd(ws.arrive + x.row / BM, 1u);
+    }
+}
+
+// One gather warp: rows gw, gw + nw, ...; bar[2] (initialised, count 1) and buf (2 * H bytes,
+// 16-byte aligned) are the warp's own.  Every wait is bounded; on a time-out the warp records
+// DEV_TIMEOUT, waits (bounded again) for its loads in flight and stops.  Before returning, lane
+// 0 waits for its bulk stores to complete.
+__device__ inline void gather_rows(const Dims &d, const Workspace &ws, const CallArgs &c, const int32_t *cum,
+                                   const int32_t *blk, const uint32_t *recv_s, int gw, int nw, uint64_t *bar,
+                                   uint8_t *buf, uint64_t deadline, int lane)
+{
+    const int total = cum[d.E];
+    if (gw >= total)
+        return;
+    const uint32_t H = static_cast<uint32_t>(d.H);
+    PoolRow cur = resolve_row(d, ws, c, gw, cum, blk, recv_s);
+    if (lane == 0) {
+        ptx::mbar_arrive_expect_tx(&bar[0], H);
+        ptx::bulk_load(buf, c.x + static_cast<long long>(cur.t) * H, H, &bar[0]);
+    }
+    uint32_t it = 0;
+    bool ok = true;
+    for (int j = gw; j < total; j += nw, ++it) {
+        const bool more = j + nw < total;
+        PoolRow nxt{};
+        if (more) {
+            nxt = resolve_row(d, ws, c, j + nw, cum, blk, recv_s);
+            if (lane == 0) {
+                // the other buffer's last store (row j - nw) has read it
+                ptx::bulk_wait_read<0>();
+                const uint32_t nb = (it + 1) & 1u;
+                ptx::mbar_arrive_expect_tx(&bar[nb], H);
+                ptx::bulk_load(buf + nb * H, c.x + static_cast<long long>(nxt.t) * H, H, &bar[nb]);
+            }
+        }
+        row_side_data(d, ws, c, cur, lane);
+        if (lane == 0) {
+            const uint32_t b = it & 1u;
+            if (ptx::mbar_wait(&bar[b], (it >> 1) & 1u, deadline)) {
+                ptx::bulk_store(ws.pool_x + cur.row * H, buf + b * H, H);
+                ptx::bulk_commit();
+            } else {
+                ok = false;
+            }
+        }
+        if (!__shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0)) {
+            if (lane == 0) {
+                record_error(ws.hdr, DEV_TIMEOUT);
+                const uint64_t dl = ptx::globaltimer() + static_cast<uint64_t>(c.timeout_ns);
+                ptx::mbar_wait(&bar[it & 1u], (it >> 1) & 1u, dl);
+                if (more)
+                    ptx::mbar_wait(&bar[(it + 1) & 1u], ((it + 1) >> 1) & 1u, dl);
+            }
+            break;
+        }
+        cur = nxt;
     }
     if (lane == 0)
-        atomicAdd(ws.arrive + row / BM, 1u);
+        ptx::bulk_wait<0>();
 }
 
 }  // namespace route

@@ -21,12 +21,31 @@
 
 namespace cpw {
 
-// Dynamic shared memory: cnt [R*E] u32 | recv [E*R] u32 | cum [E+1] | blk [E+1] | flag
-size_t dispatch_smem_bytes(const Dims &d)
+// Dynamic shared memory of the routing kernel: cnt [R*E] u32 | recv [E*R] u32 | cum [E+1] |
+// blk [E+1] | flag, then (16-byte aligned) the gather warps' barriers [gwarps][2] and
+// (128-byte aligned) their row buffers [gwarps][2][H]: up to 192 KB of rows in flight per SM.
+struct DispatchSmem {
+    size_t bars, bufs, total;
+    int gwarps;   // warps of a CTA that gather
+};
+__host__ __device__ inline DispatchSmem dispatch_smem(const Dims &d, int threads)
 {
-    return sizeof(uint32_t) * (2 * static_cast<size_t>(d.R) * d.E) +
-           sizeof(int32_t) * 2 * (static_cast<size_t>(d.E) + 1) + 16;
+    constexpr size_t SMEM_MAX = 227 * 1024, STAGING = 192 * 1024;
+    DispatchSmem L;
+    const size_t base = sizeof(uint32_t) * (2 * static_cast<size_t>(d.R) * d.E) +
+                        sizeof(int32_t) * 2 * (static_cast<size_t>(d.E) + 1) + 16;
+    L.bars = (base + 15) & ~static_cast<size_t>(15);
+    const int maxw = threads / 32;
+    const size_t used = L.bars + 16 * static_cast<size_t>(maxw) + 128;
+    const size_t room = used < SMEM_MAX ? SMEM_MAX - used : 0;
+    const size_t stg = room < STAGING ? room : STAGING;
+    const size_t per_warp = 2 * static_cast<size_t>(d.H);
+    L.gwarps = static_cast<int>(stg / per_warp) < maxw ? static_cast<int>(stg / per_warp) : maxw;
+    L.bufs = (L.bars + 16 * static_cast<size_t>(L.gwarps) + 127) & ~static_cast<size_t>(127);
+    L.total = L.bufs + per_warp * static_cast<size_t>(L.gwarps);
+    return L;
 }
+
 
 __global__ void __launch_bounds__(DISPATCH_THREADS, 1)
     dispatch_kernel(const Dims d, const Workspace ws, const CallArgs c)
@@ -38,6 +57,14 @@ __global__ void __launch_bounds__(DISPATCH_THREADS, 1)
     int32_t *cum = reinterpret_cast<int32_t *>(recv_s + E * R);
     int32_t *blk = cum + (E + 1);
     volatile int *s_ok = reinterpret_cast<volatile int *>(blk + (E + 1));
+    const DispatchSmem L = dispatch_smem(d, blockDim.x);
+    uint64_t *gbar = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(smem_u) + L.bars);
+    uint8_t *gbuf = reinterpret_cast<uint8_t *>(smem_u) + L.bufs;
+    if (threadIdx.x == 0) {   // the gather warps' row barriers (first used after the grid barrier)
+        for (int i = 0; i < 2 * L.gwarps; ++i)
+            ptx::mbar_init(&gbar[i], 1);
+        ptx::fence_mbar_init();
+    }
 
     // the expert FFN kernel may be scheduled at once: its CTAs run their prologue as this
     // kernel's CTAs leave and then wait for the whole grid
@@ -64,21 +91,25 @@ __global__ void __launch_bounds__(DISPATCH_THREADS, 1)
     // ---- received counts, expert segments, M-block map -----------------------------------
     route::segments(d, ws, recv_s, cum, blk);
 
-    // ---- gather, one warp per received row (global order across experts) -------------------
+    // ---- gather, one warp per received row at a time (global order across experts) ------
     // (warps numbered CTA-minor, so a small batch's rows spread over every SM)
-    const int lane = threadIdx.x & 31;
-    const int gw = (threadIdx.x >> 5) * gridDim.x + blockIdx.x, nw = (gridDim.x * blockDim.x) >> 5;
-    const int total_rows = cum[E];
-    for (int j = gw; j < total_rows; j += nw) {
-        const int e = route::last_le(cum, E + 1, j);
-        route::gather_row<8>(d, ws, c, j, e, cum, blk, recv_s + e * R, lane);
-    }
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (warp < L.gwarps)
+        route::gather_rows(d, ws, c, cum, blk, recv_s, warp * gridDim.x + blockIdx.x, L.gwarps * gridDim.x,
+                           gbar + 2 * warp, gbuf + static_cast<size_t>(warp) * 2 * d.H, deadline, lane);
 }
 
 cudaError_t launch_dispatch(const Dims &d, const Workspace &ws, const CallArgs &c, int num_sms,
                             cudaStream_t s)
 {
-    const size_t smem = dispatch_smem_bytes(d);
+    // the routing steps of a large batch want every warp an SM can hold; a small batch is bound
+    // by the routing steps and the launch, which half the block does faster
+    const long long rows = static_cast<long long>(c.T) * d.K;
+    const int threads = rows >= 8LL * 1024 ? DISPATCH_THREADS : DISPATCH_THREADS / 2;
+    const DispatchSmem L = dispatch_smem(d, threads);
+    if (L.gwarps < 1)   // cannot happen for the shapes moe_create accepts (H <= 16384, R*E <= 16384)
+        return cudaErrorInvalidConfiguration;
+    const size_t smem = L.total;
     cudaError_t e = ensure_max_dynamic_smem(reinterpret_cast<const void *>(dispatch_kernel), static_cast<int>(smem));
     if (e != cudaSuccess)
         return e;
@@ -86,10 +117,6 @@ cudaError_t launch_dispatch(const Dims &d, const Workspace &ws, const CallArgs &
     Workspace ww = ws;
     CallArgs cc = c;
     void *args[] = {&dd, &ww, &cc};
-    // the gather of a large batch wants every warp an SM can hold; a small batch is bound by
-    // the routing steps and the launch, which half the block does faster
-    const long long rows = static_cast<long long>(c.T) * d.K;
-    const int threads = rows >= 8LL * 1024 ? DISPATCH_THREADS : DISPATCH_THREADS / 2;
     return cudaLaunchCooperativeKernel(reinterpret_cast<void *>(dispatch_kernel), dim3(num_sms), dim3(threads), args,
                                        smem, s);
 }

@@ -198,3 +198,21 @@ def test_in_kernel_combine_host_entry_point(name):
         assert torch.equal(bits(dev), bits(page))
     assert moe.get_error() == 0
     moe.close()
+
+
+def test_widest_route_32_slots():
+    """topk = 32 (the largest routed-slot count, the full width of a token's slot mask; four
+    rounds of eight plane loads in the reduce) with skipped slots: both combine modes against
+    the oracle on every token, and bit-identical to each other."""
+    T = 128
+    wl = Workload("in-ffn-k32", T=T, H=256, I=128, E=40, topk=32, R=2, skip_frac=0.1, seed=84)
+    moe, inp = layer(wl)
+    ref = oracle_ref(inp, np.arange(T))
+    outs = []
+    for mode in (KERNEL, IN_FFN):
+        out = forward_mode(moe, inp, mode)
+        rel = rel_l2(out, ref)
+        assert np.all(rel <= TOL), rel.max()
+        outs.append(out.clone())
+    assert torch.equal(bits(outs[0]), bits(outs[1]))
+    moe.close()

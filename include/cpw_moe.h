@@ -141,7 +141,8 @@ int moe_forward(moe_handle_t h, int T, const uint8_t *x, const float *x_sf,
  * the stream has finished.  Inputs in pinned (page-locked, device-mapped) memory with
  * 16-byte aligned addresses are read in place by one staging kernel into the handle's
  * device staging buffers; others are copied there by cudaMemcpyAsync.  A pinned, 16-byte
- * aligned `host_out` is written in place by the combine kernel; otherwise the result is
+ * aligned `host_out` is written in place by the kernel that completes the combine (the FFN
+ * kernel itself in the default combine mode, see MOE_OPT_COMBINE_MODE); otherwise the result is
  * copied back from a staging buffer.  Pageable buffers work but are slower. */
 int moe_forward_host(moe_handle_t h, int T, const uint8_t *host_x, const float *host_x_sf,
                      const int64_t *host_topk_idx, const float *host_topk_w,
@@ -246,7 +247,9 @@ int moe_set_option(moe_handle_t h, int option, int64_t value);
  * the 1st, (N+1)-th, (2N+1)-th ... moe_forward from now records an event before and after
  * each of its three kernels (dispatch; expert FFN = gate_up GEMM + SwiGLU + down GEMM +
  * weighted scatter; combine) — N > 1 samples the forwards, so the events (which serialise
- * the kernels they sit between) disturb only one step in N; enable = 0 stops.
+ * the kernels they sit between) disturb only one step in N; enable = 0 stops.  With the
+ * combine inside the FFN kernel the combine stage brackets no kernel (its time is ~0 and the
+ * FFN stage includes the reduce).
  * moe_profile_read waits for the last stream, returns the summed milliseconds of each
  * stage over the recorded forwards in stage_ms[3] and their number in *calls, and starts
  * a new window.  At most 8192 forwards are recorded per window (later ones are counted in

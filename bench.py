@@ -243,7 +243,9 @@ def work_model(inp) -> dict:
                        "flops": 2 * M * H * 2 * I + 2 * M * I * H},
         "combine": {"bytes": M * H * 2 + T * H * 2 + T * K * 8, "flops": M * H},
     }
+    from combine_persistent_warp_gb300.workloads import skew_ratio
     return {"M": M, "touched_experts": touched, "stages": st, "compulsory_bytes": compulsory,
+            "hot_expert_rows_over_mean": round(float(skew_ratio(idx, E)), 3),
             "intermediate_bytes": intermediate, "flops": 6 * M * H * I, "weight_bytes": w1 + w2}
 
 
@@ -394,6 +396,7 @@ def config_of(wl, model: dict, world: int, flush: bool) -> dict:
     return {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E,
             "topk": wl.topk, "R": wl.R, "routing": wl.routing, "scales": wl.scales,
             "weights": wl.weights, "routed_rows_per_step": model["M"],
+            **({"hot_expert_rows_over_mean": model["hot_expert_rows_over_mean"]} if wl.routing == "zipf" else {}),
             "parallelism": f"replicas x{world}",
             "l2": ("L2 flushed (%d MB written) before every timed step, steps timed one by one"
                    % (2 * L2_BYTES >> 20) if flush else

@@ -49,9 +49,9 @@ PROFILE_EVERY = 8            # timed steps per step carrying the per-kernel stag
 # DRAM bytes per launch from one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum),
 # valid only while the kernel sources hash to `src_sha`; see profiles/.
 NCU_TRAFFIC = {
-    ("large", "expert_ffn"): {"bytes": 3243558400 + 1255286016, "src_sha": "13d73c603fb41646"},
-    ("decode", "expert_ffn"): {"bytes": 1421092864 + 5978880, "src_sha": "13d73c603fb41646"},
-    ("prefill", "expert_ffn"): {"bytes": 1981654528 + 520409344, "src_sha": "13d73c603fb41646"},
+    ("large", "expert_ffn"): {"bytes": 3243875328 + 1254976000, "src_sha": "647639520b05b2bc"},
+    ("decode", "expert_ffn"): {"bytes": 1420943104 + 5985536, "src_sha": "647639520b05b2bc"},
+    ("prefill", "expert_ffn"): {"bytes": 1996200960 + 520273920, "src_sha": "647639520b05b2bc"},
 }
 # sources each stage's kernel is compiled from (a recorded traffic figure is used only while
 # these hash to its `src_sha`)

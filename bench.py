@@ -236,12 +236,13 @@ def work_model(inp) -> dict:
     compulsory = w1 + w2 + T * (H + (H // 128) * 4) + T * K * 12 + T * H * 2
     intermediate = 2 * x_rows + 2 * act_rows + 2 * M * H * 2 + M * 12
     st = {
-        "dispatch": {"bytes": T * K * 8 + 2 * x_rows + M * (12 + 8), "flops": 0},
+        "dispatch": {"bytes": T * K * 8 + 2 * x_rows + M * (12 + 8) + T * 4, "flops": 0},
         # gate_up GEMM + SwiGLU + down GEMM + weighted scatter (one kernel): weights, the
         # gathered rows in, the SwiGLU rows out and back in, the bf16 planes out
         "expert_ffn": {"bytes": w1 + w2 + x_rows + 2 * act_rows + M * H * 2 + M * 16,
                        "flops": 2 * M * H * 2 * I + 2 * M * I * H},
-        "combine": {"bytes": M * H * 2 + T * H * 2 + T * K * 8, "flops": M * H},
+        # the bf16 planes in, the output out, one slot-mask word per token
+        "combine": {"bytes": M * H * 2 + T * H * 2 + T * 4, "flops": M * H},
     }
     from combine_persistent_warp_gb300.workloads import skew_ratio
     return {"M": M, "touched_experts": touched, "stages": st, "compulsory_bytes": compulsory,

@@ -163,10 +163,11 @@ __device__ inline void count_claim_table(const Dims &d, const Workspace &ws, con
     }
 }
 
-// For the combine inside the FFN kernel (topk_combine.cuh): tok_mask[t] = the routed top-k
-// slots of token t (bit k set when topk_idx[t][k] >= 0; topk + shared slots <= 32), and the
-// output row of a token with no routed slot is zero (the combine's empty sum), written here
-// because no down tile will ever count it.  One thread per token of the grid.
+// tok_mask[t] = the routed top-k slots of token t (bit k set when topk_idx[t][k] >= 0; topk +
+// shared slots <= 32), read by the combine kernel and by the combine inside the FFN kernel
+// (topk_combine.cuh); for the latter the output row of a token with no routed slot is zero (the
+// combine's empty sum), written here because no down tile will ever count it.  One thread per
+// token of the grid.
 __device__ inline void token_masks(const Dims &d, const Workspace &ws, const CallArgs &c)
 {
     const int K = d.K;
@@ -178,7 +179,7 @@ __device__ inline void token_masks(const Dims &d, const Workspace &ws, const Cal
         for (int k = 0; k < K; ++k)
             m |= (id[k] >= 0 ? 1u : 0u) << k;
         ws.tok_mask[t] = m;
-        if (m == 0) {
+        if (m == 0 && c.fused_combine) {
             uint4 *o = reinterpret_cast<uint4 *>(c.out + static_cast<long long>(t) * d.H);
             for (int v = 0; v < d.H / 8; ++v)
                 o[v] = make_uint4(0u, 0u, 0u, 0u);

@@ -77,9 +77,9 @@ __global__ void __launch_bounds__(DISPATCH_THREADS, 1)
 
     // ---- count, packed claim, index table ------------------------------------------------
     route::count_claim_table(d, ws, c, cnt);
-    // in-kernel combine: each token's routed slots, and the zero rows of unrouted tokens
-    if (c.fused_combine)
-        route::token_masks(d, ws, c);
+    // each token's routed slots (read by either combine), and with the in-kernel combine the
+    // zero rows of unrouted tokens
+    route::token_masks(d, ws, c);
 
     // ---- grid barrier: every claim and table entry is visible past this point -----------
     const bool skip = c.debug_skip_barrier != 0 && blockIdx.x == 0;
@@ -148,9 +148,7 @@ __global__ void __launch_bounds__(COMBINE_THREADS, 2)
             for (int v = 0; v < 2; ++v) {
                 if (v == 1 && !live1)
                     break;
-                const long long t = g[v] / H8;
-                for (int kk = 0; kk < K; ++kk)
-                    mask[v] |= (__ldg(c.idx + t * K + kk) >= 0 ? 1u : 0u) << kk;
+                mask[v] = __ldcg(ws.tok_mask + g[v] / H8);   // the routing kernel's slot mask
             }
             float acc[2][8];
 #pragma unroll

@@ -128,6 +128,9 @@ cudaError_t launch_dispatch(const Dims &d, const Workspace &ws, const CallArgs &
 __global__ void __launch_bounds__(COMBINE_THREADS, 2)
     combine_kernel(const Dims d, const Workspace ws, const CallArgs c)
 {
+    // launched programmatically for small batches: the FFN kernel's results are complete and
+    // visible past this point (a no-op for an ordinary launch)
+    ptx::grid_dependency_wait();
     const int K = d.K, H = d.H;
     const uint32_t err = *reinterpret_cast<volatile uint32_t *>(ws.hdr + HDR_ERR_CALL) |
                          *reinterpret_cast<volatile uint32_t *>(ws.hdr + HDR_ERR_STICKY);
@@ -199,9 +202,14 @@ __global__ void __launch_bounds__(COMBINE_THREADS, 2)
 cudaError_t launch_combine(const Dims &d, const Workspace &ws, const CallArgs &c, int num_sms,
                            cudaStream_t s)
 {
-    // two CTAs per SM (128 registers a thread keep 16 plane loads in flight), all resident
-    // an ordinary launch: letting it start during the FFN kernel's last tiles (programmatic
-    // launch) measured 1.3% slower on the large batch and about 1 us faster at decode
+    // two CTAs per SM (128 registers a thread keep 16 plane loads in flight), all resident.
+    // A small batch (at most 4096 routed rows, the threshold at which "MOE融合算子",
+    // vllm-ascend dispatch_ffn_combine §4, switches to its small-batch combine) is launched
+    // programmatically, so the launch overlaps the FFN kernel's last
+    // CTAs; a large one ordinarily (programmatic there measured 1.3% slower: its CTAs wait on the
+    // SMs the FFN CTAs leave)
+    if (static_cast<long long>(c.T) * d.K <= 4096)
+        return launch_programmatic(combine_kernel, num_sms * 2, COMBINE_THREADS, 0, s, d, ws, c);
     combine_kernel<<<num_sms * 2, COMBINE_THREADS, 0, s>>>(d, ws, c);
     return cudaGetLastError();
 }

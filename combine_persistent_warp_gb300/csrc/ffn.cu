@@ -116,6 +116,7 @@ struct __align__(16) FfnBars {
     uint32_t roff[TILE_RING][BM];      // down tile: combine row (slot * max_tokens + token)
     topk::Lists<TILE_RING> tk;         // in-kernel combine: pairs completed by a down tile
     int exit_flag;
+    int max_rows;                      // valid rows of the fullest M-block of the forward
 };
 constexpr int FFN_SMEM_BYTES = 1024 /*align slack*/ + STAGES * STAGE_BYTES + static_cast<int>(sizeof(FfnBars));
 static_assert(FFN_SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
@@ -186,6 +187,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             ptx::mbar_init(&bars->act_done[i], EPI_WARPS);
             ptx::mbar_init(&bars->tk.ready[i], 1);
         }
+        bars->max_rows = 0;
         ptx::fence_mbar_init();
     } else if (threadIdx.x == 32) {
         ptx::prefetch_tmap(&maps.a1);
@@ -215,6 +217,22 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             ffn_cta_exit(d, ws, &bars->exit_flag);
         return;
     }
+    // Who hands an operand stage back to the producer.  With M-blocks of at most 64 rows
+    // (decode-sized batches) the weight stream sets the rate and most epilogue warps hold only
+    // padding rows: the UMMA issuer commits the stage's release itself, so a refill never waits
+    // for an epilogue warp busy promoting.  Otherwise epilogue warp 4 releases it when it sees
+    // the partial, which keeps a second commit off the issuer of a tensor-bound batch.
+    {
+        const int nblocks = min(ws.blk_off[d.E], ws.max_blocks);
+        int mr = 0;
+        for (int b = threadIdx.x; b < nblocks; b += blockDim.x)
+            mr = max(mr, ws.block_rows[b]);
+        mr = __reduce_max_sync(0xFFFFFFFFu, mr);
+        if (lane == 0 && mr > 0)
+            atomicMax(&bars->max_rows, mr);
+        __syncthreads();
+    }
+    const bool issuer_releases = bars->max_rows <= 2 * A_ROWS_PART;
 
     const TileList tl{(2 * d.I) / BN, (d.H + BN - 1) / BN, ws.blk_off[d.E], wave_blocks};
     const int ntiles = tl.total();
@@ -377,7 +395,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                             ptx::umma_f8(dt, adesc + 2 * k, bdesc + 2 * k, IDESC, k > 0 ? 1u : 0u);
                         CPW_STAMP(2, it);
                         // the epilogue warps, once they see the partial, also release the stage
+                        // (or, for small M-blocks, this commit does)
                         ptx::umma_commit(&bars->tfull[buf]);
+                        if (issuer_releases)
+                            ptx::umma_commit(&bars->empty[s]);
                     }
                 }
                 if (!ok)
@@ -632,7 +653,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     break;
                 }
                 // the MMAs that read this K block's operand stage are complete
-                if (warp == 4 && lane == 0)
+                if (!issuer_releases && warp == 4 && lane == 0)
                     ptx::mbar_arrive(&bars->empty[s]);
                 if (warp == 4 && lane == 0)
                     CPW_STAMP(3, it);

@@ -49,9 +49,9 @@ PROFILE_EVERY = 8            # timed steps per step carrying the per-kernel stag
 # DRAM bytes per launch from one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum),
 # valid only while the kernel sources hash to `src_sha`; see profiles/.
 NCU_TRAFFIC = {
-    ("large", "expert_ffn"): {"bytes": 3243875328 + 1254976000, "src_sha": "647639520b05b2bc"},
-    ("decode", "expert_ffn"): {"bytes": 1420943104 + 5985536, "src_sha": "647639520b05b2bc"},
-    ("prefill", "expert_ffn"): {"bytes": 1996200960 + 520273920, "src_sha": "647639520b05b2bc"},
+    ("large", "expert_ffn"): {"bytes": 3241676288 + 1253330944, "src_sha": "f7fdbebcbe952963"},
+    ("decode", "expert_ffn"): {"bytes": 1420896768 + 5254144, "src_sha": "f7fdbebcbe952963"},
+    ("prefill", "expert_ffn"): {"bytes": 1969887488 + 517826304, "src_sha": "f7fdbebcbe952963"},
 }
 # sources each stage's kernel is compiled from (a recorded traffic figure is used only while
 # these hash to its `src_sha`)

@@ -367,7 +367,9 @@ int moe_reserve(moe_handle_t h, int max_tokens)
     if (encode_tile_map(&h->maps.a1, ws.pool_x, ws.P, d.H, BM) != MOE_OK ||
         encode_tile_map(&h->maps.a2, ws.act, ws.P, d.I, BM) != MOE_OK ||
         encode_tile_map(&h->maps.a1p, ws.pool_x, ws.P, d.H, A_ROWS_PART) != MOE_OK ||
-        encode_tile_map(&h->maps.a2p, ws.act, ws.P, d.I, A_ROWS_PART) != MOE_OK)
+        encode_tile_map(&h->maps.a2p, ws.act, ws.P, d.I, A_ROWS_PART) != MOE_OK ||
+        encode_tile_map(&h->maps.a1h, ws.pool_x, ws.P, d.H, 2 * A_ROWS_PART) != MOE_OK ||
+        encode_tile_map(&h->maps.a2h, ws.act, ws.P, d.I, 2 * A_ROWS_PART) != MOE_OK)
         return MOE_ERR_CUDA;
     CK(cudaDeviceSynchronize());
     h->reserved = true;

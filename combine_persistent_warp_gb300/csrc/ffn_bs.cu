@@ -17,12 +17,12 @@
 // with a group's first stage the producer bulk-copies a 512-byte A block (the 128 rows'
 // scale words, row r at byte 16*(r%32) + 4*(r/32)) and a 1 KB B block (two 512-byte halves;
 // tile column n at 512*(n/128) + 16*(n%32) + 4*((n%128)/32)), each word holding the UE8M0
-// bytes of the group's four K blocks (byte j = K block 4g + j).  The UMMA issuer copies them
-// into TMEM with tcgen05.cp 32x128b.warpx4 (every lane quarter gets the same 32 lanes),
-// where the UMMA reads row m's scale at lane m, column base + m/32, and tile column n's at
-// lane 32*q + n%32, column base + n/32, byte = the instruction's scale id, here K block % 4
-// for all four 32-deep UMMAs of a K block.  Copying once per group instead of once per K
-// block took the issue sequence from ~830 to ~700 cycles per K block.
+// bytes of the group's four K blocks (byte j = K block 4g + j), into a ring of three scale
+// slots.  The UMMA issuer copies them into the group's TMEM slot with tcgen05.cp
+// 32x128b.warpx4 (every lane quarter gets the same 32 lanes); the UMMA reads row m's scale at lane m, column base + m/32, and tile
+// column n's at lane 32*q + n%32, column base + n/32, byte = the instruction's scale id, here
+// K block % 4 for all four 32-deep UMMAs of a K block.  Copying once per group instead of
+// once per K block took the issue sequence from ~830 to ~700 cycles per K block.
 //
 // MXFP4 weights (FP4 = true): the weight tiles are packed E2M1 (64 bytes per row and 128-deep
 // K block) with one UE8M0 scale per row and 32-deep K slice (the OCP Microscaling block).  TMA
@@ -30,20 +30,26 @@
 // 16-byte slot in shared memory: the 128-byte-row image the UMMA reads for a 4-bit operand of
 // kind::mxf8f6f4 (B format E2M1), at the same swizzle and descriptor as an e4m3 tile, while
 // only the packed 16 KB per stage comes from memory.  The B scale words then change every K
-// block (byte j = the scale of the block's j-th 32-deep slice, instruction B scale id = j),
-// so the producer stages a 1 KB B scale block with every stage and the issuer copies it to
-// TMEM per K block, into the slot of the stage (reused only after the stage's next fill,
-// i.e. after the UMMAs that read it); the A scales keep their once-per-group copy.
+// block (byte j = the scale of the block's j-th 32-deep slice, instruction B scale id = j):
+// the group's B scales are its K blocks' 1 KB blocks, consecutive in memory, so they still
+// come in one bulk copy per group (up to 4 KB); the issuer copies each K block's to its own
+// columns of the group's TMEM slot just before that K block's UMMAs.
 //
-// Roles (one CTA per SM, 12 warps): warp 0 TMA producer (A, B and the two scale blocks of
-// a 128-deep K block per stage, 4 stages); warp 1 UMMA issuer (scale copies + 4 block-scaled
-// UMMAs per stage into one 256-column TMEM accumulator); warp 2 dependency warp (a down
+// Copies per K block: each load, bulk or tiled, that the producer issues costs the SM's TMA
+// unit more than its bytes at decode sizes, where a weight tile moves only 16 KB (MXFP4).  So
+// a K block stages A in one load (32, 64 or 128 rows, whichever first covers the M-block's
+// valid rows) and the scales come once per group.
+//
+// Roles (one CTA per SM, 12 warps): warp 0 TMA producer (A and B of a 128-deep K block per
+// stage, 4 or 5 stages, and a scale group's blocks with its first stage); warp 1 UMMA issuer
+// (a group's scale copies, then 4 block-scaled UMMAs per stage into one 256-column TMEM
+// accumulator); warp 2 dependency warp (a down
 // tile's gate_up completion count); warp 3, with the top-k combine inside this kernel, counts
 // each stored down tile's rows per (token, n-tile) and lists the pairs it completed
 // (topk_combine.cuh); warps 4-11 epilogue (two warpgroups, columns [0,128) / [128,256)): one
 // TMEM read per tile, then SwiGLU + UE8M0 requant (phase 1) or the weighted scatter (phase 2),
 // and with the in-kernel combine the reduce of the previous tile's completed pairs.  TMEM:
-// accumulator columns 0-255, scale slots 256 + 16*s.  All waits carry a deadline
+// accumulator columns 0-255, scale group slots 256 + 40*j.  All waits carry a deadline
 // (MOE_ERR_TIMEOUT).
 #include <cuda_bf16.h>
 
@@ -60,9 +66,17 @@ namespace {
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int EPI_WARPS = 8;
 constexpr int TILE_RING = 4;
-constexpr uint32_t SF_COL = 256;          // scale slot j: columns SF_COL + 16*j (A: +0..3, B: +4..11)
-constexpr int SF_GROUP = 4;               // K blocks per scale block (bytes of a scale word)
-constexpr uint32_t SFA_BYTES = 512, SFB_BYTES = 1024, SF_STAGE_BYTES = SFA_BYTES + SFB_BYTES;
+constexpr int SF_GROUP = 4;               // K blocks per scale group (bytes of an FP8 scale word)
+constexpr uint32_t SFA_BYTES = 512, SFB_BYTES = 1024;
+// Scale groups in shared memory: a ring of SF_SLOTS slots of [A 512 | B up to 4 x 1 KB], each
+// filled by one bulk copy per kind with a group's first stage.  The producer refills a slot
+// once the UMMAs of the last K block that read it have completed (that K block's release in
+// the stage ring, waited for only when it is less than a ring's length back).
+constexpr int SF_SLOTS = 3;
+constexpr uint32_t SF_SLOT_BYTES = SFA_BYTES + SF_GROUP * SFB_BYTES;
+// Scale groups in TMEM: group slot j at columns SF_COL + SF_TCOLS*j (A: +0..3; B: +4..11, or
+// with MXFP4 weights K block i of the group at +4+8i..+11+8i)
+constexpr uint32_t SF_COL = 256, SF_TCOLS = 40;
 static_assert(BKS == BK, "the block-scaled kernel stages whole 128-deep K blocks");
 // Stage ring layouts.  Standard: STAGES stages of [A 16 KB | B 32 KB].  Compact, when no M-block
 // of the forward holds more than 64 rows (decode-sized batches): NST_MAX stages of [A 8 KB |
@@ -77,7 +91,8 @@ constexpr int RING_BYTES = STAGES * STAGE_BYTES > NST_MAX * static_cast<int>(COM
                                : NST_MAX * static_cast<int>(COMPACT_STAGE_BYTES);
 static_assert(NST_MAX >= STAGES, "the compact ring has at least as many stages");
 static_assert(COMPACT_STAGE_BYTES % 1024 == 0 && COMPACT_A_BYTES % 1024 == 0, "128-byte swizzle atoms");
-static_assert(SF_COL + 16 * NST_MAX <= TMEM_COLS, "scale slots exceed TMEM");
+static_assert(SF_COL + SF_TCOLS * NST_MAX <= TMEM_COLS, "scale slots exceed TMEM");
+static_assert(4 + 8 * SF_GROUP <= SF_TCOLS, "a group's scale columns");
 
 // block-scaled instruction descriptor: B scale id (byte of the scale word) at bits 4-5, A
 // format e4m3 (0) at bits 7-9, B format at bits 10-12 (e4m3 = 0, E2M1 = 5), K-major A and B,
@@ -180,7 +195,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
     BsBars *bars = reinterpret_cast<BsBars *>(smem + RING_BYTES);
-    uint8_t *sf_smem = smem + RING_BYTES + 8192;   // [stage][A 512 | B 1024]
+    uint8_t *sf_smem = smem + RING_BYTES + 8192;   // [SF_SLOTS][A 512 | B 4 x 1 KB]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     // prologue (barriers, TMEM, tensor maps) while the routing kernel may still run
@@ -254,10 +269,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         v.e = ws.block_expert[v.blk];
         return v;
     };
-    // A bytes a CTA stages per K block for a tile (a partly filled M-block loads only the
-    // 32-row groups that hold valid rows), plus the scale blocks
+    // A bytes a CTA stages per K block for a tile, in one load: the first 32 or 64 rows of an
+    // M-block that holds no more valid rows, else all 128 (padding rows feed only accumulator
+    // rows that are never stored)
     auto a_stage_bytes = [&](int n_part) {
-        return n_part < BM / A_ROWS_PART ? static_cast<uint32_t>(n_part * A_ROWS_PART * BKS) : STAGE_A_BYTES;
+        return n_part <= 2 ? static_cast<uint32_t>(n_part * A_ROWS_PART * BKS) : STAGE_A_BYTES;
     };
     const int NKB1 = d.H / BK, NKB2 = d.I / BK;
     const uint32_t l1_target = static_cast<uint32_t>(EPI_WARPS * tl.NT1);
@@ -274,7 +290,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 const uint64_t pol_a = ptx::policy_evict_last();
                 const uint64_t pol_b_once = ptx::policy_evict_first();
                 const uint64_t pol_b_shared = ptx::policy_evict_normal();
-                uint32_t it = 0, tcount = 0;
+                uint32_t it = 0, tcount = 0, gcount = 0;   // K blocks, tiles, scale groups loaded
+                // the last K block whose TMEM copies read the scale slots of the last three groups
+                // (g-1, g-2, g-3; none yet: ~0): group g refills g-3's slot
+                static_assert(SF_SLOTS == 3, "one reader per slot of the ring");
+                uint32_t last1 = ~0u, last2 = ~0u, last3 = ~0u;
                 uint32_t s = 0, ph = 0;   // stage of K block `it` and its ring pass parity
                 bool ok = true;
                 // Tiles are claimed from the global counter one ahead (a CTA holds at most one
@@ -329,14 +349,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     int fstep = 0, fkb = -2;   // next tile's steps done; K block of the last one
                     const int phase = tv.phase, blk = tv.blk, nt = tv.nt, e = tv.e;
                     const uint64_t pol_b = tv_eblocks > 1 ? pol_b_shared : pol_b_once;
-                    const int n_part = (tv_rows + A_ROWS_PART - 1) / A_ROWS_PART;
-                    const bool part = n_part < BM / A_ROWS_PART;
+                    const int n_part = max(1, (tv_rows + A_ROWS_PART - 1) / A_ROWS_PART);
                     const uint32_t a_bytes = a_stage_bytes(n_part);
                     // bytes the stage's full barrier waits for (the scale blocks only with the
                     // first stage of a group of K blocks)
                     const uint32_t tx_bytes = a_bytes + B_TX;
-                    const uint32_t tx_sfa = SFA_BYTES, tx_sfb = SFB_BYTES;
-                    const CUtensorMap *ta = phase == 1 ? (part ? &maps.a1p : &maps.a1) : (part ? &maps.a2p : &maps.a2);
+                    const CUtensorMap *ta = phase == 1 ? (n_part == 1 ? &maps.a1p : n_part == 2 ? &maps.a1h : &maps.a1)
+                                                       : (n_part == 1 ? &maps.a2p : n_part == 2 ? &maps.a2h : &maps.a2);
                     const CUtensorMap *tb = phase == 1 ? &maps.b1 : &maps.b2;
                     const int nkb = phase == 1 ? NKB1 : NKB2;
                     const int wtile = e * (phase == 1 ? tl.NT1 : tl.NT2) + nt;
@@ -375,27 +394,38 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                             break;
                         }
                         uint8_t *sa = smem + s * sbytes;
-                        uint8_t *ss = sf_smem + s * SF_STAGE_BYTES;
-                        const bool sf_k = kb % SF_GROUP == 0;   // first K block of a scale group
-                        const int grp = kb / SF_GROUP;
-                        const bool sfb_k = FP4 || sf_k;         // a B scale block with this stage
-                        const int bb = FP4 ? kb : grp;          // its index within the tile
-                        ptx::mbar_arrive_expect_tx(&bars->full[s],
-                                                   tx_bytes + (sf_k ? tx_sfa : 0u) + (sfb_k ? tx_sfb : 0u));
-                        {
-                            if (part) {
-                                for (int g = 0; g < n_part; ++g)
-                                    ptx::tma_load_2d(sa + g * A_ROWS_PART * BKS, ta, &bars->full[s], kb * BK,
-                                                     blk * BM + g * A_ROWS_PART, pol_a);
-                            } else {
-                                ptx::tma_load_2d(sa, ta, &bars->full[s], kb * BK, blk * BM, pol_a);
+                        // the first K block of a scale group brings the group's scale blocks into
+                        // the next scale slot: A 512 bytes, B 1 KB (MXFP4: 1 KB per K block of the
+                        // group, copied to TMEM with that K block)
+                        const bool sf_k = kb % SF_GROUP == 0;
+                        uint8_t *ss = nullptr;
+                        uint32_t sfb_bytes = 0;
+                        if (sf_k) {
+                            const uint32_t j = gcount % SF_SLOTS;
+                            ++gcount;
+                            const int glen = min(SF_GROUP, nkb - kb);
+                            // the slot's last reader: released above unless less than nst K blocks
+                            // back (short groups); its stage is not refilled before that release
+                            const uint32_t x = last3;
+                            if (x != ~0u && x + nst > it &&
+                                !ptx::mbar_wait(&bars->empty[x % nst], (x / nst) & 1u, deadline)) {
+                                ok = false;
+                                break;
                             }
-                            ptx::tma_load_2d(sa + a_reg, tb, &bars->full[s], 0, (tile0 + kb) * BN, pol_b);
-                            if (sf_k)
-                                ptx::bulk_load(ss, sfa_src + grp * SFA_BYTES, SFA_BYTES, &bars->full[s]);
-                            if (sfb_k)
-                                ptx::bulk_load(ss + SFA_BYTES, sfb_src + static_cast<long long>(bb) * SFB_BYTES,
-                                               SFB_BYTES, &bars->full[s]);
+                            last3 = last2;
+                            last2 = last1;
+                            last1 = it + (FP4 ? static_cast<uint32_t>(glen - 1) : 0u);
+                            ss = sf_smem + j * SF_SLOT_BYTES;
+                            sfb_bytes = (FP4 ? static_cast<uint32_t>(glen) : 1u) * SFB_BYTES;
+                        }
+                        ptx::mbar_arrive_expect_tx(&bars->full[s], tx_bytes + (sf_k ? SFA_BYTES + sfb_bytes : 0u));
+                        ptx::tma_load_2d(sa, ta, &bars->full[s], kb * BK, blk * BM, pol_a);
+                        ptx::tma_load_2d(sa + a_reg, tb, &bars->full[s], 0, (tile0 + kb) * BN, pol_b);
+                        if (sf_k) {
+                            const int grp = kb / SF_GROUP;
+                            ptx::bulk_load(ss, sfa_src + grp * SFA_BYTES, SFA_BYTES, &bars->full[s]);
+                            ptx::bulk_load(ss + SFA_BYTES, sfb_src + static_cast<long long>(FP4 ? kb : grp) * SFB_BYTES,
+                                           sfb_bytes, &bars->full[s]);
                         }
                     }
                     while (ok && fstep < 3)
@@ -449,13 +479,14 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         } else if (warp == 1) {
             // -------------------------------------------------------- UMMA issuer -----
             if (lane == 0) {
-                uint32_t it = 0, tcount = 0, acc_n = 0;
-                uint32_t s = 0, ph = 0, gslot = 0;   // stage of K block `it`, its pass parity; next scale slot
-                // scale groups copied so far: group g goes to TMEM slot g % nst, reused only after
-                // nst more groups, whose first stage's arrival implies (through the stage ring)
-                // that every UMMA of group g has completed (MXFP4: the per-K-block B scales go
-                // to the B columns of the stage's slot, reused after the stage's next fill)
-                uint32_t sfa = 0, sfb = 0;
+                uint32_t it = 0, tcount = 0, acc_n = 0, gcount = 0;
+                uint32_t s = 0, ph = 0, gslot = 0;   // stage of K block `it`, its pass parity; next TMEM scale slot
+                // Scale group g is copied from shared-memory slot g % SF_SLOTS (MXFP4: each K
+                // block's B scales with that K block) to TMEM group slot g % NST_MAX.  That TMEM
+                // slot is reused only after NST_MAX more groups, i.e. at least NST_MAX K blocks
+                // after group g's last, whose first stage's arrival implies (through the stage
+                // ring of at most NST_MAX stages) that every UMMA reading group g has completed.
+                uint32_t sfa = 0, ssg = 0;   // TMEM slot and shared-memory slot of the current group
                 bool ok = true;
                 while (ok) {
                     const uint32_t slot = tcount % TILE_RING, sph = (tcount / TILE_RING) & 1u;
@@ -483,21 +514,25 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                             break;
                         }
                         ptx::tc_fence_after();
-                        const uint32_t ss = ptx::smem_u32(sf_smem + s * SF_STAGE_BYTES);
                         if (kb % SF_GROUP == 0) {
-                            sfa = tmem + SF_COL + 16 * gslot;
-                            gslot = gslot + 1 == nst ? 0u : gslot + 1;
-                            sf_copy(sfa, ss);
+                            ssg = ptx::smem_u32(sf_smem + (gcount % SF_SLOTS) * SF_SLOT_BYTES);
+                            ++gcount;
+                            sfa = tmem + SF_COL + SF_TCOLS * gslot;
+                            gslot = gslot + 1 == NST_MAX ? 0u : gslot + 1;
+                            sf_copy(sfa, ssg);
                             if constexpr (!FP4) {
-                                sfb = sfa + 4;
-                                sf_copy(sfb, ss + SFA_BYTES);
-                                sf_copy(sfb + 4, ss + SFA_BYTES + 512);
+                                sf_copy(sfa + 4, ssg + SFA_BYTES);
+                                sf_copy(sfa + 8, ssg + SFA_BYTES + 512);
                             }
                         }
+                        uint32_t sfb = sfa + 4;
                         if constexpr (FP4) {
-                            sfb = tmem + SF_COL + 16 * s + 4;
-                            sf_copy(sfb, ss + SFA_BYTES);
-                            sf_copy(sfb + 4, ss + SFA_BYTES + 512);
+                            // copied per K block: the group's copies spread over its K blocks
+                            // measured faster than all at its start
+                            const uint32_t i = static_cast<uint32_t>(kb % SF_GROUP);
+                            sfb += 8 * i;
+                            sf_copy(sfb, ssg + SFA_BYTES + i * SFB_BYTES);
+                            sf_copy(sfb + 4, ssg + SFA_BYTES + i * SFB_BYTES + 512);
                         }
                         const uint32_t a_addr = ptx::smem_u32(smem + s * sbytes);
                         const uint64_t adesc = ptx::kmajor_swizzled_desc<BKS>(a_addr);
@@ -782,7 +817,7 @@ cudaError_t launch_ffn_bs(const FfnMaps &maps, const Dims &d, const Workspace &w
                           const uint8_t *sfb1, const uint8_t *sfb2, int wave_blocks, int num_sms, bool fp4,
                           cudaStream_t s)
 {
-    constexpr int SMEM = 1024 + RING_BYTES + 8192 + NST_MAX * SF_STAGE_BYTES;
+    constexpr int SMEM = 1024 + RING_BYTES + 8192 + SF_SLOTS * static_cast<int>(SF_SLOT_BYTES);
     static_assert(sizeof(BsBars) <= 8192, "barrier block");
     static_assert(SMEM <= 227 * 1024, "shared memory per CTA");
     const bool fu = c.fused_combine != 0;

@@ -123,6 +123,7 @@ constexpr int A_ROWS_PART = 32;   // row granularity of partial A-tile loads
 struct FfnMaps {
     CUtensorMap a1, b1, a2, b2;   // pool x / W1 tiles (gate_up), act / W2 tiles (down)
     CUtensorMap a1p, a2p;         // pool x / act with 32-row boxes (partly filled M-blocks)
+    CUtensorMap a1h, a2h;         // pool x / act with 64-row boxes (block-scaled kernel)
 };
 // the fp32-scale FFN kernel (ffn.cu): one CTA per SM, tiles claimed in list order
 cudaError_t launch_ffn(const FfnMaps &maps, const Dims &d, const Workspace &ws, const CallArgs &c,

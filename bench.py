@@ -49,9 +49,12 @@ PROFILE_EVERY = 8            # timed steps per step carrying the per-kernel stag
 # DRAM bytes per launch from one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum),
 # valid only while the kernel sources hash to `src_sha`; see profiles/.
 NCU_TRAFFIC = {
-    ("large", "expert_ffn"): {"bytes": 3241676288 + 1253330944, "src_sha": "f7fdbebcbe952963"},
-    ("decode", "expert_ffn"): {"bytes": 1420896768 + 5254144, "src_sha": "f7fdbebcbe952963"},
-    ("prefill", "expert_ffn"): {"bytes": 1969887488 + 517826304, "src_sha": "f7fdbebcbe952963"},
+    ("large", "expert_ffn"): {"bytes": 3240100608 + 1253056000, "src_sha": "df9e155d5d29d48e"},
+    ("decode", "expert_ffn"): {"bytes": 1420896512 + 5160960, "src_sha": "df9e155d5d29d48e"},
+    ("prefill", "expert_ffn"): {"bytes": 1972355840 + 517857792, "src_sha": "df9e155d5d29d48e"},
+    # the block-scaled kernel (power-of-two scales, MXFP4 weights)
+    ("decode-mxfp4", "expert_ffn"): {"bytes": 759937792 + 4401664, "src_sha": "a2befd31d661562d"},
+    ("prefill-pow2", "expert_ffn"): {"bytes": 2100153088 + 516071168, "src_sha": "a2befd31d661562d"},
 }
 # sources each stage's kernel is compiled from (a recorded traffic figure is used only while
 # these hash to its `src_sha`)

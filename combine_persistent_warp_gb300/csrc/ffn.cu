@@ -291,13 +291,14 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     // an expert's weight tile is re-read by each of its M-blocks: keep it in L2
                     // unless this block is the expert's only one
                     const uint64_t pol_b = cur.eblocks > 1 ? pol_b_shared : pol_b_once;
-                    // a partly filled M-block loads only its 32-row groups that hold valid rows
-                    // (the UMMA still reads 128 rows; the rest only feed padding rows)
-                    const int n_part = (rows + A_ROWS_PART - 1) / A_ROWS_PART;
-                    const bool part = n_part < BM / A_ROWS_PART;
-                    const uint32_t a_bytes = part ? static_cast<uint32_t>(n_part * A_ROWS_PART * BKS) : STAGE_A_BYTES;
+                    // A rows in one load per K block: the first 32 or 64 rows of a partly filled
+                    // M-block that holds no more valid rows, else all 128 (the UMMA reads 128
+                    // rows; the rest only feed padding rows, never stored)
+                    const int n_part = max(1, (rows + A_ROWS_PART - 1) / A_ROWS_PART);
+                    const uint32_t a_bytes = n_part <= 2 ? static_cast<uint32_t>(n_part * A_ROWS_PART * BKS) : STAGE_A_BYTES;
                     const uint32_t tx_bytes = a_bytes + STAGE_B_BYTES;
-                    const CUtensorMap *ta = phase == 1 ? (part ? &maps.a1p : &maps.a1) : (part ? &maps.a2p : &maps.a2);
+                    const CUtensorMap *ta = phase == 1 ? (n_part == 1 ? &maps.a1p : n_part == 2 ? &maps.a1h : &maps.a1)
+                                                       : (n_part == 1 ? &maps.a2p : n_part == 2 ? &maps.a2h : &maps.a2);
                     const CUtensorMap *tb = phase == 1 ? &maps.b1 : &maps.b2;
                     const int nkb = phase == 1 ? NKB1 : NKB2;
                     // weight tiles are contiguous [E][NT][KB][256][128]: this tile's K block
@@ -328,13 +329,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                         uint8_t *sa = smem + s * STAGE_BYTES;
                         CPW_STAMP(0, it);
                         ptx::mbar_arrive_expect_tx(&bars->full[s], tx_bytes);
-                        if (part) {
-                            for (int g = 0; g < n_part; ++g)
-                                ptx::tma_load_2d(sa + g * A_ROWS_PART * BKS, ta, &bars->full[s], kb * BK,
-                                                 blk * BM + g * A_ROWS_PART, pol_a);
-                        } else {
-                            ptx::tma_load_2d(sa, ta, &bars->full[s], kb * BK, blk * BM, pol_a);
-                        }
+                        ptx::tma_load_2d(sa, ta, &bars->full[s], kb * BK, blk * BM, pol_a);
                         ptx::tma_load_2d(sa + STAGE_A_BYTES, tb, &bars->full[s], 0, (tile0 + kb) * BN, pol_b);
                         if (!pushed) {
                             pushed = true;

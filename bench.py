@@ -431,8 +431,10 @@ def bench_config(name: str, args, dist: Dist, steps: int, warmup: int, *, e2e_st
     if wl.scales == "pow2":   # power-of-two scales: the hardware block-scaled path
         moe.set_option(native.OPT_SCALE_MODE, 1)
     # the automatic mode runs the combine inside the FFN kernel only for an output in pinned host
-    # memory: the end-to-end loop below, not the device-buffer loop
+    # memory (the end-to-end loop below, not the device-buffer loop) and only on the block-scaled
+    # kernel (power-of-two scales or MXFP4 weights)
     in_ffn = args.combine == "in-ffn"
+    block_scaled = wl.scales == "pow2" or wl.weights == "mxfp4"
     moe.set_option(native.OPT_COMBINE_MODE, {"kernel": native.COMBINE_KERNEL, "in-ffn": native.COMBINE_IN_FFN,
                                              "auto": native.COMBINE_AUTO}[args.combine])
     if in_ffn:
@@ -491,8 +493,9 @@ def bench_config(name: str, args, dist: Dist, steps: int, warmup: int, *, e2e_st
         "ms_per_step": t_max / steps * 1e3,
         "config": config_of(wl, model, dist.world, flush),
         "combine": {"device_buffers": "inside the expert FFN kernel" if in_ffn else "separate kernel",
-                    "host_buffers": ("separate kernel" if args.combine == "kernel"
-                                     else "inside the expert FFN kernel")},
+                    "host_buffers": ("inside the expert FFN kernel"
+                                     if args.combine == "in-ffn" or (args.combine == "auto" and block_scaled)
+                                     else "separate kernel")},
         "roofline": roofline_for(dominant, stage_ms[dominant] / calls / 1e3, model, wl.name, fp8_measured),
         "layer_roofline": layer_roofline(model, t_max / steps, fp8_measured),
         "stages_us_per_launch": {k: v / calls * 1e3 for k, v in stage_ms.items()},
@@ -680,7 +683,7 @@ def main(argv=None):
                     help="expert FFN kernel mode: 0 automatic, 1 one CTA per tile")
     ap.add_argument("--combine", choices=["auto", "kernel", "in-ffn"], default="auto",
                     help="top-k combine: a separate kernel, inside the expert FFN kernel, or automatic "
-                         "(inside it for an output in pinned host memory)")
+                         "(inside the block-scaled FFN kernel for an output in pinned host memory)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

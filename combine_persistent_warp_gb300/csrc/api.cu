@@ -596,7 +596,10 @@ static int forward_impl(moe_handle_t h, int T, const uint8_t *x, const float *x_
     if ((h->scale_mode == 1 && !h->weights_pow2) || (h->scale_mode == 0 && h->mxfp4))
         return MOE_ERR_BAD_SCALE;
     const bool bs = h->mxfp4 || h->scale_mode == 1 || (h->scale_mode == 2 && h->weights_pow2);
-    const int fused = h->combine_mode == 2 ? (out_is_host ? 1 : 0) : h->combine_mode;
+    // automatic combine: inside the FFN kernel for an output written in place into pinned host
+    // memory by the block-scaled kernel, whose epilogue warps have slack; the fp32-scale kernel's
+    // epilogue is its critical path, so there the combine kernel writes the output in place
+    const int fused = h->combine_mode == 2 ? ((out_is_host && bs) ? 1 : 0) : h->combine_mode;
     CallArgs c{T, x, x_sf, topk_idx, topk_w, out, h->timeout_ns, h->debug_skip_barrier, bs ? 1 : 0, fused};
     if (h->S > 0) {
         // shared experts: each token's route gains slots K_routed.. naming expert E_routed + s

@@ -141,8 +141,9 @@ int moe_forward(moe_handle_t h, int T, const uint8_t *x, const float *x_sf,
  * the stream has finished.  Inputs in pinned (page-locked, device-mapped) memory with
  * 16-byte aligned addresses are read in place by one staging kernel into the handle's
  * device staging buffers; others are copied there by cudaMemcpyAsync.  A pinned, 16-byte
- * aligned `host_out` is written in place by the kernel that completes the combine (the FFN
- * kernel itself in the default combine mode, see MOE_OPT_COMBINE_MODE); otherwise the result is
+ * aligned `host_out` is written in place by the kernel that completes the combine (with
+ * power-of-two scales or MXFP4 weights the FFN kernel itself in the default combine mode, see
+ * MOE_OPT_COMBINE_MODE); otherwise the result is
  * copied back from a staging buffer.  Pageable buffers work but are slower. */
 int moe_forward_host(moe_handle_t h, int T, const uint8_t *host_x, const float *host_x_sf,
                      const int64_t *host_topk_idx, const float *host_topk_w,
@@ -232,8 +233,10 @@ int moe_get_info(moe_handle_t h, moe_info *info);
  * (token, n-tile) whose routed rows are all scattered while other tiles are still being
  * computed (the forward is then two kernels, three with shared experts); 2 = automatic
  * (default): 1 when a host-buffer entry point writes the output into pinned host memory in
- * place (its rows then cross to the host while the GEMMs still run), else 0.  All modes give
- * the same output bits.  Other values are refused. */
+ * place and the block-scaled FFN kernel runs (power-of-two scales or MXFP4 weights: its rows
+ * then cross to the host while the GEMMs still run), else 0 (with arbitrary fp32 scales the
+ * reduce would lengthen the FFN kernel's critical epilogue more than it saves).  All modes
+ * give the same output bits.  Other values are refused. */
 enum moe_option {
     MOE_OPT_TIMEOUT_NS = 0,
     MOE_OPT_DEBUG_SKIP_BARRIER = 1,

@@ -177,8 +177,9 @@ def test_in_kernel_combine_errors_then_recovers():
 @pytest.mark.parametrize("name", ["tiny", "tiny-pow2", "tiny-mxfp4"])
 def test_in_kernel_combine_host_entry_point(name):
     """Host buffers: the pinned output written in place by the FFN kernel (in-kernel mode, and
-    the automatic mode, which picks it for a pinned output), a misaligned pinned output through
-    the staging buffer, and pageable buffers: all equal the device entry point."""
+    the automatic mode, which picks it for a pinned output of the block-scaled kernel and the
+    combine kernel otherwise), a misaligned pinned output through the staging buffer, and
+    pageable buffers: all equal the device entry point."""
     moe, inp = layer(name)
     dev = forward_mode(moe, inp, KERNEL).cpu()
     pin = lambda t: t.cpu().pin_memory()

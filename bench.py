@@ -661,7 +661,7 @@ def run_reference(args, dist: Dist) -> dict | None:
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=200)   # ~0.6 s timed at the large batch: several clock samples
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="large",
                     help="tiny, decode, prefill, skewed, large, or one of them with -pow2 "

@@ -663,8 +663,8 @@ static void *mapped_host(const void *p)
 // a set is refilled only after the forward that read it).  Otherwise pinned inputs are read
 // in place by one staging kernel (16-byte aligned buffers) and pageable ones copied on the
 // forward's stream.  The output is written in place when it is pinned and 16-byte aligned (by
-// the FFN kernel in the automatic combine mode, else by the combine kernel), else copied back
-// from the staging buffer.
+// the block-scaled FFN kernel in the automatic combine mode, else by the combine kernel), else
+// copied back from the staging buffer.
 static int forward_host_impl(moe_handle_t h, int T, const uint8_t *host_x, const float *host_x_sf,
                              const int64_t *host_topk_idx, const float *host_topk_w, uint16_t *host_out,
                              void *stream, bool wait)

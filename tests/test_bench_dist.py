@@ -1,4 +1,5 @@
-"""The benchmark's multi-rank bookkeeping on CPU (gloo, world size 2).
+"""The benchmark's bookkeeping on CPU: multi-rank aggregation (gloo, world size 2), the
+reference arm's rank, the work model and the recorded DRAM-traffic lookup.
 
 The layer runs as independent replicas on several GPUs; the benchmark only sums the
 routed rows of all ranks and divides by the slowest rank's time.
@@ -58,3 +59,25 @@ def test_work_model_counts_valid_rows_only():
     m = bench.work_model(inp)
     assert m["M"] == 64 * 2 - 1
     assert m["flops"] == 6 * m["M"] * 256 * 128
+
+
+def test_recorded_traffic_is_used_only_for_the_sources_it_was_taken_on(monkeypatch):
+    """A recorded DRAM-traffic figure enters the roofline line only while the kernel's
+    sources hash to the state it was captured on; block-scaled workloads look up the
+    block-scaled kernel's sources."""
+    from combine_persistent_warp_gb300.workloads import make_inputs
+    m = bench.work_model(make_inputs("tiny"))
+    cur = bench.kernel_sources_sha("expert_ffn")
+    cur_bs = bench.kernel_sources_sha("expert_ffn_bs")
+    assert cur != cur_bs
+    monkeypatch.setattr(bench, "NCU_TRAFFIC", {
+        ("tiny", "expert_ffn"): {"bytes": 1234, "src_sha": cur},
+        ("tiny-pow2", "expert_ffn"): {"bytes": 5678, "src_sha": cur_bs},
+        ("tiny-mxfp4", "expert_ffn"): {"bytes": 999, "src_sha": cur},   # the other kernel's state
+    })
+    assert bench.roofline_for("expert_ffn", 1e-5, m, "tiny", None)["traffic"] == 1234
+    assert bench.roofline_for("expert_ffn", 1e-5, m, "tiny-pow2", None)["traffic"] == 5678
+    assert bench.roofline_for("expert_ffn", 1e-5, m, "tiny-mxfp4", None)["traffic"] is None
+    assert bench.roofline_for("expert_ffn", 1e-5, m, "decode", None)["traffic"] is None
+    monkeypatch.setattr(bench, "NCU_TRAFFIC", {("tiny", "expert_ffn"): {"bytes": 1234, "src_sha": "0" * 16}})
+    assert bench.roofline_for("expert_ffn", 1e-5, m, "tiny", None)["traffic"] is None

@@ -30,17 +30,19 @@
 // other piece of work is kept off the epilogue warps' path:
 //
 // Roles of the 12 warps of a CTA (one CTA per SM):
-//   warp 0     TMA producer: A and B tiles of one 128-deep K block per stage into a 4-deep
-//              ring (192 KB)
+//   warp 0     TMA producer: A and B tiles of one 128-deep K block per stage into a 3-deep
+//              ring (144 KB)
 //   warp 1     UMMA issuer: four 128x256x32 tcgen05.mma per K block into a fresh TMEM partial
 //   warp 2     stager: per tile, the weight scales of all its K blocks, the A-row scales of
 //              its first K block and (down tiles) each row's gate weight and combine row,
 //              into the tile's ring slot, so a tile starts without a dependent global load
 //   warp 3     release warp: publishes a gate_up tile's stored SwiGLU rows to the down tiles
 //              of every CTA (proxy fence + GPU-scope release add on l1_done), so no epilogue
-//              warp waits for its own stores to drain; with the top-k combine inside this
-//              kernel it also counts each stored down tile's rows per (token, n-tile) and
-//              lists the (token, n-tile) pairs the tile completed (topk_combine.cuh)
+//              warp waits for its own stores to drain; stores each down tile's bf16 rows,
+//              which the epilogue warps stage in shared memory (64 KB), one full row per warp
+//              store, so the epilogue goes on to the next tile at once; with the top-k combine
+//              inside this kernel it then counts the tile's rows per (token, n-tile) and lists
+//              the (token, n-tile) pairs the tile completed (topk_combine.cuh)
 //   warps 4-11 two epilogue warpgroups, columns [0,128) and [128,256) of the tile; with the
 //              in-kernel combine they reduce the previous tile's completed pairs after each
 //              tile
@@ -94,16 +96,24 @@ __device__ __forceinline__ int trace_slot()
     } while (0)
 #endif
 
+// Shared memory: a 3-stage operand ring of [A 16 KB | B 32 KB], then a down tile's bf16 output,
+// staged by the epilogue warps for the release warp's stores: 128 rows x 512 bytes, 16-byte
+// chunk c of row r at r*512 + 16*(c ^ (r % 32)) (conflict-free for a lane per row or a lane per
+// chunk).  Three stages keep a tensor-bound batch's pipe fed (four measured the same at the
+// large and prefill batches and 2.5% faster at decode, which the staged stores do not pay for).
+constexpr int FSTAGES = 3;
+constexpr int OUT_STAGE_BYTES = BM * 2 * BN;
 struct __align__(16) FfnBars {
-    uint64_t full[STAGES];
-    uint64_t empty[STAGES];           // epilogue warp 4, once the stage's MMAs are complete
+    uint64_t full[FSTAGES];
+    uint64_t empty[FSTAGES];           // epilogue warp 4, once the stage's MMAs are complete
     uint64_t tfull[2];
     uint64_t tempty[2];
     uint64_t xbar;                    // row-amax exchange between the two epilogue warpgroups
     uint64_t tile_full[TILE_RING];    // producer -> all: next tile, its expert and valid rows
     uint64_t tile_empty[TILE_RING];   // issuer, stager, release warp and epilogue warps are done with the slot
     uint64_t meta_ready[TILE_RING];   // stager -> epilogue: the slot's scales / row data are in place
-    uint64_t act_done[TILE_RING];     // epilogue -> release warp: the slot's tile is stored
+    uint64_t act_done[TILE_RING];     // epilogue -> release warp: the slot's tile is stored (a down tile: staged)
+    uint64_t out_free;                // release warp -> epilogue: the staged down tile is stored
     int tile_ring[TILE_RING];
     int tile_e[TILE_RING];
     int tile_rows[TILE_RING];
@@ -118,7 +128,7 @@ struct __align__(16) FfnBars {
     int exit_flag;
     int max_rows;                      // valid rows of the fullest M-block of the forward
 };
-constexpr int FFN_SMEM_BYTES = 1024 /*align slack*/ + STAGES * STAGE_BYTES + static_cast<int>(sizeof(FfnBars));
+constexpr int FFN_SMEM_BYTES = 1024 /*align slack*/ + FSTAGES * STAGE_BYTES + OUT_STAGE_BYTES + static_cast<int>(sizeof(FfnBars));
 static_assert(FFN_SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
 
 // Tile list: waves of `wave_blocks` M-blocks; inside a wave all phase-1 tiles (block-major,
@@ -166,12 +176,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
-    FfnBars *bars = reinterpret_cast<FfnBars *>(smem + STAGES * STAGE_BYTES);
+    uint8_t *out_stage = smem + FSTAGES * STAGE_BYTES;
+    FfnBars *bars = reinterpret_cast<FfnBars *>(out_stage + OUT_STAGE_BYTES);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     // prologue (barriers, TMEM, tensor maps) while the routing kernel may still run
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
+        for (int s = 0; s < FSTAGES; ++s) {
             ptx::mbar_init(&bars->full[s], 1);
             ptx::mbar_init(&bars->empty[s], 1);
         }
@@ -180,6 +191,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             ptx::mbar_init(&bars->tempty[b], EPI_WARPS);
         }
         ptx::mbar_init(&bars->xbar, 32 * EPI_WARPS);       // every epilogue thread
+        ptx::mbar_init(&bars->out_free, 1);
         for (int i = 0; i < TILE_RING; ++i) {
             ptx::mbar_init(&bars->tile_full[i], 1);
             ptx::mbar_init(&bars->tile_empty[i], 3 + EPI_WARPS);
@@ -321,7 +333,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                         ptx::fence_proxy_async_global();
                     }
                     for (int kb = 0; kb < nkb && ok; ++kb, ++it) {
-                        const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+                        const uint32_t s = it % FSTAGES, ph = (it / FSTAGES) & 1u;
                         if (!ptx::mbar_wait(&bars->empty[s], ph ^ 1u, deadline)) {
                             ok = false;
                             break;
@@ -344,8 +356,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     record_error(ws.hdr, DEV_TIMEOUT);
                 // drain: every issued load has landed before the CTA may exit
                 const uint64_t dl = ptx::globaltimer() + static_cast<uint64_t>(c.timeout_ns);
-                for (uint32_t i = it > STAGES ? it - STAGES : 0; i < it; ++i)
-                    ptx::mbar_wait(&bars->full[i % STAGES], (i / STAGES) & 1u, dl);
+                for (uint32_t i = it > FSTAGES ? it - FSTAGES : 0; i < it; ++i)
+                    ptx::mbar_wait(&bars->full[i % FSTAGES], (i / FSTAGES) & 1u, dl);
             }
         } else if (warp == 1) {
             // -------------------------------------------------------- UMMA issuer -----
@@ -374,7 +386,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                             break;
                         }
                         CPW_STAMP(8, it);
-                        const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+                        const uint32_t s = it % FSTAGES, ph = (it / FSTAGES) & 1u;
                         if (!ptx::mbar_wait(&bars->full[s], ph, deadline)) {
                             ok = false;
                             break;
@@ -517,10 +529,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             // a tile; for a gate_up tile that means its SwiGLU rows and scales are stored, and
             // lane 0 publishes them for the down tiles of every CTA: the CTA-scope barrier
             // orders the epilogue's stores before this thread's GPU-scope release (release is
-            // cumulative), and the proxy fence covers the TMA loads that read them.  With the
-            // combine inside this kernel the warp also counts every stored down tile's rows per
-            // (token, n-tile) and lists the pairs the tile completed for the epilogue warps,
-            // which reduce them at the end of their next tile (topk_combine.cuh).
+            // cumulative), and the proxy fence covers the TMA loads that read them.  For a down
+            // tile it means the tile's bf16 rows are staged in shared memory: this warp stores
+            // them and hands the buffer back.  With the combine inside this kernel the warp
+            // then counts the down tile's rows per (token, n-tile) (its own stores, fenced
+            // first) and lists the pairs the tile completed for the epilogue warps, which
+            // reduce them at the end of their next tile (topk_combine.cuh).
             uint32_t tcount = 0;
             bool ok = true;
             while (ok) {
@@ -548,6 +562,24 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 if (phase == 1 && lane == 0) {
                     ptx::fence_proxy_async_global();
                     ptx::red_release_add(ws.l1_done + blk, static_cast<uint32_t>(EPI_WARPS));
+                }
+                if (phase == 2) {
+                    // the staged down tile: lane l stores 16-byte chunk l of each valid row, the
+                    // warp one full 512-byte row per instruction (only its first half when the
+                    // tile's second column half lies past H); then the buffer is free again
+                    const int rows = bars->tile_rows[slot];
+                    const bool half2 = nt * BN + 128 < d.H;
+                    const bool mine = lane < 16 || half2;
+                    uint16_t *dst0 = ws.combine + nt * BN + lane * 8;
+#pragma unroll 4
+                    for (int r = 0; r < rows; ++r) {
+                        const uint4 v = *reinterpret_cast<const uint4 *>(out_stage + r * (2 * BN) + ((lane ^ (r & 31)) << 4));
+                        if (mine)
+                            *reinterpret_cast<uint4 *>(dst0 + static_cast<long long>(bars->roff[slot][r]) * d.H) = v;
+                    }
+                    __syncwarp();
+                    if (lane == 0)
+                        ptx::mbar_arrive(&bars->out_free);
                 }
                 if (FUSED) {
                     const int n = phase == 2 ? topk::count_rows(d, ws, static_cast<long long>(blk) * BM,
@@ -577,7 +609,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         const int q = warp & 3;                  // TMEM lane quarter this warp may access
         const int row = q * 32 + lane;           // tile row = TMEM lane
         const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
-        uint32_t it = 0, xcount = 0, tcount = 0;
+        uint32_t it = 0, xcount = 0, tcount = 0, dcount = 0;   // dcount: down tiles staged
         bool ok = true;
         // in-kernel combine: the (token, n-tile) pairs the release warp listed for the previous
         // tile are reduced by the eight epilogue warps at the end of the next one
@@ -636,7 +668,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             for (int j = 0; j < 128; ++j)
                 acc[j] = 0.0f;
             for (int kb = 0; kb < nkb; ++kb, ++it) {
-                const uint32_t s = it % STAGES;
+                const uint32_t s = it % FSTAGES;
                 const uint32_t buf = it & 1u, bph = (it >> 1) & 1u;
                 const float s0 = a_nx * sb0[kb], s1 = a_nx * sb1[kb];
                 if (kb + 1 < nkb && !dead) {
@@ -750,55 +782,32 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     if (wg == 0)
                         ws.act_sf[static_cast<long long>(nt) * ws.P + prow] = sf;
                 }
-            } else if (!dead) {
-                // Weighted scatter of this warp's 32 rows x 128 columns (256 bytes of bf16 per
-                // row, each row to its own (slot, token) row of the combine buffer).  Stored
-                // straight from the TMEM layout (a lane per row), every store instruction would
-                // touch 32 rows with 16 bytes each, and that stream of partial-line writes holds
-                // up this SM's TMA loads of the next tile.  So each group of 8 lanes first
-                // transposes its 8 rows x 8 16-byte chunks (per 128-byte half) with three
-                // xor-shuffle stages; then store (h, i) has the group write row i's half h as
-                // one full 128-byte line, four lines per instruction.
-                const float gw = bars->gw[slot][row];
-                const uint32_t roff = bars->roff[slot][row];   // combine row: slot * max_tokens + token
-                uint32_t w[64];   // chunk k (columns 8k..8k+7) = w[4k..4k+3]
-#pragma unroll
-                for (int j = 0; j < 64; ++j) {
-                    const __nv_bfloat162 b2 = __floats2bfloat162_rn(gw * acc[2 * j], gw * acc[2 * j + 1]);
-                    w[j] = *reinterpret_cast<const uint32_t *>(&b2);
+            } else {
+                // Weighted scatter of this warp's 32 rows x 128 columns: bf16(gate weight x row)
+                // into the output staging buffer (row r's 512 bytes, this column half's 16-byte
+                // chunks at 16*(c ^ (r % 32)) for c = 16*wg .. 16*wg+15); the release warp stores
+                // each staged row with one full-line warp store into its (slot, token) combine
+                // row while these warps go on with the next tile.  The buffer is rewritten once
+                // the release warp has stored the previous down tile.
+                if (!warp_wait(&bars->out_free, (dcount & 1u) ^ 1u, deadline)) {
+                    ok = false;
+                    break;
                 }
-                // stage b swaps bit b of (lane, chunk) wherever they differ: afterwards lane
-                // p of a group holds, in chunk slot 8h + i, chunk 8h + p of the group's row i
-                const int p8 = lane & 7, g8 = lane & ~7;
+                ++dcount;
+                if (!dead) {
+                    const float gw = bars->gw[slot][row];
+                    uint8_t *orow = out_stage + row * (2 * BN);
 #pragma unroll
-                for (int b = 4; b >= 1; b >>= 1) {
-                    const bool hi = (p8 & b) != 0;
+                    for (int k = 0; k < 16; ++k) {
+                        uint32_t w4[4];
 #pragma unroll
-                    for (int h = 0; h < 2; ++h)
-#pragma unroll
-                        for (int c0 = 0; c0 < 8; ++c0) {
-                            if (c0 & b)
-                                continue;
-#pragma unroll
-                            for (int u = 0; u < 4; ++u) {
-                                uint32_t &e0 = w[(8 * h + c0) * 4 + u];
-                                uint32_t &e1 = w[(8 * h + (c0 | b)) * 4 + u];
-                                const uint32_t y = __shfl_xor_sync(0xFFFFFFFFu, hi ? e0 : e1, b);
-                                e0 = hi ? y : e0;
-                                e1 = hi ? e1 : y;
-                            }
+                        for (int u = 0; u < 4; ++u) {
+                            const __nv_bfloat162 b2 =
+                                __floats2bfloat162_rn(gw * acc[8 * k + 2 * u], gw * acc[8 * k + 2 * u + 1]);
+                            w4[u] = *reinterpret_cast<const uint32_t *>(&b2);
                         }
-                }
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const uint32_t ro = __shfl_sync(0xFFFFFFFFu, roff, g8 + i);
-                    if (q * 32 + g8 + i < rows) {
-                        uint16_t *dst = ws.combine + static_cast<long long>(ro) * d.H + nt * BN + wg * 128 + p8 * 8;
-#pragma unroll
-                        for (int h = 0; h < 2; ++h)
-                            *reinterpret_cast<uint4 *>(dst + h * 64) =
-                                make_uint4(w[(8 * h + i) * 4], w[(8 * h + i) * 4 + 1], w[(8 * h + i) * 4 + 2],
-                                           w[(8 * h + i) * 4 + 3]);
+                        const int ch = (wg * 16 + k) ^ (row & 31);
+                        *reinterpret_cast<uint4 *>(orow + ch * 16) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
                     }
                 }
             }

@@ -36,13 +36,12 @@
 //   warp 2     stager: per tile, the weight scales of all its K blocks, the A-row scales of
 //              its first K block and (down tiles) each row's gate weight and combine row,
 //              into the tile's ring slot, so a tile starts without a dependent global load
-//   warp 3     release warp: publishes a gate_up tile's stored SwiGLU rows to the down tiles
-//              of every CTA (proxy fence + GPU-scope release add on l1_done), so no epilogue
-//              warp waits for its own stores to drain; stores each down tile's bf16 rows,
-//              which the epilogue warps stage in shared memory (64 KB), one full row per warp
-//              store, so the epilogue goes on to the next tile at once; with the top-k combine
-//              inside this kernel it then counts the tile's rows per (token, n-tile) and lists
-//              the (token, n-tile) pairs the tile completed (topk_combine.cuh)
+//   warp 3     release warp: stores each tile's output rows, which the epilogue warps stage
+//              in shared memory (64 KB), as full-line warp stores, so the epilogue goes on to
+//              the next tile at once; then publishes a gate_up tile's SwiGLU rows to the down
+//              tiles of every CTA (proxy fence + GPU-scope release add on l1_done); with the
+//              top-k combine inside this kernel it counts a down tile's rows per (token,
+//              n-tile) and lists the (token, n-tile) pairs the tile completed (topk_combine.cuh)
 //   warps 4-11 two epilogue warpgroups, columns [0,128) and [128,256) of the tile; with the
 //              in-kernel combine they reduce the previous tile's completed pairs after each
 //              tile
@@ -96,10 +95,11 @@ __device__ __forceinline__ int trace_slot()
     } while (0)
 #endif
 
-// Shared memory: a 3-stage operand ring of [A 16 KB | B 32 KB], then a down tile's bf16 output,
-// staged by the epilogue warps for the release warp's stores: 128 rows x 512 bytes, 16-byte
-// chunk c of row r at r*512 + 16*(c ^ (r % 32)) (conflict-free for a lane per row or a lane per
-// chunk).  Three stages keep a tensor-bound batch's pipe fed (four measured the same at the
+// Shared memory: a 3-stage operand ring of [A 16 KB | B 32 KB], then a tile's output, staged by
+// the epilogue warps for the release warp's stores: a down tile's bf16 rows (128 x 512 bytes,
+// 16-byte chunk c of row r at r*512 + 16*(c ^ (r % 32))) or a gate_up tile's FP8 act rows (128
+// x 128 bytes, chunk c at r*128 + 16*(c ^ (r % 8))); both conflict-free for a lane per row or a
+// lane per chunk.  Three stages keep a tensor-bound batch's pipe fed (four measured the same at the
 // large and prefill batches and 2.5% faster at decode, which the staged stores do not pay for).
 constexpr int FSTAGES = 3;
 constexpr int OUT_STAGE_BYTES = BM * 2 * BN;
@@ -526,12 +526,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         } else {
             // -------------------------------------------------------- release warp ----
             // The epilogue warps arrive on the slot's act_done barrier when they are done with
-            // a tile; for a gate_up tile that means its SwiGLU rows and scales are stored, and
-            // lane 0 publishes them for the down tiles of every CTA: the CTA-scope barrier
-            // orders the epilogue's stores before this thread's GPU-scope release (release is
-            // cumulative), and the proxy fence covers the TMA loads that read them.  For a down
-            // tile it means the tile's bf16 rows are staged in shared memory: this warp stores
-            // them and hands the buffer back.  With the combine inside this kernel the warp
+            // a tile: its output rows are staged in shared memory (and a gate_up tile's row
+            // scales stored).  This warp stores the rows and hands the buffer back; for a
+            // gate_up tile lane 0 then publishes them for the down tiles of every CTA: the
+            // CTA-scope barriers order the stores before this thread's GPU-scope release
+            // (release is cumulative), and the proxy fence covers the TMA loads that read them.  With the combine inside this kernel the warp
             // then counts the down tile's rows per (token, n-tile) (its own stores, fenced
             // first) and lists the pairs the tile completed for the epilogue warps, which
             // reduce them at the end of their next tile (topk_combine.cuh).
@@ -559,9 +558,20 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     CPW_STAMP(12, tcount - 1);
                 int phase, blk, nt;
                 tl.at(tile, phase, blk, nt);
-                if (phase == 1 && lane == 0) {
-                    ptx::fence_proxy_async_global();
-                    ptx::red_release_add(ws.l1_done + blk, static_cast<uint32_t>(EPI_WARPS));
+                if (phase == 1) {
+                    // the staged act rows: lanes 8i..8i+7 store row 4k+i's 128 bytes (a full line)
+                    const int rows = bars->tile_rows[slot];
+                    const int c = lane & 7;
+                    for (int r = lane >> 3; r < rows; r += 4) {
+                        const uint4 v = *reinterpret_cast<const uint4 *>(out_stage + r * 128 + ((c ^ (r & 7)) << 4));
+                        *reinterpret_cast<uint4 *>(ws.act + (static_cast<long long>(blk) * BM + r) * d.I + nt * 128 + c * 16) = v;
+                    }
+                    __syncwarp();
+                    if (lane == 0) {
+                        ptx::mbar_arrive(&bars->out_free);
+                        ptx::fence_proxy_async_global();
+                        ptx::red_release_add(ws.l1_done + blk, static_cast<uint32_t>(EPI_WARPS));
+                    }
                 }
                 if (phase == 2) {
                     // the staged down tile: lane l stores 16-byte chunk l of each valid row, the
@@ -609,7 +619,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         const int q = warp & 3;                  // TMEM lane quarter this warp may access
         const int row = q * 32 + lane;           // tile row = TMEM lane
         const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
-        uint32_t it = 0, xcount = 0, tcount = 0, dcount = 0;   // dcount: down tiles staged
+        uint32_t it = 0, xcount = 0, tcount = 0, dcount = 0;   // dcount: tiles staged
         bool ok = true;
         // in-kernel combine: the (token, n-tile) pairs the release warp listed for the previous
         // tile are reduced by the eight epilogue warps at the end of the next one
@@ -762,11 +772,19 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     ok = false;
                     break;
                 }
+                // the act rows go through the staging buffer too (row r's 128 bytes at r*128,
+                // 16-byte chunk c at 16*(c ^ (r % 8))): the release warp stores them as full
+                // lines before it publishes the tile
+                if (!warp_wait(&bars->out_free, (dcount & 1u) ^ 1u, deadline)) {
+                    ok = false;
+                    break;
+                }
+                ++dcount;
                 if (live) {
                     amax = fmaxf(fmaxf(bars->amax[tp][0][row], bars->amax[tp][1][row]), 1e-4f);
                     const float sf = amax / 448.0f;
                     const float inv = 448.0f / amax;
-                    uint4 *dst = reinterpret_cast<uint4 *>(ws.act + prow * d.I + nt * 128 + wg * 64);
+                    uint8_t *orow = out_stage + row * 128;
 #pragma unroll
                     for (int v = 0; v < 4; ++v) {
                         uint32_t w4[4];
@@ -777,7 +795,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                             const uint32_t hi = ptx::cvt_e4m3x2(acc[m + 2] * inv, acc[m + 3] * inv);
                             w4[p] = lo | (hi << 16);
                         }
-                        dst[v] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                        *reinterpret_cast<uint4 *>(orow + (((wg * 4 + v) ^ (row & 7)) << 4)) =
+                            make_uint4(w4[0], w4[1], w4[2], w4[3]);
                     }
                     if (wg == 0)
                         ws.act_sf[static_cast<long long>(nt) * ws.P + prow] = sf;
@@ -788,7 +807,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 // chunks at 16*(c ^ (r % 32)) for c = 16*wg .. 16*wg+15); the release warp stores
                 // each staged row with one full-line warp store into its (slot, token) combine
                 // row while these warps go on with the next tile.  The buffer is rewritten once
-                // the release warp has stored the previous down tile.
+                // the release warp has stored the previous tile.
                 if (!warp_wait(&bars->out_free, (dcount & 1u) ^ 1u, deadline)) {
                     ok = false;
                     break;

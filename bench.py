@@ -49,9 +49,9 @@ PROFILE_EVERY = 8            # timed steps per step carrying the per-kernel stag
 # DRAM bytes per launch from one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum),
 # valid only while the kernel sources hash to `src_sha`; see profiles/.
 NCU_TRAFFIC = {
-    ("large", "expert_ffn"): {"bytes": 3245236736 + 1250612480, "src_sha": "6dc8bd8a6cdc8cd5"},
-    ("decode", "expert_ffn"): {"bytes": 1420884992 + 5098496, "src_sha": "6dc8bd8a6cdc8cd5"},
-    ("prefill", "expert_ffn"): {"bytes": 1992667648 + 517031680, "src_sha": "6dc8bd8a6cdc8cd5"},
+    ("large", "expert_ffn"): {"bytes": 3246707712 + 1247772416, "src_sha": "05d9ff51cb1a7884"},
+    ("decode", "expert_ffn"): {"bytes": 1421868032 + 4820736, "src_sha": "05d9ff51cb1a7884"},
+    ("prefill", "expert_ffn"): {"bytes": 1998627328 + 515535104, "src_sha": "05d9ff51cb1a7884"},
     # the block-scaled kernel (power-of-two scales, MXFP4 weights)
     ("decode-mxfp4", "expert_ffn"): {"bytes": 759937792 + 4401664, "src_sha": "a2befd31d661562d"},
     ("prefill-pow2", "expert_ffn"): {"bytes": 2100153088 + 516071168, "src_sha": "a2befd31d661562d"},
